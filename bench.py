@@ -1,0 +1,417 @@
+#!/usr/bin/env python3
+"""Benchmark: strict-FP32 SGEMM GFLOP/s on one GB300, as a fraction of the
+measured FP32 FFMA ceiling.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+A step is one SGEMM call, C = alpha*A*B + beta*C, on the named synthetic
+workload (default: M = N = K = 4096, uniform[-1, 1], alpha = 1, beta = 0,
+the pages' headline shape). The inputs (A + B + C = 201 MB) are larger than
+the 129 MB L2, so no flush is needed between steps.
+
+Prints ONE JSON line. ``value`` is GFLOP/s = 2MNK / (device time per step)
+with the inputs resident in HBM; ``e2e`` is the same metric when every step
+also copies A and B (and C when beta != 0) from pinned host memory and
+copies C back. ``roofline`` reports the SGEMM kernel against the FP32
+CUDA-core peak (SMs x 128 lanes x 2 FLOP x max SM clock, ``bound: alu``);
+``fp32_ceiling`` is the pure-FFMA microbenchmark measured in this run (the
+metric's denominator). ``cpu_baseline`` is the double-accumulating CPU
+oracle timed on this host on a row block of the same problem.
+
+``--impl reference`` times that CPU oracle instead (the reference arm): each
+step is a bounded row block of the workload.
+
+With --gpus N > 1 (launched by torchrun) every rank runs an independent
+replica of the workload (the problem is single-GPU; there is no collective
+on the data path); ``value`` is the sum over ranks of the work divided by
+the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "FP32 SGEMM GFLOP/s (2MNK/t) at 4096³; % of measured GB300 FP32 FMA ceiling"
+L2_BYTES = 129 * 1024 * 1024
+FP32_LANES_PER_SM = 128
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="sq4096_uniform")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--peak-ms", type=float, default=300.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=0,
+                    help="rows of C in the CPU baseline sample (0: sized to ~10 s)")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons (every 200 ms)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return self
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=5)
+        sm, mx, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+def kernel_sources_digest() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "dense_fp32_matrix_strict_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None, None
+    with open(path) as f:
+        data = json.load(f)
+    rec = data.get(workload, {})
+    if rec.get("kernel") != kernel or rec.get("csrc_digest") != kernel_sources_digest():
+        return None, None
+    return rec.get("dram_bytes_per_launch"), rec.get("note")
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f)
+    return {}
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------
+def cpu_oracle_rows(w, A, B, C0, rows: int, nthreads: int = 0):
+    """Time the CPU oracle on the first `rows` rows of C; returns (seconds, flops)."""
+    import oracle
+    r = min(rows, w.M)
+    c0 = C0[:r] if w.beta != 0 else None
+    t0 = time.perf_counter()
+    oracle.sgemm_ref(w.alpha, A[:r], B, w.beta, c0, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return dt, 2.0 * r * w.N * w.K
+
+
+def cpu_baseline(w, A, B, C0, rows: int):
+    import oracle
+    oracle.build()
+    threads = oracle.num_threads()
+    if rows <= 0:
+        # Calibrate on a small block, then size the sample to ~10 s.
+        probe = max(1, min(w.M, 64))
+        dt, fl = cpu_oracle_rows(w, A, B, C0, probe)
+        rate = fl / max(dt, 1e-6)
+        rows = int(min(w.M, max(1, 10.0 * rate / (2.0 * w.N * w.K))))
+    dt, fl = cpu_oracle_rows(w, A, B, C0, rows)
+    return {"value": fl / dt / 1e9, "unit": "GFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"first {min(rows, w.M)} of {w.M} rows of C (all N={w.N}, K={w.K}), "
+                      f"{fl / 1e9:.1f} GFLOP in {dt:.2f} s, double accumulation, OpenMP"}
+
+
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, w):
+    """Reference arm: the CPU oracle, bounded row blocks of the workload."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    A, B, C0 = w.make()
+    # One step = one row block sized so the whole run stays within minutes.
+    probe_dt, probe_fl = cpu_oracle_rows(w, A, B, C0, min(w.M, 16))
+    rate = probe_fl / max(probe_dt, 1e-6)
+    total_steps = args.steps + args.warmup
+    rows = int(max(1, min(w.M, (120.0 / max(total_steps, 1)) * rate / (2.0 * w.N * w.K))))
+    for _ in range(args.warmup):
+        cpu_oracle_rows(w, A, B, C0, rows)
+    times, flops = [], 0.0
+    for _ in range(args.steps):
+        dt, fl = cpu_oracle_rows(w, A, B, C0, rows)
+        times.append(dt)
+        flops = fl
+    total = sum(times)
+    value = flops * args.steps / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, None, None),
+        "cpu_baseline": {"value": value, "unit": "GFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"each step: first {rows} of {w.M} rows of C (all N, K)"},
+        "e2e": {"value": value, "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w, kernel, grid):
+    nbytes = 4 * (w.M * w.K + w.K * w.N + w.M * w.N)
+    cfg = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "alpha": w.alpha, "beta": w.beta,
+           "dist": f"A~{w.dist_a}, B~{w.dist_b}, C0~{w.dist_c}", "seed": w.seed,
+           "layout": "row-major, lda=K, ldb=ldc=N",
+           "l2": (f"inputs larger than L2 ({nbytes / 2**20:.0f} MiB > 129 MiB), no flush"
+                  if nbytes > L2_BYTES else "L2 flushed between steps")}
+    if kernel is not None:
+        cfg["kernel"] = kernel
+        cfg["grid"] = grid
+    return cfg
+
+
+def run_ours(args, w):
+    import torch
+    import dense_fp32_matrix_strict_gb300 as sg
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+    props = torch.cuda.get_device_properties(dev)
+    sg.load()
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+
+    A, B, C0 = w.make()
+    dA = torch.from_numpy(A).cuda()
+    dB = torch.from_numpy(B).cuda()
+    dC = torch.from_numpy(C0).cuda()
+    nbytes_in = 4 * (w.M * w.K + w.K * w.N + w.M * w.N)
+    flush = None
+    if nbytes_in <= L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+    kernel, grid = sg.plan_tensors(w.alpha, dA, dB, w.beta, dC)
+
+    def step():
+        if flush is not None:
+            flush.zero_()
+        sg.sgemm_tensors(w.alpha, dA, dB, w.beta, dC, stream=stream)
+
+    # Measured FFMA ceiling, same process, right before the GEMM.
+    clk_peak = ClockSampler(dev).start()
+    peak = sg.fp32_peak(target_ms=args.peak_ms)
+    peak_clocks = clk_peak.stop()
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    sg.check_status()
+
+    # Timed region: K steps between barriers + syncs; per-launch events too.
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clk = ClockSampler(dev).start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        if flush is not None:
+            flush.zero_()
+        ev[i][0].record(stream)
+        sg.sgemm_tensors(w.alpha, dA, dB, w.beta, dC, stream=stream)
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = clk.stop()
+    sg.check_status()
+    total_ms = t_start.elapsed_time(t_end)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    flops = w.flops
+    ms_step = total_ms / args.steps
+    kernel_ms = statistics.mean(launch_ms)
+    value = world * flops / (ms_step * 1e-3) / 1e9
+
+    # End to end through the public API with host buffers.
+    hA = torch.from_numpy(A).pin_memory()
+    hB = torch.from_numpy(B).pin_memory()
+    hC0 = torch.from_numpy(C0).pin_memory()
+    hOut = torch.empty_like(hC0).pin_memory()
+    use_c = w.beta != 0
+    h2d = 4 * (w.M * w.K + w.K * w.N + (w.M * w.N if use_c else 0))
+    d2h = 4 * w.M * w.N
+
+    def e2e_step():
+        dA.copy_(hA, non_blocking=True)
+        dB.copy_(hB, non_blocking=True)
+        if use_c:
+            dC.copy_(hC0, non_blocking=True)
+        sg.sgemm_tensors(w.alpha, dA, dB, w.beta, dC, stream=stream)
+        hOut.copy_(dC, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    sg.check_status()
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    mp = measured_peaks()
+    sm_max = float(mp.get("sm_max_mhz") or 2070.0)
+    datasheet = props.multi_processor_count * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e9
+    achieved = flops / (kernel_ms * 1e-3) / 1e12
+    traffic, traffic_note = recorded_traffic(kernel, w.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": config_of(w, kernel, grid),
+        "frac_of_measured_fp32_ceiling": value / world / peak["gflops"],
+        "frac_of_datasheet_fp32": value / world / datasheet,
+        "fp32_ceiling": {"measured_gflops": peak["gflops"], "ms": peak["ms"],
+                         "clocks": peak_clocks, "datasheet_gflops": datasheet,
+                         "datasheet_basis": f"{props.multi_processor_count} SMs x 128 FP32 lanes "
+                                            f"x 2 FLOP x {sm_max:.0f} MHz"},
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": datasheet / 1e3,
+                     "unit": "TFLOP/s", "frac": achieved / (datasheet / 1e3),
+                     "peak_basis": "FP32 CUDA-core FFMA: SMs x 128 x 2 x max SM clock",
+                     "measured_ceiling": peak["gflops"] / 1e3,
+                     "frac_of_measured_ceiling": achieved / (peak["gflops"] / 1e3),
+                     "kernel": kernel, "kernel_ms": kernel_ms,
+                     "traffic": traffic, "traffic_note": traffic_note},
+        "clocks": clocks,
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e9, "unit": "GFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps * (2 if flush is not None else 1),
+        "gpu_launches_note": "one sgemm kernel per step" + (
+            " plus one L2-flush fill" if flush is not None else ""),
+    }
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, A, B, C0, args.cpu_rows)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    from dense_fp32_matrix_strict_gb300 import inputs
+    if args.workload not in inputs.WORKLOADS:
+        raise SystemExit(f"unknown workload {args.workload}; one of {list(inputs.WORKLOADS)}")
+    w = inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,15 @@
+"""dense_fp32_matrix_strict_gb300 — strict-FP32 SGEMM for GB300 (sm_103a).
+
+C = alpha * A @ B + beta * C on row-major float32 matrices, computed by
+hand-written FFMA kernels behind the C ABI in ``include/sgemm.h``. This
+package is the thin Python binding over that library (``_binding``), its
+build step (``build``) and the seeded synthetic inputs used to test and
+measure it (``inputs``). PyTorch serves only for device memory and streams.
+"""
+from ._binding import (  # noqa: F401
+    EXPORTED_SYMBOLS, SGEMM_ERR_CUDA, SGEMM_ERR_DEVICE_TIMEOUT, SGEMM_ERR_INVALID_VALUE,
+    SGEMM_ERR_LAUNCH, SGEMM_ERR_UNSUPPORTED_DEVICE, SGEMM_OK, SgemmError, check_status,
+    fp32_peak, library_path, load, plan_tensors, sgemm, sgemm_check_status, sgemm_error_string,
+    sgemm_fp32_peak, sgemm_last_cuda_error, sgemm_plan, sgemm_selftest_wait_timeout,
+    sgemm_set_config, sgemm_set_wait_timeout_ns, sgemm_tensors,
+)

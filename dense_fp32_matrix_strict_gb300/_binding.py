@@ -1,0 +1,220 @@
+"""ctypes binding of ``libsgemm_gb300.so`` — argument marshalling only.
+
+Each function here has the name and argument order of the C entry point in
+``include/sgemm.h``. All arithmetic happens in the CUDA kernels; there is no
+CPU path. If the shared library has not been built, every call raises
+``RuntimeError`` (build it with ``dense_fp32_matrix_strict_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+SGEMM_OK = 0
+SGEMM_ERR_INVALID_VALUE = 1
+SGEMM_ERR_UNSUPPORTED_DEVICE = 2
+SGEMM_ERR_LAUNCH = 3
+SGEMM_ERR_DEVICE_TIMEOUT = 4
+SGEMM_ERR_CUDA = 5
+
+# Every function include/sgemm.h declares.
+EXPORTED_SYMBOLS = (
+    "sgemm", "sgemm_check_status", "sgemm_error_string", "sgemm_last_cuda_error",
+    "sgemm_plan", "sgemm_set_config", "sgemm_set_wait_timeout_ns", "sgemm_fp32_peak",
+    "sgemm_selftest_wait_timeout",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SgemmError(RuntimeError):
+    """A non-zero return code from the library."""
+
+    def __init__(self, func: str, code: int):
+        self.code = int(code)
+        msg = _lib.sgemm_error_string(code).decode() if _lib is not None else str(code)
+        cuda = _lib.sgemm_last_cuda_error() if _lib is not None else 0
+        extra = f" (CUDA error {cuda})" if cuda and code in (SGEMM_ERR_LAUNCH, SGEMM_ERR_CUDA) else ""
+        super().__init__(f"{func} failed: {msg} [code {code}]{extra}")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load():
+    """Load the shared library (once). Raises RuntimeError if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: the CUDA library has not been built "
+                "(run `python -m dense_fp32_matrix_strict_gb300.build`); there is no CPU path")
+        lib = ctypes.CDLL(path)
+        i64, f32, vp, ci, f64p = (ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_int,
+                                  ctypes.POINTER(ctypes.c_double))
+        lib.sgemm.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
+        lib.sgemm.restype = ci
+        lib.sgemm_check_status.argtypes = [vp, ctypes.POINTER(ci)]
+        lib.sgemm_check_status.restype = ci
+        lib.sgemm_error_string.argtypes = [ci]
+        lib.sgemm_error_string.restype = ctypes.c_char_p
+        lib.sgemm_last_cuda_error.argtypes = []
+        lib.sgemm_last_cuda_error.restype = ci
+        lib.sgemm_plan.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64,
+                                   ctypes.c_char_p, ci, ctypes.POINTER(ci)]
+        lib.sgemm_plan.restype = ci
+        lib.sgemm_set_config.argtypes = [ctypes.c_char_p]
+        lib.sgemm_set_config.restype = ci
+        lib.sgemm_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+        lib.sgemm_set_wait_timeout_ns.restype = ci
+        lib.sgemm_fp32_peak.argtypes = [ctypes.c_double, f64p, f64p, f64p, vp]
+        lib.sgemm_fp32_peak.restype = ci
+        lib.sgemm_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+        lib.sgemm_selftest_wait_timeout.restype = ci
+        _lib = lib
+        return lib
+
+
+def _check(func: str, rc: int) -> int:
+    if rc != SGEMM_OK:
+        raise SgemmError(func, rc)
+    return rc
+
+
+# ---- raw entry points (same names and argument order as the C ABI) --------
+
+def sgemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
+    """C = alpha*A*B + beta*C on device pointers (ints); returns the raw code."""
+    return load().sgemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def sgemm_check_status(stream=0):
+    """Returns (code, bits)."""
+    bits = ctypes.c_int(0)
+    rc = load().sgemm_check_status(stream, ctypes.byref(bits))
+    return rc, bits.value
+
+
+def sgemm_error_string(code: int) -> str:
+    return load().sgemm_error_string(code).decode()
+
+
+def sgemm_last_cuda_error() -> int:
+    return load().sgemm_last_cuda_error()
+
+
+def sgemm_plan(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc):
+    """Returns (code, kernel name, grid)."""
+    buf = ctypes.create_string_buffer(128)
+    grid = ctypes.c_int(0)
+    rc = load().sgemm_plan(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, buf, 128,
+                           ctypes.byref(grid))
+    return rc, buf.value.decode(), grid.value
+
+
+def sgemm_set_config(name: str) -> int:
+    return load().sgemm_set_config(name.encode())
+
+
+def sgemm_set_wait_timeout_ns(ns: int) -> int:
+    return load().sgemm_set_wait_timeout_ns(int(ns))
+
+
+def sgemm_fp32_peak(target_ms: float = 200.0, stream=0):
+    """Returns (code, gflops, ms, flops)."""
+    g, m, f = ctypes.c_double(0), ctypes.c_double(0), ctypes.c_double(0)
+    rc = load().sgemm_fp32_peak(float(target_ms), ctypes.byref(g), ctypes.byref(m),
+                                ctypes.byref(f), stream)
+    return rc, g.value, m.value, f.value
+
+
+def sgemm_selftest_wait_timeout(timeout_ns: int, stream=0) -> int:
+    return load().sgemm_selftest_wait_timeout(int(timeout_ns), stream)
+
+
+# ---- torch tensor convenience (marshalling only) --------------------------
+
+def _ld(t, rows, cols, name):
+    import torch
+    if t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32, got {t.dtype}")
+    if not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dim() != 2 or tuple(t.shape) != (rows, cols):
+        raise ValueError(f"{name} must have shape {(rows, cols)}, got {tuple(t.shape)}")
+    if rows == 0 or cols == 0:
+        return max(cols, 1)
+    if cols > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} must be row-major with contiguous columns")
+    return max(t.stride(0) if rows > 1 else cols, cols, 1)
+
+
+def _stream_handle(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def sgemm_tensors(alpha, A, B, beta, C, stream=None) -> None:
+    """C = alpha * A @ B + beta * C in place on row-major float32 CUDA tensors.
+
+    Rows may be strided (leading dimension = stride(0)). Launches on
+    ``stream`` (default: torch's current stream on C's device). Raises
+    SgemmError on a non-zero return code.
+    """
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError(f"inner dimensions differ: A is {tuple(A.shape)}, B is {tuple(B.shape)}")
+    lda = _ld(A, M, K, "A")
+    ldb = _ld(B, K, N, "B")
+    ldc = _ld(C, M, N, "C")
+    if not (A.device == B.device == C.device):
+        raise ValueError("A, B and C must be on the same device")
+    import torch
+    with torch.cuda.device(C.device):
+        rc = sgemm(M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(), ldb, float(beta),
+                   C.data_ptr(), ldc, _stream_handle(stream, C.device))
+    _check("sgemm", rc)
+
+
+def plan_tensors(alpha, A, B, beta, C):
+    """Kernel name and grid sgemm_tensors would use for these tensors."""
+    M, K = A.shape
+    N = B.shape[1]
+    import torch
+    with torch.cuda.device(C.device):
+        rc, name, grid = sgemm_plan(M, N, K, float(alpha), A.data_ptr(), _ld(A, M, K, "A"),
+                                    B.data_ptr(), _ld(B, K, N, "B"), float(beta), C.data_ptr(),
+                                    _ld(C, M, N, "C"))
+    _check("sgemm_plan", rc)
+    return name, grid
+
+
+def check_status(stream=None, device=None) -> int:
+    """Synchronise and read/clear the device status word; raise on a time-out."""
+    import torch
+    dev = device if device is not None else torch.cuda.current_device()
+    with torch.cuda.device(dev):
+        rc, bits = sgemm_check_status(_stream_handle(stream, dev))
+    _check("sgemm_check_status", rc)
+    return bits
+
+
+def fp32_peak(target_ms: float = 200.0, stream=None, device=None):
+    """Measured FP32 FFMA ceiling: dict(gflops, ms, flops)."""
+    import torch
+    dev = device if device is not None else torch.cuda.current_device()
+    with torch.cuda.device(dev):
+        rc, g, m, f = sgemm_fp32_peak(target_ms, _stream_handle(stream, dev))
+    _check("sgemm_fp32_peak", rc)
+    return {"gflops": g, "ms": m, "flops": f}

@@ -1,0 +1,102 @@
+// fp32_peak.cu — pure-FFMA microbenchmark: the device's measured FP32 ceiling.
+//
+// The Tinyforge README measures its card's real FP32 rate with a pure-FMA
+// kernel (6,884 GFLOPS against a 9,100 GFLOPS datasheet figure) and quotes
+// every GEMM result as a fraction of that. This is the same measurement for
+// sm_103a: every thread keeps kChains independent FFMA dependency chains so
+// that each SM sub-partition can issue one FFMA per clock; the loop body is
+// kUnroll x kChains FFMAs against two loop-control instructions. The result
+// is stored only under a condition the host never makes true, so the chains
+// stay live without memory traffic.
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "sgemm.h"
+
+int sgemm_internal_device_ready();
+int sgemm_internal_sm_count();
+void sgemm_internal_set_cuda_error(int e);
+
+namespace {
+
+constexpr int kChains = 8;
+constexpr int kUnroll = 32;
+constexpr int kThreads = 256;
+constexpr int kCtasPerSm = 8;
+
+__device__ float g_peak_sink[kThreads];
+
+__global__ void __launch_bounds__(kThreads)
+fp32_peak_kernel(float mul, float add, long long iters, int sink_key) {
+    float x[kChains];
+#pragma unroll
+    for (int c = 0; c < kChains; ++c) x[c] = 1.0f + 1e-3f * static_cast<float>(threadIdx.x + c);
+    for (long long it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+            for (int c = 0; c < kChains; ++c) x[c] = fmaf(x[c], mul, add);
+    }
+    float s = 0.0f;
+#pragma unroll
+    for (int c = 0; c < kChains; ++c) s += x[c];
+    if (static_cast<int>(blockIdx.x) == sink_key) g_peak_sink[threadIdx.x] = s;
+}
+
+}  // namespace
+
+extern "C" int sgemm_fp32_peak(double target_ms, double* gflops, double* ms, double* flops,
+                               cudaStream_t stream) {
+    if (!(target_ms >= 1.0) || target_ms > 60000.0) return SGEMM_ERR_INVALID_VALUE;
+    int rc = sgemm_internal_device_ready();
+    if (rc != SGEMM_OK) return rc;
+    const int sms = sgemm_internal_sm_count();
+    const int grid = sms * kCtasPerSm;
+    // mul slightly below 1 and a small add keep the chains bounded and finite.
+    const float mul = 0.999999f, add = 1e-6f;
+    const int no_sink = -1;   // blockIdx.x is never -1: the store never happens
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    cudaError_t e;
+    if ((e = cudaEventCreate(&e0)) != cudaSuccess || (e = cudaEventCreate(&e1)) != cudaSuccess) {
+        if (e0) cudaEventDestroy(e0);
+        sgemm_internal_set_cuda_error(static_cast<int>(e));
+        return SGEMM_ERR_CUDA;
+    }
+    auto run = [&](long long iters, float* out_ms) -> cudaError_t {
+        cudaError_t err = cudaEventRecord(e0, stream);
+        if (err != cudaSuccess) return err;
+        fp32_peak_kernel<<<grid, kThreads, 0, stream>>>(mul, add, iters, no_sink);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        if ((err = cudaEventRecord(e1, stream)) != cudaSuccess) return err;
+        if ((err = cudaEventSynchronize(e1)) != cudaSuccess) return err;
+        return cudaEventElapsedTime(out_ms, e0, e1);
+    };
+    float t = 0.0f;
+    long long iters = 256;
+    int result = SGEMM_OK;
+    // Calibrate: grow until a launch takes >= 5 ms, then scale to the target.
+    for (;;) {
+        if ((e = run(iters, &t)) != cudaSuccess) { result = SGEMM_ERR_LAUNCH; break; }
+        if (t >= 5.0f || iters > (1ll << 40)) break;
+        iters *= 4;
+    }
+    if (result == SGEMM_OK) {
+        long long want = static_cast<long long>(static_cast<double>(iters) * target_ms / t);
+        if (want < 1) want = 1;
+        // Warm-up of the same length (clocks settle under the load), then time.
+        if ((e = run(want, &t)) != cudaSuccess || (e = run(want, &t)) != cudaSuccess) {
+            result = SGEMM_ERR_LAUNCH;
+        } else {
+            const double f = 2.0 * kChains * kUnroll * static_cast<double>(want) *
+                             static_cast<double>(grid) * kThreads;
+            if (gflops) *gflops = f / (static_cast<double>(t) * 1e-3) / 1e9;
+            if (ms) *ms = t;
+            if (flops) *flops = f;
+        }
+    }
+    if (result != SGEMM_OK) sgemm_internal_set_cuda_error(static_cast<int>(e));
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    return result;
+}

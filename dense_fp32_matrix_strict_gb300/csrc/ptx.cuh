@@ -1,0 +1,97 @@
+// ptx.cuh — thin inline-PTX wrappers for sm_103a: mbarrier, TMA tile loads,
+// element-wise cp.async, timers.
+//
+// Every wait built on these is bounded by the caller (see sgemm_kernel.cuh):
+// nothing here spins.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace sg {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- mbarrier --------------------------------------------------------------
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+
+// Make barrier initialisation visible to the async proxy (TMA) and to the
+// other threads of the CTA (followed by a __syncthreads at the call site).
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("{\n\t.reg .b64 st;\n\t"
+                 "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}"
+                 :: "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("{\n\t.reg .b64 st;\n\t"
+                 "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
+                 :: "r"(bar), "r"(bytes) : "memory");
+}
+
+// True once the phase with the given parity has completed. Never blocks for
+// long: the hardware may suspend the thread for a bounded, system-defined
+// time before returning false.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// ---- TMA (cp.async.bulk.tensor) --------------------------------------------
+
+__device__ __forceinline__ void tma_prefetch_desc(const void* desc) {
+    asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(desc)) : "memory");
+}
+
+// 2-D tile load: box at (x = inner coordinate, y = outer coordinate) into
+// shared memory at dst; completion is signalled as transaction bytes on bar.
+// The caller guarantees x * 4 bytes is a multiple of 16 (x is a multiple of
+// the tile width, itself a multiple of 4 floats).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* desc, uint32_t bar,
+                                            int32_t x, int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+// ---- element-wise cp.async (4 bytes, zero-fill) ----------------------------
+
+// Copies 4 bytes from src to shared dst; when !valid no byte is read and the
+// destination is zero-filled (src-size 0). src must still be a valid address.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const float* src, bool valid) {
+    const uint32_t n = valid ? 4u : 0u;
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;"
+                 :: "r"(dst), "l"(src), "r"(n) : "memory");
+}
+
+// Arrive on bar once every cp.async this thread issued so far has landed.
+// .noinc: the arrival is counted in the barrier's expected count.
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
+}
+
+// ---- timers ----------------------------------------------------------------
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+}  // namespace sg

@@ -1,0 +1,414 @@
+// sgemm_api.cu — the C ABI: argument checks, per-device set-up, kernel plan
+// (CTA tile, TMA or cp.async per operand, persistent grid), TMA descriptor
+// encoding, and launches on the caller's stream.
+#include <atomic>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "sgemm.h"
+#include "kernels.h"
+
+namespace sg {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kNumTiles = 2;      // 0: 128x128, 1: 64x64
+constexpr int kStatusBytes = 256;
+
+struct DeviceState {
+    bool ready = false;
+    int error = SGEMM_OK;
+    int sm_count = 0;
+    int* status = nullptr;                 // device status word (256 bytes)
+    int ctas_per_sm[kNumTiles][4] = {};
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+bool g_env_read = false;
+
+// Forced configuration: tile 0 = auto, 128 or 64; cp = force cp.async loads.
+std::atomic<int> g_force_tile{0};
+std::atomic<int> g_force_cp{0};
+std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+
+thread_local int t_last_cuda_error = 0;
+
+const KernelEntry* table_for(int tile) {
+    return tile == 0 ? ws_kernels_128x128() : ws_kernels_64x64();
+}
+
+int parse_config(const char* name, int* tile, int* cp) {
+    if (name == nullptr) return SGEMM_ERR_INVALID_VALUE;
+    char buf[64];
+    std::strncpy(buf, name, sizeof(buf) - 1);
+    buf[sizeof(buf) - 1] = '\0';
+    int want_cp = 0;
+    char* colon = std::strchr(buf, ':');
+    if (colon != nullptr) {
+        if (std::strcmp(colon + 1, "cpasync") != 0) return SGEMM_ERR_INVALID_VALUE;
+        want_cp = 1;
+        *colon = '\0';
+    }
+    int t;
+    if (std::strcmp(buf, "auto") == 0 || buf[0] == '\0') t = 0;
+    else if (std::strcmp(buf, "128x128") == 0) t = 128;
+    else if (std::strcmp(buf, "64x64") == 0) t = 64;
+    else return SGEMM_ERR_INVALID_VALUE;
+    *tile = t;
+    *cp = want_cp;
+    return SGEMM_OK;
+}
+
+int cuda_fail(cudaError_t e, int code) {
+    t_last_cuda_error = static_cast<int>(e);
+    return code;
+}
+
+// Per-device set-up, once per device (under the lock): properties, status
+// word, kernel attributes and occupancy, TMA encoder entry point.
+int device_setup(DeviceState** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_CUDA);
+    if (dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_env_read) {
+        g_env_read = true;
+        const char* env = std::getenv("SGEMM_FORCE_CONFIG");
+        int tile = 0, cp = 0;
+        if (env != nullptr && parse_config(env, &tile, &cp) == SGEMM_OK) {
+            g_force_tile = tile;
+            g_force_cp = cp;
+        }
+    }
+    DeviceState& st = g_dev[dev];
+    if (st.ready) {
+        *out = &st;
+        return SGEMM_OK;
+    }
+    if (st.error != SGEMM_OK) return st.error;
+    int major = 0, minor = 0, sms = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return cuda_fail(e, SGEMM_ERR_CUDA);
+    if (major != 10 || minor != 3) {
+        st.error = SGEMM_ERR_UNSUPPORTED_DEVICE;
+        return st.error;
+    }
+    if (g_encode == nullptr) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return cuda_fail(e == cudaSuccess ? cudaErrorNotSupported : e, SGEMM_ERR_CUDA);
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    for (int t = 0; t < kNumTiles; ++t) {
+        const KernelEntry* tab = table_for(t);
+        for (int m = 0; m < 4; ++m) {
+            int n = 0;
+            e = tab[m].prepare(&n);
+            if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_CUDA);
+            st.ctas_per_sm[t][m] = n > 0 ? n : 1;
+        }
+    }
+    void* status = nullptr;
+    if ((e = cudaMalloc(&status, kStatusBytes)) != cudaSuccess) return cuda_fail(e, SGEMM_ERR_CUDA);
+    if ((e = cudaMemset(status, 0, kStatusBytes)) != cudaSuccess) {
+        cudaFree(status);
+        return cuda_fail(e, SGEMM_ERR_CUDA);
+    }
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess) {
+        cudaFree(status);
+        return cuda_fail(e, SGEMM_ERR_CUDA);
+    }
+    st.status = static_cast<int*>(status);
+    st.sm_count = sms;
+    st.ready = true;
+    *out = &st;
+    return SGEMM_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// [lo, hi) byte range of a rows x cols matrix with leading dimension ld.
+void extent(const void* p, int64_t rows, int64_t cols, int64_t ld, uintptr_t* lo, uintptr_t* hi) {
+    *lo = reinterpret_cast<uintptr_t>(p);
+    *hi = *lo + static_cast<uintptr_t>(((rows - 1) * ld + cols) * 4);
+}
+
+int check_args(int64_t M, int64_t N, int64_t K, float alpha, const float* A, int64_t lda,
+               const float* B, int64_t ldb, const float* C, int64_t ldc) {
+    const int64_t kMax = 0x7fffffff;
+    if (M < 0 || N < 0 || K < 0 || M > kMax || N > kMax || K > kMax) return SGEMM_ERR_INVALID_VALUE;
+    if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
+        return SGEMM_ERR_INVALID_VALUE;
+    // Offsets up to rows * ld must fit comfortably in int64 bytes.
+    const int64_t kOff = (int64_t)1 << 60;
+    if ((M > 0 && lda > kOff / M) || (K > 0 && ldb > kOff / K) || (M > 0 && ldc > kOff / M))
+        return SGEMM_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    if (C == nullptr || !aligned(C, 4)) return SGEMM_ERR_INVALID_VALUE;
+    const bool reads_ab = (alpha != 0.0f) && (K > 0);
+    if (reads_ab) {
+        if (A == nullptr || B == nullptr || !aligned(A, 4) || !aligned(B, 4))
+            return SGEMM_ERR_INVALID_VALUE;
+        uintptr_t clo, chi, lo, hi;
+        extent(C, M, N, ldc, &clo, &chi);
+        extent(A, M, K, lda, &lo, &hi);
+        if (lo < chi && clo < hi) return SGEMM_ERR_INVALID_VALUE;
+        extent(B, K, N, ldb, &lo, &hi);
+        if (lo < chi && clo < hi) return SGEMM_ERR_INVALID_VALUE;
+    }
+    return SGEMM_OK;
+}
+
+// 2-D row-major fp32 tensor map: rows x cols, row stride ld floats, box of
+// box_rows x box_cols, optional 128-byte swizzle. Returns false if the
+// driver rejects it.
+bool encode_2d(CUtensorMap* map, const float* base, int64_t rows, int64_t cols, int64_t ld,
+               int box_rows, int box_cols, bool swizzle128) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool tma_ok(const float* p, int64_t ld, int64_t rows, int64_t cols) {
+    return aligned(p, 16) && (ld % 4) == 0 && ld < ((int64_t)1 << 38) && rows >= 1 && cols >= 1 &&
+           rows <= 0xffffffffll && cols <= 0xffffffffll;
+}
+
+struct Plan {
+    int kind = 0;                 // 0: none, 1: scale, 2: gemm
+    const KernelEntry* k = nullptr;
+    CUtensorMap tmA, tmB;
+    GemmParams p;
+    int grid = 0;
+};
+
+int make_plan(DeviceState* st, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+              int64_t lda, const float* B, int64_t ldb, float beta, const float* C, int64_t ldc,
+              Plan* pl) {
+    if (M == 0 || N == 0) {
+        pl->kind = 0;
+        return SGEMM_OK;
+    }
+    if (alpha == 0.0f || K == 0) {
+        pl->kind = 1;
+        return SGEMM_OK;
+    }
+    pl->kind = 2;
+    const int sms = st->sm_count;
+    int tile = g_force_tile.load();
+    if (tile == 0) {
+        const int64_t tiles128 = ((M + 127) / 128) * ((N + 127) / 128);
+        tile = (tiles128 * 2 >= sms) ? 128 : 64;
+    }
+    const int ti = tile == 128 ? 0 : 1;
+    const int bm = tile, bn = tile, bk = 32;
+    const bool force_cp = g_force_cp.load() != 0;
+    std::memset(&pl->tmA, 0, sizeof(CUtensorMap));
+    std::memset(&pl->tmB, 0, sizeof(CUtensorMap));
+    int a_mode = LOAD_CPASYNC, b_mode = LOAD_CPASYNC;
+    if (!force_cp && tma_ok(A, lda, M, K) && encode_2d(&pl->tmA, A, M, K, lda, bm, bk, true))
+        a_mode = LOAD_TMA;
+    if (!force_cp && tma_ok(B, ldb, K, N) && encode_2d(&pl->tmB, B, K, N, ldb, bk, bn, false))
+        b_mode = LOAD_TMA;
+    const int mi = mode_index(a_mode, b_mode);
+    pl->k = &table_for(ti)[mi];
+
+    GemmParams& p = pl->p;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.tiles_m = static_cast<int>((M + bm - 1) / bm);
+    p.tiles_n = static_cast<int>((N + bn - 1) / bn);
+    p.k_tiles = static_cast<int>((K + bk - 1) / bk);
+    p.group_m = 8;
+    p.c_vec = (aligned(C, 16) && (ldc % 4) == 0) ? 1 : 0;
+    p.A = A;
+    p.B = B;
+    p.C = const_cast<float*>(C);
+    p.lda = lda;
+    p.ldb = ldb;
+    p.ldc = ldc;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.timeout_ns = g_timeout_ns.load();
+    p.status = st->status;
+    const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+    if (tiles > 0x7fffffffll) return SGEMM_ERR_INVALID_VALUE;
+    const int64_t slots = static_cast<int64_t>(st->ctas_per_sm[ti][mi]) * sms;
+    pl->grid = static_cast<int>(tiles < slots ? tiles : slots);
+    return SGEMM_OK;
+}
+
+// C = beta * C over an M x N matrix (beta == 0 writes zeros, never reads C).
+__global__ void scale_kernel(float* __restrict__ C, long long ldc, int M, int N, float beta) {
+    for (long long m = blockIdx.y; m < M; m += gridDim.y) {
+        float* row = C + m * ldc;
+        for (int n = blockIdx.x * blockDim.x + threadIdx.x; n < N; n += blockDim.x * gridDim.x)
+            row[n] = (beta == 0.0f) ? 0.0f : beta * row[n];
+    }
+}
+
+__global__ void wait_timeout_kernel(GemmParams p) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) wait_bounded(b, 0, p, STATUS_CONSUMER_TIMEOUT);
+}
+
+}  // namespace
+}  // namespace sg
+
+using namespace sg;
+
+extern "C" int sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float* A, int64_t lda,
+                     const float* B, int64_t ldb, float beta, float* C, int64_t ldc,
+                     cudaStream_t stream) {
+    int rc = check_args(M, N, K, alpha, A, lda, B, ldb, C, ldc);
+    if (rc != SGEMM_OK) return rc;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    DeviceState* st = nullptr;
+    if ((rc = device_setup(&st)) != SGEMM_OK) return rc;
+    Plan pl;
+    if ((rc = make_plan(st, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, &pl)) != SGEMM_OK)
+        return rc;
+    cudaError_t e;
+    if (pl.kind == 1) {
+        const int bx = static_cast<int>(N < 256 * 16 ? (N + 255) / 256 : 16);
+        const int by = static_cast<int>(M < 4096 ? M : 4096);
+        scale_kernel<<<dim3(bx, by), 256, 0, stream>>>(C, ldc, static_cast<int>(M),
+                                                       static_cast<int>(N), beta);
+        e = cudaGetLastError();
+    } else {
+        e = pl.k->launch(&pl.tmA, &pl.tmB, &pl.p, pl.grid, stream);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
+    return SGEMM_OK;
+}
+
+extern "C" int sgemm_plan(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                          int64_t lda, const float* B, int64_t ldb, float beta, const float* C,
+                          int64_t ldc, char* buf, int buflen, int* grid) {
+    int rc = check_args(M, N, K, alpha, A, lda, B, ldb, C, ldc);
+    if (rc != SGEMM_OK) return rc;
+    const char* name = "none";
+    int g = 0;
+    Plan pl;
+    if (M != 0 && N != 0) {
+        DeviceState* st = nullptr;
+        if ((rc = device_setup(&st)) != SGEMM_OK) return rc;
+        if ((rc = make_plan(st, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, &pl)) != SGEMM_OK)
+            return rc;
+        if (pl.kind == 1) name = "scale";
+        if (pl.kind == 2) {
+            name = pl.k->name;
+            g = pl.grid;
+        }
+    }
+    if (buf != nullptr && buflen > 0) {
+        std::strncpy(buf, name, static_cast<size_t>(buflen) - 1);
+        buf[buflen - 1] = '\0';
+    }
+    if (grid != nullptr) *grid = g;
+    return SGEMM_OK;
+}
+
+extern "C" int sgemm_check_status(cudaStream_t stream, int* bits) {
+    DeviceState* st = nullptr;
+    int rc = device_setup(&st);
+    if (rc != SGEMM_OK) return rc;
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_CUDA);
+    int v = 0;
+    if ((e = cudaMemcpyAsync(&v, st->status, sizeof(int), cudaMemcpyDeviceToHost, stream)) != cudaSuccess ||
+        (e = cudaMemsetAsync(st->status, 0, sizeof(int), stream)) != cudaSuccess ||
+        (e = cudaStreamSynchronize(stream)) != cudaSuccess)
+        return cuda_fail(e, SGEMM_ERR_CUDA);
+    if (bits != nullptr) *bits = v;
+    return v != 0 ? SGEMM_ERR_DEVICE_TIMEOUT : SGEMM_OK;
+}
+
+extern "C" const char* sgemm_error_string(int code) {
+    switch (code) {
+        case SGEMM_OK: return "success";
+        case SGEMM_ERR_INVALID_VALUE: return "invalid argument";
+        case SGEMM_ERR_UNSUPPORTED_DEVICE: return "unsupported device (need compute capability 10.3)";
+        case SGEMM_ERR_LAUNCH: return "kernel launch failed";
+        case SGEMM_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel timed out";
+        case SGEMM_ERR_CUDA: return "CUDA runtime error";
+        default: return "unknown error code";
+    }
+}
+
+extern "C" int sgemm_last_cuda_error(void) { return t_last_cuda_error; }
+
+extern "C" int sgemm_set_config(const char* name) {
+    int tile = 0, cp = 0;
+    int rc = parse_config(name, &tile, &cp);
+    if (rc != SGEMM_OK) return rc;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        g_env_read = true;   // an explicit choice overrides the environment
+    }
+    g_force_tile = tile;
+    g_force_cp = cp;
+    return SGEMM_OK;
+}
+
+extern "C" int sgemm_set_wait_timeout_ns(uint64_t ns) {
+    if (ns < 1000) return SGEMM_ERR_INVALID_VALUE;
+    g_timeout_ns = ns;
+    return SGEMM_OK;
+}
+
+extern "C" int sgemm_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stream) {
+    if (timeout_ns < 1000 || timeout_ns > 10000000000ull) return SGEMM_ERR_INVALID_VALUE;
+    DeviceState* st = nullptr;
+    int rc = device_setup(&st);
+    if (rc != SGEMM_OK) return rc;
+    GemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.timeout_ns = timeout_ns;
+    p.status = st->status;
+    wait_timeout_kernel<<<1, 32, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
+    return SGEMM_OK;
+}
+
+// Shared with fp32_peak.cu: per-device readiness check without the lock
+// dance duplicated there.
+int sgemm_internal_device_ready() {
+    DeviceState* st = nullptr;
+    return device_setup(&st);
+}
+int sgemm_internal_sm_count() {
+    DeviceState* st = nullptr;
+    if (device_setup(&st) != SGEMM_OK) return 0;
+    return st->sm_count;
+}
+void sgemm_internal_set_cuda_error(int e) { t_last_cuda_error = e; }

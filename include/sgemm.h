@@ -1,0 +1,165 @@
+/*
+ * sgemm.h — C ABI of the GB300 (sm_103a) strict-FP32 SGEMM library
+ * (libsgemm_gb300.so).
+ *
+ * The operation is the one every page on hand-written FP32 SGEMM defines
+ * ("Optimizing SGEMM in CUDA", section "What is a SGEMM?"; "The road to a
+ * fast GEMM", section "The problem and the ceiling"):
+ *
+ *     C[i][j] = alpha * sum_{k<K} A[i][k] * B[k][j] + beta * C[i][j]
+ *
+ * with row-major A (M x K), B (K x N) and C (M x N). The argument order
+ * follows those pages' kernels, (M, N, K, alpha, A, B, beta, C), with the
+ * leading dimensions cuBLAS-style calls pass beside each matrix ("Optimizing
+ * SGEMM in CUDA", section "cuBLAS implementation").
+ *
+ * Strictness: every product is accumulated by single-rounding FP32 FMAs on
+ * the CUDA cores. No TF32, no reduced precision, no fast-math. Summation
+ * order is not fixed, so results are not bit-identical to a sequential loop
+ * on real-valued inputs; on integer-valued inputs whose partial sums stay
+ * below 2^24 they are exact.
+ *
+ * All pointers are DEVICE pointers on the current CUDA device, owned by the
+ * caller. The library keeps only per-device set-up state (created on the
+ * first call on a device: device properties, a 256-byte device status word,
+ * kernel attributes) and allocates nothing per call.
+ */
+#ifndef SGEMM_GB300_H
+#define SGEMM_GB300_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define SGEMM_API __attribute__((visibility("default")))
+#else
+#define SGEMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define SGEMM_OK 0
+#define SGEMM_ERR_INVALID_VALUE 1      /* an argument violates the contract below      */
+#define SGEMM_ERR_UNSUPPORTED_DEVICE 2 /* current device is not compute capability 10.3 */
+#define SGEMM_ERR_LAUNCH 3             /* a kernel launch failed; see sgemm_last_cuda_error */
+#define SGEMM_ERR_DEVICE_TIMEOUT 4     /* a bounded wait inside a kernel gave up          */
+#define SGEMM_ERR_CUDA 5               /* another CUDA runtime call failed               */
+
+/*
+ * sgemm — C = alpha * A * B + beta * C (row-major, FP32).
+ *
+ *   M, N, K   problem size, each in [0, 2^31 - 1].
+ *   alpha     scale of the product.
+ *   A         M x K, element (i, k) at A[i * lda + k]; lda >= max(1, K).
+ *   B         K x N, element (k, j) at B[k * ldb + j]; ldb >= max(1, N).
+ *   beta      scale of the old C.
+ *   C         M x N, element (i, j) at C[i * ldc + j]; ldc >= max(1, N);
+ *             read (when beta != 0) and written in place.
+ *   stream    CUDA stream the work is enqueued on (0 = legacy default).
+ *
+ * Layout and alignment: any leading dimension and any 4-byte-aligned base
+ * pointer is accepted. Operands whose base is 16-byte aligned and whose
+ * leading dimension is a multiple of 4 are loaded by TMA; others by 4-byte
+ * cp.async. Elements between the end of a row and the next row (ld > width)
+ * are never read or written.
+ *
+ * Readings (BLAS conventions; the pages always evaluate beta * C):
+ *   - M == 0 or N == 0: nothing is done.
+ *   - beta == 0: C is not read (NaN/Inf in C do not propagate).
+ *   - alpha == 0 or K == 0: A and B are not read; C = beta * C (zeros if
+ *     beta == 0).
+ *
+ * Errors: returns SGEMM_ERR_INVALID_VALUE, without enqueuing anything, if
+ * M, N or K is negative or above 2^31 - 1; an ld is below its minimum or so
+ * large that an offset overflows; A or B is NULL while alpha != 0 and K > 0;
+ * C is NULL; a pointer is not 4-byte aligned; or the memory of A or B
+ * overlaps the memory of C. SGEMM_ERR_UNSUPPORTED_DEVICE if the current
+ * device is not sm_103. SGEMM_ERR_LAUNCH if the launch fails (the CUDA
+ * error code is kept for sgemm_last_cuda_error).
+ *
+ * The call is asynchronous: it returns once the kernel is enqueued. Device
+ * time-outs are reported later by sgemm_check_status. A, B and C must stay
+ * valid until the stream reaches the kernel.
+ */
+SGEMM_API int sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float* A, int64_t lda,
+          const float* B, int64_t ldb, float beta, float* C, int64_t ldc,
+          cudaStream_t stream);
+
+/*
+ * sgemm_check_status — synchronise `stream`, then read and clear the current
+ * device's status word. Returns SGEMM_OK, SGEMM_ERR_DEVICE_TIMEOUT if any
+ * kernel since the last check gave up on a bounded wait (its output is then
+ * incomplete), or SGEMM_ERR_CUDA if the synchronisation reported an error.
+ * If `bits` is not NULL it receives the raw status bits (1: a consumer
+ * timed out, 2: a producer timed out, 4: draining copies timed out).
+ */
+SGEMM_API int sgemm_check_status(cudaStream_t stream, int* bits);
+
+/* Human-readable text for a return code (static storage, never NULL). */
+SGEMM_API const char* sgemm_error_string(int code);
+
+/* The CUDA error code behind the last SGEMM_ERR_LAUNCH / SGEMM_ERR_CUDA
+ * returned on this thread (0 if none). */
+SGEMM_API int sgemm_last_cuda_error(void);
+
+/*
+ * sgemm_plan — describe, without launching, the kernel sgemm would use for
+ * these arguments: writes a NUL-terminated name such as
+ * "ws_128x128x32_s4_Atma_Btma" into buf (at most buflen bytes) and the
+ * launch grid into *grid (if not NULL). Returns the same argument errors as
+ * sgemm, or SGEMM_OK. A name of "scale" means the alpha == 0 / K == 0 path;
+ * "none" means M == 0 or N == 0.
+ */
+SGEMM_API int sgemm_plan(int64_t M, int64_t N, int64_t K, float alpha, const float* A, int64_t lda,
+               const float* B, int64_t ldb, float beta, const float* C, int64_t ldc,
+               char* buf, int buflen, int* grid);
+
+/*
+ * sgemm_set_config — force a kernel configuration for later calls in this
+ * process (for sweeps and tests). `name` is "auto" (default), "128x128" or
+ * "64x64" for the CTA tile, optionally followed by ":cpasync" to load both
+ * operands with cp.async even when TMA could be used (e.g.
+ * "128x128:cpasync", or "auto:cpasync"). Returns SGEMM_ERR_INVALID_VALUE
+ * for an unknown name. The environment variable SGEMM_FORCE_CONFIG, read on
+ * the first call, sets the same thing.
+ */
+SGEMM_API int sgemm_set_config(const char* name);
+
+/*
+ * sgemm_set_wait_timeout_ns — limit on every bounded mbarrier wait inside
+ * the kernels launched after this call (default 2e9 ns). Values below
+ * 1000 ns are rejected with SGEMM_ERR_INVALID_VALUE.
+ */
+SGEMM_API int sgemm_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * sgemm_fp32_peak — the pure-FFMA microbenchmark that measures the device's
+ * real FP32 ceiling, as the Tinyforge README's fp32_peak does (its measured
+ * 6,884 GFLOPS against a 9,100 GFLOPS datasheet figure). Every thread of a
+ * grid of 8 CTAs of 256 threads per SM runs 8 independent FFMA chains; the
+ * run is calibrated to last about target_ms (>= 1) and timed with CUDA
+ * events on `stream` after one untimed warm-up launch of the same length.
+ * Outputs (each may be NULL): *gflops = 2 * FMAs / time, *ms = time of
+ * the timed launch, *flops = floating-point operations of the timed launch.
+ * Blocking: synchronises `stream`.
+ */
+SGEMM_API int sgemm_fp32_peak(double target_ms, double* gflops, double* ms, double* flops,
+                    cudaStream_t stream);
+
+/*
+ * sgemm_selftest_wait_timeout — launch one CTA whose bounded mbarrier wait
+ * can never be satisfied (nothing arrives) with a limit of timeout_ns, to
+ * show that the time-out path returns instead of hanging. The kernel sets
+ * status bit 1 and exits; read it with sgemm_check_status. Returns launch
+ * errors like sgemm.
+ */
+SGEMM_API int sgemm_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGEMM_GB300_H */

@@ -1,0 +1,115 @@
+"""The C ABI on the CPU: the library loads, exports what include/sgemm.h
+declares, and rejects bad arguments before touching a GPU."""
+import os
+import re
+
+import pytest
+
+import dense_fp32_matrix_strict_gb300 as sg
+from dense_fp32_matrix_strict_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return sg.load()
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            with open(os.path.join(ROOT, "include", fn)) as f:
+                text = f.read()
+            names += re.findall(r"^SGEMM_API\s+[\w\s\*]+?\b(\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+def test_header_declares_the_binding_symbols():
+    assert sorted(declared_functions()) == sorted(sg.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_library_exports_nothing_else(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", sg.library_path()],
+                         capture_output=True, text=True, check=True).stdout
+    syms = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    assert syms == set(declared_functions())
+
+
+def test_error_strings(lib):
+    for code in range(6):
+        assert sg.sgemm_error_string(code)
+    assert sg.sgemm_error_string(99) == "unknown error code"
+
+
+# (M, N, K, alpha, A, lda, B, ldb, beta, C, ldc) that violate the contract.
+A_PTR, B_PTR, C_PTR = 1 << 20, 2 << 20, 3 << 20
+BAD_ARGS = [
+    (-1, 4, 4, 1.0, A_PTR, 4, B_PTR, 4, 0.0, C_PTR, 4),            # negative M
+    (4, -1, 4, 1.0, A_PTR, 4, B_PTR, 4, 0.0, C_PTR, 4),            # negative N
+    (4, 4, -1, 1.0, A_PTR, 4, B_PTR, 4, 0.0, C_PTR, 4),            # negative K
+    (1 << 31, 4, 4, 1.0, A_PTR, 4, B_PTR, 4, 0.0, C_PTR, 4),       # M too large
+    (4, 4, 8, 1.0, A_PTR, 7, B_PTR, 4, 0.0, C_PTR, 4),             # lda < K
+    (4, 8, 4, 1.0, A_PTR, 4, B_PTR, 7, 0.0, C_PTR, 8),             # ldb < N
+    (4, 8, 4, 1.0, A_PTR, 4, B_PTR, 8, 0.0, C_PTR, 7),             # ldc < N
+    (4, 4, 4, 1.0, 0, 4, B_PTR, 4, 0.0, C_PTR, 4),                 # A NULL
+    (4, 4, 4, 1.0, A_PTR, 4, 0, 4, 0.0, C_PTR, 4),                 # B NULL
+    (4, 4, 4, 1.0, A_PTR, 4, B_PTR, 4, 0.0, 0, 4),                 # C NULL
+    (4, 4, 4, 1.0, A_PTR + 2, 4, B_PTR, 4, 0.0, C_PTR, 4),         # A misaligned
+    (4, 4, 4, 1.0, A_PTR, 4, B_PTR, 4, 0.0, C_PTR + 1, 4),         # C misaligned
+    (4, 4, 4, 1.0, A_PTR, 4, B_PTR, 4, 0.0, A_PTR + 32, 4),        # C overlaps A
+    (4, 4, 4, 1.0, A_PTR, 4, C_PTR - 16, 4, 0.0, C_PTR, 4),        # C overlaps B
+    (4, 4, 4, 1.0, A_PTR, 1 << 62, B_PTR, 4, 0.0, C_PTR, 4),       # lda overflows offsets
+]
+
+
+@pytest.mark.parametrize("args", BAD_ARGS)
+def test_invalid_arguments_rejected_without_gpu(lib, args):
+    assert sg.sgemm(*args, 0) == sg.SGEMM_ERR_INVALID_VALUE
+    assert sg.sgemm_plan(*args)[0] == sg.SGEMM_ERR_INVALID_VALUE
+
+
+def test_empty_problem_is_a_no_op(lib):
+    assert sg.sgemm(0, 4, 4, 1.0, A_PTR, 4, B_PTR, 4, 0.0, C_PTR, 4, 0) == sg.SGEMM_OK
+    assert sg.sgemm(4, 0, 4, 1.0, A_PTR, 4, B_PTR, 1, 0.0, C_PTR, 1, 0) == sg.SGEMM_OK
+    assert sg.sgemm_plan(0, 4, 4, 1.0, A_PTR, 4, B_PTR, 4, 0.0, C_PTR, 4) == (0, "none", 0)
+
+
+def test_null_ab_allowed_when_not_read(lib):
+    # alpha == 0 or K == 0: A and B are not read, so NULL passes the checks
+    # (the call then needs a device; without one it reports a CUDA error).
+    rc = sg.sgemm(4, 4, 4, 0.0, 0, 4, 0, 4, 1.0, C_PTR, 4, 0)
+    assert rc != sg.SGEMM_ERR_INVALID_VALUE
+    rc = sg.sgemm(4, 4, 0, 1.0, 0, 1, 0, 4, 1.0, C_PTR, 4, 0)
+    assert rc != sg.SGEMM_ERR_INVALID_VALUE
+
+
+def test_config_names(lib):
+    for good in ["auto", "128x128", "64x64", "128x128:cpasync", "auto:cpasync"]:
+        assert sg.sgemm_set_config(good) == sg.SGEMM_OK
+    for bad in ["", "x", "256x256", "128x128:tma", "auto:"]:
+        if bad == "":
+            continue
+        assert sg.sgemm_set_config(bad) == sg.SGEMM_ERR_INVALID_VALUE
+    assert sg.sgemm_set_config("auto") == sg.SGEMM_OK
+
+
+def test_timeout_setting_bounds(lib):
+    assert sg.sgemm_set_wait_timeout_ns(10) == sg.SGEMM_ERR_INVALID_VALUE
+    assert sg.sgemm_set_wait_timeout_ns(2_000_000_000) == sg.SGEMM_OK
+    assert sg.sgemm_selftest_wait_timeout(10) == sg.SGEMM_ERR_INVALID_VALUE
+
+
+def test_tensor_wrapper_rejects_cpu_tensors(lib):
+    torch = pytest.importorskip("torch")
+    a = torch.zeros(4, 4)
+    with pytest.raises(TypeError):
+        sg.sgemm_tensors(1.0, a, a, 0.0, a.clone())

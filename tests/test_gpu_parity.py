@@ -1,0 +1,243 @@
+"""Parity of the CUDA path with the CPU oracle, through the C ABI.
+
+Real-valued inputs: every element within |C - ref| <= 4 K 2^-24 S + 1e-6
+(S = |alpha| sum_k |a_ik b_kj| + |beta c_ij|). Integer-valued inputs: bit-exact.
+Small shapes are checked on every element; the full workloads on every
+element where the oracle finishes in seconds, else on 65,536 seeded entries
+plus the whole last row and column.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import dense_fp32_matrix_strict_gb300 as sg
+from dense_fp32_matrix_strict_gb300 import inputs
+from tests import gpu_util
+
+pytestmark = pytest.mark.gpu
+
+CONFIGS = ["auto", "128x128", "64x64", "128x128:cpasync", "64x64:cpasync"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    sg.load()
+    sg.sgemm_set_config("auto")
+    yield
+    sg.sgemm_set_config("auto")
+
+
+@pytest.fixture
+def config(request):
+    name = getattr(request, "param", "auto")
+    assert sg.sgemm_set_config(name) == 0
+    yield name
+    sg.sgemm_set_config("auto")
+
+
+def gen(M, N, K, seed, dist="normal"):
+    A = inputs.fill(dist, seed, inputs.TID_A, M, K)
+    B = inputs.fill(dist, seed, inputs.TID_B, K, N)
+    C0 = inputs.fill(dist, seed, inputs.TID_C, M, N)
+    return A, B, C0
+
+
+def check_full(alpha, A, B, beta, C0, C, exact=False):
+    ref, S = oracle.sgemm_ref(alpha, A, B, beta, C0 if beta != 0 else None)
+    rep = oracle.check(C, ref, S, A.shape[1], exact=exact)
+    assert rep["ok"], rep
+    return rep
+
+
+SHAPES = [(1, 1, 1), (2, 3, 5), (7, 5, 3), (31, 33, 17), (64, 64, 32), (127, 129, 33),
+          (128, 128, 32), (129, 127, 31), (255, 257, 63), (300, 200, 100), (513, 130, 1000),
+          (1, 1000, 7), (1000, 1, 7), (65, 64, 1), (64, 65, 2), (256, 256, 256)]
+
+
+@pytest.mark.parametrize("config", CONFIGS, indirect=True)
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_small_shapes_every_element(config, shape):
+    M, N, K = shape
+    A, B, C0 = gen(M, N, K, seed=100 + M + 7 * N + 13 * K)
+    C, guards, plan = gpu_util.run(0.7, A, B, -1.3, C0)
+    assert guards, "wrote outside C"
+    check_full(0.7, A, B, -1.3, C0, C)
+    if config.endswith("cpasync"):
+        assert "Acp_Bcp" in plan[0], plan
+
+
+@pytest.mark.parametrize("config", CONFIGS, indirect=True)
+@pytest.mark.parametrize("layout", [
+    dict(lda=None, ldb=None, ldc=None, offsets=(0, 0, 0)),       # dense, 16-byte aligned
+    dict(lda=37, ldb=70, ldc=71, offsets=(0, 0, 0)),             # unaligned leading dims
+    dict(lda=40, ldb=72, ldc=72, offsets=(1, 2, 3)),             # aligned lds, shifted bases
+    dict(lda=36, ldb=68, ldc=68, offsets=(4, 8, 0)),             # padded, 16-byte aligned
+], ids=["dense", "odd_ld", "odd_base", "padded"])
+def test_leading_dims_and_offsets(config, layout):
+    M, N, K = 133, 66, 35
+    A, B, C0 = gen(M, N, K, seed=7)
+    C, guards, plan = gpu_util.run(1.1, A, B, 0.5, C0, **layout)
+    assert guards, "wrote outside C (padding or guard band)"
+    check_full(1.1, A, B, 0.5, C0, C)
+
+
+def test_tma_chosen_only_when_aligned():
+    A, B, C0 = gen(256, 256, 256, seed=8)
+    _, _, plan = gpu_util.run(1.0, A, B, 0.0, C0)
+    assert "Atma_Btma" in plan[0], plan
+    _, _, plan = gpu_util.run(1.0, A, B, 0.0, C0, lda=257)
+    assert "Acp_Btma" in plan[0], plan
+    _, _, plan = gpu_util.run(1.0, A, B, 0.0, C0, offsets=(0, 1, 0))
+    assert "Atma_Bcp" in plan[0], plan
+
+
+@pytest.mark.parametrize("config", ["auto", "128x128", "64x64", "128x128:cpasync"], indirect=True)
+def test_integer_inputs_bit_exact(config):
+    w = inputs.WORKLOADS["sq1024_int"]
+    A, B, C0 = w.make()
+    C, guards, _ = gpu_util.run(w.alpha, A, B, w.beta, C0)
+    assert guards
+    check_full(w.alpha, A, B, w.beta, C0, C, exact=True)
+
+
+def test_all_ones_closed_form():
+    M, N, K = 300, 260, 777
+    A = np.ones((M, K), np.float32)
+    B = np.ones((K, N), np.float32)
+    C0 = inputs.fill("int", 9, inputs.TID_C, M, N)
+    C, _, _ = gpu_util.run(2.0, A, B, -1.0, C0)
+    assert np.array_equal(C, (2.0 * K - C0).astype(np.float32))
+
+
+def test_identity_closed_form():
+    n, N = 200, 150
+    A = np.eye(n, dtype=np.float32)
+    B = inputs.fill("normal", 10, inputs.TID_B, n, N)
+    C, _, _ = gpu_util.run(1.0, A, B, 0.0, None)
+    assert np.array_equal(C, B)
+
+
+# ---- degenerate cases (BLAS readings) --------------------------------------
+
+def test_beta_zero_never_reads_c():
+    A, B, _ = gen(70, 90, 40, seed=11)
+    C, _, _ = gpu_util.run(1.0, A, B, 0.0, None)          # C starts as NaN
+    assert np.all(np.isfinite(C))
+    check_full(1.0, A, B, 0.0, None, C)
+
+
+def test_alpha_zero_scales_c_without_reading_ab():
+    _, _, C0 = gen(50, 40, 30, seed=12)
+    A = np.full((50, 30), np.nan, np.float32)
+    B = np.full((30, 40), np.nan, np.float32)
+    C, guards, plan = gpu_util.run(0.0, A, B, -1.5, C0)
+    assert plan[0] == "scale" and guards
+    assert np.array_equal(C, (np.float32(-1.5) * C0).astype(np.float32))
+    C, _, _ = gpu_util.run(0.0, A, B, 0.0, None)
+    assert np.array_equal(C, np.zeros_like(C))
+
+
+def test_k_zero():
+    _, _, C0 = gen(33, 17, 1, seed=13)
+    A = np.zeros((33, 0), np.float32)
+    B = np.zeros((0, 17), np.float32)
+    C, guards, plan = gpu_util.run(2.0, A, B, 0.25, C0)
+    assert plan[0] == "scale" and guards
+    assert np.array_equal(C, (np.float32(0.25) * C0).astype(np.float32))
+
+
+def test_empty_m_or_n_leaves_c_alone():
+    torch = pytest.importorskip("torch")
+    A, B, C0 = gen(4, 4, 4, seed=14)
+    for (M, N) in [(0, 4), (4, 0)]:
+        dA = torch.zeros(M, 4, device="cuda")
+        dB = torch.zeros(4, N, device="cuda")
+        dC = torch.zeros(M, N, device="cuda")
+        sg.sgemm_tensors(1.0, dA, dB, 0.0, dC)
+    torch.cuda.synchronize()
+
+
+# ---- streams, repeat calls, status word -------------------------------------
+
+def test_runs_on_a_side_stream_in_order():
+    torch = pytest.importorskip("torch")
+    M = N = K = 512
+    A, B, C0 = gen(M, N, K, seed=15)
+    s = torch.cuda.Stream()
+    dA = torch.from_numpy(A).cuda()
+    dB = torch.from_numpy(B).cuda()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        dC = torch.from_numpy(C0).to("cuda", non_blocking=False)
+        for _ in range(3):                     # C = 0.5 AB + 1 C, three times in order
+            sg.sgemm_tensors(0.5, dA, dB, 1.0, dC, stream=s)
+    s.synchronize()
+    ref, S = oracle.sgemm_ref(1.5, A, B, 1.0, C0)
+    rep = oracle.check(dC.cpu().numpy(), ref, 3 * S, K * 3)
+    assert rep["ok"], rep
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    torch = pytest.importorskip("torch")
+    assert sg.check_status() == 0
+    assert sg.sgemm_selftest_wait_timeout(20_000_000) == 0       # 20 ms
+    rc, bits = sg.sgemm_check_status(torch.cuda.current_stream().cuda_stream)
+    assert rc == sg.SGEMM_ERR_DEVICE_TIMEOUT and bits == 1
+    assert sg.check_status() == 0                                 # cleared
+    A, B, C0 = gen(64, 64, 64, seed=16)
+    C, _, _ = gpu_util.run(1.0, A, B, 1.0, C0)                    # still usable
+    check_full(1.0, A, B, 1.0, C0, C)
+
+
+def test_fp32_peak_is_plausible():
+    torch = pytest.importorskip("torch")
+    props = torch.cuda.get_device_properties(0)
+    r = sg.fp32_peak(target_ms=50)
+    datasheet = props.multi_processor_count * 128 * 2 * 2.07  # GFLOP/s at 2070 MHz
+    assert 0.2 * datasheet < r["gflops"] < 1.05 * datasheet, (r, datasheet)
+    assert r["ms"] > 10
+
+
+# ---- the five workloads, in the launch configuration the bench times --------
+
+def _workload(name, full):
+    torch = pytest.importorskip("torch")
+    w = inputs.WORKLOADS[name]
+    A, B, C0 = w.make()
+    C, guards, plan = gpu_util.run(w.alpha, A, B, w.beta, C0 if w.beta != 0 else None)
+    assert guards
+    c0 = C0 if w.beta != 0 else None
+    if full:
+        rep = check_full(w.alpha, A, B, w.beta, c0, C, exact=w.exact)
+    else:
+        rows, cols = inputs.sample_entries(w.M, w.N)
+        ref, S = oracle.sgemm_ref_sampled(w.alpha, A, B, w.beta, c0, rows, cols)
+        rep = oracle.check(C[rows, cols], ref, S, w.K, exact=w.exact)
+        assert rep["ok"], rep
+    assert np.all(np.isfinite(C))
+    return rep, plan
+
+
+def test_workload_sq256_uniform():
+    _workload("sq256_uniform", full=True)
+
+
+def test_workload_sq1024_int_bit_exact():
+    _workload("sq1024_int", full=True)
+
+
+def test_workload_sq4096_uniform_sampled():
+    rep, plan = _workload("sq4096_uniform", full=False)
+    assert "128x128" in plan[0]
+
+
+def test_workload_ragged_every_element():
+    rep, plan = _workload("ragged_4093x5120x1531_normal", full=True)
+    assert "Acp_Btma" in plan[0], plan        # lda = 1531 is not 16-byte aligned
+
+
+def test_workload_llm_projection_sampled():
+    _workload("llm_8192x14336x4096", full=False)
