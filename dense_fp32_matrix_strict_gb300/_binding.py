@@ -24,7 +24,7 @@ SGEMM_ERR_CUDA = 5
 EXPORTED_SYMBOLS = (
     "sgemm", "sgemm_check_status", "sgemm_error_string", "sgemm_last_cuda_error",
     "sgemm_plan", "sgemm_set_config", "sgemm_set_wait_timeout_ns", "sgemm_fp32_peak",
-    "sgemm_selftest_wait_timeout",
+    "sgemm_selftest_wait_timeout", "sgemm_config_names",
 )
 
 _lock = threading.Lock()
@@ -73,6 +73,8 @@ def load():
         lib.sgemm_plan.restype = ci
         lib.sgemm_set_config.argtypes = [ctypes.c_char_p]
         lib.sgemm_set_config.restype = ci
+        lib.sgemm_config_names.argtypes = [ctypes.c_char_p, ci]
+        lib.sgemm_config_names.restype = ci
         lib.sgemm_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
         lib.sgemm_set_wait_timeout_ns.restype = ci
         lib.sgemm_fp32_peak.argtypes = [ctypes.c_double, f64p, f64p, f64p, vp]
@@ -122,6 +124,14 @@ def sgemm_plan(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc):
 
 def sgemm_set_config(name: str) -> int:
     return load().sgemm_set_config(name.encode())
+
+
+def sgemm_config_names():
+    """Returns (code, [family names])."""
+    buf = ctypes.create_string_buffer(4096)
+    rc = load().sgemm_config_names(buf, 4096)
+    names = buf.value.decode().split(",") if rc == SGEMM_OK and buf.value else []
+    return rc, names
 
 
 def sgemm_set_wait_timeout_ns(ns: int) -> int:

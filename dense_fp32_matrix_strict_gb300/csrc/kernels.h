@@ -33,19 +33,39 @@ cudaError_t ws_launch(const CUtensorMap* tmA, const CUtensorMap* tmB, const Gemm
     return cudaGetLastError();
 }
 
-#define SG_WS_ENTRY(NAME, BM, BN, S, AM, BMD)                                              \
-    KernelEntry {                                                                          \
-        NAME, BM, BN, 32, S, AM, BMD, Cfg<BM, BN, 32, S, AM, BMD>::THREADS,                \
-            Cfg<BM, BN, 32, S, AM, BMD>::SMEM_BYTES, &ws_prepare<Cfg<BM, BN, 32, S, AM, BMD>>, \
-            &ws_launch<Cfg<BM, BN, 32, S, AM, BMD>>                                        \
+// One kernel family: a CTA tile and tuning knobs, instantiated for the four
+// (A, B) load-mode pairs in mode_index order.
+struct KernelFamily {
+    const char* name;
+    int bm, bn;
+    KernelEntry modes[4];
+};
+
+// Index into a family's modes: TMA/TMA, CP/TMA, TMA/CP, CP/CP.
+inline constexpr int mode_index(int a_mode, int b_mode) { return a_mode + 2 * b_mode; }
+
+template <int BM, int BN, int S, int AM, int BMD, int LMAP, int XPF, int FORDER, int ISSUE>
+constexpr KernelEntry make_entry(const char* name) {
+    using C = Cfg<BM, BN, 32, S, AM, BMD, LMAP, XPF, FORDER, ISSUE>;
+    return KernelEntry{name, BM, BN, 32, S, AM, BMD, C::THREADS, C::SMEM_BYTES,
+                       &ws_prepare<C>, &ws_launch<C>};
+}
+
+#define SG_FAMILY(NAME, BM, BN, S, LMAP, XPF, FORDER, ISSUE)                                      \
+    KernelFamily {                                                                               \
+        NAME, BM, BN, {                                                                          \
+            make_entry<BM, BN, S, LOAD_TMA, LOAD_TMA, LMAP, XPF, FORDER, ISSUE>(NAME "_Atma_Btma"),  \
+            make_entry<BM, BN, S, LOAD_CPASYNC, LOAD_TMA, LMAP, XPF, FORDER, ISSUE>(NAME "_Acp_Btma"), \
+            make_entry<BM, BN, S, LOAD_TMA, LOAD_CPASYNC, LMAP, XPF, FORDER, ISSUE>(NAME "_Atma_Bcp"), \
+            make_entry<BM, BN, S, LOAD_CPASYNC, LOAD_CPASYNC, LMAP, XPF, FORDER, ISSUE>(NAME "_Acp_Bcp") \
+        }                                                                                        \
     }
 
-// Each returns its table (4 entries: A/B load modes TMA/TMA, CP/TMA, TMA/CP,
-// CP/CP, in that order). Defined in one translation unit per CTA tile.
-const KernelEntry* ws_kernels_128x128();
-const KernelEntry* ws_kernels_64x64();
-
-// Index into a 4-entry table.
-inline int mode_index(int a_mode, int b_mode) { return a_mode + 2 * b_mode; }
+// Families, one translation unit each (compiled in parallel). The first two
+// are the ones "auto" chooses between; the rest are tuning alternatives that
+// sgemm_set_config can force.
+const KernelFamily* family_128x128();
+const KernelFamily* family_64x64();
+const KernelFamily* const* sweep_families(int* count);
 
 }  // namespace sg

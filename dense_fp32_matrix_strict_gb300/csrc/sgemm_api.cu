@@ -19,15 +19,34 @@ namespace sg {
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kNumTiles = 2;      // 0: 128x128, 1: 64x64
+constexpr int kMaxFamilies = 32;
 constexpr int kStatusBytes = 256;
+
+// All compiled kernel families: [0] 128x128 and [1] 64x64 are what "auto"
+// chooses between; the rest are tuning alternatives.
+struct Registry {
+    const KernelFamily* fam[kMaxFamilies];
+    int count = 0;
+    Registry() {
+        fam[count++] = family_128x128();
+        fam[count++] = family_64x64();
+        int n = 0;
+        const KernelFamily* const* sw = sweep_families(&n);
+        for (int i = 0; i < n && count < kMaxFamilies; ++i) fam[count++] = sw[i];
+    }
+};
+
+const Registry& registry() {
+    static const Registry r;
+    return r;
+}
 
 struct DeviceState {
     bool ready = false;
     int error = SGEMM_OK;
     int sm_count = 0;
     int* status = nullptr;                 // device status word (256 bytes)
-    int ctas_per_sm[kNumTiles][4] = {};
+    int ctas_per_sm[kMaxFamilies][4] = {};
 };
 
 std::mutex g_mu;
@@ -35,20 +54,16 @@ DeviceState g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 bool g_env_read = false;
 
-// Forced configuration: tile 0 = auto, 128 or 64; cp = force cp.async loads.
-std::atomic<int> g_force_tile{0};
+// Forced configuration: family index (-1 = auto); cp = force cp.async loads.
+std::atomic<int> g_force_family{-1};
 std::atomic<int> g_force_cp{0};
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 
 thread_local int t_last_cuda_error = 0;
 
-const KernelEntry* table_for(int tile) {
-    return tile == 0 ? ws_kernels_128x128() : ws_kernels_64x64();
-}
-
-int parse_config(const char* name, int* tile, int* cp) {
+int parse_config(const char* name, int* family, int* cp) {
     if (name == nullptr) return SGEMM_ERR_INVALID_VALUE;
-    char buf[64];
+    char buf[96];
     std::strncpy(buf, name, sizeof(buf) - 1);
     buf[sizeof(buf) - 1] = '\0';
     int want_cp = 0;
@@ -58,12 +73,17 @@ int parse_config(const char* name, int* tile, int* cp) {
         want_cp = 1;
         *colon = '\0';
     }
-    int t;
-    if (std::strcmp(buf, "auto") == 0 || buf[0] == '\0') t = 0;
-    else if (std::strcmp(buf, "128x128") == 0) t = 128;
-    else if (std::strcmp(buf, "64x64") == 0) t = 64;
-    else return SGEMM_ERR_INVALID_VALUE;
-    *tile = t;
+    int f = -2;
+    if (std::strcmp(buf, "auto") == 0 || buf[0] == '\0') f = -1;
+    else if (std::strcmp(buf, "128x128") == 0) f = 0;
+    else if (std::strcmp(buf, "64x64") == 0) f = 1;
+    else {
+        const Registry& r = registry();
+        for (int i = 0; i < r.count; ++i)
+            if (std::strcmp(buf, r.fam[i]->name) == 0) f = i;
+    }
+    if (f == -2) return SGEMM_ERR_INVALID_VALUE;
+    *family = f;
     *cp = want_cp;
     return SGEMM_OK;
 }
@@ -84,9 +104,9 @@ int device_setup(DeviceState** out) {
     if (!g_env_read) {
         g_env_read = true;
         const char* env = std::getenv("SGEMM_FORCE_CONFIG");
-        int tile = 0, cp = 0;
-        if (env != nullptr && parse_config(env, &tile, &cp) == SGEMM_OK) {
-            g_force_tile = tile;
+        int fam = -1, cp = 0;
+        if (env != nullptr && parse_config(env, &fam, &cp) == SGEMM_OK) {
+            g_force_family = fam;
             g_force_cp = cp;
         }
     }
@@ -114,13 +134,20 @@ int device_setup(DeviceState** out) {
             return cuda_fail(e == cudaSuccess ? cudaErrorNotSupported : e, SGEMM_ERR_CUDA);
         g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
-    for (int t = 0; t < kNumTiles; ++t) {
-        const KernelEntry* tab = table_for(t);
+    const Registry& reg = registry();
+    for (int f = 0; f < reg.count; ++f) {
         for (int m = 0; m < 4; ++m) {
             int n = 0;
-            e = tab[m].prepare(&n);
-            if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_CUDA);
-            st.ctas_per_sm[t][m] = n > 0 ? n : 1;
+            e = reg.fam[f]->modes[m].prepare(&n);
+            if (e != cudaSuccess || n <= 0) {
+                // The two families "auto" uses must work; a tuning
+                // alternative that cannot run here is only marked unusable.
+                if (f < 2) return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidConfiguration,
+                                            SGEMM_ERR_CUDA);
+                (void)cudaGetLastError();
+                n = 0;
+            }
+            st.ctas_per_sm[f][m] = n;
         }
     }
     void* status = nullptr;
@@ -216,13 +243,13 @@ int make_plan(DeviceState* st, int64_t M, int64_t N, int64_t K, float alpha, con
     }
     pl->kind = 2;
     const int sms = st->sm_count;
-    int tile = g_force_tile.load();
-    if (tile == 0) {
+    int fi = g_force_family.load();
+    if (fi < 0) {
         const int64_t tiles128 = ((M + 127) / 128) * ((N + 127) / 128);
-        tile = (tiles128 * 2 >= sms) ? 128 : 64;
+        fi = (tiles128 * 2 >= sms) ? 0 : 1;
     }
-    const int ti = tile == 128 ? 0 : 1;
-    const int bm = tile, bn = tile, bk = 32;
+    const KernelFamily* fam = registry().fam[fi];
+    const int bm = fam->bm, bn = fam->bn, bk = 32;
     const bool force_cp = g_force_cp.load() != 0;
     std::memset(&pl->tmA, 0, sizeof(CUtensorMap));
     std::memset(&pl->tmB, 0, sizeof(CUtensorMap));
@@ -232,7 +259,7 @@ int make_plan(DeviceState* st, int64_t M, int64_t N, int64_t K, float alpha, con
     if (!force_cp && tma_ok(B, ldb, K, N) && encode_2d(&pl->tmB, B, K, N, ldb, bk, bn, false))
         b_mode = LOAD_TMA;
     const int mi = mode_index(a_mode, b_mode);
-    pl->k = &table_for(ti)[mi];
+    pl->k = &fam->modes[mi];
 
     GemmParams& p = pl->p;
     p.M = static_cast<int>(M);
@@ -255,7 +282,8 @@ int make_plan(DeviceState* st, int64_t M, int64_t N, int64_t K, float alpha, con
     p.status = st->status;
     const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
     if (tiles > 0x7fffffffll) return SGEMM_ERR_INVALID_VALUE;
-    const int64_t slots = static_cast<int64_t>(st->ctas_per_sm[ti][mi]) * sms;
+    if (st->ctas_per_sm[fi][mi] <= 0) return cuda_fail(cudaErrorInvalidConfiguration, SGEMM_ERR_LAUNCH);
+    const int64_t slots = static_cast<int64_t>(st->ctas_per_sm[fi][mi]) * sms;
     pl->grid = static_cast<int>(tiles < slots ? tiles : slots);
     return SGEMM_OK;
 }
@@ -367,15 +395,31 @@ extern "C" const char* sgemm_error_string(int code) {
 extern "C" int sgemm_last_cuda_error(void) { return t_last_cuda_error; }
 
 extern "C" int sgemm_set_config(const char* name) {
-    int tile = 0, cp = 0;
-    int rc = parse_config(name, &tile, &cp);
+    int fam = -1, cp = 0;
+    int rc = parse_config(name, &fam, &cp);
     if (rc != SGEMM_OK) return rc;
     {
         std::lock_guard<std::mutex> lock(g_mu);
         g_env_read = true;   // an explicit choice overrides the environment
     }
-    g_force_tile = tile;
+    g_force_family = fam;
     g_force_cp = cp;
+    return SGEMM_OK;
+}
+
+extern "C" int sgemm_config_names(char* buf, int buflen) {
+    if (buf == nullptr || buflen <= 0) return SGEMM_ERR_INVALID_VALUE;
+    const Registry& r = registry();
+    size_t used = 0;
+    buf[0] = '\0';
+    for (int i = 0; i < r.count; ++i) {
+        const size_t n = std::strlen(r.fam[i]->name);
+        if (used + n + 2 > static_cast<size_t>(buflen)) return SGEMM_ERR_INVALID_VALUE;
+        if (i > 0) buf[used++] = ',';
+        std::memcpy(buf + used, r.fam[i]->name, n);
+        used += n;
+        buf[used] = '\0';
+    }
     return SGEMM_OK;
 }
 

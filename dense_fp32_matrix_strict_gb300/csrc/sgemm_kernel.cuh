@@ -63,10 +63,21 @@ struct GemmParams {
     int* status;
 };
 
-template <int BM_, int BN_, int BK_, int STAGES_, int A_MODE_, int B_MODE_>
+// Kernel configuration. LMAP: lane mapping (lane_grid); XPF: prefetch the
+// next stage's first fragments during the current stage's last k-group;
+// FORDER: FMA form of the outer product (0: scalar FFMA rows outer, 1: scalar
+// columns outer, 2: packed FFMA2 over column pairs).
+// ISSUE: 0 = dedicated producer warp(s); 1 = when both operands load by TMA,
+// consumer thread 0 issues the refills itself (no producer warp, so 256
+// threads and up to 255 registers per thread).
+template <int BM_, int BN_, int BK_, int STAGES_, int A_MODE_, int B_MODE_, int LMAP_ = 0,
+          int XPF_ = 0, int FORDER_ = 0, int ISSUE_ = 0>
 struct Cfg {
     static constexpr int BM = BM_, BN = BN_, BK = BK_, STAGES = STAGES_;
     static constexpr int A_MODE = A_MODE_, B_MODE = B_MODE_;
+    static constexpr int LMAP = LMAP_, XPF = XPF_, FORDER = FORDER_;
+    static constexpr bool INLINE =
+        (ISSUE_ == 1) && (A_MODE_ == LOAD_TMA) && (B_MODE_ == LOAD_TMA);
     static_assert(BK == 32, "A rows are one 128-byte swizzle span");
     static_assert(BM % 32 == 0 && BN % 64 == 0, "warp tile is 32 x 64");
     static constexpr int WARPS_M = BM / 32, WARPS_N = BN / 64;
@@ -76,7 +87,7 @@ struct Cfg {
     static constexpr bool ANY_TMA = (A_MODE == LOAD_TMA) || (B_MODE == LOAD_TMA);
     // cp.async producers: one warp per SM sub-partition so the copy
     // instructions do not all land on one scheduler.
-    static constexpr int PRODUCER_WARPS = ANY_CP ? 4 : 1;
+    static constexpr int PRODUCER_WARPS = INLINE ? 0 : (ANY_CP ? 4 : 1);
     static constexpr int THREADS = CONSUMERS + 32 * PRODUCER_WARPS;
     static constexpr int A_BYTES = BM * BK * 4;
     static constexpr int B_BYTES = BK * BN * 4;
@@ -85,6 +96,7 @@ struct Cfg {
     static constexpr uint32_t FULL_COUNT = (ANY_TMA ? 1 : 0) + (ANY_CP ? 32 * PRODUCER_WARPS : 0);
     static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * (A_BYTES + B_BYTES)
                                       + 2 * STAGES * 8;
+    static_assert(SMEM_BYTES <= 227 * 1024, "ring does not fit in 227 KB of shared memory");
 };
 
 // Tile index -> (tile row, tile column), grouped so that the CTAs running at
@@ -196,16 +208,124 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmA, const CUtensorM
     if (C::ANY_CP) asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// Lane -> (tr, tc) in the 4 x 8 lane grid of a 32 x 64 warp tile. The
+// mapping decides which lanes share a shared-memory quarter-warp phase:
+//   0: tr = lane / 8, tc = lane % 8   (a phase reads 1 A row, 8 B float4)
+//   1: tr = lane % 4, tc = lane / 4   (a phase reads 4 A rows, 2 B float4)
+//   2: 2 x 4 blocks per phase          (a phase reads 2 A rows, 4 B float4)
+template <int LMAP>
+__device__ __forceinline__ void lane_grid(int lane, int& tr, int& tc) {
+    if (LMAP == 0) {
+        tr = lane >> 3;
+        tc = lane & 7;
+    } else if (LMAP == 1) {
+        tr = lane & 3;
+        tc = lane >> 2;
+    } else {
+        tr = (lane & 1) | (((lane >> 3) & 1) << 1);
+        tc = ((lane >> 1) & 3) | ((lane >> 4) << 2);
+    }
+}
+
+// A fragment of k-group kq (4 consecutive k) for the lane's 8 rows
+// {tr, tr+4, ..., tr+28}: row r's 16-byte chunk kq sits at chunk kq ^ (r % 8),
+// and r % 8 is tr for even i, tr + 4 (= tr ^ 4) for odd i.
+__device__ __forceinline__ void load_a_group(float4 (&a)[8], const uint8_t* a_rows, int kq, int tr) {
+    const int c0 = ((kq ^ tr) & 7) << 4;
+    const int c1 = c0 ^ 64;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        a[i] = *reinterpret_cast<const float4*>(a_rows + i * 4 * 128 + ((i & 1) ? c1 : c0));
+}
+
+__device__ __forceinline__ float lane_of(const float4& v, int kk) {
+    return kk == 0 ? v.x : kk == 1 ? v.y : kk == 2 ? v.z : v.w;
+}
+
+// One k-step of the 8 x 8 register outer product.
+//   FORDER 0/1: scalar FFMA, rows or columns outer.
+//   FORDER 2:   packed FFMA2 (fma.rn.f32x2: two IEEE single-precision FMAs,
+//               each rounded once, in one instruction): pairs of adjacent
+//               columns share one instruction with the row's A value in both
+//               lanes. Every output still sees the same FMA sequence, so the
+//               result is bit-identical to the scalar forms.
+template <int FORDER>
+__device__ __forceinline__ void outer_product(float (&acc)[8][8], const float4 (&a)[8], int kk,
+                                              const float4& b0, const float4& b1) {
+    const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    if (FORDER == 2) {
+        const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
+                              make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float av = lane_of(a[i], kk);
+            const float2 aa = make_float2(av, av);
+#pragma unroll
+            for (int jp = 0; jp < 4; ++jp) {
+                float2 c = make_float2(acc[i][2 * jp], acc[i][2 * jp + 1]);
+                c = __ffma2_rn(aa, bp[jp], c);
+                acc[i][2 * jp] = c.x;
+                acc[i][2 * jp + 1] = c.y;
+            }
+        }
+    } else if (FORDER == 0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float av = lane_of(a[i], kk);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av, bv[j], acc[i][j]);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i][j] = fmaf(lane_of(a[i], kk), bv[j], acc[i][j]);
+    }
+}
+
+// Inline refill (Cfg::INLINE): load stage g of this CTA's sequence into ring
+// slot `slot` by TMA, completing on that slot's full barrier.
 template <class C>
-__device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_ptr,
+__device__ __forceinline__ void issue_stage(const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                            const GemmParams& p, uint32_t sA, uint32_t sB,
+                                            uint32_t full0, int g, int slot) {
+    const int i = g / p.k_tiles;
+    const int kt = g - i * p.k_tiles;
+    int tm, tn;
+    tile_coords(static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x), p, tm, tn);
+    const uint32_t full = full0 + 8 * slot;
+    mbar_arrive_expect_tx(full, C::TX_BYTES);
+    tma_load_2d(sA + slot * C::A_BYTES, tmA, full, kt * C::BK, tm * C::BM);
+    tma_load_2d(sB + slot * C::B_BYTES, tmB, full, tn * C::BN, kt * C::BK);
+}
+
+template <class C>
+__device__ __forceinline__ void consumer(const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                         const GemmParams& p, const uint8_t* sA_ptr,
                                          const uint8_t* sB_ptr, uint32_t full0, uint32_t empty0,
                                          int warp, int lane) {
+    const uint32_t sA_u32 = smem_u32(sA_ptr), sB_u32 = smem_u32(sB_ptr);
     const int num_tiles = p.tiles_m * p.tiles_n;
     const int wm = warp % C::WARPS_M, wn = warp / C::WARPS_M;
-    const int tr = lane >> 3, tc = lane & 7;
+    int tr, tc;
+    lane_grid<C::LMAP>(lane, tr, tc);
     const int row_base = wm * 32 + tr;        // rows row_base + 4 i, i = 0..7
     const int col_base = wn * 64 + 4 * tc;    // cols col_base + {0..3} and + 32 + {0..3}
+    constexpr int KQ = C::BK / 4;
 
+    // Stage sequence of this CTA: k-tile kt of its i-th tile is stage
+    // i * k_tiles + kt, held in ring slot (stage mod STAGES).
+    const int my_tiles = (num_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                         static_cast<int>(gridDim.x);
+    const int total = my_tiles * p.k_tiles;
+    const bool issuer = C::INLINE && threadIdx.x == 0;
+    if (issuer) {
+        tma_prefetch_desc(tmA);
+        tma_prefetch_desc(tmB);
+        for (int g = 0; g < total && g < C::STAGES; ++g)
+            issue_stage<C>(tmA, tmB, p, sA_u32, sB_u32, full0, g, g);
+    }
+    int g = 0;
     int s = 0;
     uint32_t ph = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
@@ -217,36 +337,70 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
 #pragma unroll
             for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
 
-        for (int kt = 0; kt < p.k_tiles; ++kt) {
+        // With XPF, the first k-group of each stage (and its first B row) is
+        // loaded while the previous stage's last k-group is multiplied.
+        float4 a_pre[8];
+        float4 b_pre0, b_pre1;
+        if (C::XPF) {
             if (!wait_bounded(full0 + 8 * s, ph, p, STATUS_CONSUMER_TIMEOUT)) return;
             const uint8_t* a_st = sA_ptr + s * C::A_BYTES + row_base * 128;
             const uint8_t* b_st = sB_ptr + s * C::B_BYTES + col_base * 4;
+            load_a_group(a_pre, a_st, 0, tr);
+            b_pre0 = *reinterpret_cast<const float4*>(b_st);
+            b_pre1 = *reinterpret_cast<const float4*>(b_st + 32 * 4);
+        }
+
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+            if (!C::XPF) {
+                if (!wait_bounded(full0 + 8 * s, ph, p, STATUS_CONSUMER_TIMEOUT)) return;
+            }
+            const uint8_t* a_st = sA_ptr + s * C::A_BYTES + row_base * 128;
+            const uint8_t* b_st = sB_ptr + s * C::B_BYTES + col_base * 4;
+            int s_next = s + 1;
+            uint32_t ph_next = ph;
+            if (s_next == C::STAGES) { s_next = 0; ph_next ^= 1u; }
 #pragma unroll
-            for (int kq = 0; kq < C::BK / 4; ++kq) {
-                // Swizzled 16-byte chunk of k-group kq in rows r with r % 8 == tr
-                // (even i) and r % 8 == tr + 4 (odd i).
-                const int c0 = ((kq ^ tr) & 7) << 4;
-                const int c1 = c0 ^ 64;
+            for (int kq = 0; kq < KQ; ++kq) {
                 float4 a[8];
+                if (C::XPF && kq == 0) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    a[i] = *reinterpret_cast<const float4*>(a_st + i * 4 * 128 + ((i & 1) ? c1 : c0));
+                    for (int i = 0; i < 8; ++i) a[i] = a_pre[i];
+                } else {
+                    load_a_group(a, a_st, kq, tr);
+                }
+                if (C::XPF && kq == KQ - 1 && kt + 1 < p.k_tiles) {
+                    if (!wait_bounded(full0 + 8 * s_next, ph_next, p, STATUS_CONSUMER_TIMEOUT))
+                        return;
+                    const uint8_t* a_nx = sA_ptr + s_next * C::A_BYTES + row_base * 128;
+                    const uint8_t* b_nx = sB_ptr + s_next * C::B_BYTES + col_base * 4;
+                    load_a_group(a_pre, a_nx, 0, tr);
+                    b_pre0 = *reinterpret_cast<const float4*>(b_nx);
+                    b_pre1 = *reinterpret_cast<const float4*>(b_nx + 32 * 4);
+                }
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    const uint8_t* brow = b_st + (kq * 4 + kk) * C::BN * 4;
-                    const float4 b0 = *reinterpret_cast<const float4*>(brow);
-                    const float4 b1 = *reinterpret_cast<const float4*>(brow + 32 * 4);
-                    const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av, bv[j], acc[i][j]);
+                    float4 b0, b1;
+                    if (C::XPF && kq == 0 && kk == 0) {
+                        b0 = b_pre0;
+                        b1 = b_pre1;
+                    } else {
+                        const uint8_t* brow = b_st + (kq * 4 + kk) * C::BN * 4;
+                        b0 = *reinterpret_cast<const float4*>(brow);
+                        b1 = *reinterpret_cast<const float4*>(brow + 32 * 4);
                     }
+                    outer_product<C::FORDER>(acc, a, kk, b0, b1);
                 }
             }
             mbar_arrive(empty0 + 8 * s);
-            if (++s == C::STAGES) { s = 0; ph ^= 1u; }
+            if (issuer && g + C::STAGES < total) {
+                // Refill this slot with stage g + STAGES once every consumer
+                // has released stage g.
+                if (!wait_bounded(empty0 + 8 * s, ph, p, STATUS_PRODUCER_TIMEOUT)) return;
+                issue_stage<C>(tmA, tmB, p, sA_u32, sB_u32, full0, g + C::STAGES, s);
+            }
+            ++g;
+            s = s_next;
+            ph = ph_next;
         }
 
         // Epilogue: C = alpha * acc + beta * C, straight from registers.
@@ -314,11 +468,11 @@ sgemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     __syncthreads();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp >= C::CONSUMER_WARPS) {
+    if (C::PRODUCER_WARPS > 0 && warp >= C::CONSUMER_WARPS) {
         producer<C>(&tmA, &tmB, p, smem_u32(sA), smem_u32(sB), full0, empty0,
                     warp - C::CONSUMER_WARPS, lane);
     } else {
-        consumer<C>(p, sA, sB, full0, empty0, warp, lane);
+        consumer<C>(&tmA, &tmB, p, sA, sB, full0, empty0, warp, lane);
     }
 }
 

@@ -1,16 +1,12 @@
-// Instantiations of the warp-specialised kernel with a 128 x 128 x 32 CTA tile
-// (8 consumer warps) and a 4-stage ring (128 KB of shared memory).
+// The 128 x 128 x 32 CTA-tile family (8 consumer warps, 4-stage ring,
+// 128 KB of shared memory, packed FFMA2 outer product): the kernel for every
+// problem with enough tiles to fill the GPU.
 #include "kernels.h"
 
 namespace sg {
 
-static const KernelEntry kTable[4] = {
-    SG_WS_ENTRY("ws_128x128x32_s4_Atma_Btma", 128, 128, 4, LOAD_TMA, LOAD_TMA),
-    SG_WS_ENTRY("ws_128x128x32_s4_Acp_Btma", 128, 128, 4, LOAD_CPASYNC, LOAD_TMA),
-    SG_WS_ENTRY("ws_128x128x32_s4_Atma_Bcp", 128, 128, 4, LOAD_TMA, LOAD_CPASYNC),
-    SG_WS_ENTRY("ws_128x128x32_s4_Acp_Bcp", 128, 128, 4, LOAD_CPASYNC, LOAD_CPASYNC),
-};
+static const KernelFamily kFamily = SG_FAMILY("ws_128x128x32_s4", 128, 128, 4, 0, 0, 2, 0);
 
-const KernelEntry* ws_kernels_128x128() { return kTable; }
+const KernelFamily* family_128x128() { return &kFamily; }
 
 }  // namespace sg

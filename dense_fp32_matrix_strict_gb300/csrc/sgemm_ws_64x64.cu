@@ -1,17 +1,12 @@
-// Instantiations of the warp-specialised kernel with a 64 x 64 x 32 CTA tile
-// (2 consumer warps) and a 4-stage ring (64 KB of shared memory), for
-// problems too small to give every SM a 128 x 128 tile.
+// The 64 x 64 x 32 CTA-tile family (2 consumer warps, 4-stage ring, 64 KB of
+// shared memory, packed FFMA2 outer product), for problems too small to give
+// every SM a 128 x 128 tile.
 #include "kernels.h"
 
 namespace sg {
 
-static const KernelEntry kTable[4] = {
-    SG_WS_ENTRY("ws_64x64x32_s4_Atma_Btma", 64, 64, 4, LOAD_TMA, LOAD_TMA),
-    SG_WS_ENTRY("ws_64x64x32_s4_Acp_Btma", 64, 64, 4, LOAD_CPASYNC, LOAD_TMA),
-    SG_WS_ENTRY("ws_64x64x32_s4_Atma_Bcp", 64, 64, 4, LOAD_TMA, LOAD_CPASYNC),
-    SG_WS_ENTRY("ws_64x64x32_s4_Acp_Bcp", 64, 64, 4, LOAD_CPASYNC, LOAD_CPASYNC),
-};
+static const KernelFamily kFamily = SG_FAMILY("ws_64x64x32_s4", 64, 64, 4, 0, 0, 2, 0);
 
-const KernelEntry* ws_kernels_64x64() { return kTable; }
+const KernelFamily* family_64x64() { return &kFamily; }
 
 }  // namespace sg

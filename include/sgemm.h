@@ -120,13 +120,22 @@ SGEMM_API int sgemm_plan(int64_t M, int64_t N, int64_t K, float alpha, const flo
 /*
  * sgemm_set_config — force a kernel configuration for later calls in this
  * process (for sweeps and tests). `name` is "auto" (default), "128x128" or
- * "64x64" for the CTA tile, optionally followed by ":cpasync" to load both
+ * "64x64" for the CTA tile, or one of the family names sgemm_config_names
+ * lists, optionally followed by ":cpasync" to load both
  * operands with cp.async even when TMA could be used (e.g.
  * "128x128:cpasync", or "auto:cpasync"). Returns SGEMM_ERR_INVALID_VALUE
  * for an unknown name. The environment variable SGEMM_FORCE_CONFIG, read on
  * the first call, sets the same thing.
  */
 SGEMM_API int sgemm_set_config(const char* name);
+
+/*
+ * sgemm_config_names — write the names sgemm_set_config accepts besides
+ * "auto", "128x128" and "64x64" (every compiled kernel family, comma
+ * separated, NUL-terminated) into buf (at most buflen bytes). Returns
+ * SGEMM_ERR_INVALID_VALUE if buf is NULL or too small.
+ */
+SGEMM_API int sgemm_config_names(char* buf, int buflen);
 
 /*
  * sgemm_set_wait_timeout_ns — limit on every bounded mbarrier wait inside

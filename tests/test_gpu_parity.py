@@ -241,3 +241,47 @@ def test_workload_ragged_every_element():
 
 def test_workload_llm_projection_sampled():
     _workload("llm_8192x14336x4096", full=False)
+
+
+# ---- every compiled kernel family (tuning alternatives included) ------------
+
+def _family_names():
+    rc, names = sg.sgemm_config_names()
+    assert rc == 0 and names
+    return names
+
+
+@pytest.mark.parametrize("cp", ["", ":cpasync"])
+def test_every_family_matches_oracle(cp):
+    for name in _family_names():
+        assert sg.sgemm_set_config(name + cp) == 0, name
+        try:
+            for (M, N, K) in [(129, 257, 95), (256, 128, 64), (7, 300, 33)]:
+                A, B, C0 = gen(M, N, K, seed=M + N + K)
+                C, guards, plan = gpu_util.run(0.7, A, B, -1.3, C0)
+                assert guards, (name, plan)
+                assert plan[0].startswith(name), (name, plan)
+                check_full(0.7, A, B, -1.3, C0, C)
+        finally:
+            sg.sgemm_set_config("auto")
+
+
+def test_families_agree_bitwise():
+    # Every family accumulates each output in the same k order with FFMA, so
+    # they must agree bit for bit (only the schedule differs).
+    torch = pytest.importorskip("torch")
+    M, N, K = 640, 512, 768
+    A, B, C0 = gen(M, N, K, seed=77)
+    dA = torch.from_numpy(A).cuda()
+    dB = torch.from_numpy(B).cuda()
+    outs = {}
+    for name in _family_names():
+        assert sg.sgemm_set_config(name) == 0
+        dC = torch.from_numpy(C0).cuda()
+        sg.sgemm_tensors(0.7, dA, dB, -1.3, dC)
+        sg.check_status()
+        outs[name] = dC.cpu().numpy()
+    sg.sgemm_set_config("auto")
+    names = list(outs)
+    for n in names[1:]:
+        assert np.array_equal(outs[names[0]], outs[n]), (names[0], n)
