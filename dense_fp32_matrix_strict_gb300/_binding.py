@@ -170,8 +170,37 @@ def _ld(t, rows, cols, name):
 def _stream_handle(stream, device):
     import torch
     if stream is None:
-        stream = torch.cuda.current_stream(device)
+        idx = device.index if hasattr(device, "index") else device
+        if idx is None:
+            idx = torch.cuda.current_device()
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:
+            return int(raw(idx))
+        stream = torch.cuda.current_stream(idx)
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+class _on_device:
+    """Make `device` current for the duration of a call (no-op if it is)."""
+
+    def __init__(self, device):
+        import torch
+        self.idx = device.index if device.index is not None else torch.cuda.current_device()
+        self.prev = None
+
+    def __enter__(self):
+        import torch
+        cur = torch.cuda.current_device()
+        if cur != self.idx:
+            self.prev = cur
+            torch.cuda.set_device(self.idx)
+        return self
+
+    def __exit__(self, *exc):
+        if self.prev is not None:
+            import torch
+            torch.cuda.set_device(self.prev)
+        return False
 
 
 def sgemm_tensors(alpha, A, B, beta, C, stream=None) -> None:
@@ -190,19 +219,18 @@ def sgemm_tensors(alpha, A, B, beta, C, stream=None) -> None:
     ldc = _ld(C, M, N, "C")
     if not (A.device == B.device == C.device):
         raise ValueError("A, B and C must be on the same device")
-    import torch
-    with torch.cuda.device(C.device):
-        rc = sgemm(M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(), ldb, float(beta),
-                   C.data_ptr(), ldc, _stream_handle(stream, C.device))
-    _check("sgemm", rc)
+    with _on_device(C.device):
+        rc = load().sgemm(M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(), ldb,
+                          float(beta), C.data_ptr(), ldc, _stream_handle(stream, C.device))
+    if rc != SGEMM_OK:
+        raise SgemmError("sgemm", rc)
 
 
 def plan_tensors(alpha, A, B, beta, C):
     """Kernel name and grid sgemm_tensors would use for these tensors."""
     M, K = A.shape
     N = B.shape[1]
-    import torch
-    with torch.cuda.device(C.device):
+    with _on_device(C.device):
         rc, name, grid = sgemm_plan(M, N, K, float(alpha), A.data_ptr(), _ld(A, M, K, "A"),
                                     B.data_ptr(), _ld(B, K, N, "B"), float(beta), C.data_ptr(),
                                     _ld(C, M, N, "C"))

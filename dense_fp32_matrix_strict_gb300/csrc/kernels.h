@@ -33,32 +33,42 @@ cudaError_t ws_launch(const CUtensorMap* tmA, const CUtensorMap* tmB, const Gemm
     return cudaGetLastError();
 }
 
+// The stream-K fixup for a BM x BN tile: one CTA per stream-K tile.
+template <int BM, int BN>
+cudaError_t fixup_launch(const GemmParams* p, int sk_tiles, cudaStream_t stream) {
+    sk_fixup_kernel<BM, BN><<<sk_tiles, 256, 0, stream>>>(*p);
+    return cudaGetLastError();
+}
+
 // One kernel family: a CTA tile and tuning knobs, instantiated for the four
-// (A, B) load-mode pairs in mode_index order.
+// (A, B) load-mode pairs in mode_index order, plus its stream-K fixup.
 struct KernelFamily {
     const char* name;
     int bm, bn;
     KernelEntry modes[4];
+    cudaError_t (*fixup)(const GemmParams* p, int sk_tiles, cudaStream_t stream);
 };
 
 // Index into a family's modes: TMA/TMA, CP/TMA, TMA/CP, CP/CP.
 inline constexpr int mode_index(int a_mode, int b_mode) { return a_mode + 2 * b_mode; }
 
-template <int BM, int BN, int S, int AM, int BMD, int LMAP, int XPF, int FORDER, int ISSUE>
+template <int BM, int BN, int S, int AM, int BMD, int FORDER>
 constexpr KernelEntry make_entry(const char* name) {
-    using C = Cfg<BM, BN, 32, S, AM, BMD, LMAP, XPF, FORDER, ISSUE>;
+    using C = Cfg<BM, BN, 32, S, AM, BMD, FORDER>;
     return KernelEntry{name, BM, BN, 32, S, AM, BMD, C::THREADS, C::SMEM_BYTES,
                        &ws_prepare<C>, &ws_launch<C>};
 }
 
-#define SG_FAMILY(NAME, BM, BN, S, LMAP, XPF, FORDER, ISSUE)                                      \
-    KernelFamily {                                                                               \
-        NAME, BM, BN, {                                                                          \
-            make_entry<BM, BN, S, LOAD_TMA, LOAD_TMA, LMAP, XPF, FORDER, ISSUE>(NAME "_Atma_Btma"),  \
-            make_entry<BM, BN, S, LOAD_CPASYNC, LOAD_TMA, LMAP, XPF, FORDER, ISSUE>(NAME "_Acp_Btma"), \
-            make_entry<BM, BN, S, LOAD_TMA, LOAD_CPASYNC, LMAP, XPF, FORDER, ISSUE>(NAME "_Atma_Bcp"), \
-            make_entry<BM, BN, S, LOAD_CPASYNC, LOAD_CPASYNC, LMAP, XPF, FORDER, ISSUE>(NAME "_Acp_Bcp") \
-        }                                                                                        \
+#define SG_FAMILY(NAME, BM, BN, S, FORDER)                                                  \
+    KernelFamily {                                                                          \
+        NAME, BM, BN,                                                                       \
+            {                                                                               \
+                make_entry<BM, BN, S, LOAD_TMA, LOAD_TMA, FORDER>(NAME "_Atma_Btma"),         \
+                make_entry<BM, BN, S, LOAD_CPASYNC, LOAD_TMA, FORDER>(NAME "_Acp_Btma"),      \
+                make_entry<BM, BN, S, LOAD_TMA, LOAD_CPASYNC, FORDER>(NAME "_Atma_Bcp"),      \
+                make_entry<BM, BN, S, LOAD_CPASYNC, LOAD_CPASYNC, FORDER>(NAME "_Acp_Bcp"),   \
+            },                                                                              \
+            &fixup_launch<BM, BN>                                                           \
     }
 
 // Families, one translation unit each (compiled in parallel). The first two

@@ -1,6 +1,7 @@
 // sgemm_api.cu — the C ABI: argument checks, per-device set-up, kernel plan
-// (CTA tile, TMA or cp.async per operand, persistent grid), TMA descriptor
-// encoding, and launches on the caller's stream.
+// (CTA tile, TMA or cp.async per operand, persistent grid, data-parallel +
+// stream-K schedule), TMA descriptor encoding, and launches on the caller's
+// stream.
 #include <atomic>
 #include <cstdint>
 #include <cstdio>
@@ -13,13 +14,13 @@
 #include <cuda_runtime.h>
 
 #include "sgemm.h"
-#include "kernels.h"
+#include "sgemm_internal.h"
 
 namespace sg {
+
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kMaxFamilies = 32;
 constexpr int kStatusBytes = 256;
 
 // All compiled kernel families: [0] 128x128 and [1] 64x64 are what "auto"
@@ -41,37 +42,52 @@ const Registry& registry() {
     return r;
 }
 
-struct DeviceState {
+struct DeviceSlot {
     bool ready = false;
     int error = SGEMM_OK;
-    int sm_count = 0;
-    int* status = nullptr;                 // device status word (256 bytes)
-    int ctas_per_sm[kMaxFamilies][4] = {};
+    DeviceInfo info;
+};
+
+// Memory the regular entry points own on a device: the status word and a
+// library-private stream-ordered pool for stream-K workspaces.
+struct DeviceMemory {
+    bool ready = false;
+    int* status = nullptr;
+    cudaMemPool_t pool = nullptr;
 };
 
 std::mutex g_mu;
-DeviceState g_dev[kMaxDevices];
+DeviceSlot g_dev[kMaxDevices];
+DeviceMemory g_mem[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 bool g_env_read = false;
 
-// Forced configuration: family index (-1 = auto); cp = force cp.async loads.
+// Forced configuration: family index (-1 = auto); cp = force cp.async loads;
+// sk = -1 auto, 0 never use the stream-K tail.
 std::atomic<int> g_force_family{-1};
 std::atomic<int> g_force_cp{0};
+std::atomic<int> g_force_sk{-1};
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 
 thread_local int t_last_cuda_error = 0;
 
-int parse_config(const char* name, int* family, int* cp) {
+// "<family>[:cpasync][:dp]" with <family> one of auto, 128x128, 64x64 or a
+// registry name.
+int parse_config(const char* name, int* family, int* cp, int* sk) {
     if (name == nullptr) return SGEMM_ERR_INVALID_VALUE;
-    char buf[96];
+    char buf[128];
     std::strncpy(buf, name, sizeof(buf) - 1);
     buf[sizeof(buf) - 1] = '\0';
-    int want_cp = 0;
-    char* colon = std::strchr(buf, ':');
-    if (colon != nullptr) {
-        if (std::strcmp(colon + 1, "cpasync") != 0) return SGEMM_ERR_INVALID_VALUE;
-        want_cp = 1;
-        *colon = '\0';
+    int want_cp = 0, want_sk = -1;
+    char* mod = std::strchr(buf, ':');
+    if (mod != nullptr) *mod++ = '\0';
+    while (mod != nullptr) {
+        char* next = std::strchr(mod, ':');
+        if (next != nullptr) *next++ = '\0';
+        if (std::strcmp(mod, "cpasync") == 0) want_cp = 1;
+        else if (std::strcmp(mod, "dp") == 0) want_sk = 0;
+        else return SGEMM_ERR_INVALID_VALUE;
+        mod = next;
     }
     int f = -2;
     if (std::strcmp(buf, "auto") == 0 || buf[0] == '\0') f = -1;
@@ -85,34 +101,152 @@ int parse_config(const char* name, int* family, int* cp) {
     if (f == -2) return SGEMM_ERR_INVALID_VALUE;
     *family = f;
     *cp = want_cp;
+    *sk = want_sk;
     return SGEMM_OK;
 }
+
+void read_env_locked() {
+    if (g_env_read) return;
+    g_env_read = true;
+    const char* env = std::getenv("SGEMM_FORCE_CONFIG");
+    int fam = -1, cp = 0, sk = -1;
+    if (env != nullptr && parse_config(env, &fam, &cp, &sk) == SGEMM_OK) {
+        g_force_family = fam;
+        g_force_cp = cp;
+        g_force_sk = sk;
+    }
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// [lo, hi) byte range of a rows x cols matrix with leading dimension ld.
+void extent(const void* p, int64_t rows, int64_t cols, int64_t ld, uintptr_t* lo, uintptr_t* hi) {
+    *lo = reinterpret_cast<uintptr_t>(p);
+    *hi = *lo + static_cast<uintptr_t>(((rows - 1) * ld + cols) * 4);
+}
+
+// 2-D row-major fp32 tensor map: rows x cols, row stride ld floats, box of
+// box_rows x box_cols, optional 128-byte swizzle. Returns false if the
+// driver rejects it.
+bool encode_2d(CUtensorMap* map, const float* base, int64_t rows, int64_t cols, int64_t ld,
+               int box_rows, int box_cols, bool swizzle128) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool tma_ok(const float* p, int64_t ld, int64_t rows, int64_t cols) {
+    return aligned(p, 16) && (ld % 4) == 0 && ld < ((int64_t)1 << 38) && rows >= 1 && cols >= 1 &&
+           rows <= 0xffffffffll && cols <= 0xffffffffll;
+}
+
+// C = beta * C over an M x N matrix (beta == 0 writes zeros, never reads C).
+__global__ void scale_kernel(float* __restrict__ C, long long ldc, int M, int N, float beta) {
+    for (long long m = blockIdx.y; m < M; m += gridDim.y) {
+        float* row = C + m * ldc;
+        for (int n = blockIdx.x * blockDim.x + threadIdx.x; n < N; n += blockDim.x * gridDim.x)
+            row[n] = (beta == 0.0f) ? 0.0f : beta * row[n];
+    }
+}
+
+__global__ void wait_timeout_kernel(GemmParams p) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) wait_bounded(b, 0, p, STATUS_CONSUMER_TIMEOUT);
+}
+
+// The status word and workspace pool of the current device (allocated on
+// first use).
+int device_memory(const DeviceInfo* info, DeviceMemory** out) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceMemory& m = g_mem[info->device];
+    if (m.ready) {
+        *out = &m;
+        return SGEMM_OK;
+    }
+    cudaError_t e;
+    void* status = nullptr;
+    if ((e = cudaMalloc(&status, kStatusBytes)) != cudaSuccess) return cuda_fail(e, SGEMM_ERR_CUDA);
+    if ((e = cudaMemset(status, 0, kStatusBytes)) != cudaSuccess ||
+        (e = cudaDeviceSynchronize()) != cudaSuccess) {
+        cudaFree(status);
+        return cuda_fail(e, SGEMM_ERR_CUDA);
+    }
+    cudaMemPoolProps props;
+    std::memset(&props, 0, sizeof(props));
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = info->device;
+    cudaMemPool_t pool = nullptr;
+    if ((e = cudaMemPoolCreate(&pool, &props)) != cudaSuccess) {
+        cudaFree(status);
+        return cuda_fail(e, SGEMM_ERR_CUDA);
+    }
+    // Keep freed workspace in the pool instead of returning it at every
+    // synchronisation.
+    uint64_t keep = UINT64_MAX;
+    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    m.status = static_cast<int*>(status);
+    m.pool = pool;
+    m.ready = true;
+    *out = &m;
+    return SGEMM_OK;
+}
+
+}  // namespace
 
 int cuda_fail(cudaError_t e, int code) {
     t_last_cuda_error = static_cast<int>(e);
     return code;
 }
 
-// Per-device set-up, once per device (under the lock): properties, status
-// word, kernel attributes and occupancy, TMA encoder entry point.
-int device_setup(DeviceState** out) {
+int check_args(int64_t M, int64_t N, int64_t K, float alpha, const float* A, int64_t lda,
+               const float* B, int64_t ldb, const float* C, int64_t ldc) {
+    const int64_t kMax = 0x7fffffff;
+    if (M < 0 || N < 0 || K < 0 || M > kMax || N > kMax || K > kMax) return SGEMM_ERR_INVALID_VALUE;
+    if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
+        return SGEMM_ERR_INVALID_VALUE;
+    // Offsets up to rows * ld must fit comfortably in int64 bytes.
+    const int64_t kOff = (int64_t)1 << 60;
+    if ((M > 0 && lda > kOff / M) || (K > 0 && ldb > kOff / K) || (M > 0 && ldc > kOff / M))
+        return SGEMM_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    if (C == nullptr || !aligned(C, 4)) return SGEMM_ERR_INVALID_VALUE;
+    const bool reads_ab = (alpha != 0.0f) && (K > 0);
+    if (reads_ab) {
+        if (A == nullptr || B == nullptr || !aligned(A, 4) || !aligned(B, 4))
+            return SGEMM_ERR_INVALID_VALUE;
+        uintptr_t clo, chi, lo, hi;
+        extent(C, M, N, ldc, &clo, &chi);
+        extent(A, M, K, lda, &lo, &hi);
+        if (lo < chi && clo < hi) return SGEMM_ERR_INVALID_VALUE;
+        extent(B, K, N, ldb, &lo, &hi);
+        if (lo < chi && clo < hi) return SGEMM_ERR_INVALID_VALUE;
+    }
+    return SGEMM_OK;
+}
+
+int device_info(const DeviceInfo** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_CUDA);
     if (dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_UNSUPPORTED_DEVICE;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_env_read) {
-        g_env_read = true;
-        const char* env = std::getenv("SGEMM_FORCE_CONFIG");
-        int fam = -1, cp = 0;
-        if (env != nullptr && parse_config(env, &fam, &cp) == SGEMM_OK) {
-            g_force_family = fam;
-            g_force_cp = cp;
-        }
-    }
-    DeviceState& st = g_dev[dev];
+    read_env_locked();
+    DeviceSlot& st = g_dev[dev];
     if (st.ready) {
-        *out = &st;
+        *out = &st.info;
         return SGEMM_OK;
     }
     if (st.error != SGEMM_OK) return st.error;
@@ -147,108 +281,55 @@ int device_setup(DeviceState** out) {
                 (void)cudaGetLastError();
                 n = 0;
             }
-            st.ctas_per_sm[f][m] = n;
+            st.info.ctas_per_sm[f][m] = n;
         }
     }
-    void* status = nullptr;
-    if ((e = cudaMalloc(&status, kStatusBytes)) != cudaSuccess) return cuda_fail(e, SGEMM_ERR_CUDA);
-    if ((e = cudaMemset(status, 0, kStatusBytes)) != cudaSuccess) {
-        cudaFree(status);
-        return cuda_fail(e, SGEMM_ERR_CUDA);
-    }
-    if ((e = cudaDeviceSynchronize()) != cudaSuccess) {
-        cudaFree(status);
-        return cuda_fail(e, SGEMM_ERR_CUDA);
-    }
-    st.status = static_cast<int*>(status);
-    st.sm_count = sms;
+    st.info.device = dev;
+    st.info.sm_count = sms;
     st.ready = true;
-    *out = &st;
+    *out = &st.info;
     return SGEMM_OK;
 }
 
-bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-// [lo, hi) byte range of a rows x cols matrix with leading dimension ld.
-void extent(const void* p, int64_t rows, int64_t cols, int64_t ld, uintptr_t* lo, uintptr_t* hi) {
-    *lo = reinterpret_cast<uintptr_t>(p);
-    *hi = *lo + static_cast<uintptr_t>(((rows - 1) * ld + cols) * 4);
-}
-
-int check_args(int64_t M, int64_t N, int64_t K, float alpha, const float* A, int64_t lda,
-               const float* B, int64_t ldb, const float* C, int64_t ldc) {
-    const int64_t kMax = 0x7fffffff;
-    if (M < 0 || N < 0 || K < 0 || M > kMax || N > kMax || K > kMax) return SGEMM_ERR_INVALID_VALUE;
-    if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
-        return SGEMM_ERR_INVALID_VALUE;
-    // Offsets up to rows * ld must fit comfortably in int64 bytes.
-    const int64_t kOff = (int64_t)1 << 60;
-    if ((M > 0 && lda > kOff / M) || (K > 0 && ldb > kOff / K) || (M > 0 && ldc > kOff / M))
-        return SGEMM_ERR_INVALID_VALUE;
-    if (M == 0 || N == 0) return SGEMM_OK;
-    if (C == nullptr || !aligned(C, 4)) return SGEMM_ERR_INVALID_VALUE;
-    const bool reads_ab = (alpha != 0.0f) && (K > 0);
-    if (reads_ab) {
-        if (A == nullptr || B == nullptr || !aligned(A, 4) || !aligned(B, 4))
-            return SGEMM_ERR_INVALID_VALUE;
-        uintptr_t clo, chi, lo, hi;
-        extent(C, M, N, ldc, &clo, &chi);
-        extent(A, M, K, lda, &lo, &hi);
-        if (lo < chi && clo < hi) return SGEMM_ERR_INVALID_VALUE;
-        extent(B, K, N, ldb, &lo, &hi);
-        if (lo < chi && clo < hi) return SGEMM_ERR_INVALID_VALUE;
-    }
-    return SGEMM_OK;
-}
-
-// 2-D row-major fp32 tensor map: rows x cols, row stride ld floats, box of
-// box_rows x box_cols, optional 128-byte swizzle. Returns false if the
-// driver rejects it.
-bool encode_2d(CUtensorMap* map, const float* base, int64_t rows, int64_t cols, int64_t ld,
-               int box_rows, int box_cols, bool swizzle128) {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims,
-                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
-bool tma_ok(const float* p, int64_t ld, int64_t rows, int64_t cols) {
-    return aligned(p, 16) && (ld % 4) == 0 && ld < ((int64_t)1 << 38) && rows >= 1 && cols >= 1 &&
-           rows <= 0xffffffffll && cols <= 0xffffffffll;
-}
-
-struct Plan {
-    int kind = 0;                 // 0: none, 1: scale, 2: gemm
-    const KernelEntry* k = nullptr;
-    CUtensorMap tmA, tmB;
-    GemmParams p;
-    int grid = 0;
-};
-
-int make_plan(DeviceState* st, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
-              int64_t lda, const float* B, int64_t ldb, float beta, const float* C, int64_t ldc,
-              Plan* pl) {
+int make_plan(const DeviceInfo* dev, int64_t M, int64_t N, int64_t K, float alpha,
+              const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
+              const float* C, int64_t ldc, bool allow_sk, Plan* pl) {
     if (M == 0 || N == 0) {
         pl->kind = 0;
         return SGEMM_OK;
     }
     if (alpha == 0.0f || K == 0) {
         pl->kind = 1;
+        GemmParams& p = pl->p;
+        std::memset(&p, 0, sizeof(p));
+        p.M = static_cast<int>(M);
+        p.N = static_cast<int>(N);
+        p.C = const_cast<float*>(C);
+        p.ldc = ldc;
+        p.beta = beta;
         return SGEMM_OK;
     }
     pl->kind = 2;
-    const int sms = st->sm_count;
+    const int sms = dev->sm_count;
     int fi = g_force_family.load();
     if (fi < 0) {
+        // The 128 x 128 tile with the stream-K tail keeps every SM busy even
+        // for small grids. Below two k-iterations of 128 x 128 x 32 per SM
+        // the second launch and the workspace cost more than they save, so
+        // such problems (and any problem when stream-K is off whose 128 x 128
+        // grid would leave most SMs idle) take the 64 x 64 family without it.
         const int64_t tiles128 = ((M + 127) / 128) * ((N + 127) / 128);
-        fi = (tiles128 * 2 >= sms) ? 0 : 1;
+        const int64_t iters128 = tiles128 * ((K + 31) / 32);
+        const bool sk_possible = allow_sk && g_force_sk.load() != 0;
+        if (sk_possible && iters128 >= 2 * static_cast<int64_t>(sms)) {
+            fi = 0;
+        } else {
+            fi = (tiles128 * 2 >= sms) ? 0 : 1;
+            if (fi == 1) allow_sk = false;
+        }
     }
     const KernelFamily* fam = registry().fam[fi];
+    pl->fam = fam;
     const int bm = fam->bm, bn = fam->bn, bk = 32;
     const bool force_cp = g_force_cp.load() != 0;
     std::memset(&pl->tmA, 0, sizeof(CUtensorMap));
@@ -262,6 +343,7 @@ int make_plan(DeviceState* st, int64_t M, int64_t N, int64_t K, float alpha, con
     pl->k = &fam->modes[mi];
 
     GemmParams& p = pl->p;
+    std::memset(&p, 0, sizeof(p));
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
@@ -279,36 +361,80 @@ int make_plan(DeviceState* st, int64_t M, int64_t N, int64_t K, float alpha, con
     p.alpha = alpha;
     p.beta = beta;
     p.timeout_ns = g_timeout_ns.load();
-    p.status = st->status;
     const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
     if (tiles > 0x7fffffffll) return SGEMM_ERR_INVALID_VALUE;
-    if (st->ctas_per_sm[fi][mi] <= 0) return cuda_fail(cudaErrorInvalidConfiguration, SGEMM_ERR_LAUNCH);
-    const int64_t slots = static_cast<int64_t>(st->ctas_per_sm[fi][mi]) * sms;
-    pl->grid = static_cast<int>(tiles < slots ? tiles : slots);
+    if (dev->ctas_per_sm[fi][mi] <= 0) return cuda_fail(cudaErrorInvalidConfiguration, SGEMM_ERR_LAUNCH);
+    const int64_t cap = static_cast<int64_t>(dev->ctas_per_sm[fi][mi]) * sms;
+
+    // Schedule: whole waves data-parallel; the last, partial wave's
+    // k-iterations spread over the CTAs (stream-K) unless it is nearly full.
+    const int64_t waves = tiles / cap, rest = tiles % cap;
+    const bool use_sk = allow_sk && g_force_sk.load() != 0 && rest != 0 &&
+                        (waves == 0 || rest * 10 < cap * 9);
+    if (!use_sk) {
+        p.dp_tiles = static_cast<int>(tiles);
+        p.sk_ctas = 0;
+        p.sk_iters = 0;
+        pl->grid = static_cast<int>(tiles < cap ? tiles : cap);
+        pl->sk_tiles = 0;
+        pl->ws_bytes = 0;
+        return SGEMM_OK;
+    }
+    const int64_t S = rest * p.k_tiles;
+    // A range is at least k_tiles / 32 iterations long, so no tile has more
+    // than 34 partial segments (the fixup handles up to kSkMaxParts).
+    const int64_t min_len = (p.k_tiles + 31) / 32;
+    int64_t G = S / min_len;
+    if (G > cap) G = cap;
+    if (G < 1) G = 1;
+    p.dp_tiles = static_cast<int>(waves * cap);
+    p.sk_ctas = static_cast<int>(G);
+    p.sk_iters = S;
+    pl->grid = static_cast<int>(waves > 0 ? cap : G);
+    pl->sk_tiles = static_cast<int>(rest);
+    pl->ws_bytes = static_cast<size_t>(2 * G) * static_cast<size_t>(bm) * bn * sizeof(float);
     return SGEMM_OK;
 }
 
-// C = beta * C over an M x N matrix (beta == 0 writes zeros, never reads C).
-__global__ void scale_kernel(float* __restrict__ C, long long ldc, int M, int N, float beta) {
-    for (long long m = blockIdx.y; m < M; m += gridDim.y) {
-        float* row = C + m * ldc;
-        for (int n = blockIdx.x * blockDim.x + threadIdx.x; n < N; n += blockDim.x * gridDim.x)
-            row[n] = (beta == 0.0f) ? 0.0f : beta * row[n];
+int launch_plan(Plan* pl, int* status, float* ws, cudaStream_t stream) {
+    cudaError_t e = cudaSuccess;
+    if (pl->kind == 0) return SGEMM_OK;
+    if (pl->kind == 1) {
+        const GemmParams& p = pl->p;
+        const int bx = p.N < 256 * 16 ? (p.N + 255) / 256 : 16;
+        const int by = p.M < 4096 ? p.M : 4096;
+        scale_kernel<<<dim3(bx, by), 256, 0, stream>>>(p.C, p.ldc, p.M, p.N, p.beta);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
+        return SGEMM_OK;
     }
+    pl->p.status = status;
+    pl->p.ws = ws;
+    if (pl->ws_bytes > 0 && ws == nullptr) return SGEMM_ERR_INVALID_VALUE;
+    e = pl->k->launch(&pl->tmA, &pl->tmB, &pl->p, pl->grid, stream);
+    if (e == cudaSuccess && pl->sk_tiles > 0) e = pl->fam->fixup(&pl->p, pl->sk_tiles, stream);
+    if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
+    return SGEMM_OK;
 }
 
-__global__ void wait_timeout_kernel(GemmParams p) {
-    __shared__ __align__(8) uint64_t bar;
-    const uint32_t b = smem_u32(&bar);
-    if (threadIdx.x == 0) {
-        mbar_init(b, 1);
-        fence_barrier_init();
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) wait_bounded(b, 0, p, STATUS_CONSUMER_TIMEOUT);
+void plan_name(const Plan& pl, char* buf, int buflen) {
+    if (buf == nullptr || buflen <= 0) return;
+    if (pl.kind == 0) std::snprintf(buf, static_cast<size_t>(buflen), "none");
+    else if (pl.kind == 1) std::snprintf(buf, static_cast<size_t>(buflen), "scale");
+    else std::snprintf(buf, static_cast<size_t>(buflen), "%s%s", pl.k->name, pl.sk_tiles > 0 ? "+sk" : "");
 }
 
-}  // namespace
+int launch_selftest_wait(unsigned long long timeout_ns, int* status, cudaStream_t stream) {
+    GemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.timeout_ns = timeout_ns;
+    p.status = status;
+    wait_timeout_kernel<<<1, 32, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
+    return SGEMM_OK;
+}
+
 }  // namespace sg
 
 using namespace sg;
@@ -319,23 +445,31 @@ extern "C" int sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float* 
     int rc = check_args(M, N, K, alpha, A, lda, B, ldb, C, ldc);
     if (rc != SGEMM_OK) return rc;
     if (M == 0 || N == 0) return SGEMM_OK;
-    DeviceState* st = nullptr;
-    if ((rc = device_setup(&st)) != SGEMM_OK) return rc;
+    const DeviceInfo* dev = nullptr;
+    if ((rc = device_info(&dev)) != SGEMM_OK) return rc;
+    DeviceMemory* mem = nullptr;
+    if ((rc = device_memory(dev, &mem)) != SGEMM_OK) return rc;
     Plan pl;
-    if ((rc = make_plan(st, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, &pl)) != SGEMM_OK)
+    if ((rc = make_plan(dev, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, true, &pl)) != SGEMM_OK)
         return rc;
-    cudaError_t e;
-    if (pl.kind == 1) {
-        const int bx = static_cast<int>(N < 256 * 16 ? (N + 255) / 256 : 16);
-        const int by = static_cast<int>(M < 4096 ? M : 4096);
-        scale_kernel<<<dim3(bx, by), 256, 0, stream>>>(C, ldc, static_cast<int>(M),
-                                                       static_cast<int>(N), beta);
-        e = cudaGetLastError();
-    } else {
-        e = pl.k->launch(&pl.tmA, &pl.tmB, &pl.p, pl.grid, stream);
+    float* ws = nullptr;
+    if (pl.ws_bytes > 0) {
+        // Stream-ordered workspace from the library's pool: concurrent calls
+        // on different streams never share it, and stream capture records it
+        // as an allocation node.
+        void* w = nullptr;
+        if (cudaMallocFromPoolAsync(&w, pl.ws_bytes, mem->pool, stream) != cudaSuccess) {
+            (void)cudaGetLastError();
+            if ((rc = make_plan(dev, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, false, &pl)) !=
+                SGEMM_OK)
+                return rc;
+        } else {
+            ws = static_cast<float*>(w);
+        }
     }
-    if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
-    return SGEMM_OK;
+    rc = launch_plan(&pl, mem->status, ws, stream);
+    if (ws != nullptr) cudaFreeAsync(ws, stream);
+    return rc;
 }
 
 extern "C" int sgemm_plan(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
@@ -343,37 +477,30 @@ extern "C" int sgemm_plan(int64_t M, int64_t N, int64_t K, float alpha, const fl
                           int64_t ldc, char* buf, int buflen, int* grid) {
     int rc = check_args(M, N, K, alpha, A, lda, B, ldb, C, ldc);
     if (rc != SGEMM_OK) return rc;
-    const char* name = "none";
-    int g = 0;
     Plan pl;
     if (M != 0 && N != 0) {
-        DeviceState* st = nullptr;
-        if ((rc = device_setup(&st)) != SGEMM_OK) return rc;
-        if ((rc = make_plan(st, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, &pl)) != SGEMM_OK)
+        const DeviceInfo* dev = nullptr;
+        if ((rc = device_info(&dev)) != SGEMM_OK) return rc;
+        if ((rc = make_plan(dev, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, true, &pl)) !=
+            SGEMM_OK)
             return rc;
-        if (pl.kind == 1) name = "scale";
-        if (pl.kind == 2) {
-            name = pl.k->name;
-            g = pl.grid;
-        }
     }
-    if (buf != nullptr && buflen > 0) {
-        std::strncpy(buf, name, static_cast<size_t>(buflen) - 1);
-        buf[buflen - 1] = '\0';
-    }
-    if (grid != nullptr) *grid = g;
+    plan_name(pl, buf, buflen);
+    if (grid != nullptr) *grid = pl.kind == 2 ? pl.grid : 0;
     return SGEMM_OK;
 }
 
 extern "C" int sgemm_check_status(cudaStream_t stream, int* bits) {
-    DeviceState* st = nullptr;
-    int rc = device_setup(&st);
+    const DeviceInfo* dev = nullptr;
+    int rc = device_info(&dev);
     if (rc != SGEMM_OK) return rc;
+    DeviceMemory* mem = nullptr;
+    if ((rc = device_memory(dev, &mem)) != SGEMM_OK) return rc;
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_CUDA);
     int v = 0;
-    if ((e = cudaMemcpyAsync(&v, st->status, sizeof(int), cudaMemcpyDeviceToHost, stream)) != cudaSuccess ||
-        (e = cudaMemsetAsync(st->status, 0, sizeof(int), stream)) != cudaSuccess ||
+    if ((e = cudaMemcpyAsync(&v, mem->status, sizeof(int), cudaMemcpyDeviceToHost, stream)) != cudaSuccess ||
+        (e = cudaMemsetAsync(mem->status, 0, sizeof(int), stream)) != cudaSuccess ||
         (e = cudaStreamSynchronize(stream)) != cudaSuccess)
         return cuda_fail(e, SGEMM_ERR_CUDA);
     if (bits != nullptr) *bits = v;
@@ -395,8 +522,8 @@ extern "C" const char* sgemm_error_string(int code) {
 extern "C" int sgemm_last_cuda_error(void) { return t_last_cuda_error; }
 
 extern "C" int sgemm_set_config(const char* name) {
-    int fam = -1, cp = 0;
-    int rc = parse_config(name, &fam, &cp);
+    int fam = -1, cp = 0, sk = -1;
+    int rc = parse_config(name, &fam, &cp, &sk);
     if (rc != SGEMM_OK) return rc;
     {
         std::lock_guard<std::mutex> lock(g_mu);
@@ -404,6 +531,7 @@ extern "C" int sgemm_set_config(const char* name) {
     }
     g_force_family = fam;
     g_force_cp = cp;
+    g_force_sk = sk;
     return SGEMM_OK;
 }
 
@@ -431,28 +559,22 @@ extern "C" int sgemm_set_wait_timeout_ns(uint64_t ns) {
 
 extern "C" int sgemm_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stream) {
     if (timeout_ns < 1000 || timeout_ns > 10000000000ull) return SGEMM_ERR_INVALID_VALUE;
-    DeviceState* st = nullptr;
-    int rc = device_setup(&st);
+    const DeviceInfo* dev = nullptr;
+    int rc = device_info(&dev);
     if (rc != SGEMM_OK) return rc;
-    GemmParams p;
-    std::memset(&p, 0, sizeof(p));
-    p.timeout_ns = timeout_ns;
-    p.status = st->status;
-    wait_timeout_kernel<<<1, 32, 0, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
-    return SGEMM_OK;
+    DeviceMemory* mem = nullptr;
+    if ((rc = device_memory(dev, &mem)) != SGEMM_OK) return rc;
+    return launch_selftest_wait(timeout_ns, mem->status, stream);
 }
 
-// Shared with fp32_peak.cu: per-device readiness check without the lock
-// dance duplicated there.
+// Used by fp32_peak.cu.
 int sgemm_internal_device_ready() {
-    DeviceState* st = nullptr;
-    return device_setup(&st);
+    const DeviceInfo* dev = nullptr;
+    return device_info(&dev);
 }
 int sgemm_internal_sm_count() {
-    DeviceState* st = nullptr;
-    if (device_setup(&st) != SGEMM_OK) return 0;
-    return st->sm_count;
+    const DeviceInfo* dev = nullptr;
+    if (device_info(&dev) != SGEMM_OK) return 0;
+    return dev->sm_count;
 }
 void sgemm_internal_set_cuda_error(int e) { t_last_cuda_error = e; }

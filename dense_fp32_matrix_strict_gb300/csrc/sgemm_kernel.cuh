@@ -1,9 +1,10 @@
 // sgemm_kernel.cuh — the warp-specialised strict-FP32 SGEMM kernel for sm_103a.
 //
 // C = alpha * A * B + beta * C, row-major A (M x K, lda), B (K x N, ldb),
-// C (M x N, ldc); every multiply-add is one FFMA on the FP32 CUDA cores.
+// C (M x N, ldc); every multiply-add is a single-rounding FP32 FMA on the
+// CUDA cores (scalar FFMA or the packed two-lane FFMA2).
 //
-// Structure (one persistent CTA per SM, static tile schedule):
+// Structure (persistent CTAs, one per SM for the 128 x 128 tile):
 //   * producer warp(s) fill an S-deep ring of shared-memory stages, each a
 //     BM x BK tile of A and a BK x BN tile of B. An operand whose base and
 //     row stride are 16-byte aligned is moved by TMA (cp.async.bulk.tensor,
@@ -17,16 +18,25 @@
 //     float4 stores where C allows it, masked scalar stores elsewhere; C is
 //     not read when beta == 0.
 //
+// Work schedule (hybrid data-parallel + stream-K): the first dp_tiles tiles
+// are whole work items handed out round-robin (tile = CTA + wave * grid).
+// The k-iterations of the remaining tiles are split into sk_ctas equal
+// contiguous ranges, one per CTA, so the last, partial wave costs a fraction
+// of a tile instead of a whole one. A range segment that does not cover a
+// whole tile writes its raw partial sums to a workspace slot; sk_fixup_kernel
+// then adds each split tile's partials in k order and applies the epilogue.
+// No CTA ever waits for another.
+//
 // The pages this follows ("The road to a fast GEMM": sections "v4:
 // two-dimensional register tiling", "v5: vectorized loads", "Where to go
-// next" on double buffering, multi-stage pipelines and warp tiling; the
-// Tinyforge README on BK = 16 + padding and XOR swizzling; the T4 article's
-// "Tiling" section on zero-filled tails) use __syncthreads double buffering
-// on sm_75..sm_89. Here the ring is deeper, the barriers are mbarriers, the
-// loads are TMA where the strides allow it, and A stays row-major in shared
-// memory with the 128-byte TMA swizzle instead of a transposing store: each
-// lane reads float4 runs along k for its 8 rows, which costs the same number
-// of shared loads per FFMA as a transposed copy.
+// next" on double buffering, multi-stage pipelines, warp tiling and split-K;
+// the Tinyforge README on BK = 16 + padding and XOR swizzling; the T4
+// article's "Tiling" section on zero-filled tails) use __syncthreads double
+// buffering on sm_75..sm_89. Here the ring is deeper, the barriers are
+// mbarriers, the loads are TMA where the strides allow it, and A stays
+// row-major in shared memory with the 128-byte TMA swizzle instead of a
+// transposing store: each lane reads float4 runs along k for its 8 rows,
+// which costs the same number of shared loads per FMA as a transposed copy.
 //
 // Every mbarrier wait is bounded (globaltimer): on timeout the thread sets a
 // bit in the device status word, lets its own copies in flight land (again
@@ -42,11 +52,13 @@ namespace sg {
 
 enum LoadMode : int { LOAD_TMA = 0, LOAD_CPASYNC = 1 };
 
-// Status bits written by the kernel when a bounded wait gives up.
+// Status bits written by the kernels when a bounded wait gives up or a
+// schedule invariant fails.
 enum : int {
     STATUS_CONSUMER_TIMEOUT = 1,
     STATUS_PRODUCER_TIMEOUT = 2,
     STATUS_DRAIN_TIMEOUT = 4,
+    STATUS_SCHEDULE = 8,
 };
 
 struct GemmParams {
@@ -61,23 +73,21 @@ struct GemmParams {
     float alpha, beta;
     unsigned long long timeout_ns;
     int* status;
+    // Schedule: tiles [0, dp_tiles) are whole items; the k-iterations of
+    // tiles [dp_tiles, tiles) (sk_iters of them) are split over sk_ctas CTAs.
+    int dp_tiles;
+    int sk_ctas;
+    long long sk_iters;
+    float* ws;          // 2 * sk_ctas partial-tile slots of BM x BN floats
 };
 
-// Kernel configuration. LMAP: lane mapping (lane_grid); XPF: prefetch the
-// next stage's first fragments during the current stage's last k-group;
-// FORDER: FMA form of the outer product (0: scalar FFMA rows outer, 1: scalar
-// columns outer, 2: packed FFMA2 over column pairs).
-// ISSUE: 0 = dedicated producer warp(s); 1 = when both operands load by TMA,
-// consumer thread 0 issues the refills itself (no producer warp, so 256
-// threads and up to 255 registers per thread).
-template <int BM_, int BN_, int BK_, int STAGES_, int A_MODE_, int B_MODE_, int LMAP_ = 0,
-          int XPF_ = 0, int FORDER_ = 0, int ISSUE_ = 0>
+// Kernel configuration. FORDER: FMA form of the outer product (0: scalar
+// FFMA, 2: packed FFMA2 over column pairs).
+template <int BM_, int BN_, int BK_, int STAGES_, int A_MODE_, int B_MODE_, int FORDER_ = 2>
 struct Cfg {
     static constexpr int BM = BM_, BN = BN_, BK = BK_, STAGES = STAGES_;
     static constexpr int A_MODE = A_MODE_, B_MODE = B_MODE_;
-    static constexpr int LMAP = LMAP_, XPF = XPF_, FORDER = FORDER_;
-    static constexpr bool INLINE =
-        (ISSUE_ == 1) && (A_MODE_ == LOAD_TMA) && (B_MODE_ == LOAD_TMA);
+    static constexpr int FORDER = FORDER_;
     static_assert(BK == 32, "A rows are one 128-byte swizzle span");
     static_assert(BM % 32 == 0 && BN % 64 == 0, "warp tile is 32 x 64");
     static constexpr int WARPS_M = BM / 32, WARPS_N = BN / 64;
@@ -87,7 +97,7 @@ struct Cfg {
     static constexpr bool ANY_TMA = (A_MODE == LOAD_TMA) || (B_MODE == LOAD_TMA);
     // cp.async producers: one warp per SM sub-partition so the copy
     // instructions do not all land on one scheduler.
-    static constexpr int PRODUCER_WARPS = INLINE ? 0 : (ANY_CP ? 4 : 1);
+    static constexpr int PRODUCER_WARPS = ANY_CP ? 4 : 1;
     static constexpr int THREADS = CONSUMERS + 32 * PRODUCER_WARPS;
     static constexpr int A_BYTES = BM * BK * 4;
     static constexpr int B_BYTES = BK * BN * 4;
@@ -111,6 +121,65 @@ __device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& tm,
     tn = r / gm;
 }
 
+// ---- work schedule ----------------------------------------------------------
+
+// One work item: k-tiles [kb, ke) of tile `tile`. slot < 0: the item covers
+// the whole tile and ends in the epilogue; otherwise its raw sums go to
+// workspace slot `slot` for sk_fixup_kernel.
+struct Item {
+    int tile, kb, ke, slot;
+};
+
+// Start of stream-K range c (of sk_ctas) over sk_iters iterations.
+__device__ __forceinline__ long long sk_start(long long c, const GemmParams& p) {
+    return (c * p.sk_iters) / p.sk_ctas;
+}
+
+struct Schedule {
+    int t_dp;            // next data-parallel tile
+    long long s, i, e;   // this CTA's stream-K range [s, e), next iteration i
+
+    __device__ __forceinline__ explicit Schedule(const GemmParams& p) {
+        t_dp = static_cast<int>(blockIdx.x);
+        if (static_cast<int>(blockIdx.x) < p.sk_ctas) {
+            s = sk_start(blockIdx.x, p);
+            e = sk_start(blockIdx.x + 1, p);
+        } else {
+            s = e = 0;
+        }
+        i = s;
+    }
+
+    __device__ __forceinline__ bool next(const GemmParams& p, Item& it) {
+        if (t_dp < p.dp_tiles) {
+            it.tile = t_dp;
+            it.kb = 0;
+            it.ke = p.k_tiles;
+            it.slot = -1;
+            t_dp += static_cast<int>(gridDim.x);
+            return true;
+        }
+        if (i >= e) return false;
+        const long long u = i / p.k_tiles;
+        const int kb = static_cast<int>(i - u * p.k_tiles);
+        const long long left = e - i;
+        const int ke = left < static_cast<long long>(p.k_tiles - kb) ? kb + static_cast<int>(left)
+                                                                      : p.k_tiles;
+        it.tile = p.dp_tiles + static_cast<int>(u);
+        it.kb = kb;
+        it.ke = ke;
+        // Only the first and the last segment of a range can be partial:
+        // the first goes to slot 2c, any later one to slot 2c + 1.
+        it.slot = (kb == 0 && ke == p.k_tiles)
+                      ? -1
+                      : 2 * static_cast<int>(blockIdx.x) + (i == s ? 0 : 1);
+        i += ke - kb;
+        return true;
+    }
+};
+
+// ---- waits ------------------------------------------------------------------
+
 // Bounded mbarrier wait. Returns false (after setting `code` in the status
 // word) if the phase did not complete within p.timeout_ns.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
@@ -128,6 +197,8 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// ---- producer -----------------------------------------------------------------
+
 // Byte offset of A element (row r, column k) inside one stage: 128-byte rows,
 // 16-byte chunk index XOR (r mod 8) — the TMA 128B swizzle pattern.
 __device__ __forceinline__ uint32_t a_swz(int r, int k) {
@@ -138,7 +209,6 @@ template <class C>
 __device__ __forceinline__ void producer(const CUtensorMap* tmA, const CUtensorMap* tmB,
                                          const GemmParams& p, uint32_t sA, uint32_t sB,
                                          uint32_t full0, uint32_t empty0, int pw, int lane) {
-    const int num_tiles = p.tiles_m * p.tiles_n;
     const bool tma_thread = C::ANY_TMA && pw == 0 && lane == 0;
     if (!C::ANY_CP && !tma_thread) return;
     if (tma_thread) {
@@ -149,11 +219,13 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmA, const CUtensorM
     uint32_t ph = 0;
     int issued = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+    Schedule sched(p);
+    Item it;
+    while (ok && sched.next(p, it)) {
         int tm, tn;
-        tile_coords(t, p, tm, tn);
+        tile_coords(it.tile, p, tm, tn);
         const int m0 = tm * C::BM, n0 = tn * C::BN;
-        for (int kt = 0; kt < p.k_tiles; ++kt) {
+        for (int kt = it.kb; kt < it.ke; ++kt) {
             if (!wait_bounded(empty0 + 8 * s, ph ^ 1u, p, STATUS_PRODUCER_TIMEOUT)) {
                 ok = false;
                 break;
@@ -208,24 +280,7 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmA, const CUtensorM
     if (C::ANY_CP) asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-// Lane -> (tr, tc) in the 4 x 8 lane grid of a 32 x 64 warp tile. The
-// mapping decides which lanes share a shared-memory quarter-warp phase:
-//   0: tr = lane / 8, tc = lane % 8   (a phase reads 1 A row, 8 B float4)
-//   1: tr = lane % 4, tc = lane / 4   (a phase reads 4 A rows, 2 B float4)
-//   2: 2 x 4 blocks per phase          (a phase reads 2 A rows, 4 B float4)
-template <int LMAP>
-__device__ __forceinline__ void lane_grid(int lane, int& tr, int& tc) {
-    if (LMAP == 0) {
-        tr = lane >> 3;
-        tc = lane & 7;
-    } else if (LMAP == 1) {
-        tr = lane & 3;
-        tc = lane >> 2;
-    } else {
-        tr = (lane & 1) | (((lane >> 3) & 1) << 1);
-        tc = ((lane >> 1) & 3) | ((lane >> 4) << 2);
-    }
-}
+// ---- consumer -----------------------------------------------------------------
 
 // A fragment of k-group kq (4 consecutive k) for the lane's 8 rows
 // {tr, tr+4, ..., tr+28}: row r's 16-byte chunk kq sits at chunk kq ^ (r % 8),
@@ -243,16 +298,15 @@ __device__ __forceinline__ float lane_of(const float4& v, int kk) {
 }
 
 // One k-step of the 8 x 8 register outer product.
-//   FORDER 0/1: scalar FFMA, rows or columns outer.
-//   FORDER 2:   packed FFMA2 (fma.rn.f32x2: two IEEE single-precision FMAs,
-//               each rounded once, in one instruction): pairs of adjacent
-//               columns share one instruction with the row's A value in both
-//               lanes. Every output still sees the same FMA sequence, so the
-//               result is bit-identical to the scalar forms.
+//   FORDER 0: scalar FFMA.
+//   FORDER 2: packed FFMA2 (fma.rn.f32x2: two IEEE single-precision FMAs,
+//             each rounded once, in one instruction): pairs of adjacent
+//             columns share one instruction with the row's A value in both
+//             lanes. Every output still sees the same FMA sequence, so the
+//             result is bit-identical to the scalar form.
 template <int FORDER>
 __device__ __forceinline__ void outer_product(float (&acc)[8][8], const float4 (&a)[8], int kk,
                                               const float4& b0, const float4& b1) {
-    const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
     if (FORDER == 2) {
         const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
                               make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
@@ -268,142 +322,77 @@ __device__ __forceinline__ void outer_product(float (&acc)[8][8], const float4 (
                 acc[i][2 * jp + 1] = c.y;
             }
         }
-    } else if (FORDER == 0) {
+    } else {
+        const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const float av = lane_of(a[i], kk);
 #pragma unroll
             for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av, bv[j], acc[i][j]);
         }
-    } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i][j] = fmaf(lane_of(a[i], kk), bv[j], acc[i][j]);
     }
 }
 
-// Inline refill (Cfg::INLINE): load stage g of this CTA's sequence into ring
-// slot `slot` by TMA, completing on that slot's full barrier.
 template <class C>
-__device__ __forceinline__ void issue_stage(const CUtensorMap* tmA, const CUtensorMap* tmB,
-                                            const GemmParams& p, uint32_t sA, uint32_t sB,
-                                            uint32_t full0, int g, int slot) {
-    const int i = g / p.k_tiles;
-    const int kt = g - i * p.k_tiles;
-    int tm, tn;
-    tile_coords(static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x), p, tm, tn);
-    const uint32_t full = full0 + 8 * slot;
-    mbar_arrive_expect_tx(full, C::TX_BYTES);
-    tma_load_2d(sA + slot * C::A_BYTES, tmA, full, kt * C::BK, tm * C::BM);
-    tma_load_2d(sB + slot * C::B_BYTES, tmB, full, tn * C::BN, kt * C::BK);
-}
-
-template <class C>
-__device__ __forceinline__ void consumer(const CUtensorMap* tmA, const CUtensorMap* tmB,
-                                         const GemmParams& p, const uint8_t* sA_ptr,
+__device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_ptr,
                                          const uint8_t* sB_ptr, uint32_t full0, uint32_t empty0,
                                          int warp, int lane) {
-    const uint32_t sA_u32 = smem_u32(sA_ptr), sB_u32 = smem_u32(sB_ptr);
-    const int num_tiles = p.tiles_m * p.tiles_n;
     const int wm = warp % C::WARPS_M, wn = warp / C::WARPS_M;
-    int tr, tc;
-    lane_grid<C::LMAP>(lane, tr, tc);
+    const int tr = lane >> 3, tc = lane & 7;
     const int row_base = wm * 32 + tr;        // rows row_base + 4 i, i = 0..7
     const int col_base = wn * 64 + 4 * tc;    // cols col_base + {0..3} and + 32 + {0..3}
     constexpr int KQ = C::BK / 4;
 
-    // Stage sequence of this CTA: k-tile kt of its i-th tile is stage
-    // i * k_tiles + kt, held in ring slot (stage mod STAGES).
-    const int my_tiles = (num_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
-                         static_cast<int>(gridDim.x);
-    const int total = my_tiles * p.k_tiles;
-    const bool issuer = C::INLINE && threadIdx.x == 0;
-    if (issuer) {
-        tma_prefetch_desc(tmA);
-        tma_prefetch_desc(tmB);
-        for (int g = 0; g < total && g < C::STAGES; ++g)
-            issue_stage<C>(tmA, tmB, p, sA_u32, sB_u32, full0, g, g);
-    }
-    int g = 0;
     int s = 0;
     uint32_t ph = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-        int tm, tn;
-        tile_coords(t, p, tm, tn);
+    Schedule sched(p);
+    Item it;
+    while (sched.next(p, it)) {
         float acc[8][8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
 #pragma unroll
             for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
 
-        // With XPF, the first k-group of each stage (and its first B row) is
-        // loaded while the previous stage's last k-group is multiplied.
-        float4 a_pre[8];
-        float4 b_pre0, b_pre1;
-        if (C::XPF) {
+        for (int kt = it.kb; kt < it.ke; ++kt) {
             if (!wait_bounded(full0 + 8 * s, ph, p, STATUS_CONSUMER_TIMEOUT)) return;
             const uint8_t* a_st = sA_ptr + s * C::A_BYTES + row_base * 128;
             const uint8_t* b_st = sB_ptr + s * C::B_BYTES + col_base * 4;
-            load_a_group(a_pre, a_st, 0, tr);
-            b_pre0 = *reinterpret_cast<const float4*>(b_st);
-            b_pre1 = *reinterpret_cast<const float4*>(b_st + 32 * 4);
-        }
-
-        for (int kt = 0; kt < p.k_tiles; ++kt) {
-            if (!C::XPF) {
-                if (!wait_bounded(full0 + 8 * s, ph, p, STATUS_CONSUMER_TIMEOUT)) return;
-            }
-            const uint8_t* a_st = sA_ptr + s * C::A_BYTES + row_base * 128;
-            const uint8_t* b_st = sB_ptr + s * C::B_BYTES + col_base * 4;
-            int s_next = s + 1;
-            uint32_t ph_next = ph;
-            if (s_next == C::STAGES) { s_next = 0; ph_next ^= 1u; }
 #pragma unroll
             for (int kq = 0; kq < KQ; ++kq) {
                 float4 a[8];
-                if (C::XPF && kq == 0) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) a[i] = a_pre[i];
-                } else {
-                    load_a_group(a, a_st, kq, tr);
-                }
-                if (C::XPF && kq == KQ - 1 && kt + 1 < p.k_tiles) {
-                    if (!wait_bounded(full0 + 8 * s_next, ph_next, p, STATUS_CONSUMER_TIMEOUT))
-                        return;
-                    const uint8_t* a_nx = sA_ptr + s_next * C::A_BYTES + row_base * 128;
-                    const uint8_t* b_nx = sB_ptr + s_next * C::B_BYTES + col_base * 4;
-                    load_a_group(a_pre, a_nx, 0, tr);
-                    b_pre0 = *reinterpret_cast<const float4*>(b_nx);
-                    b_pre1 = *reinterpret_cast<const float4*>(b_nx + 32 * 4);
-                }
+                load_a_group(a, a_st, kq, tr);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    float4 b0, b1;
-                    if (C::XPF && kq == 0 && kk == 0) {
-                        b0 = b_pre0;
-                        b1 = b_pre1;
-                    } else {
-                        const uint8_t* brow = b_st + (kq * 4 + kk) * C::BN * 4;
-                        b0 = *reinterpret_cast<const float4*>(brow);
-                        b1 = *reinterpret_cast<const float4*>(brow + 32 * 4);
-                    }
+                    const uint8_t* brow = b_st + (kq * 4 + kk) * C::BN * 4;
+                    const float4 b0 = *reinterpret_cast<const float4*>(brow);
+                    const float4 b1 = *reinterpret_cast<const float4*>(brow + 32 * 4);
                     outer_product<C::FORDER>(acc, a, kk, b0, b1);
                 }
             }
             mbar_arrive(empty0 + 8 * s);
-            if (issuer && g + C::STAGES < total) {
-                // Refill this slot with stage g + STAGES once every consumer
-                // has released stage g.
-                if (!wait_bounded(empty0 + 8 * s, ph, p, STATUS_PRODUCER_TIMEOUT)) return;
-                issue_stage<C>(tmA, tmB, p, sA_u32, sB_u32, full0, g + C::STAGES, s);
+            if (++s == C::STAGES) { s = 0; ph ^= 1u; }
+        }
+
+        if (it.slot >= 0) {
+            // Partial tile: raw sums to the workspace slot, row-major BM x BN,
+            // bypassing L1 (sk_fixup_kernel reads them from L2).
+            float* slot = p.ws + static_cast<long long>(it.slot) * (C::BM * C::BN);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float* row = slot + (row_base + 4 * i) * C::BN + col_base;
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    __stcg(reinterpret_cast<float4*>(row + 32 * h),
+                           make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2],
+                                       acc[i][4 * h + 3]));
             }
-            ++g;
-            s = s_next;
-            ph = ph_next;
+            continue;
         }
 
         // Epilogue: C = alpha * acc + beta * C, straight from registers.
+        int tm, tn;
+        tile_coords(it.tile, p, tm, tn);
         const int m0 = tm * C::BM + row_base;
         const int n0 = tn * C::BN + col_base;
         const bool use_c = p.beta != 0.0f;
@@ -468,11 +457,100 @@ sgemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     __syncthreads();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (C::PRODUCER_WARPS > 0 && warp >= C::CONSUMER_WARPS) {
+    if (warp >= C::CONSUMER_WARPS) {
         producer<C>(&tmA, &tmB, p, smem_u32(sA), smem_u32(sB), full0, empty0,
                     warp - C::CONSUMER_WARPS, lane);
     } else {
-        consumer<C>(&tmA, &tmB, p, sA, sB, full0, empty0, warp, lane);
+        consumer<C>(p, sA, sB, full0, empty0, warp, lane);
+    }
+}
+
+// ---- stream-K fixup -------------------------------------------------------------
+
+// Most partial segments a stream-K tile can have; the host never schedules
+// more (a range is at least ceil(k_tiles / kMaxParts) iterations long).
+constexpr int kSkMaxParts = 64;
+
+// One CTA per stream-K tile u (tile dp_tiles + u). If a single CTA's range
+// covered the whole tile, that CTA already wrote C and this block returns.
+// Otherwise the contributing ranges are those of CTAs c_first, c_first+1, ...
+// (in increasing k order); their partial sums are added in that order and the
+// epilogue C = alpha * sum + beta * C is applied.
+template <int BM, int BN>
+__global__ void __launch_bounds__(256)
+sk_fixup_kernel(const GemmParams p) {
+    const long long KT = p.k_tiles;
+    const long long G = p.sk_ctas;
+    const long long S = p.sk_iters;
+    const long long u = blockIdx.x;
+    const long long x0 = u * KT, x1 = x0 + KT;
+    __shared__ int parts[kSkMaxParts];
+    __shared__ int nparts;
+    if (threadIdx.x == 0) {
+        // Largest c with start(c) <= x0: the range holding the tile's first k.
+        long long c = ((x0 + 1) * G + S - 1) / S - 1;
+        if (c < 0) c = 0;
+        int n = 0;
+        bool whole = false;
+        for (; c < G; ++c) {
+            const long long s = sk_start(c, p), e = sk_start(c + 1, p);
+            if (s >= x1) break;
+            const long long a = s > x0 ? s : x0;
+            const long long b = e < x1 ? e : x1;
+            if (a >= b) continue;
+            if (a == x0 && b == x1) { whole = true; break; }
+            if (n < kSkMaxParts) parts[n] = static_cast<int>(2 * c + (a == s ? 0 : 1));
+            ++n;
+        }
+        nparts = whole ? 0 : n;
+        if (n > kSkMaxParts) {
+            atomicOr(p.status, STATUS_SCHEDULE);
+            nparts = 0;
+        }
+    }
+    __syncthreads();
+    const int np = nparts;
+    if (np == 0) return;
+
+    int tm, tn;
+    tile_coords(p.dp_tiles + static_cast<int>(u), p, tm, tn);
+    const bool use_c = p.beta != 0.0f;
+    constexpr int Q = BM * BN / 4;   // float4 per tile
+    for (int q = threadIdx.x; q < Q; q += blockDim.x) {
+        const int r = q / (BN / 4);
+        const int c4 = (q - r * (BN / 4)) * 4;
+        const int m = tm * BM + r;
+        const int n = tn * BN + c4;
+        if (m >= p.M || n >= p.N) continue;
+        float4 sum = __ldcg(reinterpret_cast<const float4*>(p.ws + static_cast<long long>(parts[0]) * (BM * BN)) + q);
+        for (int j = 1; j < np; ++j) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(p.ws + static_cast<long long>(parts[j]) * (BM * BN)) + q);
+            sum.x += v.x;
+            sum.y += v.y;
+            sum.z += v.z;
+            sum.w += v.w;
+        }
+        float* crow = p.C + (long long)m * p.ldc;
+        float v[4] = {p.alpha * sum.x, p.alpha * sum.y, p.alpha * sum.z, p.alpha * sum.w};
+        if (p.c_vec && n + 3 < p.N) {
+            float4* cp = reinterpret_cast<float4*>(crow + n);
+            if (use_c) {
+                const float4 cv = *cp;
+                v[0] = fmaf(p.beta, cv.x, v[0]);
+                v[1] = fmaf(p.beta, cv.y, v[1]);
+                v[2] = fmaf(p.beta, cv.z, v[2]);
+                v[3] = fmaf(p.beta, cv.w, v[3]);
+            }
+            *cp = make_float4(v[0], v[1], v[2], v[3]);
+        } else {
+            for (int e = 0; e < 4; ++e) {
+                if (n + e < p.N) {
+                    float out = v[e];
+                    if (use_c) out = fmaf(p.beta, crow[n + e], out);
+                    crow[n + e] = out;
+                }
+            }
+        }
     }
 }
 

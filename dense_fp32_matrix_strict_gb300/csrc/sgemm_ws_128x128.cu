@@ -5,7 +5,7 @@
 
 namespace sg {
 
-static const KernelFamily kFamily = SG_FAMILY("ws_128x128x32_s4", 128, 128, 4, 0, 0, 2, 0);
+static const KernelFamily kFamily = SG_FAMILY("ws_128x128x32_s4", 128, 128, 4, 2);
 
 const KernelFamily* family_128x128() { return &kFamily; }
 

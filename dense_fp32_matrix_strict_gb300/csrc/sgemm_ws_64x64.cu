@@ -5,7 +5,7 @@
 
 namespace sg {
 
-static const KernelFamily kFamily = SG_FAMILY("ws_64x64x32_s4", 64, 64, 4, 0, 0, 2, 0);
+static const KernelFamily kFamily = SG_FAMILY("ws_64x64x32_s4", 64, 64, 4, 2);
 
 const KernelFamily* family_64x64() { return &kFamily; }
 

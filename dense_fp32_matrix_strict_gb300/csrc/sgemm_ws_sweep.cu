@@ -5,12 +5,9 @@ namespace sg {
 
 const KernelFamily* sweep_family_a();
 const KernelFamily* sweep_family_b();
-const KernelFamily* sweep_family_c();
 
 const KernelFamily* const* sweep_families(int* count) {
-    static const KernelFamily* const list[] = {
-        sweep_family_a(), sweep_family_b(), sweep_family_c(),
-    };
+    static const KernelFamily* const list[] = {sweep_family_a(), sweep_family_b()};
     *count = static_cast<int>(sizeof(list) / sizeof(list[0]));
     return list;
 }

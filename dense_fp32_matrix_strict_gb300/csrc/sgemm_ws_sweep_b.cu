@@ -1,11 +1,9 @@
-// Tuning alternative of the 128 x 128 x 32 family: 6 stages, lane map 0,
-// cross-stage fragment prefetch 0, FMA form 2 (see Cfg).
+// Tuning alternative of the 128 x 128 x 32 family: a 6-stage ring (192 KB).
 #include "kernels.h"
 
 namespace sg {
 
-static const KernelFamily kFamily =
-    SG_FAMILY("ws_128x128x32_s6_x0_f2", 128, 128, 6, 0, 0, 2, 0);
+static const KernelFamily kFamily = SG_FAMILY("ws_128x128x32_s6", 128, 128, 6, 2);
 
 const KernelFamily* sweep_family_b() { return &kFamily; }
 

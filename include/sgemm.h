@@ -20,9 +20,16 @@
  * below 2^24 they are exact.
  *
  * All pointers are DEVICE pointers on the current CUDA device, owned by the
- * caller. The library keeps only per-device set-up state (created on the
- * first call on a device: device properties, a 256-byte device status word,
- * kernel attributes) and allocates nothing per call.
+ * caller. The library keeps per-device set-up state (created on the first
+ * call on a device: device properties, kernel attributes, a 256-byte device
+ * status word and a private stream-ordered memory pool). When a problem's
+ * last wave of tiles is split across all SMs (the stream-K tail), the call
+ * takes a workspace of at most 2 x SMs x 64 KB from that pool with
+ * cudaMallocFromPoolAsync on the call's stream and returns it with
+ * cudaFreeAsync on the same stream, so concurrent calls on different
+ * streams never share it and stream capture records it as an allocation
+ * node. If that allocation fails the call falls back to the plain
+ * data-parallel schedule.
  */
 #ifndef SGEMM_GB300_H
 #define SGEMM_GB300_H
@@ -109,9 +116,10 @@ SGEMM_API int sgemm_last_cuda_error(void);
  * sgemm_plan — describe, without launching, the kernel sgemm would use for
  * these arguments: writes a NUL-terminated name such as
  * "ws_128x128x32_s4_Atma_Btma" into buf (at most buflen bytes) and the
- * launch grid into *grid (if not NULL). Returns the same argument errors as
- * sgemm, or SGEMM_OK. A name of "scale" means the alpha == 0 / K == 0 path;
- * "none" means M == 0 or N == 0.
+ * launch grid into *grid (if not NULL). A "+sk" suffix means the last wave
+ * is split across the SMs (stream-K) and finished by a second, small fixup
+ * kernel. Returns the same argument errors as sgemm, or SGEMM_OK. A name of
+ * "scale" means the alpha == 0 / K == 0 path; "none" means M == 0 or N == 0.
  */
 SGEMM_API int sgemm_plan(int64_t M, int64_t N, int64_t K, float alpha, const float* A, int64_t lda,
                const float* B, int64_t ldb, float beta, const float* C, int64_t ldc,
@@ -121,11 +129,12 @@ SGEMM_API int sgemm_plan(int64_t M, int64_t N, int64_t K, float alpha, const flo
  * sgemm_set_config — force a kernel configuration for later calls in this
  * process (for sweeps and tests). `name` is "auto" (default), "128x128" or
  * "64x64" for the CTA tile, or one of the family names sgemm_config_names
- * lists, optionally followed by ":cpasync" to load both
- * operands with cp.async even when TMA could be used (e.g.
- * "128x128:cpasync", or "auto:cpasync"). Returns SGEMM_ERR_INVALID_VALUE
- * for an unknown name. The environment variable SGEMM_FORCE_CONFIG, read on
- * the first call, sets the same thing.
+ * lists, optionally followed by modifiers: ":cpasync" loads both operands
+ * with cp.async even when TMA could be used, ":dp" never splits the last
+ * wave (plain data-parallel schedule, no workspace), e.g.
+ * "128x128:cpasync:dp" or "auto:dp". Returns SGEMM_ERR_INVALID_VALUE for an
+ * unknown name. The environment variable SGEMM_FORCE_CONFIG, read on the
+ * first call, sets the same thing.
  */
 SGEMM_API int sgemm_set_config(const char* name);
 

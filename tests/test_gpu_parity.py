@@ -222,7 +222,8 @@ def _workload(name, full):
 
 
 def test_workload_sq256_uniform():
-    _workload("sq256_uniform", full=True)
+    rep, plan = _workload("sq256_uniform", full=True)
+    assert plan[0] == "ws_64x64x32_s4_Atma_Btma", plan     # too small to split
 
 
 def test_workload_sq1024_int_bit_exact():
@@ -267,8 +268,9 @@ def test_every_family_matches_oracle(cp):
 
 
 def test_families_agree_bitwise():
-    # Every family accumulates each output in the same k order with FFMA, so
-    # they must agree bit for bit (only the schedule differs).
+    # Under the data-parallel schedule every family accumulates each output
+    # in the same k order with single-rounding FMAs, so they must agree bit
+    # for bit (only the instruction schedule differs).
     torch = pytest.importorskip("torch")
     M, N, K = 640, 512, 768
     A, B, C0 = gen(M, N, K, seed=77)
@@ -276,7 +278,7 @@ def test_families_agree_bitwise():
     dB = torch.from_numpy(B).cuda()
     outs = {}
     for name in _family_names():
-        assert sg.sgemm_set_config(name) == 0
+        assert sg.sgemm_set_config(name + ":dp") == 0
         dC = torch.from_numpy(C0).cuda()
         sg.sgemm_tensors(0.7, dA, dB, -1.3, dC)
         sg.check_status()
@@ -285,3 +287,64 @@ def test_families_agree_bitwise():
     names = list(outs)
     for n in names[1:]:
         assert np.array_equal(outs[names[0]], outs[n]), (names[0], n)
+
+
+# ---- the stream-K tail ----------------------------------------------------------
+
+SK_SHAPES = [
+    (1024, 1024, 1024),     # 64 tiles < 152 SMs: every tile split
+    (256, 512, 2048),       # 8 tiles of 64 k-tiles over 152 CTAs: ~19 parts per tile
+    (128, 128, 16384),      # one tile, 512 k-tiles: 32 parts
+    (512, 5504, 96),        # 172 tiles: one full wave + a 20-tile tail
+    (333, 4500, 777),       # ragged edges, 1 wave + tail
+    (130, 70, 8400),        # tiles cut by both edges, 29 parts per tile
+]
+
+
+@pytest.mark.parametrize("cp", ["", ":cpasync"])
+@pytest.mark.parametrize("shape", SK_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_stream_k_tail_matches_oracle(shape, cp):
+    M, N, K = shape
+    A, B, C0 = gen(M, N, K, seed=200 + M % 97 + N % 89 + K % 83)
+    assert sg.sgemm_set_config("auto" + cp) == 0
+    try:
+        C, guards, plan = gpu_util.run(0.7, A, B, -1.3, C0)
+        assert guards
+        assert plan[0].endswith("+sk"), plan
+        check_full(0.7, A, B, -1.3, C0, C)
+        # beta == 0 through the fixup: C is not read.
+        C, guards, plan = gpu_util.run(1.5, A, B, 0.0, None)
+        assert guards and plan[0].endswith("+sk"), plan
+        check_full(1.5, A, B, 0.0, None, C)
+    finally:
+        sg.sgemm_set_config("auto")
+
+
+def test_stream_k_is_deterministic_and_close_to_dp():
+    torch = pytest.importorskip("torch")
+    M, N, K = 1000, 1100, 2000
+    A, B, C0 = gen(M, N, K, seed=300)
+    dA = torch.from_numpy(A).cuda()
+    dB = torch.from_numpy(B).cuda()
+    outs = []
+    for cfg in ["auto", "auto", "auto:dp"]:
+        assert sg.sgemm_set_config(cfg) == 0
+        dC = torch.from_numpy(C0).cuda()
+        name, _ = sg.plan_tensors(0.7, dA, dB, -1.3, dC)
+        assert name.endswith("+sk") == (cfg == "auto"), name
+        sg.sgemm_tensors(0.7, dA, dB, -1.3, dC)
+        sg.check_status()
+        outs.append(dC.cpu().numpy())
+    sg.sgemm_set_config("auto")
+    assert np.array_equal(outs[0], outs[1])          # same schedule, same bits
+    for C in (outs[0], outs[2]):
+        check_full(0.7, A, B, -1.3, C0, C)
+
+
+def test_integer_inputs_bit_exact_with_stream_k():
+    A = inputs.fill("int", 5, inputs.TID_A, 700, 1500)
+    B = inputs.fill("int", 5, inputs.TID_B, 1500, 900)
+    C0 = inputs.fill("int", 5, inputs.TID_C, 700, 900)
+    C, _, plan = gpu_util.run(2.0, A, B, -1.0, C0)
+    assert plan[0].endswith("+sk"), plan
+    check_full(2.0, A, B, -1.0, C0, C, exact=True)
