@@ -24,7 +24,7 @@ SGEMM_ERR_CUDA = 5
 EXPORTED_SYMBOLS = (
     "sgemm", "sgemm_check_status", "sgemm_error_string", "sgemm_last_cuda_error",
     "sgemm_plan", "sgemm_set_config", "sgemm_set_wait_timeout_ns", "sgemm_fp32_peak",
-    "sgemm_selftest_wait_timeout", "sgemm_config_names",
+    "sgemm_selftest_wait_timeout", "sgemm_config_names", "sgemm_noalloc",
 )
 
 _lock = threading.Lock()
@@ -81,6 +81,8 @@ def load():
         lib.sgemm_fp32_peak.restype = ci
         lib.sgemm_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
         lib.sgemm_selftest_wait_timeout.restype = ci
+        lib.sgemm_noalloc.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
+        lib.sgemm_noalloc.restype = ci
         _lib = lib
         return lib
 
@@ -96,6 +98,12 @@ def _check(func: str, rc: int) -> int:
 def sgemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
     """C = alpha*A*B + beta*C on device pointers (ints); returns the raw code."""
     return load().sgemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def sgemm_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
+    """sgemm without any device allocation (fixed scratch inside the library);
+    device pointers as ints; returns the raw code."""
+    return load().sgemm_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
 
 
 def sgemm_check_status(stream=0):

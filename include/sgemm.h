@@ -176,6 +176,34 @@ SGEMM_API int sgemm_fp32_peak(double target_ms, double* gflops, double* ms, doub
  */
 SGEMM_API int sgemm_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stream);
 
+/*
+ * sgemm_noalloc — the same operation, arguments, results and errors as
+ * sgemm, for callers that must not allocate device memory. The pages this
+ * library follows have no counterpart: it exists for code that cannot call
+ * cudaMalloc or a pool allocator — work recorded while a stream is captured
+ * into a CUDA graph in global capture mode, programs whose device memory is
+ * owned by another allocator, and latency-critical paths that may not take
+ * an allocator's locks. sgemm allocates a status word on its first call on a
+ * device and a stream-K workspace for some problems; sgemm_noalloc instead
+ * uses one fixed 32 MiB scratch array compiled into the library (held by
+ * every GPU that loads the library until the process exits).
+ *
+ * The first call on a device looks up the scratch array's device address
+ * and performs the library's per-device kernel set-up: make that first call
+ * before any stream capture begins. Every call on a device shares the
+ * scratch, which keeps the last call's contents; nothing in it needs
+ * clearing between calls. Calls that overlap on the GPU (on streams with no
+ * ordering between them) race on the scratch and can produce wrong results,
+ * so serialise them. Returns SGEMM_ERR_INVALID_VALUE, with nothing enqueued,
+ * if the problem's stream-K workspace would not fit in the scratch (never on
+ * a 152-SM GB300, which needs at most 19.5 MB). Time-outs of bounded waits
+ * inside its kernels are recorded in the scratch, not in the word that
+ * sgemm_check_status reads.
+ */
+SGEMM_API int sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                            int64_t lda, const float* B, int64_t ldb, float beta, float* C,
+                            int64_t ldc, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
