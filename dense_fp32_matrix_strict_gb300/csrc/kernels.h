@@ -52,21 +52,25 @@ struct KernelFamily {
 // Index into a family's modes: TMA/TMA, CP/TMA, TMA/CP, CP/CP.
 inline constexpr int mode_index(int a_mode, int b_mode) { return a_mode + 2 * b_mode; }
 
-template <int BM, int BN, int S, int AM, int BMD, int FORDER>
+template <int BM, int BN, int S, int AM, int BMD, int FORDER, int EARLY, int LMAP>
 constexpr KernelEntry make_entry(const char* name) {
-    using C = Cfg<BM, BN, 32, S, AM, BMD, FORDER>;
+    using C = Cfg<BM, BN, 32, S, AM, BMD, FORDER, EARLY, LMAP>;
     return KernelEntry{name, BM, BN, 32, S, AM, BMD, C::THREADS, C::SMEM_BYTES,
                        &ws_prepare<C>, &ws_launch<C>};
 }
 
-#define SG_FAMILY(NAME, BM, BN, S, FORDER)                                                  \
+#define SG_FAMILY(NAME, BM, BN, S, FORDER, EARLY, LMAP)                                     \
     KernelFamily {                                                                          \
         NAME, BM, BN,                                                                       \
             {                                                                               \
-                make_entry<BM, BN, S, LOAD_TMA, LOAD_TMA, FORDER>(NAME "_Atma_Btma"),         \
-                make_entry<BM, BN, S, LOAD_CPASYNC, LOAD_TMA, FORDER>(NAME "_Acp_Btma"),      \
-                make_entry<BM, BN, S, LOAD_TMA, LOAD_CPASYNC, FORDER>(NAME "_Atma_Bcp"),      \
-                make_entry<BM, BN, S, LOAD_CPASYNC, LOAD_CPASYNC, FORDER>(NAME "_Acp_Bcp"),   \
+                make_entry<BM, BN, S, LOAD_TMA, LOAD_TMA, FORDER, EARLY, LMAP>(               \
+                    NAME "_Atma_Btma"),                                                     \
+                make_entry<BM, BN, S, LOAD_CPASYNC, LOAD_TMA, FORDER, EARLY, LMAP>(           \
+                    NAME "_Acp_Btma"),                                                      \
+                make_entry<BM, BN, S, LOAD_TMA, LOAD_CPASYNC, FORDER, EARLY, LMAP>(           \
+                    NAME "_Atma_Bcp"),                                                      \
+                make_entry<BM, BN, S, LOAD_CPASYNC, LOAD_CPASYNC, FORDER, EARLY, LMAP>(       \
+                    NAME "_Acp_Bcp"),                                                       \
             },                                                                              \
             &fixup_launch<BM, BN>                                                           \
     }

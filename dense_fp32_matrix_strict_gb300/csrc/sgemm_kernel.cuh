@@ -82,12 +82,24 @@ struct GemmParams {
 };
 
 // Kernel configuration. FORDER: FMA form of the outer product (0: scalar
-// FFMA, 2: packed FFMA2 over column pairs).
-template <int BM_, int BN_, int BK_, int STAGES_, int A_MODE_, int B_MODE_, int FORDER_ = 2>
+// FFMA, 2: packed FFMA2 over column pairs, rows outer, 3: the same with the
+// column pairs outer).
+// EARLY: halfway through a stage, probe (without blocking) whether the next
+// stage of the same work item has landed, so the blocking wait at the stage
+// boundary is skipped when it has.
+// LMAP: lane -> (row group tr, column group tc) of the 4 x 8 lane grid.
+//   0: tr = lane / 8, tc = lane % 8. A quarter-warp (8 lanes) reads one A
+//      chunk and the same 8 B chunks as every other quarter: a B float4 load
+//      costs 4 shared-memory wavefronts, an A load 2.
+//   1: tr = lane % 4, tc = lane / 4. A quarter-warp reads 2 B chunks and 4 A
+//      chunks: both loads cost 2 wavefronts (measured on sm_103a), a third
+//      fewer wavefronts per FMA.
+template <int BM_, int BN_, int BK_, int STAGES_, int A_MODE_, int B_MODE_, int FORDER_ = 2,
+          int EARLY_ = 0, int LMAP_ = 0>
 struct Cfg {
     static constexpr int BM = BM_, BN = BN_, BK = BK_, STAGES = STAGES_;
     static constexpr int A_MODE = A_MODE_, B_MODE = B_MODE_;
-    static constexpr int FORDER = FORDER_;
+    static constexpr int FORDER = FORDER_, EARLY = EARLY_, LMAP = LMAP_;
     static_assert(BK == 32, "A rows are one 128-byte swizzle span");
     static_assert(BM % 32 == 0 && BN % 64 == 0, "warp tile is 32 x 64");
     static constexpr int WARPS_M = BM / 32, WARPS_N = BN / 64;
@@ -107,6 +119,8 @@ struct Cfg {
     static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * (A_BYTES + B_BYTES)
                                       + 2 * STAGES * 8;
     static_assert(SMEM_BYTES <= 227 * 1024, "ring does not fit in 227 KB of shared memory");
+    // Tiles of at most 128 x 64 are sized to run two CTAs per SM.
+    static constexpr int MIN_BLOCKS = (BM * BN <= 128 * 64) ? 2 : 1;
 };
 
 // Tile index -> (tile row, tile column), grouped so that the CTAs running at
@@ -307,7 +321,23 @@ __device__ __forceinline__ float lane_of(const float4& v, int kk) {
 template <int FORDER>
 __device__ __forceinline__ void outer_product(float (&acc)[8][8], const float4 (&a)[8], int kk,
                                               const float4& b0, const float4& b1) {
-    if (FORDER == 2) {
+    if (FORDER == 3) {
+        // FFMA2 with the column pairs outer: consecutive instructions share
+        // the B pair and change the A value.
+        const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
+                              make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
+#pragma unroll
+        for (int jp = 0; jp < 4; ++jp) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float av = lane_of(a[i], kk);
+                float2 c = make_float2(acc[i][2 * jp], acc[i][2 * jp + 1]);
+                c = __ffma2_rn(make_float2(av, av), bp[jp], c);
+                acc[i][2 * jp] = c.x;
+                acc[i][2 * jp + 1] = c.y;
+            }
+        }
+    } else if (FORDER == 2) {
         const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
                               make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
 #pragma unroll
@@ -338,7 +368,8 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
                                          const uint8_t* sB_ptr, uint32_t full0, uint32_t empty0,
                                          int warp, int lane) {
     const int wm = warp % C::WARPS_M, wn = warp / C::WARPS_M;
-    const int tr = lane >> 3, tc = lane & 7;
+    const int tr = C::LMAP == 1 ? (lane & 3) : (lane >> 3);
+    const int tc = C::LMAP == 1 ? (lane >> 2) : (lane & 7);
     const int row_base = wm * 32 + tr;        // rows row_base + 4 i, i = 0..7
     const int col_base = wn * 64 + 4 * tc;    // cols col_base + {0..3} and + 32 + {0..3}
     constexpr int KQ = C::BK / 4;
@@ -354,12 +385,18 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
 #pragma unroll
             for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
 
+        bool ready = false;   // EARLY: stage s already seen complete
         for (int kt = it.kb; kt < it.ke; ++kt) {
-            if (!wait_bounded(full0 + 8 * s, ph, p, STATUS_CONSUMER_TIMEOUT)) return;
+            if (!ready && !wait_bounded(full0 + 8 * s, ph, p, STATUS_CONSUMER_TIMEOUT)) return;
+            ready = false;
             const uint8_t* a_st = sA_ptr + s * C::A_BYTES + row_base * 128;
             const uint8_t* b_st = sB_ptr + s * C::B_BYTES + col_base * 4;
+            const int s_nx = (s + 1 == C::STAGES) ? 0 : s + 1;
+            const uint32_t ph_nx = (s + 1 == C::STAGES) ? (ph ^ 1u) : ph;
 #pragma unroll
             for (int kq = 0; kq < KQ; ++kq) {
+                if (C::EARLY && kq == KQ / 2 && kt + 1 < it.ke)
+                    ready = mbar_test_wait(full0 + 8 * s_nx, ph_nx);
                 float4 a[8];
                 load_a_group(a, a_st, kq, tr);
 #pragma unroll
@@ -371,7 +408,8 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
                 }
             }
             mbar_arrive(empty0 + 8 * s);
-            if (++s == C::STAGES) { s = 0; ph ^= 1u; }
+            s = s_nx;
+            ph = ph_nx;
         }
 
         if (it.slot >= 0) {
@@ -433,7 +471,7 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
 }
 
 template <class C>
-__global__ void __launch_bounds__(C::THREADS, 1)
+__global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
 sgemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];

@@ -5,9 +5,10 @@ namespace sg {
 
 const KernelFamily* sweep_family_a();
 const KernelFamily* sweep_family_b();
+const KernelFamily* sweep_family_c();
 
 const KernelFamily* const* sweep_families(int* count) {
-    static const KernelFamily* const list[] = {sweep_family_a(), sweep_family_b()};
+    static const KernelFamily* const list[] = {sweep_family_a(), sweep_family_b(), sweep_family_c()};
     *count = static_cast<int>(sizeof(list) / sizeof(list[0]));
     return list;
 }

@@ -4,7 +4,7 @@
 
 namespace sg {
 
-static const KernelFamily kFamily = SG_FAMILY("ws_128x128x32_s4_ffma", 128, 128, 4, 0);
+static const KernelFamily kFamily = SG_FAMILY("ws_128x128x32_s4_ffma", 128, 128, 4, 0, 0, 0);
 
 const KernelFamily* sweep_family_a() { return &kFamily; }
 
