@@ -155,6 +155,30 @@ __global__ void scale_kernel(float* __restrict__ C, long long ldc, int M, int N,
     }
 }
 
+// dst (rows x ldd, ldd = cols rounded up to 4) <- src (rows x cols, row
+// stride lds, any alignment), one float4 of dst per thread per step; the
+// padding columns get zeros. HBM-bound: one read and one write of the
+// operand.
+__global__ void pack_rows_kernel(const float* __restrict__ src, long long lds,
+                                 float* __restrict__ dst, long long ldd, int rows, int cols) {
+    const int quads = (cols + 3) >> 2;
+    const long long total = static_cast<long long>(rows) * quads;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long r = i / quads;
+        const int c = static_cast<int>(i - r * quads) * 4;
+        const float* s = src + r * lds + c;
+        float4 v;
+        v.x = s[0];
+        v.y = c + 1 < cols ? s[1] : 0.0f;
+        v.z = c + 2 < cols ? s[2] : 0.0f;
+        v.w = c + 3 < cols ? s[3] : 0.0f;
+        *reinterpret_cast<float4*>(dst + r * ldd + c) = v;
+    }
+}
+
+size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
+
 __global__ void wait_timeout_kernel(GemmParams p) {
     __shared__ __align__(8) uint64_t bar;
     const uint32_t b = smem_u32(&bar);
@@ -293,7 +317,7 @@ int device_info(const DeviceInfo** out) {
 
 int make_plan(const DeviceInfo* dev, int64_t M, int64_t N, int64_t K, float alpha,
               const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
-              const float* C, int64_t ldc, bool allow_sk, Plan* pl) {
+              const float* C, int64_t ldc, bool allow_sk, bool allow_pack, Plan* pl) {
     if (M == 0 || N == 0) {
         pl->kind = 0;
         return SGEMM_OK;
@@ -311,6 +335,7 @@ int make_plan(const DeviceInfo* dev, int64_t M, int64_t N, int64_t K, float alph
     }
     pl->kind = 2;
     const int sms = dev->sm_count;
+    pl->sms = sms;
     int fi = g_force_family.load();
     if (fi < 0) {
         // The 128 x 128 tile with the stream-K tail keeps every SM busy even
@@ -335,10 +360,37 @@ int make_plan(const DeviceInfo* dev, int64_t M, int64_t N, int64_t K, float alph
     std::memset(&pl->tmA, 0, sizeof(CUtensorMap));
     std::memset(&pl->tmB, 0, sizeof(CUtensorMap));
     int a_mode = LOAD_CPASYNC, b_mode = LOAD_CPASYNC;
+    pl->pack_a = pl->pack_b = false;
+    pl->pack_a_bytes = pl->pack_b_bytes = 0;
     if (!force_cp && tma_ok(A, lda, M, K) && encode_2d(&pl->tmA, A, M, K, lda, bm, bk, true))
         a_mode = LOAD_TMA;
     if (!force_cp && tma_ok(B, ldb, K, N) && encode_2d(&pl->tmB, B, K, N, ldb, bk, bn, false))
         b_mode = LOAD_TMA;
+    // An operand TMA cannot describe in place is copied once to an aligned
+    // buffer when the GEMM reads it often enough (A is read once per
+    // 128-column tile of C, B once per 128-row tile): from 256 columns (rows)
+    // the 4-byte cp.async loads it saves cost more than the extra pass. The
+    // descriptor is encoded here against a placeholder address to make sure
+    // the driver accepts the shape, and again on the real buffer at launch.
+    const float* kPlaceholder = reinterpret_cast<const float*>(uintptr_t{1} << 20);
+    if (a_mode != LOAD_TMA && allow_pack && !force_cp && N >= 256) {
+        const int64_t ld = (K + 3) & ~int64_t{3};
+        if (tma_ok(kPlaceholder, ld, M, K) && encode_2d(&pl->tmA, kPlaceholder, M, K, ld, bm, bk, true)) {
+            a_mode = LOAD_TMA;
+            pl->pack_a = true;
+            pl->lda_pack = ld;
+            pl->pack_a_bytes = align256(static_cast<size_t>(M) * static_cast<size_t>(ld) * 4);
+        }
+    }
+    if (b_mode != LOAD_TMA && allow_pack && !force_cp && M >= 256) {
+        const int64_t ld = (N + 3) & ~int64_t{3};
+        if (tma_ok(kPlaceholder, ld, K, N) && encode_2d(&pl->tmB, kPlaceholder, K, N, ld, bk, bn, false)) {
+            b_mode = LOAD_TMA;
+            pl->pack_b = true;
+            pl->ldb_pack = ld;
+            pl->pack_b_bytes = align256(static_cast<size_t>(K) * static_cast<size_t>(ld) * 4);
+        }
+    }
     const int mi = mode_index(a_mode, b_mode);
     pl->k = &fam->modes[mi];
 
@@ -377,7 +429,8 @@ int make_plan(const DeviceInfo* dev, int64_t M, int64_t N, int64_t K, float alph
         p.sk_iters = 0;
         pl->grid = static_cast<int>(tiles < cap ? tiles : cap);
         pl->sk_tiles = 0;
-        pl->ws_bytes = 0;
+        pl->sk_bytes = 0;
+        pl->ws_bytes = pl->pack_a_bytes + pl->pack_b_bytes;
         return SGEMM_OK;
     }
     const int64_t S = rest * p.k_tiles;
@@ -392,7 +445,8 @@ int make_plan(const DeviceInfo* dev, int64_t M, int64_t N, int64_t K, float alph
     p.sk_iters = S;
     pl->grid = static_cast<int>(waves > 0 ? cap : G);
     pl->sk_tiles = static_cast<int>(rest);
-    pl->ws_bytes = static_cast<size_t>(2 * G) * static_cast<size_t>(bm) * bn * sizeof(float);
+    pl->sk_bytes = static_cast<size_t>(2 * G) * static_cast<size_t>(bm) * bn * sizeof(float);
+    pl->ws_bytes = pl->pack_a_bytes + pl->pack_b_bytes + pl->sk_bytes;
     return SGEMM_OK;
 }
 
@@ -409,8 +463,31 @@ int launch_plan(Plan* pl, int* status, float* ws, cudaStream_t stream) {
         return SGEMM_OK;
     }
     pl->p.status = status;
-    pl->p.ws = ws;
     if (pl->ws_bytes > 0 && ws == nullptr) return SGEMM_ERR_INVALID_VALUE;
+    unsigned char* w = reinterpret_cast<unsigned char*>(ws);
+    GemmParams& p = pl->p;
+    const int pack_grid = 16 * (pl->sms > 0 ? pl->sms : 1);
+    if (pl->pack_a) {
+        float* a2 = reinterpret_cast<float*>(w);
+        pack_rows_kernel<<<pack_grid, 256, 0, stream>>>(p.A, p.lda, a2, pl->lda_pack, p.M, p.K);
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
+        if (!encode_2d(&pl->tmA, a2, p.M, p.K, pl->lda_pack, pl->fam->bm, 32, true))
+            return cuda_fail(cudaErrorInvalidValue, SGEMM_ERR_LAUNCH);
+        p.A = a2;
+        p.lda = pl->lda_pack;
+    }
+    if (pl->pack_b) {
+        float* b2 = reinterpret_cast<float*>(w + pl->pack_a_bytes);
+        pack_rows_kernel<<<pack_grid, 256, 0, stream>>>(p.B, p.ldb, b2, pl->ldb_pack, p.K, p.N);
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
+        if (!encode_2d(&pl->tmB, b2, p.K, p.N, pl->ldb_pack, 32, pl->fam->bn, false))
+            return cuda_fail(cudaErrorInvalidValue, SGEMM_ERR_LAUNCH);
+        p.B = b2;
+        p.ldb = pl->ldb_pack;
+    }
+    p.ws = pl->sk_bytes > 0
+               ? reinterpret_cast<float*>(w + pl->pack_a_bytes + pl->pack_b_bytes)
+               : nullptr;
     e = pl->k->launch(&pl->tmA, &pl->tmB, &pl->p, pl->grid, stream);
     if (e == cudaSuccess && pl->sk_tiles > 0) e = pl->fam->fixup(&pl->p, pl->sk_tiles, stream);
     if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
@@ -421,7 +498,9 @@ void plan_name(const Plan& pl, char* buf, int buflen) {
     if (buf == nullptr || buflen <= 0) return;
     if (pl.kind == 0) std::snprintf(buf, static_cast<size_t>(buflen), "none");
     else if (pl.kind == 1) std::snprintf(buf, static_cast<size_t>(buflen), "scale");
-    else std::snprintf(buf, static_cast<size_t>(buflen), "%s%s", pl.k->name, pl.sk_tiles > 0 ? "+sk" : "");
+    else std::snprintf(buf, static_cast<size_t>(buflen), "%s%s%s%s", pl.k->name,
+                       pl.pack_a ? "+packA" : "", pl.pack_b ? "+packB" : "",
+                       pl.sk_tiles > 0 ? "+sk" : "");
 }
 
 int launch_selftest_wait(unsigned long long timeout_ns, int* status, cudaStream_t stream) {
@@ -450,18 +529,19 @@ extern "C" int sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float* 
     DeviceMemory* mem = nullptr;
     if ((rc = device_memory(dev, &mem)) != SGEMM_OK) return rc;
     Plan pl;
-    if ((rc = make_plan(dev, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, true, &pl)) != SGEMM_OK)
+    if ((rc = make_plan(dev, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, true, true, &pl)) !=
+        SGEMM_OK)
         return rc;
     float* ws = nullptr;
     if (pl.ws_bytes > 0) {
-        // Stream-ordered workspace from the library's pool: concurrent calls
-        // on different streams never share it, and stream capture records it
-        // as an allocation node.
+        // Stream-ordered workspace (packed operands, stream-K slots) from the
+        // library's pool: concurrent calls on different streams never share
+        // it, and stream capture records it as an allocation node.
         void* w = nullptr;
         if (cudaMallocFromPoolAsync(&w, pl.ws_bytes, mem->pool, stream) != cudaSuccess) {
             (void)cudaGetLastError();
-            if ((rc = make_plan(dev, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, false, &pl)) !=
-                SGEMM_OK)
+            if ((rc = make_plan(dev, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, false, false,
+                                &pl)) != SGEMM_OK)
                 return rc;
         } else {
             ws = static_cast<float*>(w);
@@ -481,7 +561,7 @@ extern "C" int sgemm_plan(int64_t M, int64_t N, int64_t K, float alpha, const fl
     if (M != 0 && N != 0) {
         const DeviceInfo* dev = nullptr;
         if ((rc = device_info(&dev)) != SGEMM_OK) return rc;
-        if ((rc = make_plan(dev, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, true, &pl)) !=
+        if ((rc = make_plan(dev, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, true, true, &pl)) !=
             SGEMM_OK)
             return rc;
     }

@@ -33,8 +33,17 @@ struct Plan {
     CUtensorMap tmA, tmB;
     GemmParams p;
     int grid = 0;
+    int sms = 0;                  // SMs of the device (grid of the packing copies)
     int sk_tiles = 0;             // tiles finished by the stream-K fixup
-    size_t ws_bytes = 0;          // stream-K workspace the launch needs
+    // Operands TMA cannot describe in place (base or row stride not 16-byte
+    // aligned) but worth it: copied first to an aligned workspace buffer
+    // with row stride ld_pack (a multiple of 4 floats).
+    bool pack_a = false, pack_b = false;
+    int64_t lda_pack = 0, ldb_pack = 0;
+    // Workspace the launch needs: [packed A | packed B | stream-K slots],
+    // each region a multiple of 256 bytes.
+    size_t pack_a_bytes = 0, pack_b_bytes = 0, sk_bytes = 0;
+    size_t ws_bytes = 0;
 };
 
 // Validates the arguments of sgemm (SGEMM_OK or SGEMM_ERR_INVALID_VALUE).
@@ -45,18 +54,21 @@ int check_args(int64_t M, int64_t N, int64_t K, float alpha, const float* A, int
 int device_info(const DeviceInfo** out);
 
 // Chooses kernel, load modes, grid and schedule. allow_sk = false forces the
-// data-parallel schedule (no workspace); otherwise ws_bytes tells the caller
-// how much workspace to pass to launch_plan.
+// data-parallel schedule; allow_pack = false never copies an operand to an
+// aligned buffer. ws_bytes tells the caller how much workspace to pass to
+// launch_plan (0 when both are false).
 int make_plan(const DeviceInfo* dev, int64_t M, int64_t N, int64_t K, float alpha,
               const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
-              const float* C, int64_t ldc, bool allow_sk, Plan* pl);
+              const float* C, int64_t ldc, bool allow_sk, bool allow_pack, Plan* pl);
 
 // Enqueues the plan on `stream`. status: device status word; ws: at least
-// pl->ws_bytes of device memory (may be null when ws_bytes == 0).
+// pl->ws_bytes of 256-byte-aligned device memory (may be null when
+// ws_bytes == 0).
 int launch_plan(Plan* pl, int* status, float* ws, cudaStream_t stream);
 
 // Human-readable plan name into buf ("none", "scale", or the kernel name,
-// with "+sk" when the stream-K tail is used).
+// with "+packA" / "+packB" for operands copied to aligned buffers and "+sk"
+// when the stream-K tail is used).
 void plan_name(const Plan& pl, char* buf, int buflen);
 
 // Records a CUDA error for sgemm_last_cuda_error and returns `code`.

@@ -88,7 +88,10 @@ extern "C" int sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alpha, const
     unsigned char* scratch = nullptr;
     if ((rc = scratch_address(dev->device, &scratch)) != SGEMM_OK) return rc;
     Plan pl;
-    if ((rc = make_plan(dev, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, true, &pl)) != SGEMM_OK)
+    // No packed copies of unaligned operands here: they would not fit the
+    // scratch for large problems, so such operands keep the cp.async loads.
+    if ((rc = make_plan(dev, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, true, false, &pl)) !=
+        SGEMM_OK)
         return rc;
     // The stream-K workspace must fit in the fixed scratch: 2 slots of
     // 128 x 128 floats per SM, 19.5 MB on a 152-SM GB300.

@@ -22,14 +22,16 @@
  * All pointers are DEVICE pointers on the current CUDA device, owned by the
  * caller. The library keeps per-device set-up state (created on the first
  * call on a device: device properties, kernel attributes, a 256-byte device
- * status word and a private stream-ordered memory pool). When a problem's
- * last wave of tiles is split across all SMs (the stream-K tail), the call
- * takes a workspace of at most 2 x SMs x 64 KB from that pool with
- * cudaMallocFromPoolAsync on the call's stream and returns it with
- * cudaFreeAsync on the same stream, so concurrent calls on different
- * streams never share it and stream capture records it as an allocation
- * node. If that allocation fails the call falls back to the plain
- * data-parallel schedule.
+ * status word and a private stream-ordered memory pool). Two kinds of call
+ * take a workspace from that pool with cudaMallocFromPoolAsync on the call's
+ * stream and return it with cudaFreeAsync on the same stream (so concurrent
+ * calls on different streams never share it and stream capture records it
+ * as an allocation node): a problem whose last wave of tiles is split across
+ * all SMs (the stream-K tail, at most 2 x SMs x 64 KB), and an operand that
+ * TMA cannot load in place (base or leading dimension not 16-byte aligned)
+ * but that the kernel reads often enough (A when N >= 256, B when M >= 256)
+ * is first copied to an aligned buffer (rows x cols rounded up to 4 floats).
+ * If that allocation fails the call uses neither.
  */
 #ifndef SGEMM_GB300_H
 #define SGEMM_GB300_H
@@ -116,9 +118,10 @@ SGEMM_API int sgemm_last_cuda_error(void);
  * sgemm_plan — describe, without launching, the kernel sgemm would use for
  * these arguments: writes a NUL-terminated name such as
  * "ws_128x128x32_s4_Atma_Btma" into buf (at most buflen bytes) and the
- * launch grid into *grid (if not NULL). A "+sk" suffix means the last wave
- * is split across the SMs (stream-K) and finished by a second, small fixup
- * kernel. Returns the same argument errors as sgemm, or SGEMM_OK. A name of
+ * launch grid into *grid (if not NULL). "+packA" / "+packB" mean that
+ * operand is first copied to an aligned buffer by a small copy kernel; a
+ * "+sk" suffix means the last wave is split across the SMs (stream-K) and
+ * finished by a second, small fixup kernel. Returns the same argument errors as sgemm, or SGEMM_OK. A name of
  * "scale" means the alpha == 0 / K == 0 path; "none" means M == 0 or N == 0.
  */
 SGEMM_API int sgemm_plan(int64_t M, int64_t N, int64_t K, float alpha, const float* A, int64_t lda,

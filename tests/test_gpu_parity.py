@@ -85,13 +85,40 @@ def test_leading_dims_and_offsets(config, layout):
 
 
 def test_tma_chosen_only_when_aligned():
-    A, B, C0 = gen(256, 256, 256, seed=8)
+    # 128 x 128: operands that TMA cannot describe are read too rarely to be
+    # worth an aligned copy, so they take cp.async.
+    A, B, C0 = gen(128, 128, 256, seed=8)
     _, _, plan = gpu_util.run(1.0, A, B, 0.0, C0)
-    assert "Atma_Btma" in plan[0], plan
+    assert "Atma_Btma" in plan[0] and "pack" not in plan[0], plan
     _, _, plan = gpu_util.run(1.0, A, B, 0.0, C0, lda=257)
     assert "Acp_Btma" in plan[0], plan
     _, _, plan = gpu_util.run(1.0, A, B, 0.0, C0, offsets=(0, 1, 0))
     assert "Atma_Bcp" in plan[0], plan
+
+
+@pytest.mark.parametrize("layout,tags", [
+    (dict(lda=1003), ["+packA"]),
+    (dict(ldb=515), ["+packB"]),
+    (dict(lda=1001, ldb=514, offsets=(1, 3, 0)), ["+packA", "+packB"]),
+    (dict(offsets=(2, 0, 1), ldc=513), ["+packA"]),
+], ids=["A", "B", "AB", "A_base_C_odd"])
+def test_unaligned_operands_packed_then_tma(layout, tags):
+    M, N, K = 300, 512, 1000
+    A, B, C0 = gen(M, N, K, seed=9)
+    C, guards, plan = gpu_util.run(0.7, A, B, -1.3, C0, **layout)
+    assert guards
+    assert "Atma_Btma" in plan[0], plan
+    for t in tags:
+        assert t in plan[0], plan
+    check_full(0.7, A, B, -1.3, C0, C)
+    # Forcing cp.async turns the copies off.
+    assert sg.sgemm_set_config("auto:cpasync") == 0
+    try:
+        C2, _, plan2 = gpu_util.run(0.7, A, B, -1.3, C0, **layout)
+        assert "pack" not in plan2[0] and "Acp_Bcp" in plan2[0], plan2
+        check_full(0.7, A, B, -1.3, C0, C2)
+    finally:
+        sg.sgemm_set_config("auto")
 
 
 @pytest.mark.parametrize("config", ["auto", "128x128", "64x64", "128x128:cpasync"], indirect=True)
@@ -237,7 +264,8 @@ def test_workload_sq4096_uniform_sampled():
 
 def test_workload_ragged_every_element():
     rep, plan = _workload("ragged_4093x5120x1531_normal", full=True)
-    assert "Acp_Btma" in plan[0], plan        # lda = 1531 is not 16-byte aligned
+    # lda = 1531 is not 16-byte aligned: A is copied to an aligned buffer.
+    assert "Atma_Btma+packA" in plan[0], plan
 
 
 def test_workload_llm_projection_sampled():
