@@ -193,6 +193,23 @@ def cpu_baseline(w, A, B, C0, rows: int):
 
 
 # ---------------------------------------------------------------------------
+def max_over_ranks(x: float, world: int, device: str = "cuda") -> float:
+    """The largest x over all ranks (x itself when world == 1)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(flops_per_rank: float, ms_per_step: float, world: int) -> float:
+    """GFLOP/s of `world` independent replicas: every rank's work divided by
+    the slowest rank's time per step (ms_per_step must already be the max)."""
+    return world * flops_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -354,15 +371,12 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     sg.check_status()
     launch_ms = [a.elapsed_time(b) for a, b in ev]
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world)
 
     flops = w.flops
     ms_step = total_ms / args.steps
     kernel_ms = statistics.mean(launch_ms)
-    value = world * flops / (ms_step * 1e-3) / 1e9
+    value = replica_throughput(flops, ms_step, world)
 
     # End to end through the public API with host buffers.
     hA = torch.from_numpy(A).pin_memory()
@@ -392,10 +406,7 @@ def run_ours(args, w):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world)
     sg.check_status()
 
     if rank != 0:
@@ -428,7 +439,7 @@ def run_ours(args, w):
                      "kernel_ms_covers": "every kernel of one sgemm call",
                      "traffic": traffic, "traffic_note": traffic_note},
         "clocks": clocks,
-        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e9, "unit": "GFLOP/s",
+        "e2e": {"value": replica_throughput(flops, e2e_ms, world), "unit": "GFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": args.steps * launches_per_step,
         "gpu_launches_note": ("per step: the sgemm kernel" +
