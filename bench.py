@@ -19,6 +19,11 @@ CUDA-core peak (SMs x 128 lanes x 2 FLOP x max SM clock, ``bound: alu``);
 metric's denominator). ``cpu_baseline`` is the double-accumulating CPU
 oracle timed on this host on a row block of the same problem.
 
+``tcgen05_3xtf32`` times the separately reported tensor-core entry point
+(sgemm_3xtf32: TF32 hi/lo split, three tcgen05 MMAs per product, FP32
+accumulation, same error bound) on the same workload, with its own roofline
+against the TF32 tensor peak.
+
 ``--impl reference`` times that CPU oracle instead (the reference arm): each
 step is a bounded row block of the workload.
 
@@ -59,6 +64,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--peak-ms", type=float, default=300.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-tf32x3", action="store_true",
+                    help="skip the separately reported tcgen05 3xTF32 measurement")
     ap.add_argument("--cpu-rows", type=int, default=0,
                     help="rows of C in the CPU baseline sample (0: sized to ~10 s)")
     return ap.parse_args()
@@ -378,6 +385,46 @@ def run_ours(args, w):
     kernel_ms = statistics.mean(launch_ms)
     value = replica_throughput(flops, ms_step, world)
 
+    # The tcgen05 3xTF32 path, reported separately (same workload, same
+    # FP32 error bound, different arithmetic unit).
+    tf32x3 = None
+    if not args.no_tf32x3:
+        call3 = call
+        for _ in range(3):
+            rc = lib.sgemm_3xtf32(*call3)
+            if rc != 0:
+                raise sg.SgemmError("sgemm_3xtf32", rc)
+        torch.cuda.synchronize()
+        n3 = max(10, args.steps // 5)
+        x0 = torch.cuda.Event(enable_timing=True)
+        x1 = torch.cuda.Event(enable_timing=True)
+        x0.record(stream)
+        for _ in range(n3):
+            if flush is not None:
+                flush.zero_()
+            rc = lib.sgemm_3xtf32(*call3)
+            if rc != 0:
+                raise sg.SgemmError("sgemm_3xtf32", rc)
+        x1.record(stream)
+        torch.cuda.synchronize()
+        sg.check_status()
+        ms3 = max_over_ranks(x0.elapsed_time(x1) / n3, world)
+        mp_ = measured_peaks()
+        bf16 = float(mp_.get("bf16_tflops") or 1900.0)
+        tf32_peak = bf16 * (1.1 / 2.25)      # nominal TF32 : BF16 dense ratio
+        tf32_rate = 3.0 * flops / (ms3 * 1e-3) / 1e12
+        tf32x3 = {"value": replica_throughput(flops, ms3, world), "unit": "GFLOP/s",
+                  "ms_per_step": ms3, "steps": n3,
+                  "note": "sgemm_3xtf32: A, B split into TF32 hi/lo, 3 tcgen05 MMAs per product, "
+                          "FP32 accumulation in TMEM; same FP32 error bound; times include the "
+                          "split pre-passes" + (" and the L2 flush" if flush is not None else ""),
+                  "roofline": {"bound": "tensor", "achieved": tf32_rate, "peak": tf32_peak,
+                               "unit": "TFLOP/s", "frac": tf32_rate / tf32_peak,
+                               "peak_basis": f"measured bf16 {bf16:.1f} TFLOP/s x 1.1/2.25 "
+                                             "(nominal TF32:BF16 dense ratio)",
+                               "achieved_basis": "3 x 2MNK TF32 FLOP per step / step time"},
+                  "gpu_launches_per_step": 3}
+
     # End to end through the public API with host buffers.
     hA = torch.from_numpy(A).pin_memory()
     hB = torch.from_numpy(B).pin_memory()
@@ -448,6 +495,8 @@ def run_ours(args, w):
                               (" + packing copy of B" if "+packB" in kernel else "")) + (
             " (plus one torch L2-flush fill, not ours)" if flush is not None else ""),
     }
+    if tf32x3 is not None:
+        line["tcgen05_3xtf32"] = tf32x3
     if world > 1:
         torch.distributed.destroy_process_group()
     if not args.no_cpu_baseline:

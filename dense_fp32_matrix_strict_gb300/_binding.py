@@ -24,7 +24,7 @@ SGEMM_ERR_CUDA = 5
 EXPORTED_SYMBOLS = (
     "sgemm", "sgemm_check_status", "sgemm_error_string", "sgemm_last_cuda_error",
     "sgemm_plan", "sgemm_set_config", "sgemm_set_wait_timeout_ns", "sgemm_fp32_peak",
-    "sgemm_selftest_wait_timeout", "sgemm_config_names", "sgemm_noalloc",
+    "sgemm_selftest_wait_timeout", "sgemm_config_names", "sgemm_noalloc", "sgemm_3xtf32",
 )
 
 _lock = threading.Lock()
@@ -83,6 +83,8 @@ def load():
         lib.sgemm_selftest_wait_timeout.restype = ci
         lib.sgemm_noalloc.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
         lib.sgemm_noalloc.restype = ci
+        lib.sgemm_3xtf32.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
+        lib.sgemm_3xtf32.restype = ci
         _lib = lib
         return lib
 
@@ -104,6 +106,11 @@ def sgemm_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int
     """sgemm without any device allocation (fixed scratch inside the library);
     device pointers as ints; returns the raw code."""
     return load().sgemm_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def sgemm_3xtf32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
+    """The tcgen05 3xTF32 path (device pointers as ints); returns the raw code."""
+    return load().sgemm_3xtf32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
 
 
 def sgemm_check_status(stream=0):
@@ -232,6 +239,22 @@ def sgemm_tensors(alpha, A, B, beta, C, stream=None) -> None:
                           float(beta), C.data_ptr(), ldc, _stream_handle(stream, C.device))
     if rc != SGEMM_OK:
         raise SgemmError("sgemm", rc)
+
+
+def sgemm_3xtf32_tensors(alpha, A, B, beta, C, stream=None) -> None:
+    """sgemm_tensors through the tcgen05 3xTF32 entry point."""
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError(f"inner dimensions differ: A is {tuple(A.shape)}, B is {tuple(B.shape)}")
+    lda = _ld(A, M, K, "A")
+    ldb = _ld(B, K, N, "B")
+    ldc = _ld(C, M, N, "C")
+    with _on_device(C.device):
+        rc = load().sgemm_3xtf32(M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(), ldb,
+                                 float(beta), C.data_ptr(), ldc, _stream_handle(stream, C.device))
+    if rc != SGEMM_OK:
+        raise SgemmError("sgemm_3xtf32", rc)
 
 
 def plan_tensors(alpha, A, B, beta, C):

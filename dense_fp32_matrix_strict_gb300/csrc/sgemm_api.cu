@@ -503,6 +503,19 @@ void plan_name(const Plan& pl, char* buf, int buflen) {
                        pl.sk_tiles > 0 ? "+sk" : "");
 }
 
+int device_memory_handles(const DeviceInfo* dev, int** status, cudaMemPool_t* pool) {
+    DeviceMemory* mem = nullptr;
+    const int rc = device_memory(dev, &mem);
+    if (rc != SGEMM_OK) return rc;
+    *status = mem->status;
+    *pool = mem->pool;
+    return SGEMM_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() { return g_encode; }
+
+unsigned long long wait_timeout_ns() { return g_timeout_ns.load(); }
+
 int launch_selftest_wait(unsigned long long timeout_ns, int* status, cudaStream_t stream) {
     GemmParams p;
     std::memset(&p, 0, sizeof(p));

@@ -9,6 +9,7 @@
 #include <cstdint>
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "kernels.h"
@@ -73,5 +74,15 @@ void plan_name(const Plan& pl, char* buf, int buflen);
 
 // Records a CUDA error for sgemm_last_cuda_error and returns `code`.
 int cuda_fail(cudaError_t e, int code);
+
+// The status word and the workspace pool of the regular entry points on the
+// current device (allocated on first use).
+int device_memory_handles(const DeviceInfo* dev, int** status, cudaMemPool_t* pool);
+
+// cuTensorMapEncodeTiled, resolved by device_info().
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
+// Current limit of the kernels' bounded waits.
+unsigned long long wait_timeout_ns();
 
 }  // namespace sg

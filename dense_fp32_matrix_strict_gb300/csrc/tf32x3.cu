@@ -1,0 +1,518 @@
+// tf32x3.cu — sgemm_3xtf32: FP32 SGEMM on the 5th-generation tensor cores
+// (tcgen05, TMEM accumulators) by the three-term TF32 split.
+//
+// Every FP32 input x is split into x_hi = tf32(x) and x_lo = tf32(x - x_hi)
+// (round to nearest, ties away). Then
+//     a * b ~ a_hi*b_hi + a_hi*b_lo + a_lo*b_hi,
+// where each TF32 x TF32 product is exact in FP32 and only a_lo*b_lo
+// (|.| <= 2^-22 |a b|) and the split remainders (|x - x_hi - x_lo| <=
+// 2^-22 |x|) are dropped: about 3 * 2^-22 |a b| per product, i.e. within the
+// library's FP32 bound 4 K 2^-24 (|alpha| sum|a b| + |beta c|) for K >= 3.
+// The tensor cores accumulate in FP32 in TMEM. This path is optional and
+// reported separately from the FFMA kernels; the pages measure TF32 only as
+// a faster, less accurate mode (Tinyforge README: cuBLAS TF32 7,728 GFLOPS,
+// failing the FP32 tolerance) and do not describe a split.
+//
+// Steps per call (all on the caller's stream):
+//   1. tf32_split_rows: A (M x K, lda) -> A_hi, A_lo (M x Kp, Kp = K rounded
+//      up to 4), K-major as A already is.
+//   2. tf32_split_transpose: B (K x N, ldb) -> B_hi^T, B_lo^T (N x Kp): the
+//      MMA takes both operands K-major.
+//   3. tf32x3_kernel: persistent, one CTA per SM, 128 x BN output tiles
+//      (BN = 128 with a 3-stage ring by default, 256 with 2 stages).
+//      warp 0: TMA producer (one thread) filling the ring, each stage the
+//              128 x 32 A_hi/A_lo and BN x 32 B_hi/B_lo tiles (64 or 96 KB,
+//              128-byte swizzle);
+//      warp 1: allocates 2 BN TMEM columns (two 128 x BN FP32 accumulators)
+//              and one thread issues tcgen05.mma.kind::tf32 (M 128, N BN,
+//              K 8): for each 8-wide k-slice, hi*hi, hi*lo and lo*hi into the
+//              tile's accumulator; tcgen05.commit releases the stage and, at
+//              the end of a tile, hands the accumulator to the epilogue;
+//      warps 2-5: the epilogue: tcgen05.ld of their 32 TMEM lanes (rows),
+//              C = alpha * acc + beta * C, then release the accumulator.
+//   Every wait is bounded; all roles meet at one exit where the MMA thread
+//   has waited for its MMAs and warp 1 frees the TMEM.
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "sgemm.h"
+#include "sgemm_internal.h"
+
+namespace sg {
+namespace tf32x3 {
+
+constexpr int BM = 128, BK = 32;
+constexpr int THREADS = 192;
+constexpr int A_BYTES = BM * BK * 4;        // 16 KB
+
+// Tile width BN (the MMA's N) and ring depth. Two accumulators of BN TMEM
+// columns each, so the epilogue of one tile overlaps the MMAs of the next.
+template <int BN_, int STAGES_>
+struct TcCfg {
+    static constexpr int BN = BN_, STAGES = STAGES_;
+    static constexpr int B_BYTES = BN * BK * 4;
+    static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+    static_assert(BN == 128 || BN == 256, "MMA N");
+    static_assert(SMEM_BYTES <= 227 * 1024, "ring too large");
+    // Instruction descriptor of kind::tf32: D FP32 (bits 4-5 = 1), A and B
+    // TF32 (bits 7-9 and 10-12 = 2), both K-major (bits 15, 16 = 0), N >> 3
+    // in bits 17-22, M >> 4 in bits 24-28.
+    static constexpr uint32_t IDESC = (1u << 4) | (2u << 7) | (2u << 10) |
+                                      (static_cast<uint32_t>(BN >> 3) << 17) |
+                                      (static_cast<uint32_t>(BM >> 4) << 24);
+};
+
+struct Params {
+    int M, N, K;
+    int tiles_m, tiles_n, k_tiles, group_m;
+    int c_vec;
+    float* C;
+    long long ldc;
+    float alpha, beta;
+    unsigned long long timeout_ns;
+    int* status;
+};
+
+// ---- tcgen05 helpers ---------------------------------------------------------
+
+// Shared-memory operand descriptor for a K-major tile with the 128-byte
+// swizzle: rows of 128 bytes, 8-row (1024-byte) swizzle atoms stacked along
+// M/N. Fields: start address >> 4 (bits 0-13), leading byte offset >> 4
+// (bits 16-29; not used by swizzled K-major layouts, set to 1), stride byte
+// offset >> 4 (bits 32-45: 1024 bytes between 8-row groups), descriptor
+// version 1 (bits 46-47), swizzle mode 2 = 128-byte (bits 61-63).
+__device__ __forceinline__ uint64_t desc_k_sw128(uint32_t smem_addr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>(1u) << 16;
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t acc) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
+                 :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+
+// Arrive once on bar when every tcgen05.mma this thread issued has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive FP32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                   "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
+                   "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+                   "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+                   "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ float to_tf32(float x) {
+    uint32_t h;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(h) : "f"(x));
+    return __uint_as_float(h);
+}
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Params& p, int code) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > p.timeout_ns) {
+            atomicOr(p.status, code);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tile_of(int t, const Params& p, int& tm, int& tn) {
+    const int per_group = p.group_m * p.tiles_n;
+    const int g = t / per_group;
+    const int first = g * p.group_m;
+    const int gm = min(p.tiles_m - first, p.group_m);
+    const int r = t - g * per_group;
+    tm = first + r % gm;
+    tn = r / gm;
+}
+
+// ---- split pre-passes ---------------------------------------------------------
+
+// hi/lo (rows x ldd) <- src (rows x cols, row stride lds), zeros in the
+// padding columns [cols, ldd).
+__global__ void split_rows_kernel(const float* __restrict__ src, long long lds, float* __restrict__ hi,
+                                  float* __restrict__ lo, long long ldd, int rows, int cols) {
+    const long long total = static_cast<long long>(rows) * ldd;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long r = i / ldd;
+        const long long c = i - r * ldd;
+        const float x = c < cols ? src[r * lds + c] : 0.0f;
+        const float h = to_tf32(x);
+        hi[i] = h;
+        lo[i] = to_tf32(x - h);
+    }
+}
+
+// hiT/loT (cols x ldd) <- transpose of src (rows x cols, row stride lds):
+// hiT[j][k] = split(src[k][j]); zeros for k in [rows, ldd). 32 x 32 tiles
+// through shared memory so both sides stay coalesced.
+__global__ void split_transpose_kernel(const float* __restrict__ src, long long lds,
+                                       float* __restrict__ hiT, float* __restrict__ loT,
+                                       long long ldd, int rows, int cols) {
+    __shared__ float tile[32][33];
+    const int tiles_k = static_cast<int>((ldd + 31) / 32);
+    const int tiles_n = (cols + 31) / 32;
+    for (int t = blockIdx.x; t < tiles_k * tiles_n; t += gridDim.x) {
+        const int k0 = (t / tiles_n) * 32, n0 = (t % tiles_n) * 32;
+        for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+            const int k = k0 + r, n = n0 + threadIdx.x;
+            tile[r][threadIdx.x] = (k < rows && n < cols) ? src[static_cast<long long>(k) * lds + n] : 0.0f;
+        }
+        __syncthreads();
+        for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+            const int n = n0 + r, k = k0 + threadIdx.x;
+            if (n < cols && k < ldd) {
+                const float x = tile[threadIdx.x][r];
+                const float h = to_tf32(x);
+                const long long o = static_cast<long long>(n) * ldd + k;
+                hiT[o] = h;
+                loT[o] = to_tf32(x - h);
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// ---- the tensor-core kernel ---------------------------------------------------
+
+template <class T>
+__global__ void __launch_bounds__(THREADS, 1)
+tf32x3_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmAl,
+              const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmBl,
+              const Params p) {
+    constexpr int BN = T::BN, STAGES = T::STAGES, B_BYTES = T::B_BYTES;
+    constexpr int STAGE_BYTES = T::STAGE_BYTES, TMEM_COLS = T::TMEM_COLS;
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t s0 = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    // barriers: full[2], empty[2], acc_full[2], acc_empty[2], done; then the TMEM address
+    const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * STAGES;
+    const uint32_t accf0 = empty0 + 8 * STAGES, acce0 = accf0 + 16, done_bar = acce0 + 16;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf0 + 8 * b, 1);
+            mbar_init(acce0 + 8 * b, 128);
+        }
+        mbar_init(done_bar, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     :: "r"(smem_u32(tmem_slot)), "r"(TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int num_tiles = p.tiles_m * p.tiles_n;
+    if (warp == 0) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tmAh);
+            tma_prefetch_desc(&tmAl);
+            tma_prefetch_desc(&tmBh);
+            tma_prefetch_desc(&tmBl);
+            int s = 0;
+            uint32_t ph = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                int tm, tn;
+                tile_of(t, p, tm, tn);
+                for (int kt = 0; kt < p.k_tiles; ++kt) {
+                    if (!wait_bar(empty0 + 8 * s, ph ^ 1u, p, STATUS_PRODUCER_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t full = full0 + 8 * s;
+                    const uint32_t st = s0 + s * STAGE_BYTES;
+                    mbar_arrive_expect_tx(full, STAGE_BYTES);
+                    tma_load_2d(st, &tmAh, full, kt * BK, tm * BM);
+                    tma_load_2d(st + A_BYTES, &tmAl, full, kt * BK, tm * BM);
+                    tma_load_2d(st + 2 * A_BYTES, &tmBh, full, kt * BK, tn * BN);
+                    tma_load_2d(st + 2 * A_BYTES + B_BYTES, &tmBl, full, kt * BK, tn * BN);
+                    ++issued;
+                    if (++s == STAGES) { s = 0; ph ^= 1u; }
+                }
+            }
+            if (!ok) {
+                // Let this thread's copies land before the CTA can exit.
+                const int n = issued < STAGES ? issued : STAGES;
+                int ss = s;
+                uint32_t pp = ph;
+                for (int i = 0; i < n; ++i) {
+                    if (--ss < 0) { ss = STAGES - 1; pp ^= 1u; }
+                    wait_bar(full0 + 8 * ss, pp, p, STATUS_DRAIN_TIMEOUT);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++it) {
+                const int b = it & 1;
+                const uint32_t acc_phase = static_cast<uint32_t>((it >> 1) & 1);
+                // Wait until the epilogue has emptied this accumulator.
+                if (!wait_bar(acce0 + 8 * b, acc_phase ^ 1u, p, STATUS_CONSUMER_TIMEOUT)) break;
+                fence_after();
+                const uint32_t d = tmem + static_cast<uint32_t>(b * BN);
+                for (int kt = 0; kt < p.k_tiles; ++kt) {
+                    if (!wait_bar(full0 + 8 * s, ph, p, STATUS_CONSUMER_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after();
+                    const uint32_t st = s0 + s * STAGE_BYTES;
+                    const uint64_t ah = desc_k_sw128(st), al = desc_k_sw128(st + A_BYTES);
+                    const uint64_t bh = desc_k_sw128(st + 2 * A_BYTES);
+                    const uint64_t bl = desc_k_sw128(st + 2 * A_BYTES + B_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 8; ++kk) {
+                        // 8 TF32 = 32 bytes further along the swizzled row.
+                        const uint64_t off = static_cast<uint64_t>((kk * 32) >> 4);
+                        const uint32_t first = (kt == 0 && kk == 0) ? 0u : 1u;
+                        mma_tf32(d, ah + off, bh + off, T::IDESC, first);
+                        mma_tf32(d, ah + off, bl + off, T::IDESC, 1u);
+                        mma_tf32(d, al + off, bh + off, T::IDESC, 1u);
+                    }
+                    mma_commit(empty0 + 8 * s);          // stage free once these finish
+                    if (++s == STAGES) { s = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                mma_commit(accf0 + 8 * b);               // accumulator ready
+            }
+            // Every MMA this thread issued has finished before TMEM is freed.
+            mma_commit(done_bar);
+            wait_bar(done_bar, 0, p, STATUS_DRAIN_TIMEOUT);
+        }
+    } else {
+        // Epilogue warpgroup: warp w reads TMEM lanes 32 (w % 4) .. + 31.
+        const int q = warp & 3;
+        int it = 0;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
+            const int b = it & 1;
+            const uint32_t acc_phase = static_cast<uint32_t>((it >> 1) & 1);
+            if (!wait_bar(accf0 + 8 * b, acc_phase, p, STATUS_CONSUMER_TIMEOUT)) break;
+            __syncwarp();          // tcgen05.ld is warp-collective: reconverge first
+            fence_after();
+            int tm, tn;
+            tile_of(t, p, tm, tn);
+            const int m = tm * BM + 32 * q + lane;
+            const bool row_ok = m < p.M;
+            float* crow = p.C + static_cast<long long>(row_ok ? m : 0) * p.ldc;
+            const bool use_c = p.beta != 0.0f;
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                float v[32];
+                tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) +
+                              static_cast<uint32_t>(b * BN + ch * 32), v);
+                if (!row_ok) continue;
+                const int n0 = tn * BN + ch * 32;
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    const int n = n0 + j;
+                    float o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[e] = p.alpha * v[j + e];
+                    if (p.c_vec && n + 3 < p.N) {
+                        float4* cp = reinterpret_cast<float4*>(crow + n);
+                        if (use_c) {
+                            const float4 c = *cp;
+                            o[0] = fmaf(p.beta, c.x, o[0]);
+                            o[1] = fmaf(p.beta, c.y, o[1]);
+                            o[2] = fmaf(p.beta, c.z, o[2]);
+                            o[3] = fmaf(p.beta, c.w, o[3]);
+                        }
+                        *cp = make_float4(o[0], o[1], o[2], o[3]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            if (n + e < p.N) {
+                                float out = o[e];
+                                if (use_c) out = fmaf(p.beta, crow[n + e], out);
+                                crow[n + e] = out;
+                            }
+                        }
+                    }
+                }
+            }
+            fence_before();
+            mbar_arrive(acce0 + 8 * b);                 // accumulator may be reused
+        }
+    }
+
+    // Single exit: every role is done (or gave up after its bounded waits),
+    // the MMA thread has seen its MMAs finish; free the TMEM.
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                     :: "r"(tmem), "r"(TMEM_COLS) : "memory");
+    }
+}
+
+bool encode(CUtensorMap* map, const float* base, int64_t rows, int64_t cols, int64_t ld, int box_rows,
+            PFN_cuTensorMapEncodeTiled_v12000 enc) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tile width of the tensor-core kernel: 128 (default) or 256, from the
+// environment variable SGEMM_3XTF32_TILE ("128x128" or "128x256").
+int tile_width(const DeviceInfo*) {
+    static const int w = [] {
+        const char* env = std::getenv("SGEMM_3XTF32_TILE");
+        return (env != nullptr && std::strcmp(env, "128x256") == 0) ? 256 : 128;
+    }();
+    return w;
+}
+
+template <class T>
+cudaError_t launch(const DeviceInfo* dev, const float* a_hi, const float* a_lo, const float* b_hi,
+                   const float* b_lo, int64_t kp, Params p, cudaStream_t stream) {
+    static bool attr_set[64] = {};
+    if (!attr_set[dev->device]) {
+        const cudaError_t e = cudaFuncSetAttribute(tf32x3_kernel<T>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   T::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set[dev->device] = true;
+    }
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    CUtensorMap mah, mal, mbh, mbl;
+    if (!(encode(&mah, a_hi, p.M, p.K, kp, BM, enc) && encode(&mal, a_lo, p.M, p.K, kp, BM, enc) &&
+          encode(&mbh, b_hi, p.N, p.K, kp, T::BN, enc) && encode(&mbl, b_lo, p.N, p.K, kp, T::BN, enc)))
+        return cudaErrorInvalidValue;
+    p.tiles_n = (p.N + T::BN - 1) / T::BN;
+    const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+    const int grid = static_cast<int>(tiles < dev->sm_count ? tiles : dev->sm_count);
+    tf32x3_kernel<T><<<grid, THREADS, T::SMEM_BYTES, stream>>>(mah, mal, mbh, mbl, p);
+    return cudaGetLastError();
+}
+
+}  // namespace tf32x3
+}  // namespace sg
+
+using namespace sg;
+
+extern "C" int sgemm_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                            int64_t lda, const float* B, int64_t ldb, float beta, float* C,
+                            int64_t ldc, cudaStream_t stream) {
+    int rc = check_args(M, N, K, alpha, A, lda, B, ldb, C, ldc);
+    if (rc != SGEMM_OK) return rc;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    // Short reductions (the dropped lo*lo terms are not covered by the bound
+    // below K = 3), alpha == 0 and K == 0 go to the FFMA path.
+    if (K < 16 || alpha == 0.0f) return sgemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+    const DeviceInfo* dev = nullptr;
+    if ((rc = device_info(&dev)) != SGEMM_OK) return rc;
+    int* status = nullptr;
+    cudaMemPool_t pool = nullptr;
+    if ((rc = device_memory_handles(dev, &status, &pool)) != SGEMM_OK) return rc;
+    using namespace tf32x3;
+    const int64_t kp = (K + 3) & ~int64_t{3};
+    const size_t a_bytes = static_cast<size_t>(M) * static_cast<size_t>(kp) * 4;
+    const size_t b_bytes = static_cast<size_t>(N) * static_cast<size_t>(kp) * 4;
+    const size_t a_pad = (a_bytes + 255) & ~size_t{255}, b_pad = (b_bytes + 255) & ~size_t{255};
+    void* w = nullptr;
+    if (cudaMallocFromPoolAsync(&w, 2 * a_pad + 2 * b_pad, pool, stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return sgemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+    }
+    unsigned char* ws = static_cast<unsigned char*>(w);
+    float* a_hi = reinterpret_cast<float*>(ws);
+    float* a_lo = reinterpret_cast<float*>(ws + a_pad);
+    float* b_hi = reinterpret_cast<float*>(ws + 2 * a_pad);
+    float* b_lo = reinterpret_cast<float*>(ws + 2 * a_pad + b_pad);
+    const int sms = dev->sm_count;
+    cudaError_t e;
+    split_rows_kernel<<<16 * sms, 256, 0, stream>>>(A, lda, a_hi, a_lo, kp, static_cast<int>(M),
+                                                    static_cast<int>(K));
+    if ((e = cudaGetLastError()) == cudaSuccess)
+        split_transpose_kernel<<<16 * sms, dim3(32, 8), 0, stream>>>(B, ldb, b_hi, b_lo, kp,
+                                                                     static_cast<int>(K),
+                                                                     static_cast<int>(N));
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e == cudaSuccess) {
+        Params p;
+        std::memset(&p, 0, sizeof(p));
+        p.M = static_cast<int>(M);
+        p.N = static_cast<int>(N);
+        p.K = static_cast<int>(K);
+        p.tiles_m = static_cast<int>((M + BM - 1) / BM);
+        p.k_tiles = static_cast<int>((K + BK - 1) / BK);
+        p.group_m = 8;
+        p.c_vec = ((reinterpret_cast<uintptr_t>(C) % 16) == 0 && (ldc % 4) == 0) ? 1 : 0;
+        p.C = C;
+        p.ldc = ldc;
+        p.alpha = alpha;
+        p.beta = beta;
+        p.timeout_ns = wait_timeout_ns();
+        p.status = status;
+        const bool wide = tile_width(dev) == 256;
+        e = wide ? launch<TcCfg<256, 2>>(dev, a_hi, a_lo, b_hi, b_lo, kp, p, stream)
+                 : launch<TcCfg<128, 3>>(dev, a_hi, a_lo, b_hi, b_lo, kp, p, stream);
+    }
+    cudaFreeAsync(w, stream);
+    if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
+    return SGEMM_OK;
+}

@@ -180,6 +180,28 @@ SGEMM_API int sgemm_fp32_peak(double target_ms, double* gflops, double* ms, doub
 SGEMM_API int sgemm_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stream);
 
 /*
+ * sgemm_3xtf32 — the same operation, arguments and errors as sgemm, computed
+ * on the tcgen05 tensor cores with the three-term TF32 split: each FP32
+ * input x = x_hi + x_lo (x_hi = tf32(x), x_lo = tf32(x - x_hi)) and
+ * a*b ~ a_hi*b_hi + a_hi*b_lo + a_lo*b_hi with FP32 accumulation in TMEM.
+ * The dropped terms are at most about 3 * 2^-22 |a b| per product, which
+ * keeps every element within the FP32 bound 4 K 2^-24 (|alpha| sum|a b| +
+ * |beta c|) for K >= 3; calls with K < 16 or alpha == 0 run the FFMA path
+ * (sgemm). It is reported separately from the strict FFMA path: the tensor
+ * cores do not round every accumulation step like FFMA, so results differ
+ * from sgemm's in the last bits. The pages measure TF32 only as an inexact
+ * mode and describe no split; this entry point is this library's own.
+ *
+ * Each call splits A and the transpose of B into a workspace of
+ * 8 * (M + N) * K bytes (K rounded up to 4) taken from the library's
+ * stream-ordered pool, so it allocates like sgemm's stream-K tail; if that
+ * allocation fails it runs sgemm instead.
+ */
+SGEMM_API int sgemm_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                           int64_t lda, const float* B, int64_t ldb, float beta, float* C,
+                           int64_t ldc, cudaStream_t stream);
+
+/*
  * sgemm_noalloc — the same operation, arguments, results and errors as
  * sgemm, for callers that must not allocate device memory. The pages this
  * library follows have no counterpart: it exists for code that cannot call
