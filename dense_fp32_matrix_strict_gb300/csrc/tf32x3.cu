@@ -169,18 +169,31 @@ __device__ __forceinline__ void tile_of(int t, const Params& p, int& tm, int& tn
 // ---- split pre-passes ---------------------------------------------------------
 
 // hi/lo (rows x ldd) <- src (rows x cols, row stride lds), zeros in the
-// padding columns [cols, ldd).
+// padding columns [cols, ldd). ldd is a multiple of 4, so every thread writes
+// one float4 of each output; it reads a float4 too when `vec` (src 16-byte
+// aligned and lds % 4 == 0), else four scalars. blockIdx.y walks rows.
 __global__ void split_rows_kernel(const float* __restrict__ src, long long lds, float* __restrict__ hi,
-                                  float* __restrict__ lo, long long ldd, int rows, int cols) {
-    const long long total = static_cast<long long>(rows) * ldd;
-    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-         i += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const long long r = i / ldd;
-        const long long c = i - r * ldd;
-        const float x = c < cols ? src[r * lds + c] : 0.0f;
-        const float h = to_tf32(x);
-        hi[i] = h;
-        lo[i] = to_tf32(x - h);
+                                  float* __restrict__ lo, long long ldd, int rows, int cols, int vec) {
+    const int quads = static_cast<int>(ldd >> 2);
+    for (long long r = blockIdx.y; r < rows; r += gridDim.y) {
+        const float* srow = src + r * lds;
+        for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < quads; q += blockDim.x * gridDim.x) {
+            const int c = 4 * q;
+            float4 x;
+            if (vec && c + 3 < cols) {
+                x = *reinterpret_cast<const float4*>(srow + c);
+            } else {
+                x.x = c < cols ? srow[c] : 0.0f;
+                x.y = c + 1 < cols ? srow[c + 1] : 0.0f;
+                x.z = c + 2 < cols ? srow[c + 2] : 0.0f;
+                x.w = c + 3 < cols ? srow[c + 3] : 0.0f;
+            }
+            const float4 h = make_float4(to_tf32(x.x), to_tf32(x.y), to_tf32(x.z), to_tf32(x.w));
+            const float4 l = make_float4(to_tf32(x.x - h.x), to_tf32(x.y - h.y), to_tf32(x.z - h.z),
+                                         to_tf32(x.w - h.w));
+            *reinterpret_cast<float4*>(hi + r * ldd + c) = h;
+            *reinterpret_cast<float4*>(lo + r * ldd + c) = l;
+        }
     }
 }
 
@@ -485,8 +498,15 @@ extern "C" int sgemm_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, const 
     float* b_lo = reinterpret_cast<float*>(ws + 2 * a_pad + b_pad);
     const int sms = dev->sm_count;
     cudaError_t e;
-    split_rows_kernel<<<16 * sms, 256, 0, stream>>>(A, lda, a_hi, a_lo, kp, static_cast<int>(M),
-                                                    static_cast<int>(K));
+    {
+        const int vec = ((reinterpret_cast<uintptr_t>(A) % 16) == 0 && (lda % 4) == 0) ? 1 : 0;
+        const int64_t quads = kp / 4;
+        const int gx = static_cast<int>(quads < 256 * 8 ? (quads + 255) / 256 : 8);
+        const int gy = static_cast<int>(M < 8192 ? M : 8192);
+        split_rows_kernel<<<dim3(gx, gy), 256, 0, stream>>>(A, lda, a_hi, a_lo, kp,
+                                                           static_cast<int>(M), static_cast<int>(K),
+                                                           vec);
+    }
     if ((e = cudaGetLastError()) == cudaSuccess)
         split_transpose_kernel<<<16 * sms, dim3(32, 8), 0, stream>>>(B, ldb, b_hi, b_lo, kp,
                                                                      static_cast<int>(K),
