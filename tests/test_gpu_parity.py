@@ -376,3 +376,58 @@ def test_integer_inputs_bit_exact_with_stream_k():
     C, _, plan = gpu_util.run(2.0, A, B, -1.0, C0)
     assert plan[0].endswith("+sk"), plan
     check_full(2.0, A, B, -1.0, C0, C, exact=True)
+
+
+# ---- streams and graphs ----------------------------------------------------------
+
+def test_two_streams_concurrently_do_not_share_workspace():
+    # Both problems take the stream-K tail (a per-call workspace); run them
+    # back to back on two streams with no ordering between them.
+    torch = pytest.importorskip("torch")
+    M, N, K = 1000, 1100, 2000
+    A1, B1, C1 = gen(M, N, K, seed=401)
+    A2, B2, C2 = gen(M, N, K, seed=402)
+    d = [torch.from_numpy(x).cuda() for x in (A1, B1, C1, A2, B2, C2)]
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    for _ in range(3):
+        with torch.cuda.stream(s1):
+            c1 = d[2].clone()
+            sg.sgemm_tensors(0.7, d[0], d[1], -1.3, c1, stream=s1)
+        with torch.cuda.stream(s2):
+            c2 = d[5].clone()
+            sg.sgemm_tensors(0.7, d[3], d[4], -1.3, c2, stream=s2)
+    torch.cuda.synchronize()
+    sg.check_status()
+    check_full(0.7, A1, B1, -1.3, C1, c1.cpu().numpy())
+    check_full(0.7, A2, B2, -1.3, C2, c2.cpu().numpy())
+
+
+def test_sgemm_inside_a_captured_cuda_graph():
+    # The stream-K workspace is stream-ordered, so capture records it as an
+    # allocation node; the graph replays correctly. (The first call on the
+    # device, which allocates the status word, happens before capture.)
+    torch = pytest.importorskip("torch")
+    M, N, K = 1000, 1100, 2000
+    A, B, C0 = gen(M, N, K, seed=403)
+    dA = torch.from_numpy(A).cuda()
+    dB = torch.from_numpy(B).cuda()
+    dC = torch.from_numpy(C0).cuda()
+    name, _ = sg.plan_tensors(0.7, dA, dB, -1.3, dC)
+    assert name.endswith("+sk"), name
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        sg.sgemm_tensors(0.7, dA, dB, -1.3, dC.clone(), stream=s)   # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    work = dC.clone()
+    with torch.cuda.graph(g):
+        sg.sgemm_tensors(0.7, dA, dB, -1.3, work)
+    for _ in range(2):
+        work.copy_(dC)
+        g.replay()
+    torch.cuda.synchronize()
+    sg.check_status()
+    check_full(0.7, A, B, -1.3, C0, work.cpu().numpy())
