@@ -133,16 +133,26 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-def kernel_sources_digest() -> str:
+# Sources each timed kernel is built from (kernel body, PTX helpers, the
+# family instantiation, and the planner that picks grid and schedule). A
+# recorded DRAM-traffic figure is reused only while these files are unchanged.
+KERNEL_SOURCES = {
+    "ffma": ("sgemm_kernel.cuh", "ptx.cuh", "kernels.h", "sgemm_ws_128x128.cu",
+             "sgemm_ws_64x64.cu", "sgemm_api.cu", "sgemm_internal.h"),
+    "tf32x3": ("tf32x3.cu", "ptx.cuh", "sgemm_internal.h"),
+}
+
+
+def kernel_sources_digest(which: str = "ffma") -> str:
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "dense_fp32_matrix_strict_gb300", "csrc", "*"))):
-        with open(f, "rb") as fh:
-            h.update(os.path.basename(f).encode())
+    for name in sorted(KERNEL_SOURCES[which]):
+        with open(os.path.join(ROOT, "dense_fp32_matrix_strict_gb300", "csrc", name), "rb") as fh:
+            h.update(name.encode())
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, workload: str):
+def recorded_traffic(kernel: str, workload: str, which: str = "ffma"):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel sources; else None."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
@@ -150,8 +160,8 @@ def recorded_traffic(kernel: str, workload: str):
         return None, None
     with open(path) as f:
         data = json.load(f)
-    rec = data.get(workload, {})
-    if rec.get("kernel") != kernel or rec.get("csrc_digest") != kernel_sources_digest():
+    rec = data.get(which + ":" + workload, {})
+    if rec.get("kernel") != kernel or rec.get("csrc_digest") != kernel_sources_digest(which):
         return None, None
     return rec.get("dram_bytes_per_launch"), rec.get("note")
 
@@ -413,6 +423,9 @@ def run_ours(args, w):
         bf16 = float(mp_.get("bf16_tflops") or 1900.0)
         tf32_peak = bf16 * (1.1 / 2.25)      # nominal TF32 : BF16 dense ratio
         tf32_rate = 3.0 * flops / (ms3 * 1e-3) / 1e12
+        t3, t3_note = (None, None)
+        if os.environ.get("SGEMM_3XTF32_TILE", "128x128") == "128x128":
+            t3, t3_note = recorded_traffic("tf32x3_kernel<TcCfg<128,3>>", w.name, "tf32x3")
         tf32x3 = {"value": replica_throughput(flops, ms3, world), "unit": "GFLOP/s",
                   "ms_per_step": ms3, "steps": n3,
                   "note": "sgemm_3xtf32: A, B split into TF32 hi/lo, 3 tcgen05 MMAs per product, "
@@ -422,7 +435,8 @@ def run_ours(args, w):
                                "unit": "TFLOP/s", "frac": tf32_rate / tf32_peak,
                                "peak_basis": f"measured bf16 {bf16:.1f} TFLOP/s x 1.1/2.25 "
                                              "(nominal TF32:BF16 dense ratio)",
-                               "achieved_basis": "3 x 2MNK TF32 FLOP per step / step time"},
+                               "achieved_basis": "3 x 2MNK TF32 FLOP per step / step time",
+                               "traffic": t3, "traffic_note": t3_note},
                   "gpu_launches_per_step": 3}
 
     # End to end through the public API with host buffers.
@@ -465,7 +479,7 @@ def run_ours(args, w):
     sm_max = float(mp.get("sm_max_mhz") or 2070.0)
     datasheet = props.multi_processor_count * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e9
     achieved = flops / (kernel_ms * 1e-3) / 1e12
-    traffic, traffic_note = recorded_traffic(kernel, w.name)
+    traffic, traffic_note = recorded_traffic(kernel, w.name, "ffma")
     line = {
         "metric": METRIC, "value": value, "unit": "GFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
