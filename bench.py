@@ -133,13 +133,13 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-# Sources each timed kernel is built from (kernel body, PTX helpers, the
-# family instantiation, and the planner that picks grid and schedule). A
-# recorded DRAM-traffic figure is reused only while these files are unchanged.
+# Sources each timed kernel's device code is built from (kernel body, PTX
+# helpers, the family instantiation). A recorded DRAM-traffic figure is
+# reused only while these files are unchanged and the plan (kernel name,
+# schedule suffixes, grid) is the one it was captured on.
 KERNEL_SOURCES = {
-    "ffma": ("sgemm_kernel.cuh", "ptx.cuh", "kernels.h", "sgemm_ws_128x128.cu",
-             "sgemm_ws_64x64.cu", "sgemm_api.cu", "sgemm_internal.h"),
-    "tf32x3": ("tf32x3.cu", "ptx.cuh", "sgemm_internal.h"),
+    "ffma": ("sgemm_kernel.cuh", "ptx.cuh", "sgemm_ws_128x128.cu"),
+    "tf32x3": ("tf32x3.cu", "ptx.cuh"),
 }
 
 
@@ -152,7 +152,7 @@ def kernel_sources_digest(which: str = "ffma") -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, workload: str, which: str = "ffma"):
+def recorded_traffic(kernel: str, workload: str, which: str = "ffma", grid=None):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel sources; else None."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
@@ -162,6 +162,8 @@ def recorded_traffic(kernel: str, workload: str, which: str = "ffma"):
         data = json.load(f)
     rec = data.get(which + ":" + workload, {})
     if rec.get("kernel") != kernel or rec.get("csrc_digest") != kernel_sources_digest(which):
+        return None, None
+    if grid is not None and rec.get("grid") != grid:
         return None, None
     return rec.get("dram_bytes_per_launch"), rec.get("note")
 
@@ -479,7 +481,7 @@ def run_ours(args, w):
     sm_max = float(mp.get("sm_max_mhz") or 2070.0)
     datasheet = props.multi_processor_count * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e9
     achieved = flops / (kernel_ms * 1e-3) / 1e12
-    traffic, traffic_note = recorded_traffic(kernel, w.name, "ffma")
+    traffic, traffic_note = recorded_traffic(kernel, w.name, "ffma", grid)
     line = {
         "metric": METRIC, "value": value, "unit": "GFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,

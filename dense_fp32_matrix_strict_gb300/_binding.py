@@ -25,6 +25,7 @@ EXPORTED_SYMBOLS = (
     "sgemm", "sgemm_check_status", "sgemm_error_string", "sgemm_last_cuda_error",
     "sgemm_plan", "sgemm_set_config", "sgemm_set_wait_timeout_ns", "sgemm_fp32_peak",
     "sgemm_selftest_wait_timeout", "sgemm_config_names", "sgemm_noalloc", "sgemm_3xtf32",
+    "sgemm_set_shape_config", "sgemm_clear_shape_configs",
 )
 
 _lock = threading.Lock()
@@ -75,6 +76,10 @@ def load():
         lib.sgemm_set_config.restype = ci
         lib.sgemm_config_names.argtypes = [ctypes.c_char_p, ci]
         lib.sgemm_config_names.restype = ci
+        lib.sgemm_set_shape_config.argtypes = [i64, i64, i64, ctypes.c_char_p]
+        lib.sgemm_set_shape_config.restype = ci
+        lib.sgemm_clear_shape_configs.argtypes = []
+        lib.sgemm_clear_shape_configs.restype = ci
         lib.sgemm_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
         lib.sgemm_set_wait_timeout_ns.restype = ci
         lib.sgemm_fp32_peak.argtypes = [ctypes.c_double, f64p, f64p, f64p, vp]
@@ -139,6 +144,15 @@ def sgemm_plan(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc):
 
 def sgemm_set_config(name: str) -> int:
     return load().sgemm_set_config(name.encode())
+
+
+def sgemm_set_shape_config(M: int, N: int, K: int, name) -> int:
+    """Per-shape configuration rule; name None or "auto" removes it."""
+    return load().sgemm_set_shape_config(M, N, K, None if name is None else name.encode())
+
+
+def sgemm_clear_shape_configs() -> int:
+    return load().sgemm_clear_shape_configs()
 
 
 def sgemm_config_names():

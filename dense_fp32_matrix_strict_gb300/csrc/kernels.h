@@ -75,11 +75,12 @@ constexpr KernelEntry make_entry(const char* name) {
             &fixup_launch<BM, BN>                                                           \
     }
 
-// Families, one translation unit each (compiled in parallel). The first two
-// are the ones "auto" chooses between; the rest are tuning alternatives that
-// sgemm_set_config can force.
+// Families, one translation unit each (compiled in parallel). The first
+// three are the ones "auto" chooses between; the rest are tuning
+// alternatives that sgemm_set_config can force.
 const KernelFamily* family_128x128();
 const KernelFamily* family_64x64();
+const KernelFamily* family_128x64();
 const KernelFamily* const* sweep_families(int* count);
 
 }  // namespace sg

@@ -97,6 +97,14 @@ __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
 }
 
+// ---- L2 prefetch -------------------------------------------------------------
+
+// Bring the 128-byte line holding `p` into L2 (no register result, no fault
+// semantics the callers rely on: every address passed is inside its matrix).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" :: "l"(p));
+}
+
 // ---- timers ----------------------------------------------------------------
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {

@@ -23,14 +23,15 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kStatusBytes = 256;
 
-// All compiled kernel families: [0] 128x128 and [1] 64x64 are what "auto"
-// chooses between; the rest are tuning alternatives.
+// All compiled kernel families: [0] 128x128, [1] 64x64 and [2] 128x64 are
+// what "auto" chooses between; the rest are tuning alternatives.
 struct Registry {
     const KernelFamily* fam[kMaxFamilies];
     int count = 0;
     Registry() {
         fam[count++] = family_128x128();
         fam[count++] = family_64x64();
+        fam[count++] = family_128x64();
         int n = 0;
         const KernelFamily* const* sw = sweep_families(&n);
         for (int i = 0; i < n && count < kMaxFamilies; ++i) fam[count++] = sw[i];
@@ -71,8 +72,34 @@ std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 
 thread_local int t_last_cuda_error = 0;
 
-// "<family>[:cpasync][:dp]" with <family> one of auto, 128x128, 64x64 or a
-// registry name.
+// Per-shape configuration rules (sgemm_set_shape_config), consulted by
+// make_plan only while the global configuration is "auto". An autotuning
+// sweep installs the fastest configuration it measured for each shape here.
+struct ShapeRule {
+    int64_t M, N, K;
+    int family, cp, sk;
+};
+constexpr int kMaxShapeRules = 256;
+std::mutex g_rules_mu;
+ShapeRule g_rules[kMaxShapeRules];
+int g_nrules = 0;
+
+bool shape_rule(int64_t M, int64_t N, int64_t K, int* family, int* cp, int* sk) {
+    std::lock_guard<std::mutex> lock(g_rules_mu);
+    for (int i = 0; i < g_nrules; ++i) {
+        const ShapeRule& r = g_rules[i];
+        if (r.M == M && r.N == N && r.K == K) {
+            *family = r.family;
+            *cp = r.cp;
+            *sk = r.sk;
+            return true;
+        }
+    }
+    return false;
+}
+
+// "<family>[:cpasync][:dp]" with <family> one of auto, 128x128, 64x64,
+// 128x64 or a registry name.
 int parse_config(const char* name, int* family, int* cp, int* sk) {
     if (name == nullptr) return SGEMM_ERR_INVALID_VALUE;
     char buf[128];
@@ -93,6 +120,7 @@ int parse_config(const char* name, int* family, int* cp, int* sk) {
     if (std::strcmp(buf, "auto") == 0 || buf[0] == '\0') f = -1;
     else if (std::strcmp(buf, "128x128") == 0) f = 0;
     else if (std::strcmp(buf, "64x64") == 0) f = 1;
+    else if (std::strcmp(buf, "128x64") == 0) f = 2;
     else {
         const Registry& r = registry();
         for (int i = 0; i < r.count; ++i)
@@ -298,8 +326,9 @@ int device_info(const DeviceInfo** out) {
             int n = 0;
             e = reg.fam[f]->modes[m].prepare(&n);
             if (e != cudaSuccess || n <= 0) {
-                // The two families "auto" uses must work; a tuning
-                // alternative that cannot run here is only marked unusable.
+                // The 128 x 128 and 64 x 64 families must work; the 128 x 64
+                // family (which "auto" then skips) and a tuning alternative
+                // that cannot run here are only marked unusable.
                 if (f < 2) return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidConfiguration,
                                             SGEMM_ERR_CUDA);
                 (void)cudaGetLastError();
@@ -337,26 +366,65 @@ int make_plan(const DeviceInfo* dev, int64_t M, int64_t N, int64_t K, float alph
     const int sms = dev->sm_count;
     pl->sms = sms;
     int fi = g_force_family.load();
+    int force_cp_flag = g_force_cp.load();
+    int force_sk = g_force_sk.load();
+    if (fi < 0 && force_cp_flag == 0 && force_sk < 0)
+        shape_rule(M, N, K, &fi, &force_cp_flag, &force_sk);
+    // Under "auto" the choice below also decides whether the stream-K tail
+    // is used; a forced family keeps the fixed rule further down.
+    bool sk_decided = false;
     if (fi < 0) {
-        // The 128 x 128 tile with the stream-K tail keeps every SM busy even
-        // for small grids. Below two k-iterations of 128 x 128 x 32 per SM
-        // the second launch and the workspace cost more than they save, so
-        // such problems (and any problem when stream-K is off whose 128 x 128
-        // grid would leave most SMs idle) take the 64 x 64 family without it.
+        sk_decided = true;
+        const int64_t kt = (K + 31) / 32;
         const int64_t tiles128 = ((M + 127) / 128) * ((N + 127) / 128);
-        const int64_t iters128 = tiles128 * ((K + 31) / 32);
-        const bool sk_possible = allow_sk && g_force_sk.load() != 0;
-        if (sk_possible && iters128 >= 2 * static_cast<int64_t>(sms)) {
-            fi = 0;
+        const int64_t iters128 = tiles128 * kt;
+        const int64_t nsm = sms;
+        const bool sk_possible = allow_sk && force_sk != 0;
+        if (iters128 < 2 * nsm) {
+            // Below two 128 x 128 x 32 k-iterations per SM: the 64 x 64 tile,
+            // with the stream-K tail only if its own k-iterations still give
+            // every SM two.
+            fi = 1;
+            const int64_t iters64 = ((M + 63) / 64) * ((N + 63) / 64) * kt;
+            if (!(sk_possible && iters64 >= 2 * nsm)) allow_sk = false;
         } else {
-            fi = (tiles128 * 2 >= sms) ? 0 : 1;
-            if (fi == 1) allow_sk = false;
+            // Cost in units of one 128 x 128 x 32 k-iteration on one SM,
+            // fitted to sweeps on GB300 (152 SMs): the stream-K tail adds
+            // about 8 units (partial sums to L2, the fixup launch); a lone
+            // 128 x 64 CTA on an SM takes 0.63 units per k-iteration, two
+            // co-resident ones 1.06 units for both.
+            const int64_t cap128 = static_cast<int64_t>(dev->ctas_per_sm[0][0]) * nsm;
+            const int64_t waves = cap128 > 0 ? tiles128 / cap128 : 0;
+            const int64_t rest = cap128 > 0 ? tiles128 % cap128 : 0;
+            const double inf = 1e300;
+            const double c_dp = cap128 > 0
+                                    ? static_cast<double>((tiles128 + cap128 - 1) / cap128) * kt + 1
+                                    : inf;
+            const double c_sk = (sk_possible && rest != 0)
+                                    ? static_cast<double>(waves * kt + (rest * kt + nsm - 1) / nsm) + 8
+                                    : inf;
+            double c_64 = inf;
+            const bool a_tma = tma_ok(A, lda, M, K) || (allow_pack && N >= 256);
+            const bool b_tma = tma_ok(B, ldb, K, N) || (allow_pack && M >= 256);
+            if (force_cp_flag == 0 && a_tma && b_tma && dev->ctas_per_sm[2][0] >= 2) {
+                const int64_t tiles64 = ((M + 127) / 128) * ((N + 63) / 64);
+                c_64 = tiles64 <= nsm ? 0.63 * static_cast<double>(kt)
+                                      : static_cast<double>((tiles64 + 2 * nsm - 1) / (2 * nsm)) *
+                                            1.06 * static_cast<double>(kt);
+            }
+            if (c_64 < c_dp && c_64 < c_sk) {
+                fi = 2;
+                allow_sk = false;
+            } else {
+                fi = 0;
+                if (!(c_sk < c_dp)) allow_sk = false;
+            }
         }
     }
     const KernelFamily* fam = registry().fam[fi];
     pl->fam = fam;
     const int bm = fam->bm, bn = fam->bn, bk = 32;
-    const bool force_cp = g_force_cp.load() != 0;
+    const bool force_cp = force_cp_flag != 0;
     std::memset(&pl->tmA, 0, sizeof(CUtensorMap));
     std::memset(&pl->tmB, 0, sizeof(CUtensorMap));
     int a_mode = LOAD_CPASYNC, b_mode = LOAD_CPASYNC;
@@ -421,8 +489,8 @@ int make_plan(const DeviceInfo* dev, int64_t M, int64_t N, int64_t K, float alph
     // Schedule: whole waves data-parallel; the last, partial wave's
     // k-iterations spread over the CTAs (stream-K) unless it is nearly full.
     const int64_t waves = tiles / cap, rest = tiles % cap;
-    const bool use_sk = allow_sk && g_force_sk.load() != 0 && rest != 0 &&
-                        (waves == 0 || rest * 10 < cap * 9);
+    const bool use_sk = allow_sk && force_sk != 0 && rest != 0 &&
+                        (sk_decided || waves == 0 || rest * 10 < cap * 9);
     if (!use_sk) {
         p.dp_tiles = static_cast<int>(tiles);
         p.sk_ctas = 0;
@@ -625,6 +693,36 @@ extern "C" int sgemm_set_config(const char* name) {
     g_force_family = fam;
     g_force_cp = cp;
     g_force_sk = sk;
+    return SGEMM_OK;
+}
+
+extern "C" int sgemm_set_shape_config(int64_t M, int64_t N, int64_t K, const char* name) {
+    if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_VALUE;
+    int fam = -1, cp = 0, sk = -1;
+    if (name != nullptr) {
+        const int rc = parse_config(name, &fam, &cp, &sk);
+        if (rc != SGEMM_OK) return rc;
+    }
+    std::lock_guard<std::mutex> lock(g_rules_mu);
+    int at = -1;
+    for (int i = 0; i < g_nrules; ++i)
+        if (g_rules[i].M == M && g_rules[i].N == N && g_rules[i].K == K) at = i;
+    if (fam < 0 && cp == 0 && sk < 0) {
+        // "auto" (or NULL) removes the rule.
+        if (at >= 0) g_rules[at] = g_rules[--g_nrules];
+        return SGEMM_OK;
+    }
+    if (at < 0) {
+        if (g_nrules == kMaxShapeRules) return SGEMM_ERR_INVALID_VALUE;
+        at = g_nrules++;
+    }
+    g_rules[at] = ShapeRule{M, N, K, fam, cp, sk};
+    return SGEMM_OK;
+}
+
+extern "C" int sgemm_clear_shape_configs(void) {
+    std::lock_guard<std::mutex> lock(g_rules_mu);
+    g_nrules = 0;
     return SGEMM_OK;
 }
 

@@ -385,6 +385,21 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
 #pragma unroll
             for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
 
+        if (it.slot < 0 && p.beta != 0.0f) {
+            // The epilogue reads this tile of C: start moving it into L2 now.
+            // Lane l takes row l of the warp tile, both 128-byte lines of its
+            // 64 columns (the second only if it starts inside the matrix).
+            int tm, tn;
+            tile_coords(it.tile, p, tm, tn);
+            const int r = tm * C::BM + wm * 32 + lane;
+            const int c = tn * C::BN + wn * 64;
+            if (r < p.M && c < p.N) {
+                const float* crow = p.C + (long long)r * p.ldc + c;
+                prefetch_l2(crow);
+                if (c + 32 < p.N) prefetch_l2(crow + 32);
+            }
+        }
+
         bool ready = false;   // EARLY: stage s already seen complete
         for (int kt = it.kb; kt < it.ke; ++kt) {
             if (!ready && !wait_bounded(full0 + 8 * s, ph, p, STATUS_CONSUMER_TIMEOUT)) return;
@@ -434,34 +449,56 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
         const int m0 = tm * C::BM + row_base;
         const int n0 = tn * C::BN + col_base;
         const bool use_c = p.beta != 0.0f;
+        // Two halves of four rows: each half first reads all the old-C
+        // float4s it owns, then writes, so eight loads are in flight together
+        // instead of one round trip per store (the compiler cannot move a
+        // load of C above a store to C). Half the rows at a time keeps the
+        // extra registers within the budget of the main loop.
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int m = m0 + 4 * i;
-            if (m >= p.M) continue;
-            float* crow = p.C + (long long)m * p.ldc;
+        for (int q = 0; q < 2; ++q) {
+            float4 cold[4][2];
+            if (use_c) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int n = n0 + 32 * h;
-                float v[4];
+                for (int ii = 0; ii < 4; ++ii) {
+                    const int m = m0 + 4 * (4 * q + ii);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) v[e] = p.alpha * acc[i][4 * h + e];
-                if (p.c_vec && n + 3 < p.N) {
-                    float4* cp = reinterpret_cast<float4*>(crow + n);
-                    if (use_c) {
-                        const float4 c = *cp;
-                        v[0] = fmaf(p.beta, c.x, v[0]);
-                        v[1] = fmaf(p.beta, c.y, v[1]);
-                        v[2] = fmaf(p.beta, c.z, v[2]);
-                        v[3] = fmaf(p.beta, c.w, v[3]);
+                    for (int h = 0; h < 2; ++h) {
+                        const int n = n0 + 32 * h;
+                        cold[ii][h] = (m < p.M && p.c_vec && n + 3 < p.N)
+                                          ? *reinterpret_cast<const float4*>(p.C + (long long)m * p.ldc + n)
+                                          : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
                     }
-                    *cp = make_float4(v[0], v[1], v[2], v[3]);
-                } else {
+                }
+            }
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        if (n + e < p.N) {
-                            float out = v[e];
-                            if (use_c) out = fmaf(p.beta, crow[n + e], out);
-                            crow[n + e] = out;
+            for (int ii = 0; ii < 4; ++ii) {
+                const int i = 4 * q + ii;
+                const int m = m0 + 4 * i;
+                if (m >= p.M) continue;
+                float* crow = p.C + (long long)m * p.ldc;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int n = n0 + 32 * h;
+                    float v[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) v[e] = p.alpha * acc[i][4 * h + e];
+                    if (p.c_vec && n + 3 < p.N) {
+                        if (use_c) {
+                            const float4 c = cold[ii][h];
+                            v[0] = fmaf(p.beta, c.x, v[0]);
+                            v[1] = fmaf(p.beta, c.y, v[1]);
+                            v[2] = fmaf(p.beta, c.z, v[2]);
+                            v[3] = fmaf(p.beta, c.w, v[3]);
+                        }
+                        *reinterpret_cast<float4*>(crow + n) = make_float4(v[0], v[1], v[2], v[3]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            if (n + e < p.N) {
+                                float out = v[e];
+                                if (use_c) out = fmaf(p.beta, crow[n + e], out);
+                                crow[n + e] = out;
+                            }
                         }
                     }
                 }

@@ -130,8 +130,8 @@ SGEMM_API int sgemm_plan(int64_t M, int64_t N, int64_t K, float alpha, const flo
 
 /*
  * sgemm_set_config — force a kernel configuration for later calls in this
- * process (for sweeps and tests). `name` is "auto" (default), "128x128" or
- * "64x64" for the CTA tile, or one of the family names sgemm_config_names
+ * process (for sweeps and tests). `name` is "auto" (default), "128x128",
+ * "64x64" or "128x64" for the CTA tile, or one of the family names sgemm_config_names
  * lists, optionally followed by modifiers: ":cpasync" loads both operands
  * with cp.async even when TMA could be used, ":dp" never splits the last
  * wave (plain data-parallel schedule, no workspace), e.g.
@@ -143,11 +143,28 @@ SGEMM_API int sgemm_set_config(const char* name);
 
 /*
  * sgemm_config_names — write the names sgemm_set_config accepts besides
- * "auto", "128x128" and "64x64" (every compiled kernel family, comma
+ * "auto", "128x128", "64x64" and "128x64" (every compiled kernel family, comma
  * separated, NUL-terminated) into buf (at most buflen bytes). Returns
  * SGEMM_ERR_INVALID_VALUE if buf is NULL or too small.
  */
 SGEMM_API int sgemm_config_names(char* buf, int buflen);
+
+/*
+ * sgemm_set_shape_config — per-shape form of sgemm_set_config: later calls
+ * whose (M, N, K) equal these use configuration `name` (same syntax as
+ * sgemm_set_config) while the global configuration is "auto". `name` equal
+ * to "auto", or NULL, removes the rule for that shape. Up to 256 shapes;
+ * a new shape beyond that, a negative size or an unknown name returns
+ * SGEMM_ERR_INVALID_VALUE. The pages note that the best tile depends on
+ * the GPU and on the matrix shape and that libraries pick one per shape
+ * ("The road to a fast GEMM", section "Where to go next", autotuning), and
+ * the Tinyforge README sweeps tiles per size; this is where such a sweep's
+ * choice is installed. The package's autotune module writes it.
+ * sgemm_clear_shape_configs removes every rule. Thread-safe; affects calls
+ * on every device.
+ */
+SGEMM_API int sgemm_set_shape_config(int64_t M, int64_t N, int64_t K, const char* name);
+SGEMM_API int sgemm_clear_shape_configs(void);
 
 /*
  * sgemm_set_wait_timeout_ns — limit on every bounded mbarrier wait inside

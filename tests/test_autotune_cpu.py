@@ -1,0 +1,36 @@
+"""Host logic of the autotuning sweep: shape parsing, winner selection and
+the CSV round trip (no GPU)."""
+import pytest
+
+from dense_fp32_matrix_strict_gb300 import autotune
+
+
+def test_parse_shapes():
+    assert autotune.parse_shapes("4096x4096x4096, 4093x5120x1531") == [
+        (4096, 4096, 4096), (4093, 5120, 1531)]
+    for bad in ["4096x4096", "0x4x4", "axbxc"]:
+        with pytest.raises(ValueError):
+            autotune.parse_shapes(bad)
+
+
+def _row(m, n, k, name, ms, ok=1):
+    return {"M": m, "N": n, "K": k, "config": name, "kernel": name + "_k", "grid": 152,
+            "ms": ms, "gflops": 1.0, "err_over_bound": 0.1, "ok": ok}
+
+
+def test_best_is_fastest_good_row_per_shape():
+    rows = [_row(8, 8, 8, "auto", 2.0), _row(8, 8, 8, "a", 1.0, ok=0), _row(8, 8, 8, "b", 1.5),
+            _row(9, 9, 9, "auto", 1.0), _row(9, 9, 9, "c", "")]
+    autotune.mark_best(rows)
+    assert [r["best"] for r in rows] == [0, 0, 1, 1, 0]
+    assert autotune.best_configs(rows) == {(8, 8, 8): "b", (9, 9, 9): "auto"}
+
+
+def test_csv_round_trip(tmp_path):
+    rows = autotune.mark_best([_row(8, 8, 8, "auto", 2.0), _row(8, 8, 8, "b:dp", 1.5)])
+    p = tmp_path / "sweep.csv"
+    autotune.write_csv(rows, str(p))
+    back = autotune.load_csv(str(p))
+    assert [r["config"] for r in back] == ["auto", "b:dp"]
+    assert tuple(back[0].keys()) == autotune.FIELDS
+    assert autotune.best_configs(back) == {(8, 8, 8): "b:dp"}

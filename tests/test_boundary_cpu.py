@@ -113,3 +113,20 @@ def test_tensor_wrapper_rejects_cpu_tensors(lib):
     a = torch.zeros(4, 4)
     with pytest.raises(TypeError):
         sg.sgemm_tensors(1.0, a, a, 0.0, a.clone())
+
+
+def test_shape_config_rules(lib):
+    assert sg.sgemm_set_shape_config(-1, 4, 4, "128x128") == sg.SGEMM_ERR_INVALID_VALUE
+    assert sg.sgemm_set_shape_config(4, 4, 4, "256x256") == sg.SGEMM_ERR_INVALID_VALUE
+    assert sg.sgemm_set_shape_config(4, 4, 4, "64x64:dp") == sg.SGEMM_OK
+    assert sg.sgemm_set_shape_config(4, 4, 4, "128x128") == sg.SGEMM_OK   # replaces
+    assert sg.sgemm_set_shape_config(4, 4, 4, "auto") == sg.SGEMM_OK      # removes
+    assert sg.sgemm_set_shape_config(4, 4, 4, None) == sg.SGEMM_OK        # absent: no-op
+    # The table holds 256 shapes; a 257th new shape is refused, an update is not.
+    for i in range(256):
+        assert sg.sgemm_set_shape_config(1, 1, i + 1, "64x64") == sg.SGEMM_OK
+    assert sg.sgemm_set_shape_config(1, 1, 1000, "64x64") == sg.SGEMM_ERR_INVALID_VALUE
+    assert sg.sgemm_set_shape_config(1, 1, 7, "128x128") == sg.SGEMM_OK
+    assert sg.sgemm_set_shape_config(1, 1, 7, "auto") == sg.SGEMM_OK
+    assert sg.sgemm_set_shape_config(1, 1, 1000, "64x64") == sg.SGEMM_OK
+    assert sg.sgemm_clear_shape_configs() == sg.SGEMM_OK

@@ -332,9 +332,11 @@ SK_SHAPES = [
 @pytest.mark.parametrize("cp", ["", ":cpasync"])
 @pytest.mark.parametrize("shape", SK_SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_stream_k_tail_matches_oracle(shape, cp):
+    # The 128 x 128 family forced: its fixed rule splits every partial last
+    # wave below 90 % of the SMs (auto may prefer the 128 x 64 tile here).
     M, N, K = shape
     A, B, C0 = gen(M, N, K, seed=200 + M % 97 + N % 89 + K % 83)
-    assert sg.sgemm_set_config("auto" + cp) == 0
+    assert sg.sgemm_set_config("128x128" + cp) == 0
     try:
         C, guards, plan = gpu_util.run(0.7, A, B, -1.3, C0)
         assert guards
@@ -373,7 +375,11 @@ def test_integer_inputs_bit_exact_with_stream_k():
     A = inputs.fill("int", 5, inputs.TID_A, 700, 1500)
     B = inputs.fill("int", 5, inputs.TID_B, 1500, 900)
     C0 = inputs.fill("int", 5, inputs.TID_C, 700, 900)
-    C, _, plan = gpu_util.run(2.0, A, B, -1.0, C0)
+    assert sg.sgemm_set_config("128x128") == 0
+    try:
+        C, _, plan = gpu_util.run(2.0, A, B, -1.0, C0)
+    finally:
+        sg.sgemm_set_config("auto")
     assert plan[0].endswith("+sk"), plan
     check_full(2.0, A, B, -1.0, C0, C, exact=True)
 
