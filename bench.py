@@ -507,8 +507,10 @@ def run_ours(args, w):
         "gpu_launches": args.steps * launches_per_step,
         "gpu_launches_note": ("per step: the sgemm kernel" +
                               (" + stream-K fixup" if "+sk" in kernel else "") +
-                              (" + packing copy of A" if "+packA" in kernel else "") +
-                              (" + packing copy of B" if "+packB" in kernel else "")) + (
+                              (" + transposing copy of A" if "+packAT" in kernel else
+                               " + packing copy of A" if "+packA" in kernel else "") +
+                              (" + transposing copy of B" if "+packBT" in kernel else
+                               " + packing copy of B" if "+packB" in kernel else "")) + (
             " (plus one torch L2-flush fill, not ours)" if flush is not None else ""),
     }
     if tf32x3 is not None:

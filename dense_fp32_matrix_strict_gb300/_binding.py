@@ -25,8 +25,11 @@ EXPORTED_SYMBOLS = (
     "sgemm", "sgemm_check_status", "sgemm_error_string", "sgemm_last_cuda_error",
     "sgemm_plan", "sgemm_set_config", "sgemm_set_wait_timeout_ns", "sgemm_fp32_peak",
     "sgemm_selftest_wait_timeout", "sgemm_config_names", "sgemm_noalloc", "sgemm_3xtf32",
-    "sgemm_set_shape_config", "sgemm_clear_shape_configs",
+    "sgemm_set_shape_config", "sgemm_clear_shape_configs", "sgemm_ex", "sgemm_plan_ex",
+    "sgemm_3xtf32_ex",
 )
+
+SGEMM_OP_N, SGEMM_OP_T = 0, 1
 
 _lock = threading.Lock()
 _lib = None
@@ -90,6 +93,14 @@ def load():
         lib.sgemm_noalloc.restype = ci
         lib.sgemm_3xtf32.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
         lib.sgemm_3xtf32.restype = ci
+        lib.sgemm_ex.argtypes = [ci, ci, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
+        lib.sgemm_ex.restype = ci
+        lib.sgemm_3xtf32_ex.argtypes = [ci, ci, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp,
+                                        i64, vp]
+        lib.sgemm_3xtf32_ex.restype = ci
+        lib.sgemm_plan_ex.argtypes = [ci, ci, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64,
+                                      ctypes.c_char_p, ci, ctypes.POINTER(ci)]
+        lib.sgemm_plan_ex.restype = ci
         _lib = lib
         return lib
 
@@ -116,6 +127,24 @@ def sgemm_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int
 def sgemm_3xtf32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
     """The tcgen05 3xTF32 path (device pointers as ints); returns the raw code."""
     return load().sgemm_3xtf32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def sgemm_ex(opa, opb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
+    """C = alpha*op(A)*op(B) + beta*C (op: SGEMM_OP_N / SGEMM_OP_T); raw code."""
+    return load().sgemm_ex(opa, opb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def sgemm_3xtf32_ex(opa, opb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
+    return load().sgemm_3xtf32_ex(opa, opb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def sgemm_plan_ex(opa, opb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc):
+    """Returns (code, kernel name, grid)."""
+    buf = ctypes.create_string_buffer(128)
+    grid = ctypes.c_int(0)
+    rc = load().sgemm_plan_ex(opa, opb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, buf, 128,
+                              ctypes.byref(grid))
+    return rc, buf.value.decode(), grid.value
 
 
 def sgemm_check_status(stream=0):
@@ -232,54 +261,71 @@ class _on_device:
         return False
 
 
-def sgemm_tensors(alpha, A, B, beta, C, stream=None) -> None:
-    """C = alpha * A @ B + beta * C in place on row-major float32 CUDA tensors.
-
-    Rows may be strided (leading dimension = stride(0)). Launches on
-    ``stream`` (default: torch's current stream on C's device). Raises
-    SgemmError on a non-zero return code.
-    """
-    M, K = A.shape
-    K2, N = B.shape
+def _shapes(A, B, transa, transb):
+    """(M, N, K, lda, ldb) of op(A) op(B) from the stored tensors."""
+    M, K = (A.shape[1], A.shape[0]) if transa else (A.shape[0], A.shape[1])
+    K2, N = (B.shape[1], B.shape[0]) if transb else (B.shape[0], B.shape[1])
     if K2 != K:
-        raise ValueError(f"inner dimensions differ: A is {tuple(A.shape)}, B is {tuple(B.shape)}")
-    lda = _ld(A, M, K, "A")
-    ldb = _ld(B, K, N, "B")
+        raise ValueError(f"inner dimensions differ: op(A) is {(M, K)}, op(B) is {(K2, N)}")
+    lda = _ld(A, A.shape[0], A.shape[1], "A")
+    ldb = _ld(B, B.shape[0], B.shape[1], "B")
+    return M, N, K, lda, ldb
+
+
+def _op(flag: bool) -> int:
+    return SGEMM_OP_T if flag else SGEMM_OP_N
+
+
+def sgemm_tensors(alpha, A, B, beta, C, stream=None, transa=False, transb=False) -> None:
+    """C = alpha * op(A) @ op(B) + beta * C in place on row-major float32 CUDA tensors.
+
+    op(X) is X, or X.T when trans* is set (the tensor is then the stored,
+    untransposed matrix: A of shape (K, M), B of shape (N, K)). Rows may be
+    strided (leading dimension = stride(0)). Launches on ``stream``
+    (default: torch's current stream on C's device). Raises SgemmError on a
+    non-zero return code.
+    """
+    M, N, K, lda, ldb = _shapes(A, B, transa, transb)
     ldc = _ld(C, M, N, "C")
     if not (A.device == B.device == C.device):
         raise ValueError("A, B and C must be on the same device")
     with _on_device(C.device):
-        rc = load().sgemm(M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(), ldb,
-                          float(beta), C.data_ptr(), ldc, _stream_handle(stream, C.device))
+        h = _stream_handle(stream, C.device)
+        if transa or transb:
+            rc = load().sgemm_ex(_op(transa), _op(transb), M, N, K, float(alpha), A.data_ptr(),
+                                 lda, B.data_ptr(), ldb, float(beta), C.data_ptr(), ldc, h)
+        else:
+            rc = load().sgemm(M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(), ldb,
+                              float(beta), C.data_ptr(), ldc, h)
     if rc != SGEMM_OK:
-        raise SgemmError("sgemm", rc)
+        raise SgemmError("sgemm_ex" if (transa or transb) else "sgemm", rc)
 
 
-def sgemm_3xtf32_tensors(alpha, A, B, beta, C, stream=None) -> None:
-    """sgemm_tensors through the tcgen05 3xTF32 entry point."""
-    M, K = A.shape
-    K2, N = B.shape
-    if K2 != K:
-        raise ValueError(f"inner dimensions differ: A is {tuple(A.shape)}, B is {tuple(B.shape)}")
-    lda = _ld(A, M, K, "A")
-    ldb = _ld(B, K, N, "B")
+def sgemm_3xtf32_tensors(alpha, A, B, beta, C, stream=None, transa=False, transb=False) -> None:
+    """sgemm_tensors through the tcgen05 3xTF32 entry points."""
+    M, N, K, lda, ldb = _shapes(A, B, transa, transb)
     ldc = _ld(C, M, N, "C")
     with _on_device(C.device):
-        rc = load().sgemm_3xtf32(M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(), ldb,
-                                 float(beta), C.data_ptr(), ldc, _stream_handle(stream, C.device))
+        h = _stream_handle(stream, C.device)
+        if transa or transb:
+            rc = load().sgemm_3xtf32_ex(_op(transa), _op(transb), M, N, K, float(alpha),
+                                        A.data_ptr(), lda, B.data_ptr(), ldb, float(beta),
+                                        C.data_ptr(), ldc, h)
+        else:
+            rc = load().sgemm_3xtf32(M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(), ldb,
+                                     float(beta), C.data_ptr(), ldc, h)
     if rc != SGEMM_OK:
         raise SgemmError("sgemm_3xtf32", rc)
 
 
-def plan_tensors(alpha, A, B, beta, C):
+def plan_tensors(alpha, A, B, beta, C, transa=False, transb=False):
     """Kernel name and grid sgemm_tensors would use for these tensors."""
-    M, K = A.shape
-    N = B.shape[1]
+    M, N, K, lda, ldb = _shapes(A, B, transa, transb)
     with _on_device(C.device):
-        rc, name, grid = sgemm_plan(M, N, K, float(alpha), A.data_ptr(), _ld(A, M, K, "A"),
-                                    B.data_ptr(), _ld(B, K, N, "B"), float(beta), C.data_ptr(),
-                                    _ld(C, M, N, "C"))
-    _check("sgemm_plan", rc)
+        rc, name, grid = sgemm_plan_ex(_op(transa), _op(transb), M, N, K, float(alpha),
+                                       A.data_ptr(), lda, B.data_ptr(), ldb, float(beta),
+                                       C.data_ptr(), _ld(C, M, N, "C"))
+    _check("sgemm_plan_ex", rc)
     return name, grid
 
 

@@ -6,9 +6,10 @@ autotuning; the Tinyforge README's per-size tile sweep and its CSV of
 results). This module times every configuration the library offers on each
 requested shape and records one CSV row per (shape, configuration):
 
-  * configurations: "auto", then every kernel family sgemm_config_names
-    lists, each with the stream-K tail allowed and with ":dp" (whole tiles
-    only);
+  * configurations: "auto", "auto" with the transposed copy of A forbidden
+    (":noat") and forced (":at"), then every kernel family
+    sgemm_config_names lists, each with the stream-K tail allowed and with
+    ":dp" (whole tiles only);
   * inputs: seeded uniform [-1, 1) matrices from ``inputs.fill`` (seed 0),
     alpha = 1, beta = 0, dense leading dimensions;
   * timing: CUDA events around each call on the current stream, after
@@ -65,7 +66,7 @@ def all_configs() -> list[str]:
     rc, names = sg.sgemm_config_names()
     if rc != sg.SGEMM_OK:
         raise sg.SgemmError("sgemm_config_names", rc)
-    out = ["auto"]
+    out = ["auto", "auto:noat", "auto:at"]
     for n in names:
         out += [n, n + ":dp"]
     return out

@@ -41,39 +41,53 @@ cudaError_t fixup_launch(const GemmParams* p, int sk_tiles, cudaStream_t stream)
 }
 
 // One kernel family: a CTA tile and tuning knobs, instantiated for the four
-// (A, B) load-mode pairs in mode_index order, plus its stream-K fixup.
+// (A, B) load-mode pairs of a row-major A and the two B load modes of a
+// transposed A (TMA) in mode_index order, plus its stream-K fixup.
+constexpr int kModes = 6;
+
 struct KernelFamily {
     const char* name;
     int bm, bn;
-    KernelEntry modes[4];
+    KernelEntry modes[kModes];
     cudaError_t (*fixup)(const GemmParams* p, int sk_tiles, cudaStream_t stream);
 };
 
-// Index into a family's modes: TMA/TMA, CP/TMA, TMA/CP, CP/CP.
-inline constexpr int mode_index(int a_mode, int b_mode) { return a_mode + 2 * b_mode; }
+// Index into a family's modes: TMA/TMA, CP/TMA, TMA/CP, CP/CP for a
+// row-major A; then transposed A (TMA) with B by TMA, with B by cp.async.
+inline constexpr int mode_index(int a_mode, int b_mode, int a_t = 0) {
+    return a_t ? 4 + b_mode : a_mode + 2 * b_mode;
+}
 
-template <int BM, int BN, int S, int AM, int BMD, int FORDER, int EARLY, int LMAP>
+template <int BM, int BN, int S, int AM, int BMD, int FORDER, int EARLY, int LMAP, int AT = 0,
+          int ALOAD = 4>
 constexpr KernelEntry make_entry(const char* name) {
-    using C = Cfg<BM, BN, 32, S, AM, BMD, FORDER, EARLY, LMAP>;
+    using C = Cfg<BM, BN, 32, S, AM, BMD, FORDER, EARLY, LMAP, AT, ALOAD>;
     return KernelEntry{name, BM, BN, 32, S, AM, BMD, C::THREADS, C::SMEM_BYTES,
                        &ws_prepare<C>, &ws_launch<C>};
 }
 
-#define SG_FAMILY(NAME, BM, BN, S, FORDER, EARLY, LMAP)                                     \
+#define SG_FAMILY_A(NAME, BM, BN, S, FORDER, EARLY, LMAP, ALOAD)                           \
     KernelFamily {                                                                          \
         NAME, BM, BN,                                                                       \
             {                                                                               \
-                make_entry<BM, BN, S, LOAD_TMA, LOAD_TMA, FORDER, EARLY, LMAP>(               \
+                make_entry<BM, BN, S, LOAD_TMA, LOAD_TMA, FORDER, EARLY, LMAP, 0, ALOAD>(     \
                     NAME "_Atma_Btma"),                                                     \
-                make_entry<BM, BN, S, LOAD_CPASYNC, LOAD_TMA, FORDER, EARLY, LMAP>(           \
+                make_entry<BM, BN, S, LOAD_CPASYNC, LOAD_TMA, FORDER, EARLY, LMAP, 0, ALOAD>( \
                     NAME "_Acp_Btma"),                                                      \
-                make_entry<BM, BN, S, LOAD_TMA, LOAD_CPASYNC, FORDER, EARLY, LMAP>(           \
+                make_entry<BM, BN, S, LOAD_TMA, LOAD_CPASYNC, FORDER, EARLY, LMAP, 0, ALOAD>( \
                     NAME "_Atma_Bcp"),                                                      \
-                make_entry<BM, BN, S, LOAD_CPASYNC, LOAD_CPASYNC, FORDER, EARLY, LMAP>(       \
-                    NAME "_Acp_Bcp"),                                                       \
+                make_entry<BM, BN, S, LOAD_CPASYNC, LOAD_CPASYNC, FORDER, EARLY, LMAP, 0,     \
+                           ALOAD>(NAME "_Acp_Bcp"),                                         \
+                make_entry<BM, BN, S, LOAD_TMA, LOAD_TMA, FORDER, EARLY, LMAP, 1>(            \
+                    NAME "_ATtma_Btma"),                                                    \
+                make_entry<BM, BN, S, LOAD_TMA, LOAD_CPASYNC, FORDER, EARLY, LMAP, 1>(        \
+                    NAME "_ATtma_Bcp"),                                                     \
             },                                                                              \
             &fixup_launch<BM, BN>                                                           \
     }
+
+#define SG_FAMILY(NAME, BM, BN, S, FORDER, EARLY, LMAP) \
+    SG_FAMILY_A(NAME, BM, BN, S, FORDER, EARLY, LMAP, 4)
 
 // Families, one translation unit each (compiled in parallel). The first
 // three are the ones "auto" chooses between; the rest are tuning

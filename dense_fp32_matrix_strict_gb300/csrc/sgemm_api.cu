@@ -67,6 +67,9 @@ bool g_env_read = false;
 // sk = -1 auto, 0 never use the stream-K tail.
 std::atomic<int> g_force_family{-1};
 std::atomic<int> g_force_cp{0};
+// at = -1 auto, 0 never, 1 always copy a row-major A transposed (K x M) into
+// the workspace and run the transposed-A kernel on it.
+std::atomic<int> g_force_at{-1};
 std::atomic<int> g_force_sk{-1};
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 
@@ -75,37 +78,42 @@ thread_local int t_last_cuda_error = 0;
 // Per-shape configuration rules (sgemm_set_shape_config), consulted by
 // make_plan only while the global configuration is "auto". An autotuning
 // sweep installs the fastest configuration it measured for each shape here.
+// A configuration choice: family index (-1 auto), cp.async forced, stream-K
+// (-1 auto, 0 never), pre-transposed A (-1 auto, 0 never, 1 always).
+struct Config {
+    int family = -1, cp = 0, sk = -1, at = -1;
+    bool is_auto() const { return family < 0 && cp == 0 && sk < 0 && at < 0; }
+};
+
 struct ShapeRule {
     int64_t M, N, K;
-    int family, cp, sk;
+    Config cfg;
 };
 constexpr int kMaxShapeRules = 256;
 std::mutex g_rules_mu;
 ShapeRule g_rules[kMaxShapeRules];
 int g_nrules = 0;
 
-bool shape_rule(int64_t M, int64_t N, int64_t K, int* family, int* cp, int* sk) {
+bool shape_rule(int64_t M, int64_t N, int64_t K, Config* cfg) {
     std::lock_guard<std::mutex> lock(g_rules_mu);
     for (int i = 0; i < g_nrules; ++i) {
         const ShapeRule& r = g_rules[i];
         if (r.M == M && r.N == N && r.K == K) {
-            *family = r.family;
-            *cp = r.cp;
-            *sk = r.sk;
+            *cfg = r.cfg;
             return true;
         }
     }
     return false;
 }
 
-// "<family>[:cpasync][:dp]" with <family> one of auto, 128x128, 64x64,
-// 128x64 or a registry name.
-int parse_config(const char* name, int* family, int* cp, int* sk) {
+// "<family>[:cpasync][:dp][:at|:noat]" with <family> one of auto, 128x128,
+// 64x64, 128x64 or a registry name.
+int parse_config(const char* name, Config* out) {
     if (name == nullptr) return SGEMM_ERR_INVALID_VALUE;
     char buf[128];
     std::strncpy(buf, name, sizeof(buf) - 1);
     buf[sizeof(buf) - 1] = '\0';
-    int want_cp = 0, want_sk = -1;
+    int want_cp = 0, want_sk = -1, want_at = -1;
     char* mod = std::strchr(buf, ':');
     if (mod != nullptr) *mod++ = '\0';
     while (mod != nullptr) {
@@ -113,6 +121,8 @@ int parse_config(const char* name, int* family, int* cp, int* sk) {
         if (next != nullptr) *next++ = '\0';
         if (std::strcmp(mod, "cpasync") == 0) want_cp = 1;
         else if (std::strcmp(mod, "dp") == 0) want_sk = 0;
+        else if (std::strcmp(mod, "at") == 0) want_at = 1;
+        else if (std::strcmp(mod, "noat") == 0) want_at = 0;
         else return SGEMM_ERR_INVALID_VALUE;
         mod = next;
     }
@@ -127,22 +137,26 @@ int parse_config(const char* name, int* family, int* cp, int* sk) {
             if (std::strcmp(buf, r.fam[i]->name) == 0) f = i;
     }
     if (f == -2) return SGEMM_ERR_INVALID_VALUE;
-    *family = f;
-    *cp = want_cp;
-    *sk = want_sk;
+    out->family = f;
+    out->cp = want_cp;
+    out->sk = want_sk;
+    out->at = want_at;
     return SGEMM_OK;
+}
+
+void set_global_config(const Config& c) {
+    g_force_family = c.family;
+    g_force_cp = c.cp;
+    g_force_sk = c.sk;
+    g_force_at = c.at;
 }
 
 void read_env_locked() {
     if (g_env_read) return;
     g_env_read = true;
     const char* env = std::getenv("SGEMM_FORCE_CONFIG");
-    int fam = -1, cp = 0, sk = -1;
-    if (env != nullptr && parse_config(env, &fam, &cp, &sk) == SGEMM_OK) {
-        g_force_family = fam;
-        g_force_cp = cp;
-        g_force_sk = sk;
-    }
+    Config c;
+    if (env != nullptr && parse_config(env, &c) == SGEMM_OK) set_global_config(c);
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -205,6 +219,73 @@ __global__ void pack_rows_kernel(const float* __restrict__ src, long long lds,
     }
 }
 
+// dst (C x ldd, ldd = R rounded up to 4) <- the transpose of src (R x C, row
+// stride lds): dst[c][r] = src[r][c], zeros in the padding columns r >= R.
+// A block moves a 64 x 64 tile through shared memory (one padding column
+// against bank conflicts): float4 reads along src rows when src allows them,
+// float4 writes along dst rows (ldd is a multiple of 4 and dst 16-byte
+// aligned), so both sides stay coalesced in 16-byte pieces. HBM-bound: one
+// read and one write of the operand.
+constexpr int kTpTile = 64;
+
+__global__ void __launch_bounds__(256) transpose_pack_kernel(const float* __restrict__ src,
+                                                             long long lds, float* __restrict__ dst,
+                                                             long long ldd, int R, int C) {
+    __shared__ float tile[kTpTile][kTpTile + 1];
+    const bool vec = (reinterpret_cast<uintptr_t>(src) % 16 == 0) && (lds % 4 == 0);
+    const long long c0 = static_cast<long long>(blockIdx.x) * kTpTile;
+    const long long tiles_r = (ldd + kTpTile - 1) / kTpTile;
+    const int t = threadIdx.x;
+    for (long long tr = blockIdx.y; tr < tiles_r; tr += gridDim.y) {
+        const long long r0 = tr * kTpTile;
+        // 64 rows x 16 float4 of src; 16 consecutive threads read one row.
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int q = t + 256 * j;
+            const int rr = q >> 4, cc = (q & 15) * 4;
+            const long long r = r0 + rr, c = c0 + cc;
+            float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (r < R) {
+                const float* sp = src + r * lds + c;
+                if (vec && c + 3 < C) {
+                    v = *reinterpret_cast<const float4*>(sp);
+                } else {
+                    if (c < C) v.x = sp[0];
+                    if (c + 1 < C) v.y = sp[1];
+                    if (c + 2 < C) v.z = sp[2];
+                    if (c + 3 < C) v.w = sp[3];
+                }
+            }
+            tile[rr][cc] = v.x;
+            tile[rr][cc + 1] = v.y;
+            tile[rr][cc + 2] = v.z;
+            tile[rr][cc + 3] = v.w;
+        }
+        __syncthreads();
+        // 64 dst rows (src columns) x 16 float4 along r.
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int q = t + 256 * j;
+            const int cc = q >> 4, rr = (q & 15) * 4;
+            const long long c = c0 + cc, r = r0 + rr;
+            if (c < C && r < ldd)
+                *reinterpret_cast<float4*>(dst + c * ldd + r) =
+                    make_float4(tile[rr][cc], tile[rr + 1][cc], tile[rr + 2][cc], tile[rr + 3][cc]);
+        }
+        __syncthreads();
+    }
+}
+
+// Launches transpose_pack_kernel for an R x C source.
+cudaError_t launch_transpose_pack(const float* src, long long lds, float* dst, long long ldd,
+                                  int R, int C, cudaStream_t stream) {
+    const long long tiles_r = (ldd + kTpTile - 1) / kTpTile;
+    const dim3 grid(static_cast<unsigned>((C + kTpTile - 1) / kTpTile),
+                    static_cast<unsigned>(tiles_r < 65535 ? tiles_r : 65535));
+    transpose_pack_kernel<<<grid, 256, 0, stream>>>(src, lds, dst, ldd, R, C);
+    return cudaGetLastError();
+}
+
 size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
 
 __global__ void wait_timeout_kernel(GemmParams p) {
@@ -265,13 +346,24 @@ int cuda_fail(cudaError_t e, int code) {
 
 int check_args(int64_t M, int64_t N, int64_t K, float alpha, const float* A, int64_t lda,
                const float* B, int64_t ldb, const float* C, int64_t ldc) {
+    return check_args_ex(0, 0, M, N, K, alpha, A, lda, B, ldb, C, ldc);
+}
+
+int check_args_ex(int opa, int opb, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                  int64_t lda, const float* B, int64_t ldb, const float* C, int64_t ldc) {
     const int64_t kMax = 0x7fffffff;
+    if ((opa != 0 && opa != 1) || (opb != 0 && opb != 1)) return SGEMM_ERR_INVALID_VALUE;
     if (M < 0 || N < 0 || K < 0 || M > kMax || N > kMax || K > kMax) return SGEMM_ERR_INVALID_VALUE;
-    if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
+    // Stored shapes: A is M x K (K x M when transposed), B is K x N (N x K).
+    const int64_t a_rows = opa ? K : M, a_cols = opa ? M : K;
+    const int64_t b_rows = opb ? N : K, b_cols = opb ? K : N;
+    if (lda < (a_cols > 1 ? a_cols : 1) || ldb < (b_cols > 1 ? b_cols : 1) ||
+        ldc < (N > 1 ? N : 1))
         return SGEMM_ERR_INVALID_VALUE;
     // Offsets up to rows * ld must fit comfortably in int64 bytes.
     const int64_t kOff = (int64_t)1 << 60;
-    if ((M > 0 && lda > kOff / M) || (K > 0 && ldb > kOff / K) || (M > 0 && ldc > kOff / M))
+    if ((a_rows > 0 && lda > kOff / a_rows) || (b_rows > 0 && ldb > kOff / b_rows) ||
+        (M > 0 && ldc > kOff / M))
         return SGEMM_ERR_INVALID_VALUE;
     if (M == 0 || N == 0) return SGEMM_OK;
     if (C == nullptr || !aligned(C, 4)) return SGEMM_ERR_INVALID_VALUE;
@@ -281,9 +373,9 @@ int check_args(int64_t M, int64_t N, int64_t K, float alpha, const float* A, int
             return SGEMM_ERR_INVALID_VALUE;
         uintptr_t clo, chi, lo, hi;
         extent(C, M, N, ldc, &clo, &chi);
-        extent(A, M, K, lda, &lo, &hi);
+        extent(A, a_rows, a_cols, lda, &lo, &hi);
         if (lo < chi && clo < hi) return SGEMM_ERR_INVALID_VALUE;
-        extent(B, K, N, ldb, &lo, &hi);
+        extent(B, b_rows, b_cols, ldb, &lo, &hi);
         if (lo < chi && clo < hi) return SGEMM_ERR_INVALID_VALUE;
     }
     return SGEMM_OK;
@@ -322,7 +414,7 @@ int device_info(const DeviceInfo** out) {
     }
     const Registry& reg = registry();
     for (int f = 0; f < reg.count; ++f) {
-        for (int m = 0; m < 4; ++m) {
+        for (int m = 0; m < kModes; ++m) {
             int n = 0;
             e = reg.fam[f]->modes[m].prepare(&n);
             if (e != cudaSuccess || n <= 0) {
@@ -347,6 +439,16 @@ int device_info(const DeviceInfo** out) {
 int make_plan(const DeviceInfo* dev, int64_t M, int64_t N, int64_t K, float alpha,
               const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
               const float* C, int64_t ldc, bool allow_sk, bool allow_pack, Plan* pl) {
+    return make_plan_ex(dev, 0, 0, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, allow_sk,
+                        allow_pack, pl);
+}
+
+int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, int64_t K,
+                 float alpha, const float* A, int64_t lda, const float* B, int64_t ldb,
+                 float beta, const float* C, int64_t ldc, bool allow_sk, bool allow_pack,
+                 Plan* pl) {
+    pl->a_t = opa != 0;
+    pl->b_t = opb != 0;
     if (M == 0 || N == 0) {
         pl->kind = 0;
         return SGEMM_OK;
@@ -365,11 +467,15 @@ int make_plan(const DeviceInfo* dev, int64_t M, int64_t N, int64_t K, float alph
     pl->kind = 2;
     const int sms = dev->sm_count;
     pl->sms = sms;
-    int fi = g_force_family.load();
-    int force_cp_flag = g_force_cp.load();
-    int force_sk = g_force_sk.load();
-    if (fi < 0 && force_cp_flag == 0 && force_sk < 0)
-        shape_rule(M, N, K, &fi, &force_cp_flag, &force_sk);
+    Config cfg;
+    cfg.family = g_force_family.load();
+    cfg.cp = g_force_cp.load();
+    cfg.sk = g_force_sk.load();
+    cfg.at = g_force_at.load();
+    if (cfg.is_auto()) shape_rule(M, N, K, &cfg);
+    int fi = cfg.family;
+    const int force_cp_flag = cfg.cp;
+    const int force_sk = cfg.sk;
     // Under "auto" the choice below also decides whether the stream-K tail
     // is used; a forced family keeps the fixed rule further down.
     bool sk_decided = false;
@@ -404,9 +510,12 @@ int make_plan(const DeviceInfo* dev, int64_t M, int64_t N, int64_t K, float alph
                                     ? static_cast<double>(waves * kt + (rest * kt + nsm - 1) / nsm) + 8
                                     : inf;
             double c_64 = inf;
-            const bool a_tma = tma_ok(A, lda, M, K) || (allow_pack && N >= 256);
-            const bool b_tma = tma_ok(B, ldb, K, N) || (allow_pack && M >= 256);
-            if (force_cp_flag == 0 && a_tma && b_tma && dev->ctas_per_sm[2][0] >= 2) {
+            // A transposed A always goes by TMA (in place or packed); a
+            // transposed B is always copied to the row-major layout first.
+            const bool a_tma = opa ? true : (tma_ok(A, lda, M, K) || (allow_pack && N >= 256));
+            const bool b_tma = opb ? true : (tma_ok(B, ldb, K, N) || (allow_pack && M >= 256));
+            if (force_cp_flag == 0 && a_tma && b_tma &&
+                dev->ctas_per_sm[2][mode_index(LOAD_TMA, LOAD_TMA, opa)] >= 2) {
                 const int64_t tiles64 = ((M + 127) / 128) * ((N + 63) / 64);
                 c_64 = tiles64 <= nsm ? 0.63 * static_cast<double>(kt)
                                       : static_cast<double>((tiles64 + 2 * nsm - 1) / (2 * nsm)) *
@@ -425,23 +534,61 @@ int make_plan(const DeviceInfo* dev, int64_t M, int64_t N, int64_t K, float alph
     pl->fam = fam;
     const int bm = fam->bm, bn = fam->bn, bk = 32;
     const bool force_cp = force_cp_flag != 0;
+    // Pre-transposed A: a row-major A is copied once, transposed, into the
+    // workspace, and the kernel reads it through the transposed-A path
+    // ([BK][BM] stages, two float4 per lane and k-step), which keeps the FMA
+    // pipe busier (90 % against 83 % of active cycles at 4096^3 on GB300).
+    // "auto" takes it when the saving, about 8.5 % of the main loop (2MNK
+    // FLOP at ~66 TFLOP/s), exceeds the copy: ~5 us of launch and allocation
+    // plus one read and one write of A at ~3 TB/s (fitted to sweeps on GB300).
+    pl->a_pre = false;
+    if (!pl->a_t && allow_pack && !force_cp && cfg.at != 0) {
+        const double mk = static_cast<double>(M) * static_cast<double>(K);
+        const double gain = 0.085 * 2.0 * mk * static_cast<double>(N) / 66e12;
+        const double cost = 5e-6 + 8.0 * mk / 3e12;
+        pl->a_pre = cfg.at == 1 || gain > cost;
+    }
     std::memset(&pl->tmA, 0, sizeof(CUtensorMap));
     std::memset(&pl->tmB, 0, sizeof(CUtensorMap));
     int a_mode = LOAD_CPASYNC, b_mode = LOAD_CPASYNC;
     pl->pack_a = pl->pack_b = false;
     pl->pack_a_bytes = pl->pack_b_bytes = 0;
-    if (!force_cp && tma_ok(A, lda, M, K) && encode_2d(&pl->tmA, A, M, K, lda, bm, bk, true))
-        a_mode = LOAD_TMA;
-    if (!force_cp && tma_ok(B, ldb, K, N) && encode_2d(&pl->tmB, B, K, N, ldb, bk, bn, false))
+    const float* kPlaceholderA = reinterpret_cast<const float*>(uintptr_t{1} << 20);
+    if (pl->a_pre) {
+        const int64_t ld = (M + 3) & ~int64_t{3};
+        if (tma_ok(kPlaceholderA, ld, K, M) &&
+            encode_2d(&pl->tmA, kPlaceholderA, K, M, ld, bk, bm, false)) {
+            a_mode = LOAD_TMA;
+            pl->pack_a = true;
+            pl->lda_pack = ld;
+            pl->pack_a_bytes = align256(static_cast<size_t>(K) * static_cast<size_t>(ld) * 4);
+        } else {
+            pl->a_pre = false;
+        }
+    }
+    if (pl->a_pre) {
+        // (A is loaded from the transposed copy.)
+    } else if (!pl->a_t) {
+        if (!force_cp && tma_ok(A, lda, M, K) && encode_2d(&pl->tmA, A, M, K, lda, bm, bk, true))
+            a_mode = LOAD_TMA;
+    } else {
+        // Transposed A (stored K x M): [BK][BM] boxes, no swizzle, TMA only
+        // (":cpasync" does not apply to it).
+        if (tma_ok(A, lda, K, M) && encode_2d(&pl->tmA, A, K, M, lda, bk, bm, false))
+            a_mode = LOAD_TMA;
+    }
+    if (!pl->b_t && !force_cp && tma_ok(B, ldb, K, N) &&
+        encode_2d(&pl->tmB, B, K, N, ldb, bk, bn, false))
         b_mode = LOAD_TMA;
     // An operand TMA cannot describe in place is copied once to an aligned
     // buffer when the GEMM reads it often enough (A is read once per
     // 128-column tile of C, B once per 128-row tile): from 256 columns (rows)
-    // the 4-byte cp.async loads it saves cost more than the extra pass. The
+    // the 4-byte cp.async loads it saves cost more than the extra pass. A
+    // transposed A has no cp.async path, so it is always copied then. The
     // descriptor is encoded here against a placeholder address to make sure
     // the driver accepts the shape, and again on the real buffer at launch.
     const float* kPlaceholder = reinterpret_cast<const float*>(uintptr_t{1} << 20);
-    if (a_mode != LOAD_TMA && allow_pack && !force_cp && N >= 256) {
+    if (!pl->a_t && !pl->a_pre && a_mode != LOAD_TMA && allow_pack && !force_cp && N >= 256) {
         const int64_t ld = (K + 3) & ~int64_t{3};
         if (tma_ok(kPlaceholder, ld, M, K) && encode_2d(&pl->tmA, kPlaceholder, M, K, ld, bm, bk, true)) {
             a_mode = LOAD_TMA;
@@ -450,7 +597,31 @@ int make_plan(const DeviceInfo* dev, int64_t M, int64_t N, int64_t K, float alph
             pl->pack_a_bytes = align256(static_cast<size_t>(M) * static_cast<size_t>(ld) * 4);
         }
     }
-    if (b_mode != LOAD_TMA && allow_pack && !force_cp && M >= 256) {
+    if (pl->a_t && a_mode != LOAD_TMA) {
+        if (!allow_pack) return cuda_fail(cudaErrorMemoryAllocation, SGEMM_ERR_CUDA);
+        const int64_t ld = (M + 3) & ~int64_t{3};
+        if (!(tma_ok(kPlaceholder, ld, K, M) &&
+              encode_2d(&pl->tmA, kPlaceholder, K, M, ld, bk, bm, false)))
+            return cuda_fail(cudaErrorInvalidValue, SGEMM_ERR_LAUNCH);
+        a_mode = LOAD_TMA;
+        pl->pack_a = true;
+        pl->lda_pack = ld;
+        pl->pack_a_bytes = align256(static_cast<size_t>(K) * static_cast<size_t>(ld) * 4);
+    }
+    if (pl->b_t) {
+        // Transposed B (stored N x K): transposed once into a row-major K x N
+        // buffer. Read in place it would sit in shared memory as [BN][BK],
+        // and the packed FFMA2 needs two adjacent columns at one k in one
+        // register pair; the copy costs one HBM pass of B instead.
+        if (!allow_pack) return cuda_fail(cudaErrorMemoryAllocation, SGEMM_ERR_CUDA);
+        const int64_t ld = (N + 3) & ~int64_t{3};
+        pl->pack_b = true;
+        pl->ldb_pack = ld;
+        pl->pack_b_bytes = align256(static_cast<size_t>(K) * static_cast<size_t>(ld) * 4);
+        if (!force_cp && tma_ok(kPlaceholder, ld, K, N) &&
+            encode_2d(&pl->tmB, kPlaceholder, K, N, ld, bk, bn, false))
+            b_mode = LOAD_TMA;
+    } else if (b_mode != LOAD_TMA && allow_pack && !force_cp && M >= 256) {
         const int64_t ld = (N + 3) & ~int64_t{3};
         if (tma_ok(kPlaceholder, ld, K, N) && encode_2d(&pl->tmB, kPlaceholder, K, N, ld, bk, bn, false)) {
             b_mode = LOAD_TMA;
@@ -459,7 +630,7 @@ int make_plan(const DeviceInfo* dev, int64_t M, int64_t N, int64_t K, float alph
             pl->pack_b_bytes = align256(static_cast<size_t>(K) * static_cast<size_t>(ld) * 4);
         }
     }
-    const int mi = mode_index(a_mode, b_mode);
+    const int mi = mode_index(a_mode, b_mode, (pl->a_t || pl->a_pre) ? 1 : 0);
     pl->k = &fam->modes[mi];
 
     GemmParams& p = pl->p;
@@ -537,17 +708,34 @@ int launch_plan(Plan* pl, int* status, float* ws, cudaStream_t stream) {
     const int pack_grid = 16 * (pl->sms > 0 ? pl->sms : 1);
     if (pl->pack_a) {
         float* a2 = reinterpret_cast<float*>(w);
-        pack_rows_kernel<<<pack_grid, 256, 0, stream>>>(p.A, p.lda, a2, pl->lda_pack, p.M, p.K);
-        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
-        if (!encode_2d(&pl->tmA, a2, p.M, p.K, pl->lda_pack, pl->fam->bm, 32, true))
-            return cuda_fail(cudaErrorInvalidValue, SGEMM_ERR_LAUNCH);
+        if (pl->a_pre) {
+            // Row-major A (M x K) -> its transpose (K x lda_pack).
+            e = launch_transpose_pack(p.A, p.lda, a2, pl->lda_pack, p.M, p.K, stream);
+        } else {
+            // A transposed keeps its stored (K x M) layout in the copy.
+            const int rows = pl->a_t ? p.K : p.M, cols = pl->a_t ? p.M : p.K;
+            pack_rows_kernel<<<pack_grid, 256, 0, stream>>>(p.A, p.lda, a2, pl->lda_pack, rows,
+                                                            cols);
+            e = cudaGetLastError();
+        }
+        if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
+        const bool kt = pl->a_t || pl->a_pre;
+        const bool ok = kt ? encode_2d(&pl->tmA, a2, p.K, p.M, pl->lda_pack, 32, pl->fam->bm, false)
+                           : encode_2d(&pl->tmA, a2, p.M, p.K, pl->lda_pack, pl->fam->bm, 32, true);
+        if (!ok) return cuda_fail(cudaErrorInvalidValue, SGEMM_ERR_LAUNCH);
         p.A = a2;
         p.lda = pl->lda_pack;
     }
     if (pl->pack_b) {
         float* b2 = reinterpret_cast<float*>(w + pl->pack_a_bytes);
-        pack_rows_kernel<<<pack_grid, 256, 0, stream>>>(p.B, p.ldb, b2, pl->ldb_pack, p.K, p.N);
-        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
+        if (pl->b_t) {
+            // B stored N x K -> row-major K x ldb_pack.
+            e = launch_transpose_pack(p.B, p.ldb, b2, pl->ldb_pack, p.N, p.K, stream);
+        } else {
+            pack_rows_kernel<<<pack_grid, 256, 0, stream>>>(p.B, p.ldb, b2, pl->ldb_pack, p.K, p.N);
+            e = cudaGetLastError();
+        }
+        if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
         if (!encode_2d(&pl->tmB, b2, p.K, p.N, pl->ldb_pack, 32, pl->fam->bn, false))
             return cuda_fail(cudaErrorInvalidValue, SGEMM_ERR_LAUNCH);
         p.B = b2;
@@ -567,7 +755,8 @@ void plan_name(const Plan& pl, char* buf, int buflen) {
     if (pl.kind == 0) std::snprintf(buf, static_cast<size_t>(buflen), "none");
     else if (pl.kind == 1) std::snprintf(buf, static_cast<size_t>(buflen), "scale");
     else std::snprintf(buf, static_cast<size_t>(buflen), "%s%s%s%s", pl.k->name,
-                       pl.pack_a ? "+packA" : "", pl.pack_b ? "+packB" : "",
+                       pl.pack_a ? (pl.a_pre ? "+packAT" : "+packA") : "",
+                       pl.pack_b ? (pl.b_t ? "+packBT" : "+packB") : "",
                        pl.sk_tiles > 0 ? "+sk" : "");
 }
 
@@ -599,10 +788,12 @@ int launch_selftest_wait(unsigned long long timeout_ns, int* status, cudaStream_
 
 using namespace sg;
 
-extern "C" int sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float* A, int64_t lda,
-                     const float* B, int64_t ldb, float beta, float* C, int64_t ldc,
-                     cudaStream_t stream) {
-    int rc = check_args(M, N, K, alpha, A, lda, B, ldb, C, ldc);
+namespace {
+
+int run_sgemm(int opa, int opb, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+              int64_t lda, const float* B, int64_t ldb, float beta, float* C, int64_t ldc,
+              cudaStream_t stream) {
+    int rc = check_args_ex(opa, opb, M, N, K, alpha, A, lda, B, ldb, C, ldc);
     if (rc != SGEMM_OK) return rc;
     if (M == 0 || N == 0) return SGEMM_OK;
     const DeviceInfo* dev = nullptr;
@@ -610,8 +801,8 @@ extern "C" int sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float* 
     DeviceMemory* mem = nullptr;
     if ((rc = device_memory(dev, &mem)) != SGEMM_OK) return rc;
     Plan pl;
-    if ((rc = make_plan(dev, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, true, true, &pl)) !=
-        SGEMM_OK)
+    if ((rc = make_plan_ex(dev, opa, opb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, true, true,
+                           &pl)) != SGEMM_OK)
         return rc;
     float* ws = nullptr;
     if (pl.ws_bytes > 0) {
@@ -621,8 +812,8 @@ extern "C" int sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float* 
         void* w = nullptr;
         if (cudaMallocFromPoolAsync(&w, pl.ws_bytes, mem->pool, stream) != cudaSuccess) {
             (void)cudaGetLastError();
-            if ((rc = make_plan(dev, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, false, false,
-                                &pl)) != SGEMM_OK)
+            if ((rc = make_plan_ex(dev, opa, opb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                                   false, false, &pl)) != SGEMM_OK)
                 return rc;
         } else {
             ws = static_cast<float*>(w);
@@ -633,22 +824,48 @@ extern "C" int sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float* 
     return rc;
 }
 
-extern "C" int sgemm_plan(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
-                          int64_t lda, const float* B, int64_t ldb, float beta, const float* C,
-                          int64_t ldc, char* buf, int buflen, int* grid) {
-    int rc = check_args(M, N, K, alpha, A, lda, B, ldb, C, ldc);
+int plan_sgemm(int opa, int opb, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+               int64_t lda, const float* B, int64_t ldb, float beta, const float* C, int64_t ldc,
+               char* buf, int buflen, int* grid) {
+    int rc = check_args_ex(opa, opb, M, N, K, alpha, A, lda, B, ldb, C, ldc);
     if (rc != SGEMM_OK) return rc;
     Plan pl;
     if (M != 0 && N != 0) {
         const DeviceInfo* dev = nullptr;
         if ((rc = device_info(&dev)) != SGEMM_OK) return rc;
-        if ((rc = make_plan(dev, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, true, true, &pl)) !=
-            SGEMM_OK)
+        if ((rc = make_plan_ex(dev, opa, opb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, true,
+                               true, &pl)) != SGEMM_OK)
             return rc;
     }
     plan_name(pl, buf, buflen);
     if (grid != nullptr) *grid = pl.kind == 2 ? pl.grid : 0;
     return SGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" int sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float* A, int64_t lda,
+                     const float* B, int64_t ldb, float beta, float* C, int64_t ldc,
+                     cudaStream_t stream) {
+    return run_sgemm(0, 0, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+}
+
+extern "C" int sgemm_ex(int opa, int opb, int64_t M, int64_t N, int64_t K, float alpha,
+                        const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
+                        float* C, int64_t ldc, cudaStream_t stream) {
+    return run_sgemm(opa, opb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+}
+
+extern "C" int sgemm_plan(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                          int64_t lda, const float* B, int64_t ldb, float beta, const float* C,
+                          int64_t ldc, char* buf, int buflen, int* grid) {
+    return plan_sgemm(0, 0, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, buf, buflen, grid);
+}
+
+extern "C" int sgemm_plan_ex(int opa, int opb, int64_t M, int64_t N, int64_t K, float alpha,
+                             const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
+                             const float* C, int64_t ldc, char* buf, int buflen, int* grid) {
+    return plan_sgemm(opa, opb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, buf, buflen, grid);
 }
 
 extern "C" int sgemm_check_status(cudaStream_t stream, int* bits) {
@@ -683,40 +900,38 @@ extern "C" const char* sgemm_error_string(int code) {
 extern "C" int sgemm_last_cuda_error(void) { return t_last_cuda_error; }
 
 extern "C" int sgemm_set_config(const char* name) {
-    int fam = -1, cp = 0, sk = -1;
-    int rc = parse_config(name, &fam, &cp, &sk);
+    Config c;
+    int rc = parse_config(name, &c);
     if (rc != SGEMM_OK) return rc;
     {
         std::lock_guard<std::mutex> lock(g_mu);
         g_env_read = true;   // an explicit choice overrides the environment
     }
-    g_force_family = fam;
-    g_force_cp = cp;
-    g_force_sk = sk;
+    set_global_config(c);
     return SGEMM_OK;
 }
 
 extern "C" int sgemm_set_shape_config(int64_t M, int64_t N, int64_t K, const char* name) {
     if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_VALUE;
-    int fam = -1, cp = 0, sk = -1;
+    Config c;
     if (name != nullptr) {
-        const int rc = parse_config(name, &fam, &cp, &sk);
+        const int rc = parse_config(name, &c);
         if (rc != SGEMM_OK) return rc;
     }
     std::lock_guard<std::mutex> lock(g_rules_mu);
-    int at = -1;
+    int slot = -1;
     for (int i = 0; i < g_nrules; ++i)
-        if (g_rules[i].M == M && g_rules[i].N == N && g_rules[i].K == K) at = i;
-    if (fam < 0 && cp == 0 && sk < 0) {
+        if (g_rules[i].M == M && g_rules[i].N == N && g_rules[i].K == K) slot = i;
+    if (c.is_auto()) {
         // "auto" (or NULL) removes the rule.
-        if (at >= 0) g_rules[at] = g_rules[--g_nrules];
+        if (slot >= 0) g_rules[slot] = g_rules[--g_nrules];
         return SGEMM_OK;
     }
-    if (at < 0) {
+    if (slot < 0) {
         if (g_nrules == kMaxShapeRules) return SGEMM_ERR_INVALID_VALUE;
-        at = g_nrules++;
+        slot = g_nrules++;
     }
-    g_rules[at] = ShapeRule{M, N, K, fam, cp, sk};
+    g_rules[slot] = ShapeRule{M, N, K, c};
     return SGEMM_OK;
 }
 

@@ -24,7 +24,7 @@ constexpr int kMaxFamilies = 32;
 struct DeviceInfo {
     int device = -1;
     int sm_count = 0;
-    int ctas_per_sm[kMaxFamilies][4] = {};
+    int ctas_per_sm[kMaxFamilies][kModes] = {};
 };
 
 struct Plan {
@@ -36,6 +36,12 @@ struct Plan {
     int grid = 0;
     int sms = 0;                  // SMs of the device (grid of the packing copies)
     int sk_tiles = 0;             // tiles finished by the stream-K fixup
+    // Operand transposition: a_t, A stored K x M (loaded as [BK][BM] boxes);
+    // b_t, B stored N x K (transposed into the packed B buffer first).
+    bool a_t = false, b_t = false;
+    // a_pre: a row-major A copied transposed (K x lda_pack) into the packed
+    // A buffer, then read through the transposed-A kernel path.
+    bool a_pre = false;
     // Operands TMA cannot describe in place (base or row stride not 16-byte
     // aligned) but worth it: copied first to an aligned workspace buffer
     // with row stride ld_pack (a multiple of 4 floats).
@@ -47,9 +53,12 @@ struct Plan {
     size_t ws_bytes = 0;
 };
 
-// Validates the arguments of sgemm (SGEMM_OK or SGEMM_ERR_INVALID_VALUE).
+// Validates the arguments of sgemm (SGEMM_OK or SGEMM_ERR_INVALID_VALUE);
+// the _ex form those of sgemm_ex (opa, opb: 0 as stored, 1 transposed).
 int check_args(int64_t M, int64_t N, int64_t K, float alpha, const float* A, int64_t lda,
                const float* B, int64_t ldb, const float* C, int64_t ldc);
+int check_args_ex(int opa, int opb, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                  int64_t lda, const float* B, int64_t ldb, const float* C, int64_t ldc);
 
 // Per-device set-up of the current device (once, under a lock).
 int device_info(const DeviceInfo** out);
@@ -61,6 +70,13 @@ int device_info(const DeviceInfo** out);
 int make_plan(const DeviceInfo* dev, int64_t M, int64_t N, int64_t K, float alpha,
               const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
               const float* C, int64_t ldc, bool allow_sk, bool allow_pack, Plan* pl);
+// The same for transposed operands. A transposed B always needs the packing
+// copy, a transposed A whenever TMA cannot read it in place: with
+// allow_pack = false those return SGEMM_ERR_CUDA (allocation failure).
+int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, int64_t K,
+                 float alpha, const float* A, int64_t lda, const float* B, int64_t ldb,
+                 float beta, const float* C, int64_t ldc, bool allow_sk, bool allow_pack,
+                 Plan* pl);
 
 // Enqueues the plan on `stream`. status: device status word; ws: at least
 // pl->ws_bytes of 256-byte-aligned device memory (may be null when

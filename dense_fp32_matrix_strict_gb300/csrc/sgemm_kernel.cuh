@@ -94,12 +94,22 @@ struct GemmParams {
 //   1: tr = lane % 4, tc = lane / 4. A quarter-warp reads 2 B chunks and 4 A
 //      chunks: both loads cost 2 wavefronts (measured on sm_103a), a third
 //      fewer wavefronts per FMA.
+// A_T: A is given transposed (stored K x M, element (i, k) at A[k * lda + i]).
+//   The stage then holds A as [BK][BM] (k rows of BM contiguous m, no
+//   swizzle), the layout "The road to a fast GEMM" (v5) builds by a
+//   transposing store: a lane reads its rows as two float4 per k. TMA only.
 template <int BM_, int BN_, int BK_, int STAGES_, int A_MODE_, int B_MODE_, int FORDER_ = 2,
-          int EARLY_ = 0, int LMAP_ = 0>
+          int EARLY_ = 0, int LMAP_ = 0, int A_T_ = 0, int ALOAD_ = 4>
 struct Cfg {
     static constexpr int BM = BM_, BN = BN_, BK = BK_, STAGES = STAGES_;
     static constexpr int A_MODE = A_MODE_, B_MODE = B_MODE_;
-    static constexpr int FORDER = FORDER_, EARLY = EARLY_, LMAP = LMAP_;
+    static constexpr int FORDER = FORDER_, EARLY = EARLY_, LMAP = LMAP_, A_T = A_T_;
+    // ALOAD (row-major A only): k-values per shared load of a lane's row,
+    // 4 (float4 runs read once per 4 k-steps), 2 (float2 per 2 k-steps) or
+    // 1 (one float per row and k-step: fewest live registers).
+    static constexpr int ALOAD = ALOAD_;
+    static_assert(ALOAD == 1 || ALOAD == 2 || ALOAD == 4, "ALOAD is 1, 2 or 4");
+    static_assert(A_T == 0 || A_MODE == LOAD_TMA, "a transposed A is loaded by TMA only");
     static_assert(BK == 32, "A rows are one 128-byte swizzle span");
     static_assert(BM % 32 == 0 && BN % 64 == 0, "warp tile is 32 x 64");
     static constexpr int WARPS_M = BM / 32, WARPS_N = BN / 64;
@@ -249,7 +259,10 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmA, const CUtensorM
             const int k0 = kt * C::BK;
             if (tma_thread) {
                 mbar_arrive_expect_tx(full, C::TX_BYTES);
-                if (C::A_MODE == LOAD_TMA) tma_load_2d(dA, tmA, full, k0, m0);
+                if (C::A_MODE == LOAD_TMA) {
+                    if (C::A_T) tma_load_2d(dA, tmA, full, m0, k0);
+                    else tma_load_2d(dA, tmA, full, k0, m0);
+                }
                 if (C::B_MODE == LOAD_TMA) tma_load_2d(dB, tmB, full, n0, k0);
             }
             if (C::A_MODE == LOAD_CPASYNC) {
@@ -296,6 +309,12 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmA, const CUtensorM
 
 // ---- consumer -----------------------------------------------------------------
 
+// Offset of a lane's row i (0..7) from its row_base (see consumer()).
+template <class C>
+__device__ __forceinline__ constexpr int lane_row(int i) {
+    return C::A_T ? (i & 3) + 16 * (i >> 2) : 4 * i;
+}
+
 // A fragment of k-group kq (4 consecutive k) for the lane's 8 rows
 // {tr, tr+4, ..., tr+28}: row r's 16-byte chunk kq sits at chunk kq ^ (r % 8),
 // and r % 8 is tr for even i, tr + 4 (= tr ^ 4) for odd i.
@@ -319,7 +338,7 @@ __device__ __forceinline__ float lane_of(const float4& v, int kk) {
 //             lanes. Every output still sees the same FMA sequence, so the
 //             result is bit-identical to the scalar form.
 template <int FORDER>
-__device__ __forceinline__ void outer_product(float (&acc)[8][8], const float4 (&a)[8], int kk,
+__device__ __forceinline__ void outer_product(float (&acc)[8][8], const float (&av8)[8],
                                               const float4& b0, const float4& b1) {
     if (FORDER == 3) {
         // FFMA2 with the column pairs outer: consecutive instructions share
@@ -330,7 +349,7 @@ __device__ __forceinline__ void outer_product(float (&acc)[8][8], const float4 (
         for (int jp = 0; jp < 4; ++jp) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const float av = lane_of(a[i], kk);
+                const float av = av8[i];
                 float2 c = make_float2(acc[i][2 * jp], acc[i][2 * jp + 1]);
                 c = __ffma2_rn(make_float2(av, av), bp[jp], c);
                 acc[i][2 * jp] = c.x;
@@ -342,7 +361,7 @@ __device__ __forceinline__ void outer_product(float (&acc)[8][8], const float4 (
                               make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float av = lane_of(a[i], kk);
+            const float av = av8[i];
             const float2 aa = make_float2(av, av);
 #pragma unroll
             for (int jp = 0; jp < 4; ++jp) {
@@ -356,7 +375,7 @@ __device__ __forceinline__ void outer_product(float (&acc)[8][8], const float4 (
         const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float av = lane_of(a[i], kk);
+            const float av = av8[i];
 #pragma unroll
             for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av, bv[j], acc[i][j]);
         }
@@ -370,7 +389,11 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
     const int wm = warp % C::WARPS_M, wn = warp / C::WARPS_M;
     const int tr = C::LMAP == 1 ? (lane & 3) : (lane >> 3);
     const int tc = C::LMAP == 1 ? (lane >> 2) : (lane & 7);
-    const int row_base = wm * 32 + tr;        // rows row_base + 4 i, i = 0..7
+    // Lane rows: row_base + 4 i (row-major A: one swizzled 128-byte row per
+    // row, so rows 4 apart spread over the chunks), or, for a transposed A,
+    // row_base + (i & 3) + 16 (i >> 2) with row_base a multiple of 4 (two
+    // float4 runs along m per k).
+    const int row_base = C::A_T ? wm * 32 + 4 * tr : wm * 32 + tr;
     const int col_base = wn * 64 + 4 * tc;    // cols col_base + {0..3} and + 32 + {0..3}
     constexpr int KQ = C::BK / 4;
 
@@ -404,7 +427,8 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
         for (int kt = it.kb; kt < it.ke; ++kt) {
             if (!ready && !wait_bounded(full0 + 8 * s, ph, p, STATUS_CONSUMER_TIMEOUT)) return;
             ready = false;
-            const uint8_t* a_st = sA_ptr + s * C::A_BYTES + row_base * 128;
+            const uint8_t* a_st = C::A_T ? sA_ptr + s * C::A_BYTES + row_base * 4
+                                         : sA_ptr + s * C::A_BYTES + row_base * 128;
             const uint8_t* b_st = sB_ptr + s * C::B_BYTES + col_base * 4;
             const int s_nx = (s + 1 == C::STAGES) ? 0 : s + 1;
             const uint32_t ph_nx = (s + 1 == C::STAGES) ? (ph ^ 1u) : ph;
@@ -413,13 +437,45 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
                 if (C::EARLY && kq == KQ / 2 && kt + 1 < it.ke)
                     ready = mbar_test_wait(full0 + 8 * s_nx, ph_nx);
                 float4 a[8];
-                load_a_group(a, a_st, kq, tr);
+                if (!C::A_T && C::ALOAD == 4) load_a_group(a, a_st, kq, tr);
+                // Byte offsets of the lane's chunk kq in even and odd rows.
+                const int c0 = ((kq ^ tr) & 7) << 4, c1 = c0 ^ 64;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint8_t* brow = b_st + (kq * 4 + kk) * C::BN * 4;
                     const float4 b0 = *reinterpret_cast<const float4*>(brow);
                     const float4 b1 = *reinterpret_cast<const float4*>(brow + 32 * 4);
-                    outer_product<C::FORDER>(acc, a, kk, b0, b1);
+                    float av[8];
+                    if (C::A_T) {
+                        const uint8_t* arow = a_st + (kq * 4 + kk) * C::BM * 4;
+                        const float4 a0 = *reinterpret_cast<const float4*>(arow);
+                        const float4 a1 = *reinterpret_cast<const float4*>(arow + 16 * 4);
+                        av[0] = a0.x; av[1] = a0.y; av[2] = a0.z; av[3] = a0.w;
+                        av[4] = a1.x; av[5] = a1.y; av[6] = a1.z; av[7] = a1.w;
+                    } else {
+                        if (C::ALOAD == 4) {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) av[i] = lane_of(a[i], kk);
+                        } else if (C::ALOAD == 2) {
+                            if ((kk & 1) == 0) {
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    const float2 v = *reinterpret_cast<const float2*>(
+                                        a_st + i * 4 * 128 + ((i & 1) ? c1 : c0) + kk * 4);
+                                    a[i].x = v.x;
+                                    a[i].y = v.y;
+                                }
+                            }
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) av[i] = (kk & 1) ? a[i].y : a[i].x;
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                av[i] = *reinterpret_cast<const float*>(
+                                    a_st + i * 4 * 128 + ((i & 1) ? c1 : c0) + kk * 4);
+                        }
+                    }
+                    outer_product<C::FORDER>(acc, av, b0, b1);
                 }
             }
             mbar_arrive(empty0 + 8 * s);
@@ -433,7 +489,7 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
             float* slot = p.ws + static_cast<long long>(it.slot) * (C::BM * C::BN);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                float* row = slot + (row_base + 4 * i) * C::BN + col_base;
+                float* row = slot + (row_base + lane_row<C>(i)) * C::BN + col_base;
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
                     __stcg(reinterpret_cast<float4*>(row + 32 * h),
@@ -460,7 +516,7 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
             if (use_c) {
 #pragma unroll
                 for (int ii = 0; ii < 4; ++ii) {
-                    const int m = m0 + 4 * (4 * q + ii);
+                    const int m = m0 + lane_row<C>(4 * q + ii);
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int n = n0 + 32 * h;
@@ -473,7 +529,7 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
 #pragma unroll
             for (int ii = 0; ii < 4; ++ii) {
                 const int i = 4 * q + ii;
-                const int m = m0 + 4 * i;
+                const int m = m0 + lane_row<C>(i);
                 if (m >= p.M) continue;
                 float* crow = p.C + (long long)m * p.ldc;
 #pragma unroll

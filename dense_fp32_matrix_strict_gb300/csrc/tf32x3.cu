@@ -467,15 +467,18 @@ cudaError_t launch(const DeviceInfo* dev, const float* a_hi, const float* a_lo, 
 
 using namespace sg;
 
-extern "C" int sgemm_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
-                            int64_t lda, const float* B, int64_t ldb, float beta, float* C,
-                            int64_t ldc, cudaStream_t stream) {
-    int rc = check_args(M, N, K, alpha, A, lda, B, ldb, C, ldc);
+namespace {
+
+int run_3xtf32(int opa, int opb, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+               int64_t lda, const float* B, int64_t ldb, float beta, float* C, int64_t ldc,
+               cudaStream_t stream) {
+    int rc = check_args_ex(opa, opb, M, N, K, alpha, A, lda, B, ldb, C, ldc);
     if (rc != SGEMM_OK) return rc;
     if (M == 0 || N == 0) return SGEMM_OK;
     // Short reductions (the dropped lo*lo terms are not covered by the bound
     // below K = 3), alpha == 0 and K == 0 go to the FFMA path.
-    if (K < 16 || alpha == 0.0f) return sgemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+    if (K < 16 || alpha == 0.0f)
+        return sgemm_ex(opa, opb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
     const DeviceInfo* dev = nullptr;
     if ((rc = device_info(&dev)) != SGEMM_OK) return rc;
     int* status = nullptr;
@@ -489,7 +492,7 @@ extern "C" int sgemm_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, const 
     void* w = nullptr;
     if (cudaMallocFromPoolAsync(&w, 2 * a_pad + 2 * b_pad, pool, stream) != cudaSuccess) {
         (void)cudaGetLastError();
-        return sgemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+        return sgemm_ex(opa, opb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
     }
     unsigned char* ws = static_cast<unsigned char*>(w);
     float* a_hi = reinterpret_cast<float*>(ws);
@@ -497,21 +500,31 @@ extern "C" int sgemm_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, const 
     float* b_hi = reinterpret_cast<float*>(ws + 2 * a_pad);
     float* b_lo = reinterpret_cast<float*>(ws + 2 * a_pad + b_pad);
     const int sms = dev->sm_count;
-    cudaError_t e;
-    {
-        const int vec = ((reinterpret_cast<uintptr_t>(A) % 16) == 0 && (lda % 4) == 0) ? 1 : 0;
+    // Each split writes a K-major (rows x kp) hi/lo pair: a row-wise split
+    // of an operand already stored K-major (A, or a transposed B), a
+    // transposing split otherwise (B, or a transposed A).
+    auto split_kmajor = [&](const float* X, int64_t ldx, float* hi, float* lo, int64_t rows) {
+        const int vec = ((reinterpret_cast<uintptr_t>(X) % 16) == 0 && (ldx % 4) == 0) ? 1 : 0;
         const int64_t quads = kp / 4;
         const int gx = static_cast<int>(quads < 256 * 8 ? (quads + 255) / 256 : 8);
-        const int gy = static_cast<int>(M < 8192 ? M : 8192);
-        split_rows_kernel<<<dim3(gx, gy), 256, 0, stream>>>(A, lda, a_hi, a_lo, kp,
-                                                           static_cast<int>(M), static_cast<int>(K),
-                                                           vec);
-    }
-    if ((e = cudaGetLastError()) == cudaSuccess)
-        split_transpose_kernel<<<16 * sms, dim3(32, 8), 0, stream>>>(B, ldb, b_hi, b_lo, kp,
+        const int gy = static_cast<int>(rows < 8192 ? rows : 8192);
+        split_rows_kernel<<<dim3(gx, gy), 256, 0, stream>>>(X, ldx, hi, lo, kp,
+                                                           static_cast<int>(rows),
+                                                           static_cast<int>(K), vec);
+    };
+    auto split_transposed = [&](const float* X, int64_t ldx, float* hi, float* lo, int64_t cols) {
+        split_transpose_kernel<<<16 * sms, dim3(32, 8), 0, stream>>>(X, ldx, hi, lo, kp,
                                                                      static_cast<int>(K),
-                                                                     static_cast<int>(N));
-    if (e == cudaSuccess) e = cudaGetLastError();
+                                                                     static_cast<int>(cols));
+    };
+    cudaError_t e;
+    if (opa) split_transposed(A, lda, a_hi, a_lo, M);
+    else split_kmajor(A, lda, a_hi, a_lo, M);
+    if ((e = cudaGetLastError()) == cudaSuccess) {
+        if (opb) split_kmajor(B, ldb, b_hi, b_lo, N);
+        else split_transposed(B, ldb, b_hi, b_lo, N);
+        e = cudaGetLastError();
+    }
     if (e == cudaSuccess) {
         Params p;
         std::memset(&p, 0, sizeof(p));
@@ -535,4 +548,18 @@ extern "C" int sgemm_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, const 
     cudaFreeAsync(w, stream);
     if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
     return SGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" int sgemm_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                            int64_t lda, const float* B, int64_t ldb, float beta, float* C,
+                            int64_t ldc, cudaStream_t stream) {
+    return run_3xtf32(0, 0, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+}
+
+extern "C" int sgemm_3xtf32_ex(int opa, int opb, int64_t M, int64_t N, int64_t K, float alpha,
+                               const float* A, int64_t lda, const float* B, int64_t ldb,
+                               float beta, float* C, int64_t ldc, cudaStream_t stream) {
+    return run_3xtf32(opa, opb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
 }

@@ -22,16 +22,18 @@
  * All pointers are DEVICE pointers on the current CUDA device, owned by the
  * caller. The library keeps per-device set-up state (created on the first
  * call on a device: device properties, kernel attributes, a 256-byte device
- * status word and a private stream-ordered memory pool). Two kinds of call
- * take a workspace from that pool with cudaMallocFromPoolAsync on the call's
- * stream and return it with cudaFreeAsync on the same stream (so concurrent
- * calls on different streams never share it and stream capture records it
- * as an allocation node): a problem whose last wave of tiles is split across
- * all SMs (the stream-K tail, at most 2 x SMs x 64 KB), and an operand that
- * TMA cannot load in place (base or leading dimension not 16-byte aligned)
- * but that the kernel reads often enough (A when N >= 256, B when M >= 256)
- * is first copied to an aligned buffer (rows x cols rounded up to 4 floats).
- * If that allocation fails the call uses neither.
+ * status word and a private stream-ordered memory pool). Some calls take a
+ * workspace from that pool with cudaMallocFromPoolAsync on the call's stream
+ * and return it with cudaFreeAsync on the same stream (so concurrent calls
+ * on different streams never share it and stream capture records it as an
+ * allocation node): a problem whose last wave of tiles is split across all
+ * SMs (the stream-K tail, at most 2 x SMs x 64 KB); a row-major A large
+ * enough that the kernel runs faster on its transpose, which is copied
+ * first (K x M floats, M rounded up to 4); and an operand that TMA cannot
+ * load in place (base or leading dimension not 16-byte aligned) but that
+ * the kernel reads often enough (A when N >= 256, B when M >= 256), copied
+ * to an aligned buffer (rows x cols rounded up to 4 floats). If that
+ * allocation fails the call uses none of them.
  */
 #ifndef SGEMM_GB300_H
 #define SGEMM_GB300_H
@@ -97,6 +99,43 @@ SGEMM_API int sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float* A
           const float* B, int64_t ldb, float beta, float* C, int64_t ldc,
           cudaStream_t stream);
 
+/* Operand transposition flags for the _ex entry points. */
+#define SGEMM_OP_N 0   /* the operand as stored (row-major)        */
+#define SGEMM_OP_T 1   /* the transpose of the stored matrix        */
+
+/*
+ * sgemm_ex — C = alpha * op(A) * op(B) + beta * C with cuBLAS-style
+ * transposition flags, in this library's row-major convention. The pages'
+ * kernels take square, untransposed, row-major operands only; the Tinyforge
+ * README counts transposed operands among the generality cuBLAS offers and
+ * its kernels leave out, and "The road to a fast GEMM" (benchmark harness)
+ * calls cuBLAS through the transpose identity of row- and column-major
+ * storage.
+ *
+ *   opa == SGEMM_OP_N: op(A) = A, stored M x K, (i, k) at A[i * lda + k],
+ *                      lda >= max(1, K).
+ *   opa == SGEMM_OP_T: op(A) = A^T, A stored K x M, op(A)(i, k) at
+ *                      A[k * lda + i], lda >= max(1, M).
+ *   opb == SGEMM_OP_N: op(B) = B, stored K x N, (k, j) at B[k * ldb + j],
+ *                      ldb >= max(1, N).
+ *   opb == SGEMM_OP_T: op(B) = B^T, B stored N x K, op(B)(k, j) at
+ *                      B[j * ldb + k], ldb >= max(1, K).
+ *
+ * Everything else (sizes, C, readings, errors, asynchrony) is as for sgemm;
+ * an opa or opb other than 0 or 1 returns SGEMM_ERR_INVALID_VALUE. A
+ * transposed A is read by TMA in its stored layout when its base is 16-byte
+ * aligned and lda % 4 == 0, else first copied (in that layout) to an aligned
+ * workspace buffer; a transposed B is always first transposed into a
+ * row-major K x N workspace buffer (one HBM pass over B). Those buffers come
+ * from the library's stream-ordered pool like the stream-K workspace; if the
+ * pool cannot supply one, the call returns SGEMM_ERR_CUDA with
+ * cudaErrorMemoryAllocation kept for sgemm_last_cuda_error.
+ * sgemm_ex(SGEMM_OP_N, SGEMM_OP_N, ...) is sgemm(...).
+ */
+SGEMM_API int sgemm_ex(int opa, int opb, int64_t M, int64_t N, int64_t K, float alpha,
+                       const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
+                       float* C, int64_t ldc, cudaStream_t stream);
+
 /*
  * sgemm_check_status — synchronise `stream`, then read and clear the current
  * device's status word. Returns SGEMM_OK, SGEMM_ERR_DEVICE_TIMEOUT if any
@@ -127,6 +166,13 @@ SGEMM_API int sgemm_last_cuda_error(void);
 SGEMM_API int sgemm_plan(int64_t M, int64_t N, int64_t K, float alpha, const float* A, int64_t lda,
                const float* B, int64_t ldb, float beta, const float* C, int64_t ldc,
                char* buf, int buflen, int* grid);
+
+/* sgemm_plan for sgemm_ex's arguments. A transposed A shows as "_ATtma_"
+ * in the kernel name; "+packBT" means B is first transposed into a
+ * row-major buffer. */
+SGEMM_API int sgemm_plan_ex(int opa, int opb, int64_t M, int64_t N, int64_t K, float alpha,
+                            const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
+                            const float* C, int64_t ldc, char* buf, int buflen, int* grid);
 
 /*
  * sgemm_set_config — force a kernel configuration for later calls in this
@@ -217,6 +263,14 @@ SGEMM_API int sgemm_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stre
 SGEMM_API int sgemm_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
                            int64_t lda, const float* B, int64_t ldb, float beta, float* C,
                            int64_t ldc, cudaStream_t stream);
+
+/* sgemm_3xtf32 with sgemm_ex's transposition flags and leading-dimension
+ * rules. The split pre-passes read each operand in its stored layout and
+ * write the K-major hi/lo copies the MMAs take, so transposition costs no
+ * extra pass here. */
+SGEMM_API int sgemm_3xtf32_ex(int opa, int opb, int64_t M, int64_t N, int64_t K, float alpha,
+                              const float* A, int64_t lda, const float* B, int64_t ldb,
+                              float beta, float* C, int64_t ldc, cudaStream_t stream);
 
 /*
  * sgemm_noalloc — the same operation, arguments, results and errors as

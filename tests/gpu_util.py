@@ -49,22 +49,25 @@ def untouched_outside(buf, start, rows, cols, ld, pad_value=np.nan):
 
 
 def run(alpha, A, B, beta, C0, lda=None, ldb=None, ldc=None, offsets=(0, 0, 0),
-        stream=None, c_fill=None):
+        stream=None, c_fill=None, transa=False, transb=False):
     """Run sgemm on device copies of A, B, C0; return (C, guards_ok, plan).
+
+    With transa / transb, A / B are the stored matrices (K x M / N x K) and
+    the call computes alpha * op(A) op(B) + beta * C through sgemm_ex.
 
     C0 None means C starts as NaN (only valid when beta == 0, which must not
     read C); c_fill overrides C's starting contents likewise.
     """
     torch = _torch()
-    M, K = A.shape
-    N = B.shape[1]
+    M = A.shape[1] if transa else A.shape[0]
+    N = B.shape[0] if transb else B.shape[1]
     dA, _, _ = place(A, lda, offsets[0])
     dB, _, _ = place(B, ldb, offsets[1])
     start_c = C0 if C0 is not None else np.full((M, N), np.nan if c_fill is None else c_fill,
                                                 np.float32)
     dC, bufC, startC = place(start_c, ldc, offsets[2])
-    plan = sg.plan_tensors(alpha, dA, dB, beta, dC)
-    sg.sgemm_tensors(alpha, dA, dB, beta, dC, stream=stream)
+    plan = sg.plan_tensors(alpha, dA, dB, beta, dC, transa=transa, transb=transb)
+    sg.sgemm_tensors(alpha, dA, dB, beta, dC, stream=stream, transa=transa, transb=transb)
     sg.check_status(stream=stream)
     torch.cuda.synchronize()
     C = dC.cpu().numpy()

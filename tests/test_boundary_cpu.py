@@ -93,7 +93,8 @@ def test_null_ab_allowed_when_not_read(lib):
 
 
 def test_config_names(lib):
-    for good in ["auto", "128x128", "64x64", "128x128:cpasync", "auto:cpasync"]:
+    for good in ["auto", "128x128", "64x64", "128x64", "128x128:cpasync", "auto:cpasync",
+                 "auto:at", "128x128:noat:dp"]:
         assert sg.sgemm_set_config(good) == sg.SGEMM_OK
     for bad in ["", "x", "256x256", "128x128:tma", "auto:"]:
         if bad == "":
@@ -130,3 +131,30 @@ def test_shape_config_rules(lib):
     assert sg.sgemm_set_shape_config(1, 1, 7, "auto") == sg.SGEMM_OK
     assert sg.sgemm_set_shape_config(1, 1, 1000, "64x64") == sg.SGEMM_OK
     assert sg.sgemm_clear_shape_configs() == sg.SGEMM_OK
+
+
+BAD_EX_ARGS = [
+    (2, 0, 4, 4, 4, 1.0, A_PTR, 4, B_PTR, 4, 0.0, C_PTR, 4),          # opa not 0/1
+    (0, -1, 4, 4, 4, 1.0, A_PTR, 4, B_PTR, 4, 0.0, C_PTR, 4),         # opb not 0/1
+    (1, 0, 8, 4, 4, 1.0, A_PTR, 7, B_PTR, 4, 0.0, C_PTR, 4),          # A^T: lda < M
+    (0, 1, 4, 4, 8, 1.0, A_PTR, 8, B_PTR, 7, 0.0, C_PTR, 4),          # B^T: ldb < K
+    (1, 1, 4, 4, 4, 1.0, A_PTR, 4, B_PTR, 4, 0.0, A_PTR + 32, 4),     # C overlaps A
+    (1, 0, 4, 4, 4, 1.0, A_PTR, 1 << 62, B_PTR, 4, 0.0, C_PTR, 4),    # lda overflows (K rows)
+]
+
+
+@pytest.mark.parametrize("args", BAD_EX_ARGS)
+def test_invalid_transposed_arguments_rejected_without_gpu(lib, args):
+    assert sg.sgemm_ex(*args, 0) == sg.SGEMM_ERR_INVALID_VALUE
+    assert sg.sgemm_3xtf32_ex(*args, 0) == sg.SGEMM_ERR_INVALID_VALUE
+    assert sg.sgemm_plan_ex(*args)[0] == sg.SGEMM_ERR_INVALID_VALUE
+
+
+def test_transposed_leading_dimensions_follow_the_stored_shape(lib):
+    # M = 8, K = 4: A^T is stored 4 x 8, so lda = 8 is the minimum; a plain
+    # A (8 x 4) would accept lda = 4, the transposed one must not.
+    assert sg.sgemm_plan_ex(1, 0, 8, 4, 4, 1.0, A_PTR, 4, B_PTR, 4, 0.0, C_PTR, 4)[0] == \
+        sg.SGEMM_ERR_INVALID_VALUE
+    assert sg.sgemm_plan_ex(0, 0, 8, 4, 4, 1.0, A_PTR, 4, B_PTR, 4, 0.0, C_PTR, 4)[0] != \
+        sg.SGEMM_ERR_INVALID_VALUE
+    assert sg.sgemm_ex(1, 1, 0, 4, 4, 1.0, A_PTR, 1, B_PTR, 4, 0.0, C_PTR, 4, 0) == sg.SGEMM_OK

@@ -264,8 +264,9 @@ def test_workload_sq4096_uniform_sampled():
 
 def test_workload_ragged_every_element():
     rep, plan = _workload("ragged_4093x5120x1531_normal", full=True)
-    # lda = 1531 is not 16-byte aligned: A is copied to an aligned buffer.
-    assert "Atma_Btma+packA" in plan[0], plan
+    # A (6.3 M floats, lda = 1531) is copied transposed into an aligned
+    # buffer and read through the transposed-A path.
+    assert "ATtma_Btma+packAT" in plan[0], plan
 
 
 def test_workload_llm_projection_sampled():
@@ -437,3 +438,35 @@ def test_sgemm_inside_a_captured_cuda_graph():
     torch.cuda.synchronize()
     sg.check_status()
     check_full(0.7, A, B, -1.3, C0, work.cpu().numpy())
+
+
+@pytest.mark.parametrize("config", ["128x128", "128x128:dp", "128x64:dp", "64x64"])
+def test_pretransposed_a_gives_the_same_bits(config):
+    # ":at" copies the row-major A transposed and runs the transposed-A path;
+    # every output sees the same FMA sequence as with ":noat".
+    M, N, K = 700, 900, 1500
+    A, B, C0 = gen(M, N, K, seed=61)
+    outs, plans = [], []
+    for mod in (":noat", ":at"):
+        assert sg.sgemm_set_config(config + mod) == 0
+        try:
+            C, guards, plan = gpu_util.run(0.7, A, B, -1.3, C0, lda=K + 1, offsets=(1, 0, 0))
+        finally:
+            sg.sgemm_set_config("auto")
+        assert guards
+        outs.append(C)
+        plans.append(plan[0])
+    assert "+packAT" not in plans[0] and "ATtma" not in plans[0], plans
+    assert "_ATtma_" in plans[1] and "+packAT" in plans[1], plans
+    assert np.array_equal(outs[0], outs[1]), plans
+    check_full(0.7, A, B, -1.3, C0, outs[1])
+
+
+def test_auto_pretransposes_a_large_a():
+    torch = pytest.importorskip("torch")
+    A = torch.empty(2048, 2048, device="cuda")
+    B = torch.empty(2048, 2048, device="cuda")
+    C = torch.empty(2048, 2048, device="cuda")
+    assert "+packAT" in sg.plan_tensors(1.0, A, B, 0.0, C)[0]
+    small = torch.empty(256, 256, device="cuda")
+    assert "+packAT" not in sg.plan_tensors(1.0, small, small, 0.0, small.clone())[0]
