@@ -158,10 +158,13 @@ SGEMM_API int sgemm_last_cuda_error(void);
  * these arguments: writes a NUL-terminated name such as
  * "ws_128x128x32_s4_Atma_Btma" into buf (at most buflen bytes) and the
  * launch grid into *grid (if not NULL). "+packA" / "+packB" mean that
- * operand is first copied to an aligned buffer by a small copy kernel; a
- * "+sk" suffix means the last wave is split across the SMs (stream-K) and
- * finished by a second, small fixup kernel. Returns the same argument errors as sgemm, or SGEMM_OK. A name of
- * "scale" means the alpha == 0 / K == 0 path; "none" means M == 0 or N == 0.
+ * operand is first copied to an aligned buffer by a small copy kernel;
+ * "+packAT" that A is first copied transposed and read through the
+ * transposed-A path ("_ATtma_" in the kernel name); a "+sk" suffix means the
+ * last wave is split across the SMs (stream-K) and finished by a second,
+ * small fixup kernel. Returns the same argument errors as sgemm, or
+ * SGEMM_OK. A name of "scale" means the alpha == 0 / K == 0 path; "none"
+ * means M == 0 or N == 0.
  */
 SGEMM_API int sgemm_plan(int64_t M, int64_t N, int64_t K, float alpha, const float* A, int64_t lda,
                const float* B, int64_t ldb, float beta, const float* C, int64_t ldc,
@@ -179,8 +182,10 @@ SGEMM_API int sgemm_plan_ex(int opa, int opb, int64_t M, int64_t N, int64_t K, f
  * process (for sweeps and tests). `name` is "auto" (default), "128x128",
  * "64x64" or "128x64" for the CTA tile, or one of the family names sgemm_config_names
  * lists, optionally followed by modifiers: ":cpasync" loads both operands
- * with cp.async even when TMA could be used, ":dp" never splits the last
- * wave (plain data-parallel schedule, no workspace), e.g.
+ * with cp.async even when TMA could be used (a transposed A excepted: it is
+ * always loaded by TMA), ":dp" never splits the last
+ * wave (plain data-parallel schedule), ":at" / ":noat" always / never
+ * copy a row-major A transposed first (the default decides by size), e.g.
  * "128x128:cpasync:dp" or "auto:dp". Returns SGEMM_ERR_INVALID_VALUE for an
  * unknown name. The environment variable SGEMM_FORCE_CONFIG, read on the
  * first call, sets the same thing.
@@ -254,6 +259,9 @@ SGEMM_API int sgemm_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stre
  * cores do not round every accumulation step like FFMA, so results differ
  * from sgemm's in the last bits. The pages measure TF32 only as an inexact
  * mode and describe no split; this entry point is this library's own.
+ * Infinite inputs are outside its contract: the lo part of an infinity is
+ * NaN, so an output the definition makes +-inf comes out NaN (NaN inputs
+ * still give NaN).
  *
  * Each call splits A and the transpose of B into a workspace of
  * 8 * (M + N) * K bytes (K rounded up to 4) taken from the library's
