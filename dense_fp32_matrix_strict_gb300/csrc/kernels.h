@@ -43,7 +43,7 @@ cudaError_t fixup_launch(const GemmParams* p, int sk_tiles, cudaStream_t stream)
 // One kernel family: a CTA tile and tuning knobs, instantiated for the four
 // (A, B) load-mode pairs of a row-major A and the two B load modes of a
 // transposed A (TMA) in mode_index order, plus its stream-K fixup.
-constexpr int kModes = 6;
+constexpr int kModes = 7;
 
 struct KernelFamily {
     const char* name;
@@ -53,17 +53,24 @@ struct KernelFamily {
 };
 
 // Index into a family's modes: TMA/TMA, CP/TMA, TMA/CP, CP/CP for a
-// row-major A; then transposed A (TMA) with B by TMA, with B by cp.async.
+// row-major A; then transposed A (TMA) with B by TMA, with B by cp.async;
+// then a row-major A transposed in shared memory, with B by TMA.
 inline constexpr int mode_index(int a_mode, int b_mode, int a_t = 0) {
-    return a_t ? 4 + b_mode : a_mode + 2 * b_mode;
+    return a_mode == LOAD_TMA_XP ? 6 : a_t ? 4 + b_mode : a_mode + 2 * b_mode;
 }
 
 template <int BM, int BN, int S, int AM, int BMD, int FORDER, int EARLY, int LMAP, int AT = 0,
           int ALOAD = 4>
 constexpr KernelEntry make_entry(const char* name) {
     using C = Cfg<BM, BN, 32, S, AM, BMD, FORDER, EARLY, LMAP, AT, ALOAD>;
-    return KernelEntry{name, BM, BN, 32, S, AM, BMD, C::THREADS, C::SMEM_BYTES,
-                       &ws_prepare<C>, &ws_launch<C>};
+    // A variant whose ring does not fit in shared memory is left out (no
+    // entry points); the planner never picks it.
+    if constexpr (!C::FITS)
+        return KernelEntry{name, BM, BN, 32, S, AM, BMD, C::THREADS, C::SMEM_BYTES, nullptr,
+                           nullptr};
+    else
+        return KernelEntry{name, BM, BN, 32, S, AM, BMD, C::THREADS, C::SMEM_BYTES,
+                           &ws_prepare<C>, &ws_launch<C>};
 }
 
 #define SG_FAMILY_A(NAME, BM, BN, S, FORDER, EARLY, LMAP, ALOAD)                           \
@@ -82,6 +89,8 @@ constexpr KernelEntry make_entry(const char* name) {
                     NAME "_ATtma_Btma"),                                                    \
                 make_entry<BM, BN, S, LOAD_TMA, LOAD_CPASYNC, FORDER, EARLY, LMAP, 1>(        \
                     NAME "_ATtma_Bcp"),                                                     \
+                make_entry<BM, BN, S, LOAD_TMA_XP, LOAD_TMA, FORDER, EARLY, LMAP>(            \
+                    NAME "_Axp_Btma"),                                                      \
             },                                                                              \
             &fixup_launch<BM, BN>                                                           \
     }

@@ -79,7 +79,8 @@ thread_local int t_last_cuda_error = 0;
 // make_plan only while the global configuration is "auto". An autotuning
 // sweep installs the fastest configuration it measured for each shape here.
 // A configuration choice: family index (-1 auto), cp.async forced, stream-K
-// (-1 auto, 0 never), pre-transposed A (-1 auto, 0 never, 1 always).
+// (-1 auto, 0 never), how a row-major A reaches the consumers (-1 auto, 0 as
+// stored, 1 through a transposed copy in HBM, 2 transposed in shared memory).
 struct Config {
     int family = -1, cp = 0, sk = -1, at = -1;
     bool is_auto() const { return family < 0 && cp == 0 && sk < 0 && at < 0; }
@@ -123,6 +124,7 @@ int parse_config(const char* name, Config* out) {
         else if (std::strcmp(mod, "dp") == 0) want_sk = 0;
         else if (std::strcmp(mod, "at") == 0) want_at = 1;
         else if (std::strcmp(mod, "noat") == 0) want_at = 0;
+        else if (std::strcmp(mod, "xp") == 0) want_at = 2;
         else return SGEMM_ERR_INVALID_VALUE;
         mod = next;
     }
@@ -416,13 +418,17 @@ int device_info(const DeviceInfo** out) {
     for (int f = 0; f < reg.count; ++f) {
         for (int m = 0; m < kModes; ++m) {
             int n = 0;
-            e = reg.fam[f]->modes[m].prepare(&n);
+            const KernelEntry& ke = reg.fam[f]->modes[m];
+            e = ke.prepare != nullptr ? ke.prepare(&n) : cudaSuccess;
             if (e != cudaSuccess || n <= 0) {
-                // The 128 x 128 and 64 x 64 families must work; the 128 x 64
-                // family (which "auto" then skips) and a tuning alternative
-                // that cannot run here are only marked unusable.
-                if (f < 2) return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidConfiguration,
-                                            SGEMM_ERR_CUDA);
+                // The 128 x 128 and 64 x 64 families must work in their
+                // row-major and transposed-A modes; the in-smem transpose
+                // mode, the 128 x 64 family (which "auto" then skips) and a
+                // tuning alternative that cannot run here are only marked
+                // unusable.
+                if (f < 2 && m < 6)
+                    return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidConfiguration,
+                                     SGEMM_ERR_CUDA);
                 (void)cudaGetLastError();
                 n = 0;
             }
@@ -534,19 +540,42 @@ int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, 
     pl->fam = fam;
     const int bm = fam->bm, bn = fam->bn, bk = 32;
     const bool force_cp = force_cp_flag != 0;
-    // Pre-transposed A: a row-major A is copied once, transposed, into the
-    // workspace, and the kernel reads it through the transposed-A path
-    // ([BK][BM] stages, two float4 per lane and k-step), which keeps the FMA
-    // pipe busier (90 % against 83 % of active cycles at 4096^3 on GB300).
-    // "auto" takes it when the saving, about 8.5 % of the main loop (2MNK
-    // FLOP at ~66 TFLOP/s), exceeds the copy: ~5 us of launch and allocation
-    // plus one read and one write of A at ~3 TB/s (fitted to sweeps on GB300).
+    // How a row-major A reaches the consumers. The transposed-A read
+    // ([BK][BM] stages, two float4 per lane and k-step) keeps the FMA pipe
+    // busier than the row-major read (90 % against 83 % of active cycles at
+    // 4096^3 on GB300). Two ways to get there: a transposed copy of A in the
+    // workspace ("a_pre", then the transposed-A kernel), or the in-smem
+    // transpose (mode 6, transposer warps in the kernel, no copy), possible
+    // for an A TMA can read in place, when B goes by TMA too and the family
+    // has the variant.
+    const bool b_will_tma = pl->b_t ? true : (tma_ok(B, ldb, K, N) || (allow_pack && M >= 256));
+    const bool xp_possible = !pl->a_t && !force_cp && tma_ok(A, lda, M, K) && b_will_tma &&
+                             dev->ctas_per_sm[fi][mode_index(LOAD_TMA_XP, LOAD_TMA)] > 0;
+    // Either way beats reading the row-major A as stored. Measured on GB300
+    // against that: the in-smem transpose saves ~4 % of the main loop (2MNK
+    // FLOP at ~66 TFLOP/s), the HBM copy ~8.5 % but costs ~5 us of launch and
+    // allocation plus one read and one write of A at ~3 TB/s. "auto" takes
+    // the copy where its extra saving pays for it, else the in-smem
+    // transpose where possible (not for the two-CTA 128 x 64 tile, where it
+    // gains nothing).
+    const double mk = static_cast<double>(M) * static_cast<double>(K);
+    const double t_main = 2.0 * mk * static_cast<double>(N) / 66e12;
+    const double copy_cost = 5e-6 + 8.0 * mk / 3e12;
+    const bool copy_ok = !pl->a_t && allow_pack && !force_cp;
+    const bool xp_auto = xp_possible && fi != 2;
     pl->a_pre = false;
-    if (!pl->a_t && allow_pack && !force_cp && cfg.at != 0) {
-        const double mk = static_cast<double>(M) * static_cast<double>(K);
-        const double gain = 0.085 * 2.0 * mk * static_cast<double>(N) / 66e12;
-        const double cost = 5e-6 + 8.0 * mk / 3e12;
-        pl->a_pre = cfg.at == 1 || gain > cost;
+    pl->a_xp = false;
+    if (cfg.at == 1) {
+        pl->a_pre = copy_ok;
+    } else if (cfg.at == 2) {
+        pl->a_xp = xp_possible;
+    } else if (cfg.at < 0) {
+        if (xp_auto) {
+            pl->a_pre = copy_ok && (0.085 - 0.04) * t_main > copy_cost;
+            pl->a_xp = !pl->a_pre;
+        } else {
+            pl->a_pre = copy_ok && 0.085 * t_main > copy_cost;
+        }
     }
     std::memset(&pl->tmA, 0, sizeof(CUtensorMap));
     std::memset(&pl->tmB, 0, sizeof(CUtensorMap));
@@ -629,6 +658,10 @@ int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, 
             pl->ldb_pack = ld;
             pl->pack_b_bytes = align256(static_cast<size_t>(K) * static_cast<size_t>(ld) * 4);
         }
+    }
+    if (pl->a_xp) {
+        if (a_mode == LOAD_TMA && b_mode == LOAD_TMA) a_mode = LOAD_TMA_XP;
+        else pl->a_xp = false;
     }
     const int mi = mode_index(a_mode, b_mode, (pl->a_t || pl->a_pre) ? 1 : 0);
     pl->k = &fam->modes[mi];

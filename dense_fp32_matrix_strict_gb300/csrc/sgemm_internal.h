@@ -42,6 +42,9 @@ struct Plan {
     // a_pre: a row-major A copied transposed (K x lda_pack) into the packed
     // A buffer, then read through the transposed-A kernel path.
     bool a_pre = false;
+    // a_xp: a row-major A transposed in shared memory by the kernel's
+    // transposer warps (mode LOAD_TMA_XP).
+    bool a_xp = false;
     // Operands TMA cannot describe in place (base or row stride not 16-byte
     // aligned) but worth it: copied first to an aligned workspace buffer
     // with row stride ld_pack (a multiple of 4 floats).

@@ -50,7 +50,10 @@
 
 namespace sg {
 
-enum LoadMode : int { LOAD_TMA = 0, LOAD_CPASYNC = 1 };
+// LOAD_TMA_XP (A only): TMA brings the row-major A tile into a raw staging
+// buffer and three transposer warps rewrite it as [BK][BM] for the
+// consumers (see transposer()).
+enum LoadMode : int { LOAD_TMA = 0, LOAD_CPASYNC = 1, LOAD_TMA_XP = 2 };
 
 // Status bits written by the kernels when a bounded wait gives up or a
 // schedule invariant fails.
@@ -98,6 +101,10 @@ struct GemmParams {
 //   The stage then holds A as [BK][BM] (k rows of BM contiguous m, no
 //   swizzle), the layout "The road to a fast GEMM" (v5) builds by a
 //   transposing store: a lane reads its rows as two float4 per k. TMA only.
+// A_MODE == LOAD_TMA_XP: a row-major A reaches the consumers in the same
+//   [BK][BM] layout, built in shared memory by transposer warps, with the
+//   16-byte chunks of k-row k XOR-swizzled by (k / 4) mod 8 so that both the
+//   transposing stores and the consumers' reads are free of bank conflicts.
 template <int BM_, int BN_, int BK_, int STAGES_, int A_MODE_, int B_MODE_, int FORDER_ = 2,
           int EARLY_ = 0, int LMAP_ = 0, int A_T_ = 0, int ALOAD_ = 4>
 struct Cfg {
@@ -110,25 +117,37 @@ struct Cfg {
     static constexpr int ALOAD = ALOAD_;
     static_assert(ALOAD == 1 || ALOAD == 2 || ALOAD == 4, "ALOAD is 1, 2 or 4");
     static_assert(A_T == 0 || A_MODE == LOAD_TMA, "a transposed A is loaded by TMA only");
+    static constexpr bool A_XP = A_MODE == LOAD_TMA_XP;
+    static_assert(!A_XP || B_MODE == LOAD_TMA, "the in-smem transpose runs with a TMA-loaded B");
+    // The consumers read A as [BK][BM] (a transposed A, or the transposers'
+    // output), with the chunk swizzle in the second case.
+    static constexpr bool A_KROWS = A_T || A_XP;
     static_assert(BK == 32, "A rows are one 128-byte swizzle span");
     static_assert(BM % 32 == 0 && BN % 64 == 0, "warp tile is 32 x 64");
     static constexpr int WARPS_M = BM / 32, WARPS_N = BN / 64;
     static constexpr int CONSUMER_WARPS = WARPS_M * WARPS_N;
     static constexpr int CONSUMERS = CONSUMER_WARPS * 32;
     static constexpr bool ANY_CP = (A_MODE == LOAD_CPASYNC) || (B_MODE == LOAD_CPASYNC);
-    static constexpr bool ANY_TMA = (A_MODE == LOAD_TMA) || (B_MODE == LOAD_TMA);
+    static constexpr bool ANY_TMA = (A_MODE != LOAD_CPASYNC) || (B_MODE == LOAD_TMA);
     // cp.async producers: one warp per SM sub-partition so the copy
-    // instructions do not all land on one scheduler.
-    static constexpr int PRODUCER_WARPS = ANY_CP ? 4 : 1;
+    // instructions do not all land on one scheduler. With the in-smem
+    // transpose: one TMA warp and three transposer warps (12 warps in all
+    // for 128 x 128, still three per scheduler, so 168 registers a thread).
+    static constexpr int PRODUCER_WARPS = (ANY_CP || A_XP) ? 4 : 1;
+    static constexpr int TRANSPOSERS = A_XP ? 96 : 0;
     static constexpr int THREADS = CONSUMERS + 32 * PRODUCER_WARPS;
     static constexpr int A_BYTES = BM * BK * 4;
     static constexpr int B_BYTES = BK * BN * 4;
     static constexpr uint32_t TX_BYTES =
-        (A_MODE == LOAD_TMA ? A_BYTES : 0) + (B_MODE == LOAD_TMA ? B_BYTES : 0);
-    static constexpr uint32_t FULL_COUNT = (ANY_TMA ? 1 : 0) + (ANY_CP ? 32 * PRODUCER_WARPS : 0);
-    static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * (A_BYTES + B_BYTES)
-                                      + 2 * STAGES * 8;
-    static_assert(SMEM_BYTES <= 227 * 1024, "ring does not fit in 227 KB of shared memory");
+        (A_MODE != LOAD_CPASYNC ? A_BYTES : 0) + (B_MODE == LOAD_TMA ? B_BYTES : 0);
+    // With the in-smem transpose the TMA bytes land on the "raw" barrier and
+    // "full" counts the transposer threads.
+    static constexpr uint32_t FULL_COUNT =
+        A_XP ? TRANSPOSERS : (ANY_TMA ? 1 : 0) + (ANY_CP ? 32 * PRODUCER_WARPS : 0);
+    static constexpr int RAW_BYTES = A_XP ? A_BYTES : 0;   // raw A staging, per stage
+    static constexpr int SMEM_BYTES = 1024 /* alignment slack */ +
+                                      STAGES * (A_BYTES + B_BYTES + RAW_BYTES) + 3 * STAGES * 8;
+    static constexpr bool FITS = SMEM_BYTES <= 227 * 1024;
     // Tiles of at most 128 x 64 are sized to run two CTAs per SM.
     static constexpr int MIN_BLOCKS = (BM * BN <= 128 * 64) ? 2 : 1;
 };
@@ -232,13 +251,17 @@ __device__ __forceinline__ uint32_t a_swz(int r, int k) {
 template <class C>
 __device__ __forceinline__ void producer(const CUtensorMap* tmA, const CUtensorMap* tmB,
                                          const GemmParams& p, uint32_t sA, uint32_t sB,
-                                         uint32_t full0, uint32_t empty0, int pw, int lane) {
+                                         uint32_t sRaw, uint32_t full0, uint32_t empty0,
+                                         uint32_t raw0, int pw, int lane) {
     const bool tma_thread = C::ANY_TMA && pw == 0 && lane == 0;
     if (!C::ANY_CP && !tma_thread) return;
     if (tma_thread) {
-        if (C::A_MODE == LOAD_TMA) tma_prefetch_desc(tmA);
+        if (C::A_MODE != LOAD_CPASYNC) tma_prefetch_desc(tmA);
         if (C::B_MODE == LOAD_TMA) tma_prefetch_desc(tmB);
     }
+    // The barrier the TMA bytes complete on: "full" for the consumers, or,
+    // with the in-smem transpose, "raw" for the transposer warps.
+    const uint32_t tx0 = C::A_XP ? raw0 : full0;
     int s = 0;
     uint32_t ph = 0;
     int issued = 0;
@@ -255,15 +278,18 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmA, const CUtensorM
                 break;
             }
             const uint32_t full = full0 + 8 * s;
+            const uint32_t tx = tx0 + 8 * s;
             const uint32_t dA = sA + s * C::A_BYTES, dB = sB + s * C::B_BYTES;
             const int k0 = kt * C::BK;
             if (tma_thread) {
-                mbar_arrive_expect_tx(full, C::TX_BYTES);
-                if (C::A_MODE == LOAD_TMA) {
-                    if (C::A_T) tma_load_2d(dA, tmA, full, m0, k0);
-                    else tma_load_2d(dA, tmA, full, k0, m0);
+                mbar_arrive_expect_tx(tx, C::TX_BYTES);
+                if (C::A_XP) {
+                    tma_load_2d(sRaw + s * C::A_BYTES, tmA, tx, k0, m0);
+                } else if (C::A_MODE == LOAD_TMA) {
+                    if (C::A_T) tma_load_2d(dA, tmA, tx, m0, k0);
+                    else tma_load_2d(dA, tmA, tx, k0, m0);
                 }
-                if (C::B_MODE == LOAD_TMA) tma_load_2d(dB, tmB, full, n0, k0);
+                if (C::B_MODE == LOAD_TMA) tma_load_2d(dB, tmB, tx, n0, k0);
             }
             if (C::A_MODE == LOAD_CPASYNC) {
                 // One row of BK = 32 floats per warp instruction, lane = k.
@@ -301,10 +327,55 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmA, const CUtensorM
         uint32_t pp = ph;
         for (int i = 0; i < n; ++i) {
             if (--ss < 0) { ss = C::STAGES - 1; pp ^= 1u; }
-            wait_bounded(full0 + 8 * ss, pp, p, STATUS_DRAIN_TIMEOUT);
+            wait_bounded(tx0 + 8 * ss, pp, p, STATUS_DRAIN_TIMEOUT);
         }
     }
     if (C::ANY_CP) asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// ---- transposer (A_MODE == LOAD_TMA_XP) -------------------------------------------
+
+// Three warps (t = 0..95) rewrite each landed raw A stage (BM rows of 32 k,
+// 128B-swizzled as TMA wrote it) as BK rows of BM m for the consumers. Work
+// unit: a 4 x 4 block (rows 4 mb.., k-chunk kb) read as four float4 (one per
+// row) and written as four float4 (one per k). The eight lanes of a
+// quarter-warp take kb = 0..7 of one mb: their reads hit eight different
+// chunks of one 128-byte row, and their writes, at chunk mb ^ kb of k-rows
+// 4 kb + c, eight different bank groups. Then each thread arrives on the
+// stage's "full" barrier, which counts the 96 of them.
+template <class C>
+__device__ __forceinline__ void transposer(const GemmParams& p, const uint8_t* raw, uint8_t* sA,
+                                           uint32_t raw0, uint32_t full0, int t) {
+    constexpr int BLOCKS = C::BM * 2;   // (BM / 4) row groups x 8 k-chunks
+    int s = 0;
+    uint32_t ph = 0;
+    Schedule sched(p);
+    Item it;
+    while (sched.next(p, it)) {
+        for (int kt = it.kb; kt < it.ke; ++kt) {
+            if (!wait_bounded(raw0 + 8 * s, ph, p, STATUS_PRODUCER_TIMEOUT)) return;
+            const uint8_t* src = raw + s * C::A_BYTES;
+            uint8_t* dst = sA + s * C::A_BYTES;
+#pragma unroll 1
+            for (int b = t; b < BLOCKS; b += C::TRANSPOSERS) {
+                const int kb = b & 7, mb = b >> 3;
+                float4 v[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int r = 4 * mb + j;
+                    v[j] = *reinterpret_cast<const float4*>(src + r * 128 + (((kb ^ r) & 7) << 4));
+                }
+                const int chunk = mb ^ kb;
+                uint8_t* d = dst + (4 * kb) * (C::BM * 4) + (chunk << 4);
+                *reinterpret_cast<float4*>(d) = make_float4(v[0].x, v[1].x, v[2].x, v[3].x);
+                *reinterpret_cast<float4*>(d + C::BM * 4) = make_float4(v[0].y, v[1].y, v[2].y, v[3].y);
+                *reinterpret_cast<float4*>(d + 2 * C::BM * 4) = make_float4(v[0].z, v[1].z, v[2].z, v[3].z);
+                *reinterpret_cast<float4*>(d + 3 * C::BM * 4) = make_float4(v[0].w, v[1].w, v[2].w, v[3].w);
+            }
+            mbar_arrive(full0 + 8 * s);
+            if (++s == C::STAGES) { s = 0; ph ^= 1u; }
+        }
+    }
 }
 
 // ---- consumer -----------------------------------------------------------------
@@ -312,7 +383,7 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmA, const CUtensorM
 // Offset of a lane's row i (0..7) from its row_base (see consumer()).
 template <class C>
 __device__ __forceinline__ constexpr int lane_row(int i) {
-    return C::A_T ? (i & 3) + 16 * (i >> 2) : 4 * i;
+    return C::A_KROWS ? (i & 3) + 16 * (i >> 2) : 4 * i;
 }
 
 // A fragment of k-group kq (4 consecutive k) for the lane's 8 rows
@@ -393,7 +464,7 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
     // row, so rows 4 apart spread over the chunks), or, for a transposed A,
     // row_base + (i & 3) + 16 (i >> 2) with row_base a multiple of 4 (two
     // float4 runs along m per k).
-    const int row_base = C::A_T ? wm * 32 + 4 * tr : wm * 32 + tr;
+    const int row_base = C::A_KROWS ? wm * 32 + 4 * tr : wm * 32 + tr;
     const int col_base = wn * 64 + 4 * tc;    // cols col_base + {0..3} and + 32 + {0..3}
     constexpr int KQ = C::BK / 4;
 
@@ -427,8 +498,12 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
         for (int kt = it.kb; kt < it.ke; ++kt) {
             if (!ready && !wait_bounded(full0 + 8 * s, ph, p, STATUS_CONSUMER_TIMEOUT)) return;
             ready = false;
-            const uint8_t* a_st = C::A_T ? sA_ptr + s * C::A_BYTES + row_base * 4
-                                         : sA_ptr + s * C::A_BYTES + row_base * 128;
+            // [BK][BM] stages: a transposed A is addressed directly; the
+            // transposers' output has chunk q of k-row k at q ^ ((k / 4) % 8),
+            // so the lane's two chunks are found per k-group below.
+            const uint8_t* a_st = C::A_XP ? sA_ptr + s * C::A_BYTES
+                                  : C::A_T ? sA_ptr + s * C::A_BYTES + row_base * 4
+                                           : sA_ptr + s * C::A_BYTES + row_base * 128;
             const uint8_t* b_st = sB_ptr + s * C::B_BYTES + col_base * 4;
             const int s_nx = (s + 1 == C::STAGES) ? 0 : s + 1;
             const uint32_t ph_nx = (s + 1 == C::STAGES) ? (ph ^ 1u) : ph;
@@ -437,7 +512,11 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
                 if (C::EARLY && kq == KQ / 2 && kt + 1 < it.ke)
                     ready = mbar_test_wait(full0 + 8 * s_nx, ph_nx);
                 float4 a[8];
-                if (!C::A_T && C::ALOAD == 4) load_a_group(a, a_st, kq, tr);
+                if (!C::A_KROWS && C::ALOAD == 4) load_a_group(a, a_st, kq, tr);
+                // Transposer layout: byte offsets of the lane's chunks (rows
+                // row_base.. and row_base + 16..) in k-rows 4 kq .. 4 kq + 3.
+                const int xq0 = ((((row_base >> 2) ^ kq) & 7) | ((row_base >> 2) & ~7)) << 4;
+                const int xq1 = (((((row_base >> 2) + 4) ^ kq) & 7) | (((row_base >> 2) + 4) & ~7)) << 4;
                 // Byte offsets of the lane's chunk kq in even and odd rows.
                 const int c0 = ((kq ^ tr) & 7) << 4, c1 = c0 ^ 64;
 #pragma unroll
@@ -446,10 +525,10 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
                     const float4 b0 = *reinterpret_cast<const float4*>(brow);
                     const float4 b1 = *reinterpret_cast<const float4*>(brow + 32 * 4);
                     float av[8];
-                    if (C::A_T) {
+                    if (C::A_KROWS) {
                         const uint8_t* arow = a_st + (kq * 4 + kk) * C::BM * 4;
-                        const float4 a0 = *reinterpret_cast<const float4*>(arow);
-                        const float4 a1 = *reinterpret_cast<const float4*>(arow + 16 * 4);
+                        const float4 a0 = *reinterpret_cast<const float4*>(arow + (C::A_XP ? xq0 : 0));
+                        const float4 a1 = *reinterpret_cast<const float4*>(arow + (C::A_XP ? xq1 : 16 * 4));
                         av[0] = a0.x; av[1] = a0.y; av[2] = a0.z; av[3] = a0.w;
                         av[4] = a1.x; av[5] = a1.y; av[6] = a1.z; av[7] = a1.w;
                     } else {
@@ -567,6 +646,7 @@ template <class C>
 __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
 sgemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmParams p) {
+    static_assert(C::FITS, "ring does not fit in 227 KB of shared memory");
     extern __shared__ __align__(16) uint8_t smem_raw[];
     // 1024-byte alignment: the 128B-swizzle pattern repeats every 8 rows.
     // (Pointer arithmetic on the __shared__ array keeps the shared address
@@ -574,14 +654,17 @@ sgemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* sA = smem;
     uint8_t* sB = smem + C::STAGES * C::A_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + C::STAGES * C::B_BYTES);
+    uint8_t* sRaw = sB + C::STAGES * C::B_BYTES;      // C::RAW_BYTES per stage
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sRaw + C::STAGES * C::RAW_BYTES);
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = smem_u32(bars + C::STAGES);
+    const uint32_t raw0 = smem_u32(bars + 2 * C::STAGES);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(full0 + 8 * s, C::FULL_COUNT);
             mbar_init(empty0 + 8 * s, C::CONSUMERS);
+            if (C::A_XP) mbar_init(raw0 + 8 * s, 1);
         }
         fence_barrier_init();
     }
@@ -589,8 +672,12 @@ sgemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (warp >= C::CONSUMER_WARPS) {
-        producer<C>(&tmA, &tmB, p, smem_u32(sA), smem_u32(sB), full0, empty0,
-                    warp - C::CONSUMER_WARPS, lane);
+        const int pw = warp - C::CONSUMER_WARPS;
+        if (C::A_XP && pw > 0)
+            transposer<C>(p, sRaw, sA, raw0, full0, (pw - 1) * 32 + lane);
+        else
+            producer<C>(&tmA, &tmB, p, smem_u32(sA), smem_u32(sB), smem_u32(sRaw), full0, empty0,
+                        raw0, pw, lane);
     } else {
         consumer<C>(p, sA, sB, full0, empty0, warp, lane);
     }

@@ -89,7 +89,8 @@ def test_tma_chosen_only_when_aligned():
     # worth an aligned copy, so they take cp.async.
     A, B, C0 = gen(128, 128, 256, seed=8)
     _, _, plan = gpu_util.run(1.0, A, B, 0.0, C0)
-    assert "Atma_Btma" in plan[0] and "pack" not in plan[0], plan
+    # Both by TMA; an aligned A is transposed in shared memory ("Axp").
+    assert "Axp_Btma" in plan[0] and "pack" not in plan[0], plan
     _, _, plan = gpu_util.run(1.0, A, B, 0.0, C0, lda=257)
     assert "Acp_Btma" in plan[0], plan
     _, _, plan = gpu_util.run(1.0, A, B, 0.0, C0, offsets=(0, 1, 0))
@@ -107,7 +108,7 @@ def test_unaligned_operands_packed_then_tma(layout, tags):
     A, B, C0 = gen(M, N, K, seed=9)
     C, guards, plan = gpu_util.run(0.7, A, B, -1.3, C0, **layout)
     assert guards
-    assert "Atma_Btma" in plan[0], plan
+    assert "Atma_Btma" in plan[0] or "Axp_Btma" in plan[0], plan
     for t in tags:
         assert t in plan[0], plan
     check_full(0.7, A, B, -1.3, C0, C)
@@ -250,7 +251,7 @@ def _workload(name, full):
 
 def test_workload_sq256_uniform():
     rep, plan = _workload("sq256_uniform", full=True)
-    assert plan[0] == "ws_64x64x32_s4_Atma_Btma", plan     # too small to split
+    assert plan[0] == "ws_64x64x32_s4_Axp_Btma", plan      # too small to split
 
 
 def test_workload_sq1024_int_bit_exact():
@@ -440,33 +441,64 @@ def test_sgemm_inside_a_captured_cuda_graph():
     check_full(0.7, A, B, -1.3, C0, work.cpu().numpy())
 
 
-@pytest.mark.parametrize("config", ["128x128", "128x128:dp", "128x64:dp", "64x64"])
-def test_pretransposed_a_gives_the_same_bits(config):
-    # ":at" copies the row-major A transposed and runs the transposed-A path;
-    # every output sees the same FMA sequence as with ":noat".
+@pytest.mark.parametrize("config", ["128x128", "128x128:dp", "128x64:dp", "64x64:dp"])
+@pytest.mark.parametrize("aligned", [True, False], ids=["aligned", "unaligned"])
+def test_a_paths_give_the_same_bits(config, aligned):
+    # How a row-major A reaches the consumers -- as stored (":noat"), through
+    # a transposed copy in HBM (":at") or transposed in shared memory by the
+    # kernel (":xp", aligned A only) -- changes no output bit: every output
+    # sees the same FMA sequence. (With the stream-K tail that holds only at
+    # equal grids: the split follows the CTAs per SM of the variant, which is
+    # one for every 128 x 128 variant; the 64 x 64 variants differ, so that
+    # family is compared under ":dp".)
     M, N, K = 700, 900, 1500
     A, B, C0 = gen(M, N, K, seed=61)
+    layout = {} if aligned else dict(lda=K + 1, offsets=(1, 0, 0))
     outs, plans = [], []
-    for mod in (":noat", ":at"):
+    for mod in (":noat", ":at", ":xp"):
         assert sg.sgemm_set_config(config + mod) == 0
         try:
-            C, guards, plan = gpu_util.run(0.7, A, B, -1.3, C0, lda=K + 1, offsets=(1, 0, 0))
+            C, guards, plan = gpu_util.run(0.7, A, B, -1.3, C0, **layout)
         finally:
             sg.sgemm_set_config("auto")
         assert guards
         outs.append(C)
         plans.append(plan[0])
-    assert "+packAT" not in plans[0] and "ATtma" not in plans[0], plans
+    assert "+packAT" not in plans[0] and "ATtma" not in plans[0] and "Axp" not in plans[0], plans
     assert "_ATtma_" in plans[1] and "+packAT" in plans[1], plans
-    assert np.array_equal(outs[0], outs[1]), plans
-    check_full(0.7, A, B, -1.3, C0, outs[1])
+    if aligned:
+        assert "_Axp_Btma" in plans[2], plans
+    for C in outs[1:]:
+        assert np.array_equal(outs[0], C), plans
+    check_full(0.7, A, B, -1.3, C0, outs[2])
 
 
-def test_auto_pretransposes_a_large_a():
+@pytest.mark.parametrize("shape", [(1024, 1024, 1024), (333, 4500, 776), (130, 72, 8400),
+                                   (4093, 5120, 1536)], ids=lambda s: "x".join(map(str, s)))
+def test_in_smem_transpose_with_stream_k(shape):
+    # Leading dimensions K and N multiples of 4: both operands go by TMA in
+    # place, the condition for the in-smem transpose.
+    M, N, K = shape
+    A, B, C0 = gen(M, N, K, seed=71)
+    assert sg.sgemm_set_config("128x128:xp") == 0
+    try:
+        C, guards, plan = gpu_util.run(0.7, A, B, -1.3, C0)
+    finally:
+        sg.sgemm_set_config("auto")
+    assert guards and "_Axp_Btma" in plan[0], plan
+    check_full(0.7, A, B, -1.3, C0, C)
+
+
+def test_auto_a_path_by_size():
+    # Large: the transposed copy of A pays. Medium and small: the in-smem
+    # transpose. An A TMA cannot read in place: the copy where it pays.
     torch = pytest.importorskip("torch")
-    A = torch.empty(2048, 2048, device="cuda")
-    B = torch.empty(2048, 2048, device="cuda")
-    C = torch.empty(2048, 2048, device="cuda")
-    assert "+packAT" in sg.plan_tensors(1.0, A, B, 0.0, C)[0]
-    small = torch.empty(256, 256, device="cuda")
-    assert "+packAT" not in sg.plan_tensors(1.0, small, small, 0.0, small.clone())[0]
+    def plan(M, N, K, lda=None):
+        A = torch.empty(M, lda or K, device="cuda")[:, :K]
+        B = torch.empty(K, N, device="cuda")
+        C = torch.empty(M, N, device="cuda")
+        return sg.plan_tensors(1.0, A, B, 0.0, C)[0]
+    assert "_ATtma_Btma+packAT" in plan(4096, 4096, 4096)
+    assert "_Axp_Btma" in plan(2048, 2048, 2048)
+    assert "_Axp_Btma" in plan(256, 256, 256)
+    assert "_ATtma_Btma+packAT" in plan(2048, 2048, 2047, lda=2047)
