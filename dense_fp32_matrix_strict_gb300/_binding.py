@@ -26,7 +26,7 @@ EXPORTED_SYMBOLS = (
     "sgemm_plan", "sgemm_set_config", "sgemm_set_wait_timeout_ns", "sgemm_fp32_peak",
     "sgemm_selftest_wait_timeout", "sgemm_config_names", "sgemm_noalloc", "sgemm_3xtf32",
     "sgemm_set_shape_config", "sgemm_clear_shape_configs", "sgemm_ex", "sgemm_plan_ex",
-    "sgemm_3xtf32_ex",
+    "sgemm_3xtf32_ex", "sgemm_host",
 )
 
 SGEMM_OP_N, SGEMM_OP_T = 0, 1
@@ -101,6 +101,8 @@ def load():
         lib.sgemm_plan_ex.argtypes = [ci, ci, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64,
                                       ctypes.c_char_p, ci, ctypes.POINTER(ci)]
         lib.sgemm_plan_ex.restype = ci
+        lib.sgemm_host.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
+        lib.sgemm_host.restype = ci
         _lib = lib
         return lib
 
@@ -145,6 +147,11 @@ def sgemm_plan_ex(opa, opb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc):
     rc = load().sgemm_plan_ex(opa, opb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, buf, 128,
                               ctypes.byref(grid))
     return rc, buf.value.decode(), grid.value
+
+
+def sgemm_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
+    """C = alpha*A*B + beta*C with HOST pointers (ints); returns the raw code."""
+    return load().sgemm_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
 
 
 def sgemm_check_status(stream=0):
@@ -316,6 +323,44 @@ def sgemm_3xtf32_tensors(alpha, A, B, beta, C, stream=None, transa=False, transb
                                      float(beta), C.data_ptr(), ldc, h)
     if rc != SGEMM_OK:
         raise SgemmError("sgemm_3xtf32", rc)
+
+
+def _host_ld(t, rows, cols, name):
+    import torch
+    if t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32, got {t.dtype}")
+    if t.is_cuda:
+        raise TypeError(f"{name} must be a host (CPU) tensor")
+    if t.dim() != 2 or tuple(t.shape) != (rows, cols):
+        raise ValueError(f"{name} must have shape {(rows, cols)}, got {tuple(t.shape)}")
+    if rows == 0 or cols == 0:
+        return max(cols, 1)
+    if cols > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} must be row-major with contiguous columns")
+    return max(t.stride(0) if rows > 1 else cols, cols, 1)
+
+
+def sgemm_host_tensors(alpha, A, B, beta, C, stream=None, device=None) -> None:
+    """sgemm_host on row-major float32 CPU tensors (pin them for overlap).
+
+    Enqueued on ``stream`` (default: torch's current stream on ``device``);
+    C is complete once that stream is synchronised.
+    """
+    import torch
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError(f"inner dimensions differ: A is {tuple(A.shape)}, B is {tuple(B.shape)}")
+    lda = _host_ld(A, M, K, "A")
+    ldb = _host_ld(B, K, N, "B")
+    ldc = _host_ld(C, M, N, "C")
+    dev = (torch.device("cuda", torch.cuda.current_device()) if device is None
+           else torch.device(device))
+    with _on_device(dev):
+        rc = load().sgemm_host(M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(), ldb,
+                               float(beta), C.data_ptr(), ldc, _stream_handle(stream, dev))
+    if rc != SGEMM_OK:
+        raise SgemmError("sgemm_host", rc)
 
 
 def plan_tensors(alpha, A, B, beta, C, transa=False, transb=False):

@@ -1,0 +1,206 @@
+// sgemm_host.cu — C = alpha * A * B + beta * C with A, B and C in HOST
+// memory. The host<->device copies run on two library-owned streams and
+// overlap the GEMMs of row blocks of C on the caller's stream:
+//
+//   h2d stream:  B, then A block 0 (and C block 0 when beta != 0), A block 1,
+//                ... each block into one of two device buffers;
+//   caller's stream: the GEMM of block i once its inputs have landed;
+//   d2h stream:  block i of C back to the host once its GEMM is done.
+//
+// A block's buffers are reused two blocks later, after its GEMM (A) and its
+// copy back (C) have finished. The call is ordered on the caller's stream
+// like the device entry points: the copies start after the work already
+// queued there, and the stream reaches the end of the call only when the
+// last block of C is in host memory.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "sgemm.h"
+#include "sgemm_internal.h"
+
+namespace sg {
+namespace {
+
+constexpr int kMaxHostDevices = 64;
+
+struct CopyStreams {
+    bool ready = false;
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+};
+
+std::mutex g_copy_mu;
+CopyStreams g_copy[kMaxHostDevices];
+
+// The two copy streams of the current device, created on first use.
+int copy_streams(int dev, CopyStreams** out) {
+    if (dev < 0 || dev >= kMaxHostDevices) return SGEMM_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lock(g_copy_mu);
+    CopyStreams& c = g_copy[dev];
+    if (!c.ready) {
+        cudaError_t e = cudaStreamCreateWithFlags(&c.h2d, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c.d2h, cudaStreamNonBlocking);
+        if (e != cudaSuccess) {
+            if (c.h2d != nullptr) cudaStreamDestroy(c.h2d);
+            c.h2d = c.d2h = nullptr;
+            return cuda_fail(e, SGEMM_ERR_CUDA);
+        }
+        c.ready = true;
+    }
+    *out = &c;
+    return SGEMM_OK;
+}
+
+size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
+
+int64_t round4(int64_t n) { return (n + 3) & ~int64_t{3}; }
+
+// Events of one call; destroyed when the call returns (the driver releases
+// an event still pending once it completes).
+struct CallEvents {
+    static constexpr int kCount = 7;
+    cudaEvent_t ev[kCount] = {};
+    int made = 0;
+    cudaError_t create() {
+        for (; made < kCount; ++made) {
+            const cudaError_t e = cudaEventCreateWithFlags(&ev[made], cudaEventDisableTiming);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
+    ~CallEvents() {
+        for (int i = 0; i < made; ++i) cudaEventDestroy(ev[i]);
+    }
+};
+
+}  // namespace
+}  // namespace sg
+
+using namespace sg;
+
+extern "C" int sgemm_host(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                          int64_t lda, const float* B, int64_t ldb, float beta, float* C,
+                          int64_t ldc, cudaStream_t stream) {
+    int rc = check_args(M, N, K, alpha, A, lda, B, ldb, C, ldc);
+    if (rc != SGEMM_OK) return rc;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    const DeviceInfo* dev = nullptr;
+    if ((rc = device_info(&dev)) != SGEMM_OK) return rc;
+    int* status = nullptr;
+    cudaMemPool_t pool = nullptr;
+    if ((rc = device_memory_handles(dev, &status, &pool)) != SGEMM_OK) return rc;
+    CopyStreams* cs = nullptr;
+    if ((rc = copy_streams(dev->device, &cs)) != SGEMM_OK) return rc;
+
+    const bool reads_ab = alpha != 0.0f && K > 0;
+    const bool reads_c = beta != 0.0f;
+    // Row blocks: one for problems whose GEMM is too short to hide a copy
+    // behind (below 5 GFLOP), else blocks of about 1024 rows (2 to 8), whole
+    // multiples of 128 rows so the GEMM tiles stay full.
+    int64_t nblk = 1;
+    if (2.0 * static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K) >= 5e9)
+        nblk = M / 1024 < 2 ? 2 : (M / 1024 > 8 ? 8 : M / 1024);
+    int64_t mb = (M + nblk - 1) / nblk;
+    mb = (mb + 127) / 128 * 128;
+    if (mb > M) mb = M;
+    nblk = (M + mb - 1) / mb;
+    const int nbuf = nblk > 1 ? 2 : 1;
+
+    // Device copies with leading dimensions rounded up to 4 floats, so that
+    // TMA can read them in place.
+    const int64_t ldk = round4(K > 0 ? K : 1), ldn = round4(N);
+    const size_t b_bytes = reads_ab ? align256(static_cast<size_t>(K) * ldn * 4) : 0;
+    const size_t a_bytes = reads_ab ? align256(static_cast<size_t>(mb) * ldk * 4) : 0;
+    const size_t c_bytes = align256(static_cast<size_t>(mb) * ldn * 4);
+    const size_t total = b_bytes + nbuf * (a_bytes + c_bytes);
+    void* w = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&w, total, pool, stream);
+    if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_CUDA);
+    unsigned char* base = static_cast<unsigned char*>(w);
+    float* dB = reinterpret_cast<float*>(base);
+    float* dA[2] = {reinterpret_cast<float*>(base + b_bytes),
+                    reinterpret_cast<float*>(base + b_bytes + a_bytes)};
+    float* dC[2] = {reinterpret_cast<float*>(base + b_bytes + nbuf * a_bytes),
+                    reinterpret_cast<float*>(base + b_bytes + nbuf * a_bytes + c_bytes)};
+
+    CallEvents evs;
+    if ((e = evs.create()) != cudaSuccess) {
+        cudaFreeAsync(w, stream);
+        return cuda_fail(e, SGEMM_ERR_CUDA);
+    }
+    cudaEvent_t ev_start = evs.ev[0];
+    cudaEvent_t ev_in[2] = {evs.ev[1], evs.ev[2]};      // block inputs landed
+    cudaEvent_t ev_done[2] = {evs.ev[3], evs.ev[4]};    // block GEMM finished
+    cudaEvent_t ev_out[2] = {evs.ev[5], evs.ev[6]};     // block of C back on the host
+
+    // On an error part of the pipeline may already be queued on the copy
+    // streams: join them into the caller's stream before the workspace goes
+    // back to the pool, or, if even that fails, leave it allocated.
+    auto release = [&]() {
+        if (cudaEventRecord(ev_in[0], cs->h2d) == cudaSuccess &&
+            cudaEventRecord(ev_out[0], cs->d2h) == cudaSuccess &&
+            cudaStreamWaitEvent(stream, ev_in[0], 0) == cudaSuccess &&
+            cudaStreamWaitEvent(stream, ev_out[0], 0) == cudaSuccess)
+            cudaFreeAsync(w, stream);
+    };
+    auto fail = [&](cudaError_t err, int code) {
+        release();
+        return cuda_fail(err, code);
+    };
+
+    if ((e = cudaEventRecord(ev_start, stream)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(cs->h2d, ev_start, 0)) != cudaSuccess)
+        return fail(e, SGEMM_ERR_CUDA);
+    if (reads_ab &&
+        (e = cudaMemcpy2DAsync(dB, ldn * 4, B, ldb * 4, N * 4, K, cudaMemcpyHostToDevice,
+                               cs->h2d)) != cudaSuccess)
+        return fail(e, SGEMM_ERR_CUDA);
+
+    int last = 0;
+    for (int64_t i = 0; i < nblk; ++i) {
+        const int j = static_cast<int>(i & 1);
+        const int64_t r0 = i * mb;
+        const int64_t rows = (M - r0) < mb ? (M - r0) : mb;
+        if (i >= 2) {
+            // Buffers j: block i - 2's GEMM has read A_j and written C_j, and
+            // C_j has been copied back.
+            if ((e = cudaStreamWaitEvent(cs->h2d, ev_done[j], 0)) != cudaSuccess ||
+                (e = cudaStreamWaitEvent(cs->h2d, ev_out[j], 0)) != cudaSuccess)
+                return fail(e, SGEMM_ERR_CUDA);
+        }
+        if (reads_ab &&
+            (e = cudaMemcpy2DAsync(dA[j], ldk * 4, A + r0 * lda, lda * 4, K * 4, rows,
+                                   cudaMemcpyHostToDevice, cs->h2d)) != cudaSuccess)
+            return fail(e, SGEMM_ERR_CUDA);
+        if (reads_c &&
+            (e = cudaMemcpy2DAsync(dC[j], ldn * 4, C + r0 * ldc, ldc * 4, N * 4, rows,
+                                   cudaMemcpyHostToDevice, cs->h2d)) != cudaSuccess)
+            return fail(e, SGEMM_ERR_CUDA);
+        if ((e = cudaEventRecord(ev_in[j], cs->h2d)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(stream, ev_in[j], 0)) != cudaSuccess)
+            return fail(e, SGEMM_ERR_CUDA);
+        if (i >= 2 && (e = cudaStreamWaitEvent(stream, ev_out[j], 0)) != cudaSuccess)
+            return fail(e, SGEMM_ERR_CUDA);
+        rc = sgemm(rows, N, K, alpha, reads_ab ? dA[j] : nullptr, ldk, reads_ab ? dB : nullptr,
+                   ldn, beta, dC[j], ldn, stream);
+        if (rc != SGEMM_OK) {
+            release();
+            return rc;
+        }
+        if ((e = cudaEventRecord(ev_done[j], stream)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(cs->d2h, ev_done[j], 0)) != cudaSuccess ||
+            (e = cudaMemcpy2DAsync(C + r0 * ldc, ldc * 4, dC[j], ldn * 4, N * 4, rows,
+                                   cudaMemcpyDeviceToHost, cs->d2h)) != cudaSuccess ||
+            (e = cudaEventRecord(ev_out[j], cs->d2h)) != cudaSuccess)
+            return fail(e, SGEMM_ERR_CUDA);
+        last = j;
+    }
+    // The caller's stream passes the end of the call once the last block of
+    // C (and, the d2h stream being in order, every earlier one) is back.
+    if ((e = cudaStreamWaitEvent(stream, ev_out[last], 0)) != cudaSuccess)
+        return fail(e, SGEMM_ERR_CUDA);
+    if ((e = cudaFreeAsync(w, stream)) != cudaSuccess) return cuda_fail(e, SGEMM_ERR_CUDA);
+    return SGEMM_OK;
+}

@@ -99,6 +99,30 @@ SGEMM_API int sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float* A
           const float* B, int64_t ldb, float beta, float* C, int64_t ldc,
           cudaStream_t stream);
 
+/*
+ * sgemm_host — the same operation, arguments and errors as sgemm, with A, B
+ * and C in HOST memory (page-locked memory, from cudaHostAlloc or
+ * cudaHostRegister, lets the copies overlap the computation; pageable memory
+ * works but each copy then blocks). The library copies B and row blocks of A
+ * (and of C when beta != 0) to the current device on a copy stream of its
+ * own, runs the GEMM of each block on `stream`, and copies each finished
+ * block of C back on a second copy stream, so the transfers of one block
+ * overlap the GEMMs of others. Problems below 5 GFLOP run as one block;
+ * larger ones in 2 to 8 blocks of about 1024 rows. The device buffers come
+ * from the library's stream-ordered pool (B, plus two A and two C blocks:
+ * 4 (K N + 2 mb (K + N)) bytes, mb the block height; SGEMM_ERR_CUDA if the
+ * pool cannot supply them). The call is asynchronous and ordered on
+ * `stream`: the copies start after the work already queued there, and
+ * `stream` passes the end of the call only when all of C is in host memory,
+ * so a host read of C must follow a synchronisation of `stream`. Host
+ * buffers must stay valid until then. Elements between rows (ld > width)
+ * are never read or written. Not part of the pages' design: it is this
+ * library's host-resident entry point.
+ */
+SGEMM_API int sgemm_host(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                         int64_t lda, const float* B, int64_t ldb, float beta, float* C,
+                         int64_t ldc, cudaStream_t stream);
+
 /* Operand transposition flags for the _ex entry points. */
 #define SGEMM_OP_N 0   /* the operand as stored (row-major)        */
 #define SGEMM_OP_T 1   /* the transpose of the stored matrix        */
