@@ -582,11 +582,14 @@ int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, 
     int a_mode = LOAD_CPASYNC, b_mode = LOAD_CPASYNC;
     pl->pack_a = pl->pack_b = false;
     pl->pack_a_bytes = pl->pack_b_bytes = 0;
-    const float* kPlaceholderA = reinterpret_cast<const float*>(uintptr_t{1} << 20);
+    // Copies are described to the driver against a placeholder address first
+    // (to make sure it accepts the shape) and encoded again on the real
+    // workspace buffer at launch.
+    const float* kPlaceholder = reinterpret_cast<const float*>(uintptr_t{1} << 20);
     if (pl->a_pre) {
         const int64_t ld = (M + 3) & ~int64_t{3};
-        if (tma_ok(kPlaceholderA, ld, K, M) &&
-            encode_2d(&pl->tmA, kPlaceholderA, K, M, ld, bk, bm, false)) {
+        if (tma_ok(kPlaceholder, ld, K, M) &&
+            encode_2d(&pl->tmA, kPlaceholder, K, M, ld, bk, bm, false)) {
             a_mode = LOAD_TMA;
             pl->pack_a = true;
             pl->lda_pack = ld;
@@ -613,10 +616,7 @@ int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, 
     // buffer when the GEMM reads it often enough (A is read once per
     // 128-column tile of C, B once per 128-row tile): from 256 columns (rows)
     // the 4-byte cp.async loads it saves cost more than the extra pass. A
-    // transposed A has no cp.async path, so it is always copied then. The
-    // descriptor is encoded here against a placeholder address to make sure
-    // the driver accepts the shape, and again on the real buffer at launch.
-    const float* kPlaceholder = reinterpret_cast<const float*>(uintptr_t{1} << 20);
+    // transposed A has no cp.async path, so it is always copied then.
     if (!pl->a_t && !pl->a_pre && a_mode != LOAD_TMA && allow_pack && !force_cp && N >= 256) {
         const int64_t ld = (K + 3) & ~int64_t{3};
         if (tma_ok(kPlaceholder, ld, M, K) && encode_2d(&pl->tmA, kPlaceholder, M, K, ld, bm, bk, true)) {

@@ -6,7 +6,7 @@
 //
 // Structure (persistent CTAs, one per SM for the 128 x 128 tile):
 //   * producer warp(s) fill an S-deep ring of shared-memory stages, each a
-//     BM x BK tile of A and a BK x BN tile of B. An operand whose base and
+//     tile of A (BM x BK, or BK x BM) and a BK x BN tile of B. An operand whose base and
 //     row stride are 16-byte aligned is moved by TMA (cp.async.bulk.tensor,
 //     one elected thread, zero fill past the matrix edges); otherwise by
 //     4-byte cp.async with zero fill (src-size 0). Either way the stage's
@@ -33,10 +33,13 @@
 // the Tinyforge README on BK = 16 + padding and XOR swizzling; the T4
 // article's "Tiling" section on zero-filled tails) use __syncthreads double
 // buffering on sm_75..sm_89. Here the ring is deeper, the barriers are
-// mbarriers, the loads are TMA where the strides allow it, and A stays
-// row-major in shared memory with the 128-byte TMA swizzle instead of a
-// transposing store: each lane reads float4 runs along k for its 8 rows,
-// which costs the same number of shared loads per FMA as a transposed copy.
+// mbarriers and the loads are TMA where the strides allow it. A reaches the
+// consumers in one of two shared-memory layouts: row-major under the
+// 128-byte TMA swizzle (each lane reads float4 runs along k for its 8 rows),
+// or k-major, [BK][BM], the layout of the pages' transposing store (each
+// lane reads two float4 of 4 rows per k-step; the FMA pipe stays busier).
+// The k-major layout comes from an A given transposed, from a transposed
+// copy of A, or from transposer warps that rewrite each TMA-landed stage.
 //
 // Every mbarrier wait is bounded (globaltimer): on timeout the thread sets a
 // bit in the device status word, lets its own copies in flight land (again
