@@ -33,10 +33,10 @@ cudaError_t ws_launch(const CUtensorMap* tmA, const CUtensorMap* tmB, const Gemm
     return cudaGetLastError();
 }
 
-// The stream-K fixup for a BM x BN tile: one CTA per stream-K tile.
+// The stream-K fixup for a BM x BN tile: `split` CTAs per stream-K tile.
 template <int BM, int BN>
-cudaError_t fixup_launch(const GemmParams* p, int sk_tiles, cudaStream_t stream) {
-    sk_fixup_kernel<BM, BN><<<sk_tiles, 256, 0, stream>>>(*p);
+cudaError_t fixup_launch(const GemmParams* p, int sk_tiles, int split, cudaStream_t stream) {
+    sk_fixup_kernel<BM, BN><<<sk_tiles * split, 256, 0, stream>>>(*p, split);
     return cudaGetLastError();
 }
 
@@ -49,7 +49,7 @@ struct KernelFamily {
     const char* name;
     int bm, bn;
     KernelEntry modes[kModes];
-    cudaError_t (*fixup)(const GemmParams* p, int sk_tiles, cudaStream_t stream);
+    cudaError_t (*fixup)(const GemmParams* p, int sk_tiles, int split, cudaStream_t stream);
 };
 
 // Index into a family's modes: TMA/TMA, CP/TMA, TMA/CP, CP/CP for a

@@ -778,7 +778,12 @@ int launch_plan(Plan* pl, int* status, float* ws, cudaStream_t stream) {
                ? reinterpret_cast<float*>(w + pl->pack_a_bytes + pl->pack_b_bytes)
                : nullptr;
     e = pl->k->launch(&pl->tmA, &pl->tmB, &pl->p, pl->grid, stream);
-    if (e == cudaSuccess && pl->sk_tiles > 0) e = pl->fam->fixup(&pl->p, pl->sk_tiles, stream);
+    if (e == cudaSuccess && pl->sk_tiles > 0) {
+        // Enough fixup CTAs for about two per SM, at most 8 per tile.
+        const int want = (2 * pl->sms + pl->sk_tiles - 1) / pl->sk_tiles;
+        const int split = want < 1 ? 1 : (want > 8 ? 8 : want);
+        e = pl->fam->fixup(&pl->p, pl->sk_tiles, split, stream);
+    }
     if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
     return SGEMM_OK;
 }

@@ -692,18 +692,21 @@ sgemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 // more (a range is at least ceil(k_tiles / kMaxParts) iterations long).
 constexpr int kSkMaxParts = 64;
 
-// One CTA per stream-K tile u (tile dp_tiles + u). If a single CTA's range
-// covered the whole tile, that CTA already wrote C and this block returns.
-// Otherwise the contributing ranges are those of CTAs c_first, c_first+1, ...
-// (in increasing k order); their partial sums are added in that order and the
+// `split` CTAs per stream-K tile u (tile dp_tiles + u), each taking one
+// contiguous share of the tile's float4s, so the fixup fills the GPU even
+// when few tiles are split. If a single CTA's range covered the whole tile,
+// that CTA already wrote C and these blocks return. Otherwise the
+// contributing ranges are those of CTAs c_first, c_first+1, ... (in
+// increasing k order); their partial sums are added in that order and the
 // epilogue C = alpha * sum + beta * C is applied.
 template <int BM, int BN>
 __global__ void __launch_bounds__(256)
-sk_fixup_kernel(const GemmParams p) {
+sk_fixup_kernel(const GemmParams p, int split) {
     const long long KT = p.k_tiles;
     const long long G = p.sk_ctas;
     const long long S = p.sk_iters;
-    const long long u = blockIdx.x;
+    const long long u = blockIdx.x / split;
+    const int part = static_cast<int>(blockIdx.x % split);
     const long long x0 = u * KT, x1 = x0 + KT;
     __shared__ int parts[kSkMaxParts];
     __shared__ int nparts;
@@ -737,7 +740,9 @@ sk_fixup_kernel(const GemmParams p) {
     tile_coords(p.dp_tiles + static_cast<int>(u), p, tm, tn);
     const bool use_c = p.beta != 0.0f;
     constexpr int Q = BM * BN / 4;   // float4 per tile
-    for (int q = threadIdx.x; q < Q; q += blockDim.x) {
+    const int per = (Q + split - 1) / split;
+    const int q1 = (part + 1) * per < Q ? (part + 1) * per : Q;
+    for (int q = part * per + threadIdx.x; q < q1; q += blockDim.x) {
         const int r = q / (BN / 4);
         const int c4 = (q - r * (BN / 4)) * 4;
         const int m = tm * BM + r;
