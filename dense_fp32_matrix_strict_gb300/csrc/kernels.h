@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include "sgemm_kernel.cuh"
+#include "sk_fixup.cuh"
 
 namespace sg {
 
