@@ -2,9 +2,11 @@
 // memory. The host<->device copies run on two library-owned streams and
 // overlap the GEMMs of row blocks of C on the caller's stream:
 //
-//   h2d stream:  B, then A block 0 (and C block 0 when beta != 0), A block 1,
-//                ... each block into one of two device buffers;
-//   caller's stream: the GEMM of block i once its inputs have landed;
+//   h2d stream:  A block 0 (and C block 0 when beta != 0), B in column
+//                chunks, then A block 1, ... each block into one of two
+//                device buffers;
+//   caller's stream: block 0's GEMM one column chunk at a time as B's chunks
+//                land, then the GEMM of block i once its inputs have landed;
 //   d2h stream:  block i of C back to the host once its GEMM is done.
 //
 // A block's buffers are reused two blocks later, after its GEMM (A) and its
@@ -60,7 +62,7 @@ int64_t round4(int64_t n) { return (n + 3) & ~int64_t{3}; }
 // Events of one call; destroyed when the call returns (the driver releases
 // an event still pending once it completes).
 struct CallEvents {
-    static constexpr int kCount = 7;
+    static constexpr int kCount = 11;
     cudaEvent_t ev[kCount] = {};
     int made = 0;
     cudaError_t create() {
@@ -134,6 +136,14 @@ extern "C" int sgemm_host(int64_t M, int64_t N, int64_t K, float alpha, const fl
     cudaEvent_t ev_in[2] = {evs.ev[1], evs.ev[2]};      // block inputs landed
     cudaEvent_t ev_done[2] = {evs.ev[3], evs.ev[4]};    // block GEMM finished
     cudaEvent_t ev_out[2] = {evs.ev[5], evs.ev[6]};     // block of C back on the host
+    cudaEvent_t ev_bc[4] = {evs.ev[7], evs.ev[8], evs.ev[9], evs.ev[10]};   // B chunks landed
+    // Block 0 starts on the first quarter of B instead of all of it: with
+    // several row blocks and N >= 2048, B comes in 4 column chunks (whole
+    // multiples of 128 columns) and block 0's GEMM runs chunk by chunk.
+    int nbc = (nblk > 1 && N >= 2048 && reads_ab) ? 4 : 1;
+    int64_t nc = ((N + nbc - 1) / nbc + 127) / 128 * 128;
+    if (nc > N) nc = N;
+    nbc = static_cast<int>((N + nc - 1) / nc);
 
     // On an error part of the pipeline may already be queued on the copy
     // streams: join them into the caller's stream before the workspace goes
@@ -152,10 +162,6 @@ extern "C" int sgemm_host(int64_t M, int64_t N, int64_t K, float alpha, const fl
 
     if ((e = cudaEventRecord(ev_start, stream)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(cs->h2d, ev_start, 0)) != cudaSuccess)
-        return fail(e, SGEMM_ERR_CUDA);
-    if (reads_ab &&
-        (e = cudaMemcpy2DAsync(dB, ldn * 4, B, ldb * 4, N * 4, K, cudaMemcpyHostToDevice,
-                               cs->h2d)) != cudaSuccess)
         return fail(e, SGEMM_ERR_CUDA);
 
     int last = 0;
@@ -183,11 +189,31 @@ extern "C" int sgemm_host(int64_t M, int64_t N, int64_t K, float alpha, const fl
             return fail(e, SGEMM_ERR_CUDA);
         if (i >= 2 && (e = cudaStreamWaitEvent(stream, ev_out[j], 0)) != cudaSuccess)
             return fail(e, SGEMM_ERR_CUDA);
-        rc = sgemm(rows, N, K, alpha, reads_ab ? dA[j] : nullptr, ldk, reads_ab ? dB : nullptr,
-                   ldn, beta, dC[j], ldn, stream);
-        if (rc != SGEMM_OK) {
-            release();
-            return rc;
+        if (i == 0 && reads_ab) {
+            // B in column chunks behind block 0's inputs; block 0's GEMM
+            // follows them chunk by chunk.
+            for (int c = 0; c < nbc; ++c) {
+                const int64_t c0 = c * nc;
+                const int64_t cols = (N - c0) < nc ? (N - c0) : nc;
+                if ((e = cudaMemcpy2DAsync(dB + c0, ldn * 4, B + c0, ldb * 4, cols * 4, K,
+                                           cudaMemcpyHostToDevice, cs->h2d)) != cudaSuccess ||
+                    (e = cudaEventRecord(ev_bc[c], cs->h2d)) != cudaSuccess ||
+                    (e = cudaStreamWaitEvent(stream, ev_bc[c], 0)) != cudaSuccess)
+                    return fail(e, SGEMM_ERR_CUDA);
+                rc = sgemm(rows, cols, K, alpha, dA[j], ldk, dB + c0, ldn, beta, dC[j] + c0, ldn,
+                           stream);
+                if (rc != SGEMM_OK) {
+                    release();
+                    return rc;
+                }
+            }
+        } else {
+            rc = sgemm(rows, N, K, alpha, reads_ab ? dA[j] : nullptr, ldk,
+                       reads_ab ? dB : nullptr, ldn, beta, dC[j], ldn, stream);
+            if (rc != SGEMM_OK) {
+                release();
+                return rc;
+            }
         }
         if ((e = cudaEventRecord(ev_done[j], stream)) != cudaSuccess ||
             (e = cudaStreamWaitEvent(cs->d2h, ev_done[j], 0)) != cudaSuccess ||

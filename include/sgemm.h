@@ -103,11 +103,12 @@ SGEMM_API int sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float* A
  * sgemm_host — the same operation, arguments and errors as sgemm, with A, B
  * and C in HOST memory (page-locked memory, from cudaHostAlloc or
  * cudaHostRegister, lets the copies overlap the computation; pageable memory
- * works but each copy then blocks). The library copies B and row blocks of A
- * (and of C when beta != 0) to the current device on a copy stream of its
- * own, runs the GEMM of each block on `stream`, and copies each finished
- * block of C back on a second copy stream, so the transfers of one block
- * overlap the GEMMs of others. Problems below 5 GFLOP run as one block;
+ * works but each copy then blocks). The library copies row blocks of A (and
+ * of C when beta != 0) and B (in column chunks behind the first block of A)
+ * to the current device on a copy stream of its own, runs the GEMM of each
+ * block on `stream` (the first block chunk by chunk as B arrives), and
+ * copies each finished block of C back on a second copy stream, so the
+ * transfers of one block overlap the GEMMs of others. Problems below 5 GFLOP run as one block;
  * larger ones in 2 to 8 blocks of about 1024 rows. The device buffers come
  * from the library's stream-ordered pool (B, plus two A and two C blocks:
  * 4 (K N + 2 mb (K + N)) bytes, mb the block height; SGEMM_ERR_CUDA if the

@@ -69,7 +69,8 @@ def gen(M, N, K, seed, dist="normal"):
 
 
 @pytest.mark.parametrize("shape", [(1, 1, 1), (7, 5, 3), (300, 260, 200),     # one block
-                                   (2048, 1536, 1024), (3000, 1100, 1531)],  # pipelined
+                                   (2048, 1536, 1024), (3000, 1100, 1531),   # pipelined
+                                   (2100, 2100, 700)],                       # B in 4 chunks
                          ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("beta", [0.0, -1.3])
 def test_matches_oracle(shape, beta):
