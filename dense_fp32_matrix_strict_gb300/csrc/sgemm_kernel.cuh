@@ -109,7 +109,7 @@ struct GemmParams {
 //   16-byte chunks of k-row k XOR-swizzled by (k / 4) mod 8 so that both the
 //   transposing stores and the consumers' reads are free of bank conflicts.
 template <int BM_, int BN_, int BK_, int STAGES_, int A_MODE_, int B_MODE_, int FORDER_ = 2,
-          int EARLY_ = 0, int LMAP_ = 0, int A_T_ = 0, int ALOAD_ = 4>
+          int EARLY_ = 0, int LMAP_ = 0, int A_T_ = 0, int ALOAD_ = 4, int TN_ = 8>
 struct Cfg {
     static constexpr int BM = BM_, BN = BN_, BK = BK_, STAGES = STAGES_;
     static constexpr int A_MODE = A_MODE_, B_MODE = B_MODE_;
@@ -125,9 +125,13 @@ struct Cfg {
     // The consumers read A as [BK][BM] (a transposed A, or the transposers'
     // output), with the chunk swizzle in the second case.
     static constexpr bool A_KROWS = A_T || A_XP;
+    // TN: columns a lane owns (8, or 16 for a 32 x 128 warp tile: twice the
+    // multiply-adds per shared load, for warps with up to 255 registers).
+    static constexpr int TN = TN_;
+    static_assert(TN == 8 || TN == 16, "TN is 8 or 16");
     static_assert(BK == 32, "A rows are one 128-byte swizzle span");
-    static_assert(BM % 32 == 0 && BN % 64 == 0, "warp tile is 32 x 64");
-    static constexpr int WARPS_M = BM / 32, WARPS_N = BN / 64;
+    static_assert(BM % 32 == 0 && BN % (8 * TN) == 0, "warp tile is 32 x 8 TN");
+    static constexpr int WARPS_M = BM / 32, WARPS_N = BN / (8 * TN);
     static constexpr int CONSUMER_WARPS = WARPS_M * WARPS_N;
     static constexpr int CONSUMERS = CONSUMER_WARPS * 32;
     static constexpr bool ANY_CP = (A_MODE == LOAD_CPASYNC) || (B_MODE == LOAD_CPASYNC);
@@ -404,23 +408,28 @@ __device__ __forceinline__ float lane_of(const float4& v, int kk) {
     return kk == 0 ? v.x : kk == 1 ? v.y : kk == 2 ? v.z : v.w;
 }
 
-// One k-step of the 8 x 8 register outer product.
+// One k-step of the 8 x TN register outer product (b: the lane's TN B
+// values of this k as TN / 4 float4).
 //   FORDER 0: scalar FFMA.
 //   FORDER 2: packed FFMA2 (fma.rn.f32x2: two IEEE single-precision FMAs,
 //             each rounded once, in one instruction): pairs of adjacent
 //             columns share one instruction with the row's A value in both
-//             lanes. Every output still sees the same FMA sequence, so the
-//             result is bit-identical to the scalar form.
-template <int FORDER>
-__device__ __forceinline__ void outer_product(float (&acc)[8][8], const float (&av8)[8],
-                                              const float4& b0, const float4& b1) {
-    if (FORDER == 3) {
-        // FFMA2 with the column pairs outer: consecutive instructions share
-        // the B pair and change the A value.
-        const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
-                              make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
+//             lanes, rows outer. Every output still sees the same FMA
+//             sequence, so the result is bit-identical to the scalar form.
+//   FORDER 3: the same with the column pairs outer: consecutive
+//             instructions share the B pair and change the A value.
+template <int FORDER, int TN>
+__device__ __forceinline__ void outer_product(float (&acc)[8][TN], const float (&av8)[8],
+                                              const float4 (&b)[TN / 4]) {
+    float2 bp[TN / 2];
 #pragma unroll
-        for (int jp = 0; jp < 4; ++jp) {
+    for (int h = 0; h < TN / 4; ++h) {
+        bp[2 * h] = make_float2(b[h].x, b[h].y);
+        bp[2 * h + 1] = make_float2(b[h].z, b[h].w);
+    }
+    if (FORDER == 3) {
+#pragma unroll
+        for (int jp = 0; jp < TN / 2; ++jp) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const float av = av8[i];
@@ -431,14 +440,12 @@ __device__ __forceinline__ void outer_product(float (&acc)[8][8], const float (&
             }
         }
     } else if (FORDER == 2) {
-        const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
-                              make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const float av = av8[i];
             const float2 aa = make_float2(av, av);
 #pragma unroll
-            for (int jp = 0; jp < 4; ++jp) {
+            for (int jp = 0; jp < TN / 2; ++jp) {
                 float2 c = make_float2(acc[i][2 * jp], acc[i][2 * jp + 1]);
                 c = __ffma2_rn(aa, bp[jp], c);
                 acc[i][2 * jp] = c.x;
@@ -446,12 +453,14 @@ __device__ __forceinline__ void outer_product(float (&acc)[8][8], const float (&
             }
         }
     } else {
-        const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const float av = av8[i];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av, bv[j], acc[i][j]);
+            for (int jp = 0; jp < TN / 2; ++jp) {
+                acc[i][2 * jp] = fmaf(av, bp[jp].x, acc[i][2 * jp]);
+                acc[i][2 * jp + 1] = fmaf(av, bp[jp].y, acc[i][2 * jp + 1]);
+            }
         }
     }
 }
@@ -468,7 +477,8 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
     // row_base + (i & 3) + 16 (i >> 2) with row_base a multiple of 4 (two
     // float4 runs along m per k).
     const int row_base = C::A_KROWS ? wm * 32 + 4 * tr : wm * 32 + tr;
-    const int col_base = wn * 64 + 4 * tc;    // cols col_base + {0..3} and + 32 + {0..3}
+    // Lane columns: col_base + 32 h + {0..3}, h = 0 .. TN / 4 - 1.
+    const int col_base = wn * (8 * C::TN) + 4 * tc;
     constexpr int KQ = C::BK / 4;
 
     int s = 0;
@@ -476,24 +486,25 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
     Schedule sched(p);
     Item it;
     while (sched.next(p, it)) {
-        float acc[8][8];
+        float acc[8][C::TN];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+            for (int j = 0; j < C::TN; ++j) acc[i][j] = 0.0f;
 
         if (it.slot < 0 && p.beta != 0.0f) {
             // The epilogue reads this tile of C: start moving it into L2 now.
-            // Lane l takes row l of the warp tile, both 128-byte lines of its
-            // 64 columns (the second only if it starts inside the matrix).
+            // Lane l takes row l of the warp tile, the 128-byte lines of its
+            // 8 TN columns (those that start inside the matrix).
             int tm, tn;
             tile_coords(it.tile, p, tm, tn);
             const int r = tm * C::BM + wm * 32 + lane;
-            const int c = tn * C::BN + wn * 64;
-            if (r < p.M && c < p.N) {
+            const int c = tn * C::BN + wn * (8 * C::TN);
+            if (r < p.M) {
                 const float* crow = p.C + (long long)r * p.ldc + c;
-                prefetch_l2(crow);
-                if (c + 32 < p.N) prefetch_l2(crow + 32);
+#pragma unroll
+                for (int h = 0; h < C::TN / 4; ++h)
+                    if (c + 32 * h < p.N) prefetch_l2(crow + 32 * h);
             }
         }
 
@@ -525,8 +536,10 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint8_t* brow = b_st + (kq * 4 + kk) * C::BN * 4;
-                    const float4 b0 = *reinterpret_cast<const float4*>(brow);
-                    const float4 b1 = *reinterpret_cast<const float4*>(brow + 32 * 4);
+                    float4 bq[C::TN / 4];
+#pragma unroll
+                    for (int h = 0; h < C::TN / 4; ++h)
+                        bq[h] = *reinterpret_cast<const float4*>(brow + 32 * 4 * h);
                     float av[8];
                     if (C::A_KROWS) {
                         const uint8_t* arow = a_st + (kq * 4 + kk) * C::BM * 4;
@@ -557,7 +570,7 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
                                     a_st + i * 4 * 128 + ((i & 1) ? c1 : c0) + kk * 4);
                         }
                     }
-                    outer_product<C::FORDER>(acc, av, b0, b1);
+                    outer_product<C::FORDER, C::TN>(acc, av, bq);
                 }
             }
             mbar_arrive(empty0 + 8 * s);
@@ -573,7 +586,7 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
             for (int i = 0; i < 8; ++i) {
                 float* row = slot + (row_base + lane_row<C>(i)) * C::BN + col_base;
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
+                for (int h = 0; h < C::TN / 4; ++h)
                     __stcg(reinterpret_cast<float4*>(row + 32 * h),
                            make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2],
                                        acc[i][4 * h + 3]));
@@ -594,13 +607,13 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
         // extra registers within the budget of the main loop.
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-            float4 cold[4][2];
+            float4 cold[4][C::TN / 4];
             if (use_c) {
 #pragma unroll
                 for (int ii = 0; ii < 4; ++ii) {
                     const int m = m0 + lane_row<C>(4 * q + ii);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
+                    for (int h = 0; h < C::TN / 4; ++h) {
                         const int n = n0 + 32 * h;
                         cold[ii][h] = (m < p.M && p.c_vec && n + 3 < p.N)
                                           ? *reinterpret_cast<const float4*>(p.C + (long long)m * p.ldc + n)
@@ -615,7 +628,7 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
                 if (m >= p.M) continue;
                 float* crow = p.C + (long long)m * p.ldc;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
+                for (int h = 0; h < C::TN / 4; ++h) {
                     const int n = n0 + 32 * h;
                     float v[4];
 #pragma unroll
