@@ -66,6 +66,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-tf32x3", action="store_true",
                     help="skip the separately reported tcgen05 3xTF32 measurement")
+    ap.add_argument("--no-cublas", action="store_true",
+                    help="skip the cuBLAS FP32 context measurement")
     ap.add_argument("--cpu-rows", type=int, default=0,
                     help="rows of C in the CPU baseline sample (0: sized to ~10 s)")
     return ap.parse_args()
@@ -441,6 +443,43 @@ def run_ours(args, w):
                                "traffic": t3, "traffic_note": t3_note},
                   "gpu_launches_per_step": 3}
 
+    # Context only, not part of the product: cuBLAS FP32 (torch.addmm with
+    # TF32 off) on the same operands, timed the same way on the same stream.
+    cublas = None
+    if not args.no_cublas:
+        prev_tf32 = torch.backends.cuda.matmul.allow_tf32
+        torch.backends.cuda.matmul.allow_tf32 = False
+        try:
+            out = torch.empty_like(dC)
+            for _ in range(3):
+                torch.addmm(dC, dA, dB, beta=w.beta, alpha=w.alpha, out=out)
+            torch.cuda.synchronize()
+            nc = max(10, args.steps // 5)
+            # As in the timed region: with an L2 flush, events around each
+            # call only; otherwise one pair around all of them.
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(nc if flush is not None else 1)]
+            if flush is None:
+                evs[0][0].record(stream)
+            for i in range(nc):
+                if flush is not None:
+                    flush.zero_()
+                    evs[i][0].record(stream)
+                torch.addmm(dC, dA, dB, beta=w.beta, alpha=w.alpha, out=out)
+                if flush is not None:
+                    evs[i][1].record(stream)
+            if flush is None:
+                evs[0][1].record(stream)
+            torch.cuda.synchronize()
+            msc = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs) / nc, world)
+            cublas = {"value": replica_throughput(flops, msc, world), "unit": "GFLOP/s",
+                      "ms_per_step": msc, "steps": nc,
+                      "note": "context only: torch.addmm FP32 with TF32 off (cuBLAS), same "
+                              "operands and stream, L2 handled as in the timed region"}
+            del out
+        finally:
+            torch.backends.cuda.matmul.allow_tf32 = prev_tf32
+
     # End to end through the C ABI with HOST buffers: sgemm_host copies A, B
     # (and C when beta != 0) in and C out, inside the timed region, every
     # step; it overlaps those copies with the GEMMs of row blocks. Each step
@@ -520,6 +559,8 @@ def run_ours(args, w):
     }
     if tf32x3 is not None:
         line["tcgen05_3xtf32"] = tf32x3
+    if cublas is not None:
+        line["cublas_fp32_context"] = cublas
     if world > 1:
         torch.distributed.destroy_process_group()
     if not args.no_cpu_baseline:
