@@ -61,9 +61,9 @@ inline constexpr int mode_index(int a_mode, int b_mode, int a_t = 0) {
 }
 
 template <int BM, int BN, int S, int AM, int BMD, int FORDER, int EARLY, int LMAP, int AT = 0,
-          int ALOAD = 4, int TN = 8>
+          int ALOAD = 4, int TN = 8, int KSPLIT = 1>
 constexpr KernelEntry make_entry(const char* name) {
-    using C = Cfg<BM, BN, 32, S, AM, BMD, FORDER, EARLY, LMAP, AT, ALOAD, TN>;
+    using C = Cfg<BM, BN, 32, S, AM, BMD, FORDER, EARLY, LMAP, AT, ALOAD, TN, KSPLIT>;
     // A variant whose ring does not fit in shared memory is left out (no
     // entry points); the planner never picks it.
     if constexpr (!C::FITS)
@@ -114,6 +114,29 @@ constexpr KernelEntry make_entry(const char* name) {
                 make_entry<BM, BN, S, LOAD_TMA, LOAD_CPASYNC, FORDER, EARLY, LMAP, 1, 4, TN>( \
                     NAME "_ATtma_Bcp"),                                                     \
                 make_entry<BM, BN, S, LOAD_TMA_XP, LOAD_TMA, FORDER, EARLY, LMAP, 0, 4, TN>(  \
+                    NAME "_Axp_Btma"),                                                      \
+            },                                                                              \
+            &fixup_launch<BM, BN>                                                           \
+    }
+
+// A family whose consumer warps come in KSPLIT k-groups (see Cfg).
+#define SG_FAMILY_K(NAME, BM, BN, S, KS)                                                    \
+    KernelFamily {                                                                          \
+        NAME, BM, BN,                                                                       \
+            {                                                                               \
+                make_entry<BM, BN, S, LOAD_TMA, LOAD_TMA, 3, 1, 0, 0, 4, 8, KS>(              \
+                    NAME "_Atma_Btma"),                                                     \
+                make_entry<BM, BN, S, LOAD_CPASYNC, LOAD_TMA, 3, 1, 0, 0, 4, 8, KS>(          \
+                    NAME "_Acp_Btma"),                                                      \
+                make_entry<BM, BN, S, LOAD_TMA, LOAD_CPASYNC, 3, 1, 0, 0, 4, 8, KS>(          \
+                    NAME "_Atma_Bcp"),                                                      \
+                make_entry<BM, BN, S, LOAD_CPASYNC, LOAD_CPASYNC, 3, 1, 0, 0, 4, 8, KS>(      \
+                    NAME "_Acp_Bcp"),                                                       \
+                make_entry<BM, BN, S, LOAD_TMA, LOAD_TMA, 3, 1, 0, 1, 4, 8, KS>(              \
+                    NAME "_ATtma_Btma"),                                                    \
+                make_entry<BM, BN, S, LOAD_TMA, LOAD_CPASYNC, 3, 1, 0, 1, 4, 8, KS>(          \
+                    NAME "_ATtma_Bcp"),                                                     \
+                make_entry<BM, BN, S, LOAD_TMA_XP, LOAD_TMA, 3, 1, 0, 0, 4, 8, KS>(           \
                     NAME "_Axp_Btma"),                                                      \
             },                                                                              \
             &fixup_launch<BM, BN>                                                           \

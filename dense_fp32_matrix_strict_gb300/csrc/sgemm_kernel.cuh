@@ -109,7 +109,8 @@ struct GemmParams {
 //   16-byte chunks of k-row k XOR-swizzled by (k / 4) mod 8 so that both the
 //   transposing stores and the consumers' reads are free of bank conflicts.
 template <int BM_, int BN_, int BK_, int STAGES_, int A_MODE_, int B_MODE_, int FORDER_ = 2,
-          int EARLY_ = 0, int LMAP_ = 0, int A_T_ = 0, int ALOAD_ = 4, int TN_ = 8>
+          int EARLY_ = 0, int LMAP_ = 0, int A_T_ = 0, int ALOAD_ = 4, int TN_ = 8,
+          int KSPLIT_ = 1>
 struct Cfg {
     static constexpr int BM = BM_, BN = BN_, BK = BK_, STAGES = STAGES_;
     static constexpr int A_MODE = A_MODE_, B_MODE = B_MODE_;
@@ -132,7 +133,14 @@ struct Cfg {
     static_assert(BK == 32, "A rows are one 128-byte swizzle span");
     static_assert(BM % 32 == 0 && BN % (8 * TN) == 0, "warp tile is 32 x 8 TN");
     static constexpr int WARPS_M = BM / 32, WARPS_N = BN / (8 * TN);
-    static constexpr int CONSUMER_WARPS = WARPS_M * WARPS_N;
+    // KSPLIT: groups of consumer warps that each cover the whole tile for
+    // their own share of every stage's k (k-groups g KQ/KSPLIT .. ), their
+    // sums added in group order in shared memory at the end of each work
+    // item: more warps per SM for tiles too few to fill the GPU.
+    static constexpr int KSPLIT = KSPLIT_;
+    static_assert(KSPLIT == 1 || KSPLIT == 2 || KSPLIT == 4, "KSPLIT is 1, 2 or 4");
+    static constexpr int GROUP_WARPS = WARPS_M * WARPS_N;
+    static constexpr int CONSUMER_WARPS = GROUP_WARPS * KSPLIT;
     static constexpr int CONSUMERS = CONSUMER_WARPS * 32;
     static constexpr bool ANY_CP = (A_MODE == LOAD_CPASYNC) || (B_MODE == LOAD_CPASYNC);
     static constexpr bool ANY_TMA = (A_MODE != LOAD_CPASYNC) || (B_MODE == LOAD_TMA);
@@ -152,11 +160,13 @@ struct Cfg {
     static constexpr uint32_t FULL_COUNT =
         A_XP ? TRANSPOSERS : (ANY_TMA ? 1 : 0) + (ANY_CP ? 32 * PRODUCER_WARPS : 0);
     static constexpr int RAW_BYTES = A_XP ? A_BYTES : 0;   // raw A staging, per stage
+    static constexpr int RED_BYTES = (KSPLIT - 1) * BM * BN * 4;   // k-group sums
     static constexpr int SMEM_BYTES = 1024 /* alignment slack */ +
-                                      STAGES * (A_BYTES + B_BYTES + RAW_BYTES) + 3 * STAGES * 8;
+                                      STAGES * (A_BYTES + B_BYTES + RAW_BYTES) + RED_BYTES +
+                                      (3 * STAGES + 2) * 8;
     static constexpr bool FITS = SMEM_BYTES <= 227 * 1024;
     // Tiles of at most 128 x 64 are sized to run two CTAs per SM.
-    static constexpr int MIN_BLOCKS = (BM * BN <= 128 * 64) ? 2 : 1;
+    static constexpr int MIN_BLOCKS = (BM * BN * KSPLIT <= 128 * 64) ? 2 : 1;
 };
 
 // Tile index -> (tile row, tile column), grouped so that the CTAs running at
@@ -468,8 +478,13 @@ __device__ __forceinline__ void outer_product(float (&acc)[8][TN], const float (
 template <class C>
 __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_ptr,
                                          const uint8_t* sB_ptr, uint32_t full0, uint32_t empty0,
+                                         float4* red, uint32_t red_full, uint32_t red_empty,
                                          int warp, int lane) {
-    const int wm = warp % C::WARPS_M, wn = warp / C::WARPS_M;
+    // k-group of this warp (KSPLIT > 1) and its place in the group's tile.
+    const int grp = C::KSPLIT > 1 ? warp / C::GROUP_WARPS : 0;
+    const int wq = C::KSPLIT > 1 ? warp % C::GROUP_WARPS : warp;
+    const int wm = wq % C::WARPS_M, wn = wq / C::WARPS_M;
+    uint32_t red_ph = 0;
     const int tr = C::LMAP == 1 ? (lane & 3) : (lane >> 3);
     const int tc = C::LMAP == 1 ? (lane >> 2) : (lane & 7);
     // Lane rows: row_base + 4 i (row-major A: one swizzled 128-byte row per
@@ -492,7 +507,7 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
 #pragma unroll
             for (int j = 0; j < C::TN; ++j) acc[i][j] = 0.0f;
 
-        if (it.slot < 0 && p.beta != 0.0f) {
+        if (it.slot < 0 && p.beta != 0.0f && grp == 0) {
             // The epilogue reads this tile of C: start moving it into L2 now.
             // Lane l takes row l of the warp tile, the 128-byte lines of its
             // 8 TN columns (those that start inside the matrix).
@@ -521,9 +536,11 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
             const uint8_t* b_st = sB_ptr + s * C::B_BYTES + col_base * 4;
             const int s_nx = (s + 1 == C::STAGES) ? 0 : s + 1;
             const uint32_t ph_nx = (s + 1 == C::STAGES) ? (ph ^ 1u) : ph;
+            constexpr int KQG = KQ / C::KSPLIT;   // k-groups of 4 k per k-group of warps
 #pragma unroll
-            for (int kq = 0; kq < KQ; ++kq) {
-                if (C::EARLY && kq == KQ / 2 && kt + 1 < it.ke)
+            for (int kql = 0; kql < KQG; ++kql) {
+                const int kq = grp * KQG + kql;
+                if (C::EARLY && kql == KQG / 2 && kt + 1 < it.ke)
                     ready = mbar_test_wait(full0 + 8 * s_nx, ph_nx);
                 float4 a[8];
                 if (!C::A_KROWS && C::ALOAD == 4) load_a_group(a, a_st, kq, tr);
@@ -576,6 +593,45 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
             mbar_arrive(empty0 + 8 * s);
             s = s_nx;
             ph = ph_nx;
+        }
+
+        if (C::KSPLIT > 1) {
+            // Add the k-groups' sums in group order: groups 1.. leave theirs
+            // in shared memory (float4 j of lane l of warp wq at
+            // ((g - 1) GROUP_WARPS + wq) 2 TN + j, lane-interleaved), group 0
+            // adds them to its own and goes on to the epilogue.
+            constexpr int NF4 = 8 * C::TN / 4;   // float4 of accumulators a lane
+            if (grp > 0) {
+                if (!wait_bounded(red_empty, red_ph ^ 1u, p, STATUS_CONSUMER_TIMEOUT)) return;
+                float4* dst = red + (((grp - 1) * C::GROUP_WARPS + wq) * NF4) * 32 + lane;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int h = 0; h < C::TN / 4; ++h)
+                        dst[(i * (C::TN / 4) + h) * 32] =
+                            make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2],
+                                        acc[i][4 * h + 3]);
+                mbar_arrive(red_full);
+                red_ph ^= 1u;
+                continue;
+            }
+            if (!wait_bounded(red_full, red_ph, p, STATUS_CONSUMER_TIMEOUT)) return;
+#pragma unroll 1
+            for (int g = 1; g < C::KSPLIT; ++g) {
+                const float4* srcg = red + (((g - 1) * C::GROUP_WARPS + wq) * NF4) * 32 + lane;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int h = 0; h < C::TN / 4; ++h) {
+                        const float4 v = srcg[(i * (C::TN / 4) + h) * 32];
+                        acc[i][4 * h] += v.x;
+                        acc[i][4 * h + 1] += v.y;
+                        acc[i][4 * h + 2] += v.z;
+                        acc[i][4 * h + 3] += v.w;
+                    }
+            }
+            mbar_arrive(red_empty);
+            red_ph ^= 1u;
         }
 
         if (it.slot >= 0) {
@@ -671,16 +727,23 @@ sgemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     uint8_t* sA = smem;
     uint8_t* sB = smem + C::STAGES * C::A_BYTES;
     uint8_t* sRaw = sB + C::STAGES * C::B_BYTES;      // C::RAW_BYTES per stage
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sRaw + C::STAGES * C::RAW_BYTES);
+    float4* red = reinterpret_cast<float4*>(sRaw + C::STAGES * C::RAW_BYTES);  // RED_BYTES
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sRaw + C::STAGES * C::RAW_BYTES + C::RED_BYTES);
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = smem_u32(bars + C::STAGES);
     const uint32_t raw0 = smem_u32(bars + 2 * C::STAGES);
+    const uint32_t red_full = smem_u32(bars + 3 * C::STAGES);
+    const uint32_t red_empty = red_full + 8;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(full0 + 8 * s, C::FULL_COUNT);
             mbar_init(empty0 + 8 * s, C::CONSUMERS);
             if (C::A_XP) mbar_init(raw0 + 8 * s, 1);
+        }
+        if (C::KSPLIT > 1) {
+            mbar_init(red_full, (C::KSPLIT - 1) * C::GROUP_WARPS * 32);
+            mbar_init(red_empty, C::GROUP_WARPS * 32);
         }
         fence_barrier_init();
     }
@@ -695,7 +758,7 @@ sgemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             producer<C>(&tmA, &tmB, p, smem_u32(sA), smem_u32(sB), smem_u32(sRaw), full0, empty0,
                         raw0, pw, lane);
     } else {
-        consumer<C>(p, sA, sB, full0, empty0, warp, lane);
+        consumer<C>(p, sA, sB, full0, empty0, red, red_full, red_empty, warp, lane);
     }
 }
 
