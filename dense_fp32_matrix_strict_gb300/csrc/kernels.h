@@ -146,11 +146,13 @@ constexpr KernelEntry make_entry(const char* name) {
     SG_FAMILY_A(NAME, BM, BN, S, FORDER, EARLY, LMAP, 4)
 
 // Families, one translation unit each (compiled in parallel). The first
-// three are the ones "auto" chooses between; the rest are tuning
+// five are the ones "auto" chooses between; the rest are tuning
 // alternatives that sgemm_set_config can force.
 const KernelFamily* family_128x128();
 const KernelFamily* family_64x64();
 const KernelFamily* family_128x64();
+const KernelFamily* family_128x64_k2();
+const KernelFamily* family_64x64_k4();
 const KernelFamily* const* sweep_families(int* count);
 
 }  // namespace sg

@@ -23,8 +23,9 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kStatusBytes = 256;
 
-// All compiled kernel families: [0] 128x128, [1] 64x64 and [2] 128x64 are
-// what "auto" chooses between; the rest are tuning alternatives.
+// All compiled kernel families: [0] 128x128, [1] 64x64, [2] 128x64,
+// [3] 128x64 in two k-groups and [4] 64x64 in four k-groups are what "auto"
+// chooses between; the rest are tuning alternatives.
 struct Registry {
     const KernelFamily* fam[kMaxFamilies];
     int count = 0;
@@ -32,6 +33,8 @@ struct Registry {
         fam[count++] = family_128x128();
         fam[count++] = family_64x64();
         fam[count++] = family_128x64();
+        fam[count++] = family_128x64_k2();
+        fam[count++] = family_64x64_k4();
         int n = 0;
         const KernelFamily* const* sw = sweep_families(&n);
         for (int i = 0; i < n && count < kMaxFamilies; ++i) fam[count++] = sw[i];
@@ -487,53 +490,81 @@ int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, 
     bool sk_decided = false;
     if (fi < 0) {
         sk_decided = true;
-        const int64_t kt = (K + 31) / 32;
-        const int64_t tiles128 = ((M + 127) / 128) * ((N + 127) / 128);
-        const int64_t iters128 = tiles128 * kt;
+        auto cdiv = [](int64_t a, int64_t b) { return (a + b - 1) / b; };
+        const int64_t kt = cdiv(K, 32);
+        const double dkt = static_cast<double>(kt);
         const int64_t nsm = sms;
         const bool sk_possible = allow_sk && force_sk != 0;
-        if (iters128 < 2 * nsm) {
-            // Below two 128 x 128 x 32 k-iterations per SM: the 64 x 64 tile,
-            // with the stream-K tail only if its own k-iterations still give
-            // every SM two.
+        const int64_t tiles128 = cdiv(M, 128) * cdiv(N, 128);
+        const int64_t tiles128x64 = cdiv(M, 128) * cdiv(N, 64);
+        const int64_t tiles64 = cdiv(M, 64) * cdiv(N, 64);
+        // A transposed A always goes by TMA (in place or packed); a
+        // transposed B is always copied to the row-major layout first.
+        const bool a_tma = opa ? true : (tma_ok(A, lda, M, K) || (allow_pack && N >= 256));
+        const bool b_tma = opb ? true : (tma_ok(B, ldb, K, N) || (allow_pack && M >= 256));
+        const bool tma_both = force_cp_flag == 0 && a_tma && b_tma;
+        const int mi_tt = mode_index(LOAD_TMA, LOAD_TMA, opa);
+        if (!tma_both && tiles128 * kt < 2 * nsm) {
+            // Operands only cp.async can read, below two 128 x 128 x 32
+            // k-iterations per SM: the 64 x 64 tile, with the stream-K tail
+            // only if its own k-iterations still give every SM two.
             fi = 1;
-            const int64_t iters64 = ((M + 63) / 64) * ((N + 63) / 64) * kt;
-            if (!(sk_possible && iters64 >= 2 * nsm)) allow_sk = false;
+            if (!(sk_possible && tiles64 * kt >= 2 * nsm)) allow_sk = false;
         } else {
-            // Cost in units of one 128 x 128 x 32 k-iteration on one SM,
-            // fitted to sweeps on GB300 (152 SMs): the stream-K tail adds
-            // about 8 units (partial sums to L2, the fixup launch); a lone
-            // 128 x 64 CTA on an SM takes 0.63 units per k-iteration, two
-            // co-resident ones 1.06 units for both.
-            const int64_t cap128 = static_cast<int64_t>(dev->ctas_per_sm[0][0]) * nsm;
-            const int64_t waves = cap128 > 0 ? tiles128 / cap128 : 0;
-            const int64_t rest = cap128 > 0 ? tiles128 % cap128 : 0;
+            // Each candidate's cost in units of one 128 x 128 x 32
+            // k-iteration of a CTA alone on its SM (~2.3 us on GB300), fitted
+            // to sweeps on GB300 (152 SMs); the launch itself (~7 us) is
+            // common to all and left out. Per k-iteration of one tile: a
+            // 128 x 64 CTA alone on its SM 0.63 units, two co-resident ones
+            // 1.06 for both; 128 x 64 in two k-groups 0.54; 64 x 64 in four
+            // k-groups 0.31. The stream-K tail adds its partial sums and the
+            // fixup launch: ~5 units for 128 x 128 tiles (taken as 6, so
+            // that a tie goes to whole tiles), ~4 for 64 x 64.
             const double inf = 1e300;
-            const double c_dp = cap128 > 0
-                                    ? static_cast<double>((tiles128 + cap128 - 1) / cap128) * kt + 1
-                                    : inf;
-            const double c_sk = (sk_possible && rest != 0)
-                                    ? static_cast<double>(waves * kt + (rest * kt + nsm - 1) / nsm) + 8
-                                    : inf;
-            double c_64 = inf;
-            // A transposed A always goes by TMA (in place or packed); a
-            // transposed B is always copied to the row-major layout first.
-            const bool a_tma = opa ? true : (tma_ok(A, lda, M, K) || (allow_pack && N >= 256));
-            const bool b_tma = opb ? true : (tma_ok(B, ldb, K, N) || (allow_pack && M >= 256));
-            if (force_cp_flag == 0 && a_tma && b_tma &&
-                dev->ctas_per_sm[2][mode_index(LOAD_TMA, LOAD_TMA, opa)] >= 2) {
-                const int64_t tiles64 = ((M + 127) / 128) * ((N + 63) / 64);
-                c_64 = tiles64 <= nsm ? 0.63 * static_cast<double>(kt)
-                                      : static_cast<double>((tiles64 + 2 * nsm - 1) / (2 * nsm)) *
-                                            1.06 * static_cast<double>(kt);
+            int best_f = 0;
+            bool best_sk = false;
+            double best_c = inf;
+            auto offer = [&](int f, bool sk, double c) {
+                if (c < best_c) {
+                    best_f = f;
+                    best_sk = sk;
+                    best_c = c;
+                }
+            };
+            // Whole waves of tiles plus, with the stream-K tail, the last
+            // partial wave's k-iterations spread over the CTAs (the schedule
+            // further down: ranges at least kt/32 iterations long).
+            auto sk_iters = [&](int64_t tiles, int64_t cap) {
+                const int64_t S = (tiles % cap) * kt;
+                int64_t G = S / cdiv(kt, 32);
+                if (G > cap) G = cap;
+                if (G < 1) G = 1;
+                return static_cast<double>((tiles / cap) * kt + cdiv(S, G));
+            };
+            const int64_t cap128 = static_cast<int64_t>(dev->ctas_per_sm[0][0]) * nsm;
+            if (cap128 > 0) {
+                offer(0, false, static_cast<double>(cdiv(tiles128, cap128)) * dkt + 1);
+                if (sk_possible && tiles128 % cap128 != 0)
+                    offer(0, true, sk_iters(tiles128, cap128) + 6);
             }
-            if (c_64 < c_dp && c_64 < c_sk) {
-                fi = 2;
-                allow_sk = false;
-            } else {
-                fi = 0;
-                if (!(c_sk < c_dp)) allow_sk = false;
+            if (tma_both) {
+                if (dev->ctas_per_sm[2][mi_tt] >= 2)
+                    offer(2, false,
+                          tiles128x64 <= nsm
+                              ? 0.63 * dkt
+                              : static_cast<double>(cdiv(tiles128x64, 2 * nsm)) * 1.06 * dkt);
+                const int64_t cap_k2 = static_cast<int64_t>(dev->ctas_per_sm[3][mi_tt]) * nsm;
+                if (cap_k2 > 0)
+                    offer(3, false, static_cast<double>(cdiv(tiles128x64, cap_k2)) * 0.54 * dkt);
+                const int64_t cap_k4 = static_cast<int64_t>(dev->ctas_per_sm[4][mi_tt]) * nsm;
+                if (cap_k4 > 0) {
+                    offer(4, false, static_cast<double>(cdiv(tiles64, cap_k4)) * 0.31 * dkt);
+                    if (sk_possible && tiles64 % cap_k4 != 0)
+                        offer(4, true, sk_iters(tiles64, cap_k4) * 0.31 + 4);
+                }
             }
+            fi = best_f;
+            if (!best_sk) allow_sk = false;
         }
     }
     const KernelFamily* fam = registry().fam[fi];

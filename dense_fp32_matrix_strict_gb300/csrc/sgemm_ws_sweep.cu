@@ -12,16 +12,13 @@ const KernelFamily* sweep_family_g();
 const KernelFamily* sweep_family_h();
 const KernelFamily* sweep_family_i();
 const KernelFamily* sweep_family_j();
-const KernelFamily* sweep_family_k();
 const KernelFamily* sweep_family_l();
-const KernelFamily* sweep_family_m();
 
 const KernelFamily* const* sweep_families(int* count) {
     static const KernelFamily* const list[] = {sweep_family_a(), sweep_family_b(), sweep_family_c(),
                                                sweep_family_d(), sweep_family_e(), sweep_family_g(),
                                                sweep_family_h(), sweep_family_i(),
-                                               sweep_family_j(), sweep_family_k(), sweep_family_l(),
-                                               sweep_family_m()};
+                                               sweep_family_j(), sweep_family_l()};
     *count = static_cast<int>(sizeof(list) / sizeof(list[0]));
     return list;
 }

@@ -253,7 +253,7 @@ def _workload(name, full):
 
 def test_workload_sq256_uniform():
     rep, plan = _workload("sq256_uniform", full=True)
-    assert plan[0] == "ws_64x64x32_s4_Axp_Btma", plan      # too small to split
+    assert plan[0] == "ws_64x64x32_s4_k4_Axp_Btma", plan   # too small to split
 
 
 def test_workload_sq1024_int_bit_exact():
@@ -388,15 +388,19 @@ def test_stream_k_is_deterministic_and_close_to_dp():
     dA = torch.from_numpy(A).cuda()
     dB = torch.from_numpy(B).cuda()
     outs = []
-    for cfg in ["auto", "auto", "auto:dp"]:
-        assert sg.sgemm_set_config(cfg) == 0
-        dC = torch.from_numpy(C0).cuda()
-        name, _ = sg.plan_tensors(0.7, dA, dB, -1.3, dC)
-        assert name.endswith("+sk") == (cfg == "auto"), name
-        sg.sgemm_tensors(0.7, dA, dB, -1.3, dC)
-        sg.check_status()
-        outs.append(dC.cpu().numpy())
-    sg.sgemm_set_config("auto")
+    # The 128 x 128 family forced: its 72 tiles leave SMs idle, so every tile
+    # is split ("auto" takes the 128 x 64 k-group tile here instead).
+    try:
+        for cfg in ["128x128", "128x128", "128x128:dp"]:
+            assert sg.sgemm_set_config(cfg) == 0
+            dC = torch.from_numpy(C0).cuda()
+            name, _ = sg.plan_tensors(0.7, dA, dB, -1.3, dC)
+            assert name.endswith("+sk") == (cfg == "128x128"), name
+            sg.sgemm_tensors(0.7, dA, dB, -1.3, dC)
+            sg.check_status()
+            outs.append(dC.cpu().numpy())
+    finally:
+        sg.sgemm_set_config("auto")
     assert np.array_equal(outs[0], outs[1])          # same schedule, same bits
     for C in (outs[0], outs[2]):
         check_full(0.7, A, B, -1.3, C0, C)
@@ -450,23 +454,27 @@ def test_sgemm_inside_a_captured_cuda_graph():
     dA = torch.from_numpy(A).cuda()
     dB = torch.from_numpy(B).cuda()
     dC = torch.from_numpy(C0).cuda()
-    name, _ = sg.plan_tensors(0.7, dA, dB, -1.3, dC)
-    assert name.endswith("+sk"), name
-    s = torch.cuda.Stream()
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        sg.sgemm_tensors(0.7, dA, dB, -1.3, dC.clone(), stream=s)   # warm-up outside capture
-    torch.cuda.current_stream().wait_stream(s)
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    work = dC.clone()
-    with torch.cuda.graph(g):
-        sg.sgemm_tensors(0.7, dA, dB, -1.3, work)
-    for _ in range(2):
-        work.copy_(dC)
-        g.replay()
-    torch.cuda.synchronize()
-    sg.check_status()
+    assert sg.sgemm_set_config("128x128") == 0      # 72 tiles: every one split
+    try:
+        name, _ = sg.plan_tensors(0.7, dA, dB, -1.3, dC)
+        assert name.endswith("+sk"), name
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            sg.sgemm_tensors(0.7, dA, dB, -1.3, dC.clone(), stream=s)   # warm-up outside capture
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        work = dC.clone()
+        with torch.cuda.graph(g):
+            sg.sgemm_tensors(0.7, dA, dB, -1.3, work)
+        for _ in range(2):
+            work.copy_(dC)
+            g.replay()
+        torch.cuda.synchronize()
+        sg.check_status()
+    finally:
+        sg.sgemm_set_config("auto")
     check_full(0.7, A, B, -1.3, C0, work.cpu().numpy())
 
 

@@ -24,12 +24,19 @@ from dense_fp32_matrix_strict_gb300 import inputs
 pytestmark = pytest.mark.gpu
 
 
-def test_noalloc_matches_sgemm_on_two_calls_in_a_row():
+@pytest.fixture
+def forced_128x128():
+    # The 128 x 128 family forced: 72 tiles < 152 SMs, every tile is split.
+    assert sg.sgemm_set_config("128x128") == 0
+    yield
+    sg.sgemm_set_config("auto")
+
+
+def test_noalloc_matches_sgemm_on_two_calls_in_a_row(forced_128x128):
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    assert sg.sgemm_set_config("auto") == 0
-    M, N, K = 1000, 1100, 2000             # 72 tiles < 152 SMs: every tile is split
+    M, N, K = 1000, 1100, 2000
     alpha, beta = 0.7, -1.3
     A = inputs.fill("normal", 501, inputs.TID_A, M, K)
     B = inputs.fill("normal", 501, inputs.TID_B, K, N)
