@@ -14,6 +14,24 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ---- programmatic dependent launch ----------------------------------------
+// A kernel launched with programmatic stream serialisation may begin while
+// the kernel before it on the stream is still running. griddep_wait blocks
+// the calling thread until that kernel has completed and its memory writes
+// are visible (for a kernel launched the ordinary way it returns at once);
+// every thread calls it before its first global-memory access.
+// griddep_launch_dependents lets the kernel after this one be scheduled once
+// every CTA of this grid has issued it (or exited); that kernel still waits
+// for this one to complete before it touches memory.
+
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- mbarrier --------------------------------------------------------------
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

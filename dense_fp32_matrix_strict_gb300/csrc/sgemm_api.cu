@@ -208,6 +208,8 @@ __global__ void scale_kernel(float* __restrict__ C, long long ldc, int M, int N,
 // operand.
 __global__ void pack_rows_kernel(const float* __restrict__ src, long long lds,
                                  float* __restrict__ dst, long long ldd, int rows, int cols) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int quads = (cols + 3) >> 2;
     const long long total = static_cast<long long>(rows) * quads;
     for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -237,6 +239,8 @@ __global__ void __launch_bounds__(256) transpose_pack_kernel(const float* __rest
                                                              long long lds, float* __restrict__ dst,
                                                              long long ldd, int R, int C) {
     __shared__ float tile[kTpTile][kTpTile + 1];
+    griddep_wait();
+    griddep_launch_dependents();
     const bool vec = (reinterpret_cast<uintptr_t>(src) % 16 == 0) && (lds % 4 == 0);
     const long long c0 = static_cast<long long>(blockIdx.x) * kTpTile;
     const long long tiles_r = (ldd + kTpTile - 1) / kTpTile;
@@ -283,12 +287,25 @@ __global__ void __launch_bounds__(256) transpose_pack_kernel(const float* __rest
 
 // Launches transpose_pack_kernel for an R x C source.
 cudaError_t launch_transpose_pack(const float* src, long long lds, float* dst, long long ldd,
-                                  int R, int C, cudaStream_t stream) {
+                                  int R, int C, cudaStream_t stream, bool pdl) {
     const long long tiles_r = (ldd + kTpTile - 1) / kTpTile;
     const dim3 grid(static_cast<unsigned>((C + kTpTile - 1) / kTpTile),
                     static_cast<unsigned>(tiles_r < 65535 ? tiles_r : 65535));
-    transpose_pack_kernel<<<grid, 256, 0, stream>>>(src, lds, dst, ldd, R, C);
-    return cudaGetLastError();
+    return launch_kernel(transpose_pack_kernel, grid, dim3(256), 0, stream, pdl, src, lds, dst,
+                         ldd, R, C);
+}
+
+// A kernel that follows a packing copy of the same call is launched by
+// programmatic stream serialisation (it is scheduled while the copy
+// finishes and waits for it on the device), unless the environment variable
+// SGEMM_PDL is "0" when the library first launches. On GB300 this saves
+// ~1.5 us of the 4096^3 call (transposing copy of A, then the GEMM).
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char* v = std::getenv("SGEMM_PDL");
+        return !(v != nullptr && std::strcmp(v, "0") == 0);
+    }();
+    return on;
 }
 
 size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
@@ -583,15 +600,15 @@ int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, 
     const bool xp_possible = !pl->a_t && !force_cp && tma_ok(A, lda, M, K) && b_will_tma &&
                              dev->ctas_per_sm[fi][mode_index(LOAD_TMA_XP, LOAD_TMA)] > 0;
     // Either way beats reading the row-major A as stored. Measured on GB300
-    // against that: the in-smem transpose saves ~4 % of the main loop (2MNK
-    // FLOP at ~66 TFLOP/s), the HBM copy ~8.5 % but costs ~5 us of launch and
-    // allocation plus one read and one write of A at ~3 TB/s. "auto" takes
-    // the copy where its extra saving pays for it, else the in-smem
-    // transpose where possible (not for the two-CTA 128 x 64 tile, where it
-    // gains nothing).
+    // against that: the HBM copy saves ~8.5 % of the main loop (2MNK FLOP at
+    // ~66 TFLOP/s), ~3.6 % more than the in-smem transpose, but costs ~5 us
+    // of launch and allocation plus one read and one write of A at ~6 TB/s.
+    // "auto" takes the copy where its extra saving pays for it, else the
+    // in-smem transpose where possible (not for the two-CTA 128 x 64 tile,
+    // where it gains nothing).
     const double mk = static_cast<double>(M) * static_cast<double>(K);
     const double t_main = 2.0 * mk * static_cast<double>(N) / 66e12;
-    const double copy_cost = 5e-6 + 8.0 * mk / 3e12;
+    const double copy_cost = 5e-6 + 8.0 * mk / 6e12;
     const bool copy_ok = !pl->a_t && allow_pack && !force_cp;
     const bool xp_auto = xp_possible && fi != 2;
     pl->a_pre = false;
@@ -602,7 +619,7 @@ int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, 
         pl->a_xp = xp_possible;
     } else if (cfg.at < 0) {
         if (xp_auto) {
-            pl->a_pre = copy_ok && (0.085 - 0.04) * t_main > copy_cost;
+            pl->a_pre = copy_ok && 0.036 * t_main > copy_cost;
             pl->a_xp = !pl->a_pre;
         } else {
             pl->a_pre = copy_ok && 0.085 * t_main > copy_cost;
@@ -770,19 +787,23 @@ int launch_plan(Plan* pl, int* status, float* ws, cudaStream_t stream) {
     unsigned char* w = reinterpret_cast<unsigned char*>(ws);
     GemmParams& p = pl->p;
     const int pack_grid = 16 * (pl->sms > 0 ? pl->sms : 1);
+    // True once a kernel of this call is on the stream: the next one may
+    // then be launched by programmatic serialisation behind it.
+    const bool pdl = pdl_enabled();
+    bool prior = false;
     if (pl->pack_a) {
         float* a2 = reinterpret_cast<float*>(w);
         if (pl->a_pre) {
             // Row-major A (M x K) -> its transpose (K x lda_pack).
-            e = launch_transpose_pack(p.A, p.lda, a2, pl->lda_pack, p.M, p.K, stream);
+            e = launch_transpose_pack(p.A, p.lda, a2, pl->lda_pack, p.M, p.K, stream, false);
         } else {
             // A transposed keeps its stored (K x M) layout in the copy.
             const int rows = pl->a_t ? p.K : p.M, cols = pl->a_t ? p.M : p.K;
-            pack_rows_kernel<<<pack_grid, 256, 0, stream>>>(p.A, p.lda, a2, pl->lda_pack, rows,
-                                                            cols);
-            e = cudaGetLastError();
+            e = launch_kernel(pack_rows_kernel, dim3(pack_grid), dim3(256), 0, stream, false, p.A,
+                              p.lda, a2, pl->lda_pack, rows, cols);
         }
         if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
+        prior = true;
         const bool kt = pl->a_t || pl->a_pre;
         const bool ok = kt ? encode_2d(&pl->tmA, a2, p.K, p.M, pl->lda_pack, 32, pl->fam->bm, false)
                            : encode_2d(&pl->tmA, a2, p.M, p.K, pl->lda_pack, pl->fam->bm, 32, true);
@@ -794,12 +815,14 @@ int launch_plan(Plan* pl, int* status, float* ws, cudaStream_t stream) {
         float* b2 = reinterpret_cast<float*>(w + pl->pack_a_bytes);
         if (pl->b_t) {
             // B stored N x K -> row-major K x ldb_pack.
-            e = launch_transpose_pack(p.B, p.ldb, b2, pl->ldb_pack, p.N, p.K, stream);
+            e = launch_transpose_pack(p.B, p.ldb, b2, pl->ldb_pack, p.N, p.K, stream,
+                                      pdl && prior);
         } else {
-            pack_rows_kernel<<<pack_grid, 256, 0, stream>>>(p.B, p.ldb, b2, pl->ldb_pack, p.K, p.N);
-            e = cudaGetLastError();
+            e = launch_kernel(pack_rows_kernel, dim3(pack_grid), dim3(256), 0, stream, pdl && prior,
+                              p.B, p.ldb, b2, pl->ldb_pack, p.K, p.N);
         }
         if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
+        prior = true;
         if (!encode_2d(&pl->tmB, b2, p.K, p.N, pl->ldb_pack, 32, pl->fam->bn, false))
             return cuda_fail(cudaErrorInvalidValue, SGEMM_ERR_LAUNCH);
         p.B = b2;
@@ -808,7 +831,7 @@ int launch_plan(Plan* pl, int* status, float* ws, cudaStream_t stream) {
     p.ws = pl->sk_bytes > 0
                ? reinterpret_cast<float*>(w + pl->pack_a_bytes + pl->pack_b_bytes)
                : nullptr;
-    e = pl->k->launch(&pl->tmA, &pl->tmB, &pl->p, pl->grid, stream);
+    e = pl->k->launch(&pl->tmA, &pl->tmB, &pl->p, pl->grid, stream, pdl && prior);
     if (e == cudaSuccess && pl->sk_tiles > 0) {
         // Enough fixup CTAs for about two per SM, at most 8 per tile.
         const int want = (2 * pl->sms + pl->sk_tiles - 1) / pl->sk_tiles;

@@ -748,6 +748,10 @@ sgemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         fence_barrier_init();
     }
     __syncthreads();
+    // Up to here only shared memory and kernel parameters were touched; the
+    // kernel before this one on the stream (a packing copy of an operand)
+    // may still be running until this returns.
+    griddep_wait();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (warp >= C::CONSUMER_WARPS) {

@@ -93,7 +93,12 @@ extern "C" {
  *
  * The call is asynchronous: it returns once the kernel is enqueued. Device
  * time-outs are reported later by sgemm_check_status. A, B and C must stay
- * valid until the stream reaches the kernel.
+ * valid until the stream reaches the kernel. A call enqueues one GEMM kernel,
+ * preceded by up to two packing copies and followed by the stream-K fixup
+ * where its plan says so (sgemm_plan); a GEMM that follows a copy of the same
+ * call is launched with programmatic stream serialisation (it waits for the
+ * copy on the device), unless the environment variable SGEMM_PDL is "0" when
+ * the library first launches.
  */
 SGEMM_API int sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float* A, int64_t lda,
           const float* B, int64_t ldb, float beta, float* C, int64_t ldc,

@@ -419,6 +419,35 @@ def test_integer_inputs_bit_exact_with_stream_k():
     check_full(2.0, A, B, -1.0, C0, C, exact=True)
 
 
+@pytest.mark.parametrize("cfg", ["ws_64x64x32_s4_k4", "ws_64x64x32_s4_k4:cpasync:dp",
+                                 "ws_128x64x32_s4_k2:dp", "ws_64x64x32_s4_k2"])
+def test_integer_inputs_bit_exact_on_ksplit_tiles(cfg):
+    # The k-groups' partial sums are integers below 2^24 here, so adding
+    # them at the end changes no bit.
+    A = inputs.fill("int", 6, inputs.TID_A, 333, 1500)
+    B = inputs.fill("int", 6, inputs.TID_B, 1500, 517)
+    C0 = inputs.fill("int", 6, inputs.TID_C, 333, 517)
+    assert sg.sgemm_set_config(cfg) == 0
+    try:
+        C, guards, plan = gpu_util.run(2.0, A, B, -1.0, C0)
+    finally:
+        sg.sgemm_set_config("auto")
+    assert guards and plan[0].startswith(cfg.split(":")[0]), plan
+    check_full(2.0, A, B, -1.0, C0, C, exact=True)
+
+
+@pytest.mark.parametrize("shape", [(256, 256, 8192), (300, 512, 1000), (130, 72, 4100)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_auto_splits_deep_k_over_small_tiles(shape):
+    # Few tiles and a deep K: "auto" takes the 64 x 64 tile in four k-groups
+    # and spreads its k-iterations over the SMs (stream-K tail).
+    M, N, K = shape
+    A, B, C0 = gen(M, N, K, seed=91)
+    C, guards, plan = gpu_util.run(0.7, A, B, -1.3, C0)
+    assert guards and plan[0].startswith("ws_64x64x32_s4_k4_") and plan[0].endswith("+sk"), plan
+    check_full(0.7, A, B, -1.3, C0, C)
+
+
 # ---- streams and graphs ----------------------------------------------------------
 
 def test_two_streams_concurrently_do_not_share_workspace():
