@@ -70,7 +70,9 @@ def gen(M, N, K, seed, dist="normal"):
 
 @pytest.mark.parametrize("shape", [(1, 1, 1), (7, 5, 3), (300, 260, 200),     # one block
                                    (2048, 1536, 1024), (3000, 1100, 1531),   # pipelined
-                                   (2100, 2100, 700)],                       # B in 4 chunks
+                                   (2100, 2100, 700),                        # B in 4 chunks
+                                   (4093, 640, 2100),      # 768, 3 x 1024, ragged 253-row tail
+                                   (1100, 2304, 2000)],    # 896 rows in B chunks, 204-row tail
                          ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("beta", [0.0, -1.3])
 def test_matches_oracle(shape, beta):
