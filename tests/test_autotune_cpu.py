@@ -34,3 +34,24 @@ def test_csv_round_trip(tmp_path):
     assert [r["config"] for r in back] == ["auto", "b:dp"]
     assert tuple(back[0].keys()) == autotune.FIELDS
     assert autotune.best_configs(back) == {(8, 8, 8): "b:dp"}
+
+
+def test_recorded_gb300_sweep_is_consistent():
+    # The sweep shipped with the package: every row checked against the
+    # bound, one winner per shape, "auto" timed on every shape and within a
+    # few percent of that shape's winner.
+    import os
+    from collections import defaultdict
+    path = os.path.join(os.path.dirname(autotune.__file__), "tuning", "sweep_gb300.csv")
+    rows = autotune.load_csv(path)
+    by_shape = defaultdict(list)
+    for r in rows:
+        assert r["ok"] == "1" and float(r["err_over_bound"]) <= 1.0, r
+        by_shape[(int(r["M"]), int(r["N"]), int(r["K"]))].append(r)
+    assert len(by_shape) >= 20
+    for shape, rs in by_shape.items():
+        assert sum(r["best"] == "1" for r in rs) == 1, shape
+        best = min(float(r["ms"]) for r in rs)
+        [auto] = [r for r in rs if r["config"] == "auto"]
+        assert float(auto["ms"]) <= 1.05 * best, (shape, auto["ms"], best)
+    assert autotune.best_configs(rows).keys() == by_shape.keys()
