@@ -507,6 +507,78 @@ def test_sgemm_inside_a_captured_cuda_graph():
     check_full(0.7, A, B, -1.3, C0, work.cpu().numpy())
 
 
+def test_copy_then_gemm_inside_a_captured_cuda_graph():
+    # 2048 x 2048 x 4096 takes the transposed copy of A, and the GEMM behind
+    # it is launched by programmatic stream serialisation: capture records
+    # that as a programmatic edge, and replays give the oracle's result.
+    torch = pytest.importorskip("torch")
+    M, N, K = 2048, 2048, 4096
+    A, B, C0 = gen(M, N, K, seed=404)
+    dA = torch.from_numpy(A).cuda()
+    dB = torch.from_numpy(B).cuda()
+    dC = torch.from_numpy(C0).cuda()
+    name, _ = sg.plan_tensors(0.7, dA, dB, -1.3, dC)
+    assert "+packAT" in name, name
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        sg.sgemm_tensors(0.7, dA, dB, -1.3, dC.clone(), stream=s)       # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    work = dC.clone()
+    with torch.cuda.graph(g):
+        sg.sgemm_tensors(0.7, dA, dB, -1.3, work)
+    for _ in range(3):
+        work.copy_(dC)
+        g.replay()
+    torch.cuda.synchronize()
+    sg.check_status()
+    C = work.cpu().numpy()
+    rows, cols = inputs.sample_entries(M, N)
+    ref, S = oracle.sgemm_ref_sampled(0.7, A, B, -1.3, C0, rows, cols)
+    rep = oracle.check(C[rows, cols], ref, S, K)
+    assert rep["ok"], rep
+    # Eager calls give the same bits as the replays.
+    eager = dC.clone()
+    sg.sgemm_tensors(0.7, dA, dB, -1.3, eager)
+    sg.check_status()
+    assert np.array_equal(eager.cpu().numpy(), C)
+
+
+def test_programmatic_launch_changes_no_bit():
+    # The same 2048 x 2048 x 4096 call in a process with SGEMM_PDL=0 (every
+    # kernel launched the ordinary way) gives the same bits.
+    import os
+    import subprocess
+    import sys
+    torch = pytest.importorskip("torch")
+    M, N, K = 2048, 2048, 4096
+    A, B, C0 = gen(M, N, K, seed=405)
+    dC = torch.from_numpy(C0).cuda()
+    sg.sgemm_tensors(0.7, torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda(), -1.3, dC)
+    sg.check_status()
+    here = dC.cpu().numpy()
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    script = (
+        "import sys, numpy as np, torch\n"
+        "import dense_fp32_matrix_strict_gb300 as sg\n"
+        "from dense_fp32_matrix_strict_gb300 import inputs as I\n"
+        f"A = I.fill('normal', 405, I.TID_A, {M}, {K})\n"
+        f"B = I.fill('normal', 405, I.TID_B, {K}, {N})\n"
+        f"C0 = I.fill('normal', 405, I.TID_C, {M}, {N})\n"
+        "dC = torch.from_numpy(C0).cuda()\n"
+        "sg.sgemm_tensors(0.7, torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda(), -1.3, dC)\n"
+        "sg.check_status()\n"
+        "sys.stdout.buffer.write(dC.cpu().numpy().tobytes())\n")
+    env = dict(os.environ, SGEMM_PDL="0")
+    out = subprocess.run([sys.executable, "-c", script], cwd=root, env=env, capture_output=True,
+                         timeout=600)
+    assert out.returncode == 0, out.stderr.decode()[-2000:]
+    there = np.frombuffer(out.stdout, dtype=np.float32).reshape(M, N)
+    assert np.array_equal(here, there)
+
+
 @pytest.mark.parametrize("config", ["128x128", "128x128:dp", "128x64:dp", "64x64:dp"])
 @pytest.mark.parametrize("aligned", [True, False], ids=["aligned", "unaligned"])
 def test_a_paths_give_the_same_bits(config, aligned):
