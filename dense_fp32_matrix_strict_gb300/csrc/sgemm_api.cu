@@ -722,7 +722,7 @@ int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, 
     p.tiles_m = static_cast<int>((M + bm - 1) / bm);
     p.tiles_n = static_cast<int>((N + bn - 1) / bn);
     p.k_tiles = static_cast<int>((K + bk - 1) / bk);
-    p.group_m = 8;
+    p.group_m = 8;      // 4, 16 and 32 measured within 0.03 % at 4096^3 and 8192x14336x4096
     p.c_vec = (aligned(C, 16) && (ldc % 4) == 0) ? 1 : 0;
     p.A = A;
     p.B = B;

@@ -533,7 +533,9 @@ int run_3xtf32(int opa, int opb, int64_t M, int64_t N, int64_t K, float alpha, c
         p.K = static_cast<int>(K);
         p.tiles_m = static_cast<int>((M + BM - 1) / BM);
         p.k_tiles = static_cast<int>((K + BK - 1) / BK);
-        p.group_m = 8;
+        // Tiles walk 16 tile-rows at a time: at 4096^3 0.552 ms against
+        // 0.556 ms with 8 and 0.561 / 0.562 ms with 4 / 32 (GB300).
+        p.group_m = 16;
         p.c_vec = ((reinterpret_cast<uintptr_t>(C) % 16) == 0 && (ldc % 4) == 0) ? 1 : 0;
         p.C = C;
         p.ldc = ldc;
