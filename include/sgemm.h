@@ -114,7 +114,9 @@ SGEMM_API int sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float* A
  * block on `stream` (the first block chunk by chunk as B arrives), and
  * copies each finished block of C back on a second copy stream, so the
  * transfers of one block overlap the GEMMs of others. Problems below 5 GFLOP run as one block;
- * larger ones in 2 to 8 blocks of about 1024 rows. The device buffers come
+ * larger ones end on a short block (128 to 256 rows, taking any ragged rows
+ * of M) after up to 8 blocks of about 1024 rows, the first of them shorter
+ * where the rows do not divide evenly. The device buffers come
  * from the library's stream-ordered pool (B, plus two A and two C blocks:
  * 4 (K N + 2 mb (K + N)) bytes, mb the block height; SGEMM_ERR_CUDA if the
  * pool cannot supply them). The call is asynchronous and ordered on

@@ -473,6 +473,45 @@ def test_two_streams_concurrently_do_not_share_workspace():
     check_full(0.7, A2, B2, -1.3, C2, c2.cpu().numpy())
 
 
+def test_host_threads_call_concurrently():
+    # Four host threads, each on its own stream, plan and launch at the same
+    # time (ctypes drops the GIL during the call): the library's per-device
+    # set-up, shape rules and workspace pool are shared between them.
+    import threading
+    torch = pytest.importorskip("torch")
+    shapes = [(1000, 1100, 2000), (700, 900, 1500), (333, 4500, 776), (2048, 2048, 1024)]
+    cases = [gen(M, N, K, seed=410 + i) for i, (M, N, K) in enumerate(shapes)]
+    dev = [(torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda(), torch.from_numpy(C0).cuda())
+           for A, B, C0 in cases]
+    c0s = [torch.from_numpy(C0).cuda() for _, _, C0 in cases]
+    streams = [torch.cuda.Stream() for _ in shapes]
+    torch.cuda.synchronize()
+    errors = []
+    start = threading.Barrier(len(shapes))
+
+    def work(i):
+        try:
+            dA, dB, dC = dev[i]
+            start.wait()
+            for _ in range(3):
+                with torch.cuda.stream(streams[i]):
+                    dC.copy_(c0s[i])
+                    sg.sgemm_tensors(0.7, dA, dB, -1.3, dC, stream=streams[i])
+                streams[i].synchronize()
+        except Exception as e:          # reported below, on the main thread
+            errors.append((i, repr(e)))
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(len(shapes))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    sg.check_status()
+    for (A, B, C0), (_, _, dC) in zip(cases, dev):
+        check_full(0.7, A, B, -1.3, C0, dC.cpu().numpy())
+
+
 def test_sgemm_inside_a_captured_cuda_graph():
     # The stream-K workspace is stream-ordered, so capture records it as an
     # allocation node; the graph replays correctly. (The first call on the
