@@ -24,8 +24,9 @@ constexpr int kMaxDevices = 64;
 constexpr int kStatusBytes = 256;
 
 // All compiled kernel families: [0] 128x128, [1] 64x64, [2] 128x64,
-// [3] 128x64 in two k-groups and [4] 64x64 in four k-groups are what "auto"
-// chooses between; the rest are tuning alternatives.
+// [3] 128x64 in two k-groups, [4] 64x64 in four k-groups and [5], [6] the
+// same in clusters of 2 and 4 CTAs are what "auto" chooses between; the
+// rest are tuning alternatives.
 struct Registry {
     const KernelFamily* fam[kMaxFamilies];
     int count = 0;
@@ -35,6 +36,8 @@ struct Registry {
         fam[count++] = family_128x64();
         fam[count++] = family_128x64_k2();
         fam[count++] = family_64x64_k4();
+        fam[count++] = family_64x64_k4_c2();
+        fam[count++] = family_64x64_k4_c4();
         int n = 0;
         const KernelFamily* const* sw = sweep_families(&n);
         for (int i = 0; i < n && count < kMaxFamilies; ++i) fam[count++] = sw[i];
@@ -291,8 +294,8 @@ cudaError_t launch_transpose_pack(const float* src, long long lds, float* dst, l
     const long long tiles_r = (ldd + kTpTile - 1) / kTpTile;
     const dim3 grid(static_cast<unsigned>((C + kTpTile - 1) / kTpTile),
                     static_cast<unsigned>(tiles_r < 65535 ? tiles_r : 65535));
-    return launch_kernel(transpose_pack_kernel, grid, dim3(256), 0, stream, pdl, src, lds, dst,
-                         ldd, R, C);
+    return launch_kernel(transpose_pack_kernel, grid, dim3(256), 0, stream, pdl, 1, src, lds,
+                         dst, ldd, R, C);
 }
 
 // A kernel that follows a packing copy of the same call is launched by
@@ -437,9 +440,11 @@ int device_info(const DeviceInfo** out) {
     const Registry& reg = registry();
     for (int f = 0; f < reg.count; ++f) {
         for (int m = 0; m < kModes; ++m) {
-            int n = 0;
+            int n = 0, ncl = 0;
             const KernelEntry& ke = reg.fam[f]->modes[m];
-            e = ke.prepare != nullptr ? ke.prepare(&n) : cudaSuccess;
+            e = ke.prepare != nullptr ? ke.prepare(&n, &ncl) : cudaSuccess;
+            // A cluster variant of which no cluster fits is as unusable.
+            if (e == cudaSuccess && reg.fam[f]->cs > 1 && ncl <= 0) n = 0;
             if (e != cudaSuccess || n <= 0) {
                 // The 128 x 128 and 64 x 64 families must work in their
                 // row-major and transposed-A modes; the in-smem transpose
@@ -451,8 +456,10 @@ int device_info(const DeviceInfo** out) {
                                      SGEMM_ERR_CUDA);
                 (void)cudaGetLastError();
                 n = 0;
+                ncl = 0;
             }
             st.info.ctas_per_sm[f][m] = n;
+            st.info.clusters[f][m] = ncl;
         }
     }
     st.info.device = dev;
@@ -578,6 +585,19 @@ int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, 
                     offer(4, false, static_cast<double>(cdiv(tiles64, cap_k4)) * 0.31 * dkt);
                     if (sk_possible && tiles64 % cap_k4 != 0)
                         offer(4, true, sk_iters(tiles64, cap_k4) * 0.31 + 4);
+                }
+                // The same tile in clusters of cs CTAs that split each tile's
+                // k-tiles: a cs-th of the k-loop per CTA, plus the hand-over of
+                // the partial sums through distributed shared memory (~0.8
+                // units with 2 CTAs, ~1.25 with 4). Only when all the
+                // clusters run at once: a second wave of clusters measured
+                // slower than the plain tile (640^3: 30.8 against 20.9 us).
+                for (int f = 5; f <= 6; ++f) {
+                    const int64_t cs = registry().fam[f]->cs;
+                    const int64_t ncl = dev->clusters[f][mi_tt];
+                    if (dev->ctas_per_sm[f][mi_tt] <= 0 || tiles64 > ncl) continue;
+                    offer(f, false,
+                          0.31 * static_cast<double>(cdiv(kt, cs)) + (cs == 2 ? 0.8 : 1.25));
                 }
             }
             fi = best_f;
@@ -737,6 +757,20 @@ int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, 
     if (tiles > 0x7fffffffll) return SGEMM_ERR_INVALID_VALUE;
     if (dev->ctas_per_sm[fi][mi] <= 0) return cuda_fail(cudaErrorInvalidConfiguration, SGEMM_ERR_LAUNCH);
     const int64_t cap = static_cast<int64_t>(dev->ctas_per_sm[fi][mi]) * sms;
+    if (fam->cs > 1) {
+        // One tile per cluster of fam->cs CTAs (each a share of its k-tiles),
+        // clusters in as many waves as it takes; no stream-K tail.
+        const int64_t g = tiles * fam->cs;
+        if (g > 0x7fffffffll) return SGEMM_ERR_INVALID_VALUE;
+        p.dp_tiles = static_cast<int>(tiles);
+        p.sk_ctas = 0;
+        p.sk_iters = 0;
+        pl->grid = static_cast<int>(g);
+        pl->sk_tiles = 0;
+        pl->sk_bytes = 0;
+        pl->ws_bytes = pl->pack_a_bytes + pl->pack_b_bytes;
+        return SGEMM_OK;
+    }
 
     // Schedule: whole waves data-parallel; the last, partial wave's
     // k-iterations spread over the CTAs (stream-K) unless it is nearly full.
@@ -799,8 +833,8 @@ int launch_plan(Plan* pl, int* status, float* ws, cudaStream_t stream) {
         } else {
             // A transposed keeps its stored (K x M) layout in the copy.
             const int rows = pl->a_t ? p.K : p.M, cols = pl->a_t ? p.M : p.K;
-            e = launch_kernel(pack_rows_kernel, dim3(pack_grid), dim3(256), 0, stream, false, p.A,
-                              p.lda, a2, pl->lda_pack, rows, cols);
+            e = launch_kernel(pack_rows_kernel, dim3(pack_grid), dim3(256), 0, stream, false, 1,
+                              p.A, p.lda, a2, pl->lda_pack, rows, cols);
         }
         if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
         prior = true;
@@ -819,7 +853,7 @@ int launch_plan(Plan* pl, int* status, float* ws, cudaStream_t stream) {
                                       pdl && prior);
         } else {
             e = launch_kernel(pack_rows_kernel, dim3(pack_grid), dim3(256), 0, stream, pdl && prior,
-                              p.B, p.ldb, b2, pl->ldb_pack, p.K, p.N);
+                              1, p.B, p.ldb, b2, pl->ldb_pack, p.K, p.N);
         }
         if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
         prior = true;

@@ -25,6 +25,7 @@ struct DeviceInfo {
     int device = -1;
     int sm_count = 0;
     int ctas_per_sm[kMaxFamilies][kModes] = {};
+    int clusters[kMaxFamilies][kModes] = {};   // co-resident clusters (cluster variants)
 };
 
 struct Plan {

@@ -108,9 +108,14 @@ struct GemmParams {
 //   [BK][BM] layout, built in shared memory by transposer warps, with the
 //   16-byte chunks of k-row k XOR-swizzled by (k / 4) mod 8 so that both the
 //   transposing stores and the consumers' reads are free of bank conflicts.
+// CS: CTAs per thread-block cluster. With CS > 1 the CTAs of a cluster share
+//   one tile: CTA rank r takes k-tiles [r kt / CS, (r + 1) kt / CS), ranks
+//   1.. hand their sums to rank 0 through its shared memory (distributed
+//   shared memory), and rank 0 adds them in rank order and writes C. The
+//   grid is tiles x CS, one tile per cluster, no stream-K tail.
 template <int BM_, int BN_, int BK_, int STAGES_, int A_MODE_, int B_MODE_, int FORDER_ = 2,
           int EARLY_ = 0, int LMAP_ = 0, int A_T_ = 0, int ALOAD_ = 4, int TN_ = 8,
-          int KSPLIT_ = 1>
+          int KSPLIT_ = 1, int CS_ = 1>
 struct Cfg {
     static constexpr int BM = BM_, BN = BN_, BK = BK_, STAGES = STAGES_;
     static constexpr int A_MODE = A_MODE_, B_MODE = B_MODE_;
@@ -161,9 +166,12 @@ struct Cfg {
         A_XP ? TRANSPOSERS : (ANY_TMA ? 1 : 0) + (ANY_CP ? 32 * PRODUCER_WARPS : 0);
     static constexpr int RAW_BYTES = A_XP ? A_BYTES : 0;   // raw A staging, per stage
     static constexpr int RED_BYTES = (KSPLIT - 1) * BM * BN * 4;   // k-group sums
+    static constexpr int CS = CS_;
+    static_assert(CS == 1 || CS == 2 || CS == 4, "CS is 1, 2 or 4");
+    static constexpr int CKS_BYTES = (CS - 1) * BM * BN * 4;        // other ranks' sums
     static constexpr int SMEM_BYTES = 1024 /* alignment slack */ +
                                       STAGES * (A_BYTES + B_BYTES + RAW_BYTES) + RED_BYTES +
-                                      (3 * STAGES + 2) * 8;
+                                      CKS_BYTES + (3 * STAGES + 3) * 8;
     static constexpr bool FITS = SMEM_BYTES <= 227 * 1024;
     // Tiles of at most 128 x 64 are sized to run two CTAs per SM.
     static constexpr int MIN_BLOCKS = (BM * BN * KSPLIT <= 128 * 64) ? 2 : 1;
@@ -195,11 +203,20 @@ __device__ __forceinline__ long long sk_start(long long c, const GemmParams& p) 
     return (c * p.sk_iters) / p.sk_ctas;
 }
 
+template <int CS = 1>
 struct Schedule {
     int t_dp;            // next data-parallel tile
     long long s, i, e;   // this CTA's stream-K range [s, e), next iteration i
 
     __device__ __forceinline__ explicit Schedule(const GemmParams& p) {
+        if (CS > 1) {
+            // One item: this cluster's tile, this rank's share of its k-tiles.
+            t_dp = static_cast<int>(cluster_id_x());
+            const long long r = cluster_ctarank();
+            s = i = r * p.k_tiles / CS;
+            e = (r + 1) * p.k_tiles / CS;
+            return;
+        }
         t_dp = static_cast<int>(blockIdx.x);
         if (static_cast<int>(blockIdx.x) < p.sk_ctas) {
             s = sk_start(blockIdx.x, p);
@@ -211,6 +228,15 @@ struct Schedule {
     }
 
     __device__ __forceinline__ bool next(const GemmParams& p, Item& it) {
+        if (CS > 1) {
+            if (t_dp < 0) return false;
+            it.tile = t_dp;
+            it.kb = static_cast<int>(s);
+            it.ke = static_cast<int>(e);
+            it.slot = -1;
+            t_dp = -1;
+            return true;
+        }
         if (t_dp < p.dp_tiles) {
             it.tile = t_dp;
             it.kb = 0;
@@ -257,6 +283,23 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// The same with acquire at cluster scope (a barrier other CTAs of the
+// cluster arrive on after writing this CTA's shared memory).
+__device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity,
+                                                     const GemmParams& p, int code) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i)
+            if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > p.timeout_ns) {
+            atomicOr(p.status, code);
+            return false;
+        }
+    }
+}
+
 // ---- producer -----------------------------------------------------------------
 
 // Byte offset of A element (row r, column k) inside one stage: 128-byte rows,
@@ -283,7 +326,7 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmA, const CUtensorM
     uint32_t ph = 0;
     int issued = 0;
     bool ok = true;
-    Schedule sched(p);
+    Schedule<C::CS> sched(p);
     Item it;
     while (ok && sched.next(p, it)) {
         int tm, tn;
@@ -366,7 +409,7 @@ __device__ __forceinline__ void transposer(const GemmParams& p, const uint8_t* r
     constexpr int BLOCKS = C::BM * 2;   // (BM / 4) row groups x 8 k-chunks
     int s = 0;
     uint32_t ph = 0;
-    Schedule sched(p);
+    Schedule<C::CS> sched(p);
     Item it;
     while (sched.next(p, it)) {
         for (int kt = it.kb; kt < it.ke; ++kt) {
@@ -479,7 +522,7 @@ template <class C>
 __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_ptr,
                                          const uint8_t* sB_ptr, uint32_t full0, uint32_t empty0,
                                          float4* red, uint32_t red_full, uint32_t red_empty,
-                                         int warp, int lane) {
+                                         float4* cks, uint32_t cks_full, int warp, int lane) {
     // k-group of this warp (KSPLIT > 1) and its place in the group's tile.
     const int grp = C::KSPLIT > 1 ? warp / C::GROUP_WARPS : 0;
     const int wq = C::KSPLIT > 1 ? warp % C::GROUP_WARPS : warp;
@@ -498,7 +541,7 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
 
     int s = 0;
     uint32_t ph = 0;
-    Schedule sched(p);
+    Schedule<C::CS> sched(p);
     Item it;
     while (sched.next(p, it)) {
         float acc[8][C::TN];
@@ -634,6 +677,44 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
             red_ph ^= 1u;
         }
 
+        if (C::CS > 1) {
+            // Cluster k-split: ranks 1.. store their sums into rank 0's
+            // shared memory (float4 j of lane l of warp wq at
+            // ((r - 1) GROUP_WARPS + wq) 2 TN + j, lane-interleaved) and
+            // arrive on its barrier; rank 0 waits for all of them and adds
+            // them in rank order. One item per CTA, so the phase is 0.
+            constexpr int NF4 = 8 * C::TN / 4;
+            const uint32_t rank = cluster_ctarank();
+            if (rank > 0) {
+                const uint32_t dst = mapa_shared(
+                    smem_u32(cks + (((rank - 1) * C::GROUP_WARPS + wq) * NF4) * 32 + lane), 0);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int h = 0; h < C::TN / 4; ++h)
+                        st_cluster_v4(dst + (i * (C::TN / 4) + h) * 32 * 16,
+                                      make_float4(acc[i][4 * h], acc[i][4 * h + 1],
+                                                  acc[i][4 * h + 2], acc[i][4 * h + 3]));
+                mbar_arrive_remote(mapa_shared(cks_full, 0));
+                continue;
+            }
+            if (!wait_bounded_cluster(cks_full, 0, p, STATUS_CONSUMER_TIMEOUT)) return;
+#pragma unroll 1
+            for (int r = 1; r < C::CS; ++r) {
+                const float4* srcr = cks + (((r - 1) * C::GROUP_WARPS + wq) * NF4) * 32 + lane;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int h = 0; h < C::TN / 4; ++h) {
+                        const float4 v = srcr[(i * (C::TN / 4) + h) * 32];
+                        acc[i][4 * h] += v.x;
+                        acc[i][4 * h + 1] += v.y;
+                        acc[i][4 * h + 2] += v.z;
+                        acc[i][4 * h + 3] += v.w;
+                    }
+            }
+        }
+
         if (it.slot >= 0) {
             // Partial tile: raw sums to the workspace slot, row-major BM x BN,
             // bypassing L1 (sk_fixup_kernel reads them from L2).
@@ -728,12 +809,15 @@ sgemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     uint8_t* sB = smem + C::STAGES * C::A_BYTES;
     uint8_t* sRaw = sB + C::STAGES * C::B_BYTES;      // C::RAW_BYTES per stage
     float4* red = reinterpret_cast<float4*>(sRaw + C::STAGES * C::RAW_BYTES);  // RED_BYTES
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sRaw + C::STAGES * C::RAW_BYTES + C::RED_BYTES);
+    float4* cks = reinterpret_cast<float4*>(sRaw + C::STAGES * C::RAW_BYTES + C::RED_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sRaw + C::STAGES * C::RAW_BYTES + C::RED_BYTES +
+                                                 C::CKS_BYTES);
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = smem_u32(bars + C::STAGES);
     const uint32_t raw0 = smem_u32(bars + 2 * C::STAGES);
     const uint32_t red_full = smem_u32(bars + 3 * C::STAGES);
     const uint32_t red_empty = red_full + 8;
+    const uint32_t cks_full = red_full + 16;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -745,9 +829,13 @@ sgemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             mbar_init(red_full, (C::KSPLIT - 1) * C::GROUP_WARPS * 32);
             mbar_init(red_empty, C::GROUP_WARPS * 32);
         }
+        if (C::CS > 1) mbar_init(cks_full, (C::CS - 1) * C::GROUP_WARPS * 32);
         fence_barrier_init();
     }
     __syncthreads();
+    // The other CTAs of the cluster arrive on cks_full only after it has
+    // been initialised: every thread of the cluster passes this first.
+    if (C::CS > 1) cluster_sync();
     // Up to here only shared memory and kernel parameters were touched; the
     // kernel before this one on the stream (a packing copy of an operand)
     // may still be running until this returns.
@@ -762,8 +850,12 @@ sgemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             producer<C>(&tmA, &tmB, p, smem_u32(sA), smem_u32(sB), smem_u32(sRaw), full0, empty0,
                         raw0, pw, lane);
     } else {
-        consumer<C>(p, sA, sB, full0, empty0, red, red_full, red_empty, warp, lane);
+        consumer<C>(p, sA, sB, full0, empty0, red, red_full, red_empty, cks, cks_full, warp,
+                    lane);
     }
+    // No CTA of a cluster leaves while another may still write its shared
+    // memory: every role returns here (all of their waits are bounded).
+    if (C::CS > 1) cluster_sync();
 }
 
 }  // namespace sg

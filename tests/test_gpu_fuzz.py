@@ -23,7 +23,8 @@ CONFIGS = ["auto", "auto:dp", "auto:noat", "auto:at", "auto:xp", "128x128", "128
            "128x128:at:dp", "64x64", "64x64:xp", "128x64", "128x64:dp", "128x128:cpasync",
            "64x64:cpasync:dp", "ws_64x128x32_s4", "ws_128x128x32_s3:xp", "ws_128x128x32_s4_l1",
            "ws_128x64x32_s4_k2", "ws_64x64x32_s4_k4:xp", "ws_64x64x32_s4_k2:at",
-           "ws_64x64x32_s4_k4:cpasync", "ws_128x64x32_s4_k2:cpasync:dp"]
+           "ws_64x64x32_s4_k4:cpasync", "ws_128x64x32_s4_k2:cpasync:dp",
+           "ws_64x64x32_s4_k4_c2", "ws_64x64x32_s4_k4_c4:xp", "ws_64x64x32_s4_k4_c4:cpasync"]
 EDGES = [1, 2, 3, 31, 32, 33, 63, 64, 65, 127, 128, 129, 255, 256, 257]
 
 

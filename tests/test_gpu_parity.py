@@ -253,7 +253,7 @@ def _workload(name, full):
 
 def test_workload_sq256_uniform():
     rep, plan = _workload("sq256_uniform", full=True)
-    assert plan[0] == "ws_64x64x32_s4_k4_Axp_Btma", plan   # too small to split
+    assert plan[0] == "ws_64x64x32_s4_k4_c4_Axp_Btma", plan   # a tile per 4-CTA cluster
 
 
 def test_workload_sq1024_int_bit_exact():
@@ -300,8 +300,9 @@ def test_every_family_matches_oracle(cp):
 
 
 def _ksplit(name):
-    # Families whose warps split each stage's k into groups ("_k2", "_k4").
-    return re.search(r"_k[0-9]+$", name) is not None
+    # Families whose warps split each stage's k into groups ("_k2", "_k4"),
+    # also with their CTAs in clusters that split each tile's k ("_c2", "_c4").
+    return re.search(r"_k[0-9]+(_c[0-9]+)?$", name) is not None
 
 
 def test_families_agree_bitwise():
@@ -436,7 +437,47 @@ def test_integer_inputs_bit_exact_on_ksplit_tiles(cfg):
     check_full(2.0, A, B, -1.0, C0, C, exact=True)
 
 
-@pytest.mark.parametrize("shape", [(256, 256, 8192), (300, 512, 1000), (130, 72, 4100)],
+@pytest.mark.parametrize("cfg", ["ws_64x64x32_s4_k4_c2", "ws_64x64x32_s4_k4_c4",
+                                 "ws_64x64x32_s4_k4_c4:cpasync", "ws_64x64x32_s4_k4_c4:at"])
+@pytest.mark.parametrize("shape", [(1, 1, 1), (5, 7, 33), (64, 64, 96), (256, 256, 256),
+                                   (300, 512, 1000), (1000, 700, 1300), (130, 72, 4100)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_cluster_k_split_matches_oracle(cfg, shape):
+    # The CTAs of a cluster share a tile, each a share of its k-tiles (none
+    # at all when K has fewer k-tiles than the cluster has CTAs), and the
+    # first adds the others' sums, read from its shared memory.
+    M, N, K = shape
+    A, B, C0 = gen(M, N, K, seed=95)
+    assert sg.sgemm_set_config(cfg) == 0
+    try:
+        C, guards, plan = gpu_util.run(0.7, A, B, -1.3, C0)
+        C1, guards1, _ = gpu_util.run(1.5, A, B, 0.0, None)
+    finally:
+        sg.sgemm_set_config("auto")
+    assert guards and guards1 and plan[0].startswith(cfg.split(":")[0] + "_"), plan
+    assert "+sk" not in plan[0], plan
+    check_full(0.7, A, B, -1.3, C0, C)
+    check_full(1.5, A, B, 0.0, None, C1)
+
+
+def test_cluster_k_split_integers_bit_exact_and_deterministic():
+    A = inputs.fill("int", 7, inputs.TID_A, 300, 2000)
+    B = inputs.fill("int", 7, inputs.TID_B, 2000, 200)
+    C0 = inputs.fill("int", 7, inputs.TID_C, 300, 200)
+    outs = []
+    for cfg in ["ws_64x64x32_s4_k4_c4", "ws_64x64x32_s4_k4_c4", "ws_64x64x32_s4_k4_c2"]:
+        assert sg.sgemm_set_config(cfg) == 0
+        try:
+            C, guards, plan = gpu_util.run(2.0, A, B, -1.0, C0)
+        finally:
+            sg.sgemm_set_config("auto")
+        assert guards, plan
+        check_full(2.0, A, B, -1.0, C0, C, exact=True)
+        outs.append(C)
+    assert np.array_equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("shape", [(256, 256, 8192), (200, 300, 6000), (130, 72, 4100)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_auto_splits_deep_k_over_small_tiles(shape):
     # Few tiles and a deep K: "auto" takes the 64 x 64 tile in four k-groups
