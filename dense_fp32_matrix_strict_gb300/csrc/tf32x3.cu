@@ -198,29 +198,64 @@ __global__ void split_rows_kernel(const float* __restrict__ src, long long lds, 
 }
 
 // hiT/loT (cols x ldd) <- transpose of src (rows x cols, row stride lds):
-// hiT[j][k] = split(src[k][j]); zeros for k in [rows, ldd). 32 x 32 tiles
-// through shared memory so both sides stay coalesced.
-__global__ void split_transpose_kernel(const float* __restrict__ src, long long lds,
-                                       float* __restrict__ hiT, float* __restrict__ loT,
-                                       long long ldd, int rows, int cols) {
-    __shared__ float tile[32][33];
-    const int tiles_k = static_cast<int>((ldd + 31) / 32);
-    const int tiles_n = (cols + 31) / 32;
-    for (int t = blockIdx.x; t < tiles_k * tiles_n; t += gridDim.x) {
-        const int k0 = (t / tiles_n) * 32, n0 = (t % tiles_n) * 32;
-        for (int r = threadIdx.y; r < 32; r += blockDim.y) {
-            const int k = k0 + r, n = n0 + threadIdx.x;
-            tile[r][threadIdx.x] = (k < rows && n < cols) ? src[static_cast<long long>(k) * lds + n] : 0.0f;
+// hiT[j][k] = split(src[k][j]); zeros for k in [rows, ldd). 64 x 64 tiles
+// through shared memory: 16 consecutive threads read one source row as
+// float4 (scalars where src is not 16-byte aligned or lds % 4 != 0, and at
+// the column edge), then write one hi and one lo row as float4 along k (ldd
+// is a multiple of 4). blockIdx.x walks column tiles, blockIdx.y row tiles.
+constexpr int kSplitTile = 64;
+
+__global__ void __launch_bounds__(256) split_transpose_kernel(const float* __restrict__ src,
+                                                              long long lds,
+                                                              float* __restrict__ hiT,
+                                                              float* __restrict__ loT,
+                                                              long long ldd, int rows, int cols) {
+    __shared__ float tile[kSplitTile][kSplitTile + 1];
+    const bool vec = (reinterpret_cast<uintptr_t>(src) % 16 == 0) && (lds % 4 == 0);
+    const long long n0 = static_cast<long long>(blockIdx.x) * kSplitTile;
+    const long long tiles_k = (ldd + kSplitTile - 1) / kSplitTile;
+    const int t = threadIdx.x;
+    for (long long tk = blockIdx.y; tk < tiles_k; tk += gridDim.y) {
+        const long long k0 = tk * kSplitTile;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int q = t + 256 * j;
+            const int kk = q >> 4, nn = (q & 15) * 4;
+            const long long k = k0 + kk, n = n0 + nn;
+            float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (k < rows) {
+                const float* sp = src + k * lds + n;
+                if (vec && n + 3 < cols) {
+                    v = *reinterpret_cast<const float4*>(sp);
+                } else {
+                    if (n < cols) v.x = sp[0];
+                    if (n + 1 < cols) v.y = sp[1];
+                    if (n + 2 < cols) v.z = sp[2];
+                    if (n + 3 < cols) v.w = sp[3];
+                }
+            }
+            tile[kk][nn] = v.x;
+            tile[kk][nn + 1] = v.y;
+            tile[kk][nn + 2] = v.z;
+            tile[kk][nn + 3] = v.w;
         }
         __syncthreads();
-        for (int r = threadIdx.y; r < 32; r += blockDim.y) {
-            const int n = n0 + r, k = k0 + threadIdx.x;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int q = t + 256 * j;
+            const int nn = q >> 4, kk = (q & 15) * 4;
+            const long long n = n0 + nn, k = k0 + kk;
             if (n < cols && k < ldd) {
-                const float x = tile[threadIdx.x][r];
-                const float h = to_tf32(x);
-                const long long o = static_cast<long long>(n) * ldd + k;
-                hiT[o] = h;
-                loT[o] = to_tf32(x - h);
+                float h[4], l[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float x = tile[kk + e][nn];
+                    h[e] = to_tf32(x);
+                    l[e] = to_tf32(x - h[e]);
+                }
+                const long long o = n * ldd + k;
+                *reinterpret_cast<float4*>(hiT + o) = make_float4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<float4*>(loT + o) = make_float4(l[0], l[1], l[2], l[3]);
             }
         }
         __syncthreads();
@@ -499,7 +534,6 @@ int run_3xtf32(int opa, int opb, int64_t M, int64_t N, int64_t K, float alpha, c
     float* a_lo = reinterpret_cast<float*>(ws + a_pad);
     float* b_hi = reinterpret_cast<float*>(ws + 2 * a_pad);
     float* b_lo = reinterpret_cast<float*>(ws + 2 * a_pad + b_pad);
-    const int sms = dev->sm_count;
     // Each split writes a K-major (rows x kp) hi/lo pair: a row-wise split
     // of an operand already stored K-major (A, or a transposed B), a
     // transposing split otherwise (B, or a transposed A).
@@ -513,9 +547,11 @@ int run_3xtf32(int opa, int opb, int64_t M, int64_t N, int64_t K, float alpha, c
                                                            static_cast<int>(K), vec);
     };
     auto split_transposed = [&](const float* X, int64_t ldx, float* hi, float* lo, int64_t cols) {
-        split_transpose_kernel<<<16 * sms, dim3(32, 8), 0, stream>>>(X, ldx, hi, lo, kp,
-                                                                     static_cast<int>(K),
-                                                                     static_cast<int>(cols));
+        const int64_t tiles_k = (kp + kSplitTile - 1) / kSplitTile;
+        const dim3 grid(static_cast<unsigned>((cols + kSplitTile - 1) / kSplitTile),
+                        static_cast<unsigned>(tiles_k < 65535 ? tiles_k : 65535));
+        split_transpose_kernel<<<grid, 256, 0, stream>>>(X, ldx, hi, lo, kp, static_cast<int>(K),
+                                                         static_cast<int>(cols));
     };
     cudaError_t e;
     if (opa) split_transposed(A, lda, a_hi, a_lo, M);
