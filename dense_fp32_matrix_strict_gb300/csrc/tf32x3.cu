@@ -32,6 +32,7 @@
 //              C = alpha * acc + beta * C, then release the accumulator.
 //   Every wait is bounded; all roles meet at one exit where the MMA thread
 //   has waited for its MMAs and warp 1 frees the TMEM.
+#include <atomic>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -477,13 +478,16 @@ int tile_width(const DeviceInfo*) {
 template <class T>
 cudaError_t launch(const DeviceInfo* dev, const float* a_hi, const float* a_lo, const float* b_hi,
                    const float* b_lo, int64_t kp, Params p, cudaStream_t stream) {
-    static bool attr_set[64] = {};
-    if (!attr_set[dev->device]) {
+    // Once per device (device_info admits indexes below 64). Host threads
+    // that race here both set the same attribute, which is harmless; the
+    // flag itself is atomic.
+    static std::atomic<bool> attr_set[64] = {};
+    if (!attr_set[dev->device].load(std::memory_order_acquire)) {
         const cudaError_t e = cudaFuncSetAttribute(tf32x3_kernel<T>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    T::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        attr_set[dev->device] = true;
+        attr_set[dev->device].store(true, std::memory_order_release);
     }
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     CUtensorMap mah, mal, mbh, mbl;
