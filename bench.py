@@ -428,8 +428,8 @@ def run_ours(args, w):
         tf32_peak = bf16 * (1.1 / 2.25)      # nominal TF32 : BF16 dense ratio
         tf32_rate = 3.0 * flops / (ms3 * 1e-3) / 1e12
         t3, t3_note = (None, None)
-        if os.environ.get("SGEMM_3XTF32_TILE", "128x128") == "128x128":
-            t3, t3_note = recorded_traffic("tf32x3_kernel<TcCfg<128,3>>", w.name, "tf32x3")
+        if os.environ.get("SGEMM_3XTF32_TILE", "128x128c2") == "128x128c2" and w.N > 128:
+            t3, t3_note = recorded_traffic("tf32x3_kernel<TcCfg<128,3,2>>", w.name, "tf32x3")
         tf32x3 = {"value": replica_throughput(flops, ms3, world), "unit": "GFLOP/s",
                   "ms_per_step": ms3, "steps": n3,
                   "note": "sgemm_3xtf32: A, B split into TF32 hi/lo, 3 tcgen05 MMAs per product, "

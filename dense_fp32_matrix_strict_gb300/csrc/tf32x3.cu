@@ -19,7 +19,11 @@
 //   2. tf32_split_transpose: B (K x N, ldb) -> B_hi^T, B_lo^T (N x Kp): the
 //      MMA takes both operands K-major.
 //   3. tf32x3_kernel: persistent, one CTA per SM, 128 x BN output tiles
-//      (BN = 128 with a 3-stage ring by default, 256 with 2 stages).
+//      (BN = 128 with a 3-stage ring by default, 256 with 2 stages). By
+//      default the CTAs run in clusters of two on neighbouring tiles of one
+//      tile row: each TMA-loads one of the row's A_hi / A_lo tiles multicast
+//      into both CTAs, and each MMA thread releases a stage in both CTAs, so
+//      A comes from L2 once per pair.
 //      warp 0: TMA producer (one thread) filling the ring, each stage the
 //              128 x 32 A_hi/A_lo and BN x 32 B_hi/B_lo tiles (64 or 96 KB,
 //              128-byte swizzle);
@@ -53,9 +57,14 @@ constexpr int A_BYTES = BM * BK * 4;        // 16 KB
 
 // Tile width BN (the MMA's N) and ring depth. Two accumulators of BN TMEM
 // columns each, so the epilogue of one tile overlaps the MMAs of the next.
-template <int BN_, int STAGES_>
+// CL: CTAs per thread-block cluster. With CL = 2 the two CTAs of a cluster
+// work on neighbouring tiles of one tile row (columns 2j and 2j + 1) and
+// share its A: each loads one of A_hi / A_lo and multicasts it into both
+// CTAs' stage, so A is read from L2 once per pair instead of twice.
+template <int BN_, int STAGES_, int CL_ = 1>
 struct TcCfg {
-    static constexpr int BN = BN_, STAGES = STAGES_;
+    static constexpr int BN = BN_, STAGES = STAGES_, CL = CL_;
+    static_assert(CL == 1 || CL == 2, "CTAs per cluster");
     static constexpr int B_BYTES = BN * BK * 4;
     static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
@@ -104,6 +113,25 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b
     asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
                  "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
                  :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+
+// The same arrive, on the barrier at offset bar in every CTA of the cluster
+// named in mask (bit r: CTA rank r).
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+                 " [%0], %1;" :: "r"(bar), "h"(mask) : "memory");
+}
+
+// 2-D TMA tile load multicast to the same shared-memory offset (dst, and the
+// barrier bar that counts the bytes) in every CTA of the cluster named in
+// mask. x * 4 bytes is a multiple of 16 (x is a multiple of BK).
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* desc, uint32_t bar,
+                                               int32_t x, int32_t y, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar), "r"(x), "r"(y), "h"(mask)
+        : "memory");
 }
 
 // Arrive once on bar when every tcgen05.mma this thread issued has completed.
@@ -285,7 +313,9 @@ tf32x3_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, 1);
+            // With CL = 2 a stage is free once both CTAs' MMAs have read
+            // it: the multicast A halves land in both.
+            mbar_init(empty0 + 8 * s, T::CL);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf0 + 8 * b, 1);
@@ -303,8 +333,19 @@ tf32x3_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ 
     __syncthreads();
     fence_after();
     const uint32_t tmem = *tmem_slot;
+    // The peer's multicast copies and commits target this CTA's barriers:
+    // both CTAs initialise theirs before either issues one.
+    if (T::CL > 1) cluster_sync();
 
-    const int num_tiles = p.tiles_m * p.tiles_n;
+    // Work items: tiles, or with CL = 2 pairs of horizontally adjacent
+    // tiles, one per CTA of the cluster (a CTA whose tile lies past the last
+    // column loads zeros and writes nothing, but still loads its A half).
+    const int rank = T::CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    const int first_item = T::CL > 1 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+    const int item_step = static_cast<int>(gridDim.x) / T::CL;
+    Params q = p;
+    if (T::CL > 1) q.tiles_n = (p.tiles_n + 1) / 2;
+    const int num_tiles = q.tiles_m * q.tiles_n;
     if (warp == 0) {
         if (lane == 0) {
             tma_prefetch_desc(&tmAh);
@@ -315,9 +356,10 @@ tf32x3_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ 
             uint32_t ph = 0;
             int issued = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            for (int t = first_item; t < num_tiles && ok; t += item_step) {
                 int tm, tn;
-                tile_of(t, p, tm, tn);
+                tile_of(t, q, tm, tn);
+                tn = tn * T::CL + rank;
                 for (int kt = 0; kt < p.k_tiles; ++kt) {
                     if (!wait_bar(empty0 + 8 * s, ph ^ 1u, p, STATUS_PRODUCER_TIMEOUT)) {
                         ok = false;
@@ -326,8 +368,14 @@ tf32x3_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ 
                     const uint32_t full = full0 + 8 * s;
                     const uint32_t st = s0 + s * STAGE_BYTES;
                     mbar_arrive_expect_tx(full, STAGE_BYTES);
-                    tma_load_2d(st, &tmAh, full, kt * BK, tm * BM);
-                    tma_load_2d(st + A_BYTES, &tmAl, full, kt * BK, tm * BM);
+                    if (T::CL > 1) {
+                        // Rank 0 brings A_hi, rank 1 A_lo, each into both CTAs.
+                        tma_load_2d_mc(st + rank * A_BYTES, rank ? &tmAl : &tmAh, full, kt * BK,
+                                       tm * BM, 0x3);
+                    } else {
+                        tma_load_2d(st, &tmAh, full, kt * BK, tm * BM);
+                        tma_load_2d(st + A_BYTES, &tmAl, full, kt * BK, tm * BM);
+                    }
                     tma_load_2d(st + 2 * A_BYTES, &tmBh, full, kt * BK, tn * BN);
                     tma_load_2d(st + 2 * A_BYTES + B_BYTES, &tmBl, full, kt * BK, tn * BN);
                     ++issued;
@@ -351,7 +399,7 @@ tf32x3_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ 
             uint32_t ph = 0;
             int it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++it) {
+            for (int t = first_item; t < num_tiles && ok; t += item_step, ++it) {
                 const int b = it & 1;
                 const uint32_t acc_phase = static_cast<uint32_t>((it >> 1) & 1);
                 // Wait until the epilogue has emptied this accumulator.
@@ -377,7 +425,9 @@ tf32x3_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ 
                         mma_tf32(d, ah + off, bl + off, T::IDESC, 1u);
                         mma_tf32(d, al + off, bh + off, T::IDESC, 1u);
                     }
-                    mma_commit(empty0 + 8 * s);          // stage free once these finish
+                    // Stage free once these finish (in both CTAs with CL = 2).
+                    if (T::CL > 1) mma_commit_mc(empty0 + 8 * s, 0x3);
+                    else mma_commit(empty0 + 8 * s);
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
@@ -389,23 +439,24 @@ tf32x3_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ 
         }
     } else {
         // Epilogue warpgroup: warp w reads TMEM lanes 32 (w % 4) .. + 31.
-        const int q = warp & 3;
+        const int wq = warp & 3;
         int it = 0;
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
+        for (int t = first_item; t < num_tiles; t += item_step, ++it) {
             const int b = it & 1;
             const uint32_t acc_phase = static_cast<uint32_t>((it >> 1) & 1);
             if (!wait_bar(accf0 + 8 * b, acc_phase, p, STATUS_CONSUMER_TIMEOUT)) break;
             __syncwarp();          // tcgen05.ld is warp-collective: reconverge first
             fence_after();
             int tm, tn;
-            tile_of(t, p, tm, tn);
-            const int m = tm * BM + 32 * q + lane;
+            tile_of(t, q, tm, tn);
+            tn = tn * T::CL + rank;
+            const int m = tm * BM + 32 * wq + lane;
             const bool row_ok = m < p.M;
             float* crow = p.C + static_cast<long long>(row_ok ? m : 0) * p.ldc;
             const bool use_c = p.beta != 0.0f;
             for (int ch = 0; ch < BN / 32; ++ch) {
                 float v[32];
-                tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) +
+                tmem_ld32(tmem + (static_cast<uint32_t>(32 * wq) << 16) +
                               static_cast<uint32_t>(b * BN + ch * 32), v);
                 if (!row_ok) continue;
                 const int n0 = tn * BN + ch * 32;
@@ -452,6 +503,10 @@ tf32x3_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ 
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
                      :: "r"(tmem), "r"(TMEM_COLS) : "memory");
     }
+    // No CTA leaves while its peer may still multicast into its shared
+    // memory or arrive on its barriers; every role of both CTAs gets here
+    // (all of their waits are bounded).
+    if (T::CL > 1) cluster_sync();
 }
 
 bool encode(CUtensorMap* map, const float* base, int64_t rows, int64_t cols, int64_t ld, int box_rows,
@@ -465,14 +520,25 @@ bool encode(CUtensorMap* map, const float* base, int64_t rows, int64_t cols, int
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Tile width of the tensor-core kernel: 128 (default) or 256, from the
-// environment variable SGEMM_3XTF32_TILE ("128x128" or "128x256").
-int tile_width(const DeviceInfo*) {
-    static const int w = [] {
+// Kernel variant. By default clusters of two CTAs that share A by multicast
+// (128 x 128 tiles, 3 stages) wherever a tile row holds two tiles, else one
+// CTA per tile. The environment variable SGEMM_3XTF32_TILE forces one:
+// "128x128c2", "128x128" (one CTA per tile) or "128x256" (2 stages).
+// Measured on GB300 (clusters against single CTAs, same box, interleaved):
+// 4096^3 0.571 against 0.581 ms, 8192x14336x4096 3.52 against 3.58 ms,
+// 4093x5120x1531 0.322 against 0.380 ms, 2048^3 even.
+enum { VARIANT_AUTO = 0, VARIANT_WIDE = 1, VARIANT_PAIR = 2, VARIANT_SINGLE = 3 };
+
+int tile_variant(const DeviceInfo*) {
+    static const int v = [] {
         const char* env = std::getenv("SGEMM_3XTF32_TILE");
-        return (env != nullptr && std::strcmp(env, "128x256") == 0) ? 256 : 128;
+        if (env == nullptr) return static_cast<int>(VARIANT_AUTO);
+        if (std::strcmp(env, "128x256") == 0) return static_cast<int>(VARIANT_WIDE);
+        if (std::strcmp(env, "128x128c2") == 0) return static_cast<int>(VARIANT_PAIR);
+        if (std::strcmp(env, "128x128") == 0) return static_cast<int>(VARIANT_SINGLE);
+        return static_cast<int>(VARIANT_AUTO);
     }();
-    return w;
+    return v;
 }
 
 template <class T>
@@ -495,10 +561,38 @@ cudaError_t launch(const DeviceInfo* dev, const float* a_hi, const float* a_lo, 
           encode(&mbh, b_hi, p.N, p.K, kp, T::BN, enc) && encode(&mbl, b_lo, p.N, p.K, kp, T::BN, enc)))
         return cudaErrorInvalidValue;
     p.tiles_n = (p.N + T::BN - 1) / T::BN;
-    const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
-    const int grid = static_cast<int>(tiles < dev->sm_count ? tiles : dev->sm_count);
-    tf32x3_kernel<T><<<grid, THREADS, T::SMEM_BYTES, stream>>>(mah, mal, mbh, mbl, p);
-    return cudaGetLastError();
+    if (T::CL == 1) {
+        const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+        const int grid = static_cast<int>(tiles < dev->sm_count ? tiles : dev->sm_count);
+        tf32x3_kernel<T><<<grid, THREADS, T::SMEM_BYTES, stream>>>(mah, mal, mbh, mbl, p);
+        return cudaGetLastError();
+    }
+    // Clusters of T::CL CTAs, as many as the GPU runs at once (a cluster
+    // sits whole in one GPC), each a persistent worker over tile pairs.
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = T::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = T::CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    static std::atomic<int> max_clusters[64] = {};
+    int ncl = max_clusters[dev->device].load(std::memory_order_relaxed);
+    if (ncl <= 0) {
+        cfg.gridDim = dim3(T::CL);
+        const cudaError_t e = cudaOccupancyMaxActiveClusters(&ncl, tf32x3_kernel<T>, &cfg);
+        if (e != cudaSuccess) return e;
+        if (ncl <= 0) return cudaErrorInvalidConfiguration;
+        max_clusters[dev->device].store(ncl, std::memory_order_relaxed);
+    }
+    const int64_t items = static_cast<int64_t>(p.tiles_m) * ((p.tiles_n + T::CL - 1) / T::CL);
+    const int clusters = static_cast<int>(items < ncl ? items : ncl);
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * T::CL));
+    return cudaLaunchKernelEx(&cfg, tf32x3_kernel<T>, mah, mal, mbh, mbl, p);
 }
 
 }  // namespace tf32x3
@@ -583,9 +677,19 @@ int run_3xtf32(int opa, int opb, int64_t M, int64_t N, int64_t K, float alpha, c
         p.beta = beta;
         p.timeout_ns = wait_timeout_ns();
         p.status = status;
-        const bool wide = tile_width(dev) == 256;
-        e = wide ? launch<TcCfg<256, 2>>(dev, a_hi, a_lo, b_hi, b_lo, kp, p, stream)
-                 : launch<TcCfg<128, 3>>(dev, a_hi, a_lo, b_hi, b_lo, kp, p, stream);
+        int v = tile_variant(dev);
+        if (v == VARIANT_AUTO) v = N > 128 ? VARIANT_PAIR : VARIANT_SINGLE;
+        switch (v) {
+            case VARIANT_WIDE:
+                e = launch<TcCfg<256, 2>>(dev, a_hi, a_lo, b_hi, b_lo, kp, p, stream);
+                break;
+            case VARIANT_PAIR:
+                e = launch<TcCfg<128, 3, 2>>(dev, a_hi, a_lo, b_hi, b_lo, kp, p, stream);
+                break;
+            default:
+                e = launch<TcCfg<128, 3>>(dev, a_hi, a_lo, b_hi, b_lo, kp, p, stream);
+                break;
+        }
     }
     cudaFreeAsync(w, stream);
     if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);

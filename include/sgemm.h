@@ -295,6 +295,10 @@ SGEMM_API int sgemm_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stre
  * NaN, so an output the definition makes +-inf comes out NaN (NaN inputs
  * still give NaN).
  *
+ * Where a tile row of C holds two 128 x 128 tiles (N > 128) the kernel's CTAs
+ * run in thread-block clusters of two that share each A tile by TMA
+ * multicast; the result is the same bit for bit.
+ *
  * Each call splits A and the transpose of B into a workspace of
  * 8 * (M + N) * K bytes (K rounded up to 4) taken from the library's
  * stream-ordered pool, so it allocates like sgemm's stream-K tail; if that

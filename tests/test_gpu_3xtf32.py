@@ -104,3 +104,49 @@ def test_workloads_sampled(name):
     rep = oracle.check(C[rows, cols], ref, S, w.K)
     assert rep["ok"], rep
     assert np.all(np.isfinite(C))
+
+
+_SINGLE_CTA_CHILD = r"""
+import sys
+import numpy as np
+import torch
+import dense_fp32_matrix_strict_gb300 as sg
+from dense_fp32_matrix_strict_gb300 import inputs
+M, N, K = (int(v) for v in sys.argv[1:4])
+A = inputs.fill("normal", 620, inputs.TID_A, M, K)
+B = inputs.fill("normal", 620, inputs.TID_B, K, N)
+C0 = inputs.fill("normal", 620, inputs.TID_C, M, N)
+dC = torch.from_numpy(C0).cuda()
+sg.sgemm_3xtf32_tensors(0.7, torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda(), -1.3, dC)
+sg.check_status()
+np.save(sys.argv[4], dC.cpu().numpy())
+"""
+
+
+@pytest.mark.parametrize("shape", [(300, 640, 500), (513, 1025, 100)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_cluster_pairs_give_the_single_cta_bits(shape, tmp_path):
+    # The default kernel runs CTAs in clusters of two that share A tiles by
+    # multicast; each tile still sees the same MMAs in the same order as with
+    # one CTA per tile (forced in a child process by SGEMM_3XTF32_TILE).
+    import os
+    import subprocess
+    import sys
+    import torch
+    M, N, K = shape
+    A = inputs.fill("normal", 620, inputs.TID_A, M, K)
+    B = inputs.fill("normal", 620, inputs.TID_B, K, N)
+    C0 = inputs.fill("normal", 620, inputs.TID_C, M, N)
+    dC = torch.from_numpy(C0).cuda()
+    sg.sgemm_3xtf32_tensors(0.7, torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda(), -1.3, dC)
+    sg.check_status()
+    pair = dC.cpu().numpy()
+    out = str(tmp_path / "single.npy")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, SGEMM_3XTF32_TILE="128x128", PYTHONPATH=root)
+    subprocess.run([sys.executable, "-c", _SINGLE_CTA_CHILD, str(M), str(N), str(K), out],
+                   check=True, env=env, cwd=root, timeout=300)
+    single = np.load(out)
+    assert np.array_equal(pair, single)
+    ref, S = oracle.sgemm_ref(0.7, A, B, -1.3, C0)
+    assert oracle.check(pair, ref, S, K)["ok"]
