@@ -574,7 +574,8 @@ def run_ours(args, w):
         line["cublas_fp32_context"] = cublas
     if world > 1:
         torch.distributed.destroy_process_group()
-    if not args.no_cpu_baseline:
+    # The CPU oracle baseline is a single-GPU figure: rank 0 times it at N = 1 only.
+    if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(w, A, B, C0, args.cpu_rows)
     print(json.dumps(line), flush=True)
 
