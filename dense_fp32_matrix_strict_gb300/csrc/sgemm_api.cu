@@ -630,7 +630,13 @@ int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, 
     const double t_main = 2.0 * mk * static_cast<double>(N) / 66e12;
     const double copy_cost = 5e-6 + 8.0 * mk / 6e12;
     const bool copy_ok = !pl->a_t && allow_pack && !force_cp;
-    const bool xp_auto = xp_possible && fi != 2;
+    // The transposer warps add a step between a stage landing and its use,
+    // which a work item of fewer than 4 k-iterations does not hide: 256^3 in
+    // clusters of 4 CTAs (2 k-iterations each) took 11.0 us with it and
+    // 10.3 us reading the row-major A (GB300); from 8 k-iterations on the
+    // two were even or the transpose ahead (640^3: 21.3 against 22.6 us).
+    const int64_t item_kt = ((K + 31) / 32 + fam->cs - 1) / fam->cs;
+    const bool xp_auto = xp_possible && fi != 2 && item_kt >= 4;
     pl->a_pre = false;
     pl->a_xp = false;
     if (cfg.at == 1) {

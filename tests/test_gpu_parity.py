@@ -91,8 +91,9 @@ def test_tma_chosen_only_when_aligned():
     # worth an aligned copy, so they take cp.async.
     A, B, C0 = gen(128, 128, 256, seed=8)
     _, _, plan = gpu_util.run(1.0, A, B, 0.0, C0)
-    # Both by TMA; an aligned A is transposed in shared memory ("Axp").
-    assert "Axp_Btma" in plan[0] and "pack" not in plan[0], plan
+    # Both by TMA in place (A row-major, "Atma", or transposed in shared
+    # memory, "Axp"), no packing copy.
+    assert ("Axp_Btma" in plan[0] or "Atma_Btma" in plan[0]) and "pack" not in plan[0], plan
     _, _, plan = gpu_util.run(1.0, A, B, 0.0, C0, lda=257)
     assert "Acp_Btma" in plan[0], plan
     _, _, plan = gpu_util.run(1.0, A, B, 0.0, C0, offsets=(0, 1, 0))
@@ -253,7 +254,8 @@ def _workload(name, full):
 
 def test_workload_sq256_uniform():
     rep, plan = _workload("sq256_uniform", full=True)
-    assert plan[0] == "ws_64x64x32_s4_k4_c4_Axp_Btma", plan   # a tile per 4-CTA cluster
+    # A tile per 4-CTA cluster, 2 k-iterations each: A read row-major in place.
+    assert plan[0] == "ws_64x64x32_s4_k4_c4_Atma_Btma", plan
 
 
 def test_workload_sq1024_int_bit_exact():
@@ -709,7 +711,9 @@ def test_in_smem_transpose_with_stream_k(shape):
 
 def test_auto_a_path_by_size():
     # Large: the transposed copy of A pays. Medium and small: the in-smem
-    # transpose. An A TMA cannot read in place: the copy where it pays.
+    # transpose, unless a CTA's work item has under 4 k-iterations (256^3 in
+    # clusters of 4), where A is read row-major in place. An A TMA cannot
+    # read in place: the copy where it pays.
     torch = pytest.importorskip("torch")
     def plan(M, N, K, lda=None):
         A = torch.empty(M, lda or K, device="cuda")[:, :K]
@@ -718,5 +722,6 @@ def test_auto_a_path_by_size():
         return sg.plan_tensors(1.0, A, B, 0.0, C)[0]
     assert "_ATtma_Btma+packAT" in plan(4096, 4096, 4096)
     assert "_Axp_Btma" in plan(2048, 2048, 2048)
-    assert "_Axp_Btma" in plan(256, 256, 256)
+    assert "_Atma_Btma" in plan(256, 256, 256)
+    assert "_Axp_Btma" in plan(640, 640, 640)
     assert "_ATtma_Btma+packAT" in plan(2048, 2048, 2047, lda=2047)
