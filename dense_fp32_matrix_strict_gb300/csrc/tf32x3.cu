@@ -14,9 +14,9 @@
 // failing the FP32 tolerance) and do not describe a split.
 //
 // Steps per call (all on the caller's stream):
-//   1. tf32_split_rows: A (M x K, lda) -> A_hi, A_lo (M x Kp, Kp = K rounded
+//   1. split_rows_kernel: A (M x K, lda) -> A_hi, A_lo (M x Kp, Kp = K rounded
 //      up to 4), K-major as A already is.
-//   2. tf32_split_transpose: B (K x N, ldb) -> B_hi^T, B_lo^T (N x Kp): the
+//   2. split_transpose_kernel: B (K x N, ldb) -> B_hi^T, B_lo^T (N x Kp): the
 //      MMA takes both operands K-major.
 //   3. tf32x3_kernel: persistent, one CTA per SM, 128 x BN output tiles
 //      (BN = 128 with a 3-stage ring by default, 256 with 2 stages). By
