@@ -4,12 +4,11 @@
 // sgemm allocates on a device twice in its life: a status word (cudaMalloc,
 // on the first call) and, for problems whose last wave of tiles is split
 // across the SMs, a stream-K workspace (cudaMallocFromPoolAsync, per call).
-// Some callers cannot allow either: code running while a stream is being
-// captured into a CUDA graph in global capture mode (where cudaMalloc is
-// forbidden), programs whose device memory is owned by another allocator
-// that must account for every byte, and real-time paths that may not take
-// an allocator's locks. sgemm_noalloc serves them: it runs the same kernels
-// with the same schedule, but its status word and stream-K partial sums
+// Some callers cannot allow either: programs whose device memory is owned
+// by another allocator that must account for every byte, and real-time
+// paths that may not take an allocator's locks. sgemm_noalloc serves them:
+// it runs the same kernels with the same schedule, but its status word and
+// stream-K partial sums
 // live in one fixed scratch array compiled into this file.
 //
 // The scratch is a file-scope __device__ array of kScratchBytes (32 MiB).

@@ -320,10 +320,9 @@ SGEMM_API int sgemm_3xtf32_ex(int opa, int opb, int64_t M, int64_t N, int64_t K,
  * sgemm_noalloc — the same operation, arguments, results and errors as
  * sgemm, for callers that must not allocate device memory. The pages this
  * library follows have no counterpart: it exists for code that cannot call
- * cudaMalloc or a pool allocator — work recorded while a stream is captured
- * into a CUDA graph in global capture mode, programs whose device memory is
- * owned by another allocator, and latency-critical paths that may not take
- * an allocator's locks. sgemm allocates a status word on its first call on a
+ * cudaMalloc or a pool allocator: programs whose device memory is owned by
+ * another allocator that must account for every byte, and latency-critical
+ * paths that may not take an allocator's locks. sgemm allocates a status word on its first call on a
  * device and a stream-K workspace for some problems; sgemm_noalloc instead
  * uses one fixed 32 MiB scratch array compiled into the library (held by
  * every GPU that loads the library until the process exits).

@@ -1,9 +1,8 @@
 """sgemm_noalloc: the SGEMM entry point that allocates no device memory.
 
-Callers such as code recorded into a CUDA graph under global stream capture,
-programs whose device memory belongs to another allocator, or latency-bound
-paths that may not take an allocator's locks cannot let the library call
-cudaMalloc or a pool allocator. sgemm_noalloc runs the same kernels with the
+Callers such as programs whose device memory belongs to another allocator,
+or latency-bound paths that may not take an allocator's locks, cannot let the
+library call cudaMalloc or a pool allocator. sgemm_noalloc runs the same kernels with the
 same schedule but keeps its status word and stream-K partial sums in a fixed
 scratch array inside the library.
 
