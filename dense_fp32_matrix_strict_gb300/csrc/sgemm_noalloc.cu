@@ -8,8 +8,8 @@
 // by another allocator that must account for every byte, and real-time
 // paths that may not take an allocator's locks. sgemm_noalloc serves them:
 // it runs the same kernels with the same schedule, but its status word and
-// stream-K partial sums
-// live in one fixed scratch array compiled into this file.
+// stream-K partial sums live in one fixed scratch array compiled into this
+// file.
 //
 // The scratch is a file-scope __device__ array of kScratchBytes (32 MiB).
 // Every GPU that loads this library's module holds it until the process
