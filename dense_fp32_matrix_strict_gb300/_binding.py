@@ -26,8 +26,11 @@ EXPORTED_SYMBOLS = (
     "sgemm_plan", "sgemm_set_config", "sgemm_set_wait_timeout_ns", "sgemm_fp32_peak",
     "sgemm_selftest_wait_timeout", "sgemm_config_names", "sgemm_noalloc", "sgemm_3xtf32",
     "sgemm_set_shape_config", "sgemm_clear_shape_configs", "sgemm_ex", "sgemm_plan_ex",
-    "sgemm_3xtf32_ex", "sgemm_host",
+    "sgemm_3xtf32_ex", "sgemm_host", "sgemm_noalloc_check_status", "sgemm_fp32_peak_ex",
+    "sgemm_null_launch",
 )
+
+SGEMM_PEAK_FFMA, SGEMM_PEAK_FFMA2 = 0, 1
 
 SGEMM_OP_N, SGEMM_OP_T = 0, 1
 
@@ -91,6 +94,12 @@ def load():
         lib.sgemm_selftest_wait_timeout.restype = ci
         lib.sgemm_noalloc.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
         lib.sgemm_noalloc.restype = ci
+        lib.sgemm_noalloc_check_status.argtypes = [vp, ctypes.POINTER(ci)]
+        lib.sgemm_noalloc_check_status.restype = ci
+        lib.sgemm_fp32_peak_ex.argtypes = [ci, ctypes.c_double, f64p, f64p, f64p, vp]
+        lib.sgemm_fp32_peak_ex.restype = ci
+        lib.sgemm_null_launch.argtypes = [vp]
+        lib.sgemm_null_launch.restype = ci
         lib.sgemm_3xtf32.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
         lib.sgemm_3xtf32.restype = ci
         lib.sgemm_ex.argtypes = [ci, ci, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
@@ -124,6 +133,13 @@ def sgemm_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int
     """sgemm without any device allocation (fixed scratch inside the library);
     device pointers as ints; returns the raw code."""
     return load().sgemm_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def sgemm_noalloc_check_status(stream=0):
+    """Returns (code, bits) of the scratch status word sgemm_noalloc writes."""
+    bits = ctypes.c_int(0)
+    rc = load().sgemm_noalloc_check_status(stream, ctypes.byref(bits))
+    return rc, bits.value
 
 
 def sgemm_3xtf32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
@@ -209,6 +225,19 @@ def sgemm_fp32_peak(target_ms: float = 200.0, stream=0):
     rc = load().sgemm_fp32_peak(float(target_ms), ctypes.byref(g), ctypes.byref(m),
                                 ctypes.byref(f), stream)
     return rc, g.value, m.value, f.value
+
+
+def sgemm_fp32_peak_ex(form: int, target_ms: float = 200.0, stream=0):
+    """Returns (code, gflops, ms, flops) of the chosen instruction form."""
+    g, m, f = ctypes.c_double(0), ctypes.c_double(0), ctypes.c_double(0)
+    rc = load().sgemm_fp32_peak_ex(int(form), float(target_ms), ctypes.byref(g),
+                                   ctypes.byref(m), ctypes.byref(f), stream)
+    return rc, g.value, m.value, f.value
+
+
+def sgemm_null_launch(stream=0) -> int:
+    """One empty kernel on `stream` (the launch-latency floor); raw code."""
+    return load().sgemm_null_launch(stream)
 
 
 def sgemm_selftest_wait_timeout(timeout_ns: int, stream=0) -> int:
@@ -384,11 +413,12 @@ def check_status(stream=None, device=None) -> int:
     return bits
 
 
-def fp32_peak(target_ms: float = 200.0, stream=None, device=None):
-    """Measured FP32 FFMA ceiling: dict(gflops, ms, flops)."""
+def fp32_peak(target_ms: float = 200.0, stream=None, device=None, form: int = SGEMM_PEAK_FFMA):
+    """Measured FP32 ceiling in one instruction form (SGEMM_PEAK_FFMA or
+    SGEMM_PEAK_FFMA2): dict(gflops, ms, flops)."""
     import torch
     dev = device if device is not None else torch.cuda.current_device()
     with torch.cuda.device(dev):
-        rc, g, m, f = sgemm_fp32_peak(target_ms, _stream_handle(stream, dev))
-    _check("sgemm_fp32_peak", rc)
+        rc, g, m, f = sgemm_fp32_peak_ex(form, target_ms, _stream_handle(stream, dev))
+    _check("sgemm_fp32_peak_ex", rc)
     return {"gflops": g, "ms": m, "flops": f}

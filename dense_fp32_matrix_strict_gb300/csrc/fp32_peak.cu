@@ -1,13 +1,18 @@
-// fp32_peak.cu — pure-FFMA microbenchmark: the device's measured FP32 ceiling.
+// fp32_peak.cu — pure-FMA microbenchmark: the device's measured FP32 ceiling.
 //
 // The Tinyforge README measures its card's real FP32 rate with a pure-FMA
 // kernel (6,884 GFLOPS against a 9,100 GFLOPS datasheet figure) and quotes
 // every GEMM result as a fraction of that. This is the same measurement for
-// sm_103a: every thread keeps kChains independent FFMA dependency chains so
-// that each SM sub-partition can issue one FFMA per clock; the loop body is
-// kUnroll x kChains FFMAs against two loop-control instructions. The result
-// is stored only under a condition the host never makes true, so the chains
-// stay live without memory traffic.
+// sm_103a, in the two instruction forms the GEMM kernels can issue:
+//   * FFMA  (form 0): every thread keeps kChains independent scalar FFMA
+//     dependency chains, so each SM sub-partition can issue one FFMA per
+//     clock;
+//   * FFMA2 (form 1): the same with kChains independent chains of the packed
+//     fma.rn.f32x2 (two IEEE single-precision FMAs, each rounded once, in
+//     one instruction), the form the SGEMM's inner loop uses.
+// The loop body is kUnroll x kChains FMA instructions against two
+// loop-control instructions. The result is stored only under a condition the
+// host never makes true, so the chains stay live without memory traffic.
 #include <cstdint>
 
 #include <cuda_runtime.h>
@@ -27,6 +32,9 @@ constexpr int kCtasPerSm = 8;
 
 __device__ float g_peak_sink[kThreads];
 
+// Does nothing: the launch-latency floor every kernel of a call pays.
+__global__ void null_kernel() {}
+
 __global__ void __launch_bounds__(kThreads)
 fp32_peak_kernel(float mul, float add, long long iters, int sink_key) {
     float x[kChains];
@@ -44,10 +52,34 @@ fp32_peak_kernel(float mul, float add, long long iters, int sink_key) {
     if (static_cast<int>(blockIdx.x) == sink_key) g_peak_sink[threadIdx.x] = s;
 }
 
+// The packed form: kChains chains of float2, one fma.rn.f32x2 per chain and
+// step (two FMAs).
+__global__ void __launch_bounds__(kThreads)
+fp32_peak2_kernel(float mul, float add, long long iters, int sink_key) {
+    float2 x[kChains];
+#pragma unroll
+    for (int c = 0; c < kChains; ++c) {
+        const float v = 1.0f + 1e-3f * static_cast<float>(threadIdx.x + c);
+        x[c] = make_float2(v, v + 5e-4f);
+    }
+    const float2 m2 = make_float2(mul, mul), a2 = make_float2(add, add);
+    for (long long it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+            for (int c = 0; c < kChains; ++c) x[c] = __ffma2_rn(x[c], m2, a2);
+    }
+    float s = 0.0f;
+#pragma unroll
+    for (int c = 0; c < kChains; ++c) s += x[c].x + x[c].y;
+    if (static_cast<int>(blockIdx.x) == sink_key) g_peak_sink[threadIdx.x] = s;
+}
+
 }  // namespace
 
-extern "C" int sgemm_fp32_peak(double target_ms, double* gflops, double* ms, double* flops,
-                               cudaStream_t stream) {
+extern "C" int sgemm_fp32_peak_ex(int form, double target_ms, double* gflops, double* ms,
+                                  double* flops, cudaStream_t stream) {
+    if (form != SGEMM_PEAK_FFMA && form != SGEMM_PEAK_FFMA2) return SGEMM_ERR_INVALID_VALUE;
     if (!(target_ms >= 1.0) || target_ms > 60000.0) return SGEMM_ERR_INVALID_VALUE;
     int rc = sgemm_internal_device_ready();
     if (rc != SGEMM_OK) return rc;
@@ -66,7 +98,10 @@ extern "C" int sgemm_fp32_peak(double target_ms, double* gflops, double* ms, dou
     auto run = [&](long long iters, float* out_ms) -> cudaError_t {
         cudaError_t err = cudaEventRecord(e0, stream);
         if (err != cudaSuccess) return err;
-        fp32_peak_kernel<<<grid, kThreads, 0, stream>>>(mul, add, iters, no_sink);
+        if (form == SGEMM_PEAK_FFMA2)
+            fp32_peak2_kernel<<<grid, kThreads, 0, stream>>>(mul, add, iters, no_sink);
+        else
+            fp32_peak_kernel<<<grid, kThreads, 0, stream>>>(mul, add, iters, no_sink);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
         if ((err = cudaEventRecord(e1, stream)) != cudaSuccess) return err;
         if ((err = cudaEventSynchronize(e1)) != cudaSuccess) return err;
@@ -88,8 +123,10 @@ extern "C" int sgemm_fp32_peak(double target_ms, double* gflops, double* ms, dou
         if ((e = run(want, &t)) != cudaSuccess || (e = run(want, &t)) != cudaSuccess) {
             result = SGEMM_ERR_LAUNCH;
         } else {
-            const double f = 2.0 * kChains * kUnroll * static_cast<double>(want) *
-                             static_cast<double>(grid) * kThreads;
+            // 2 FLOP per FMA; an FFMA2 instruction performs two FMAs.
+            const double fmas_per_instr = form == SGEMM_PEAK_FFMA2 ? 2.0 : 1.0;
+            const double f = 2.0 * fmas_per_instr * kChains * kUnroll *
+                             static_cast<double>(want) * static_cast<double>(grid) * kThreads;
             if (gflops) *gflops = f / (static_cast<double>(t) * 1e-3) / 1e9;
             if (ms) *ms = t;
             if (flops) *flops = f;
@@ -99,4 +136,19 @@ extern "C" int sgemm_fp32_peak(double target_ms, double* gflops, double* ms, dou
     cudaEventDestroy(e0);
     cudaEventDestroy(e1);
     return result;
+}
+
+extern "C" int sgemm_fp32_peak(double target_ms, double* gflops, double* ms, double* flops,
+                               cudaStream_t stream) {
+    return sgemm_fp32_peak_ex(SGEMM_PEAK_FFMA, target_ms, gflops, ms, flops, stream);
+}
+
+extern "C" int sgemm_null_launch(cudaStream_t stream) {
+    null_kernel<<<1, 32, 0, stream>>>();
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        sgemm_internal_set_cuda_error(static_cast<int>(e));
+        return SGEMM_ERR_LAUNCH;
+    }
+    return SGEMM_OK;
 }

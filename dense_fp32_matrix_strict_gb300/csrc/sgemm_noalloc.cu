@@ -22,9 +22,12 @@
 // All calls on a device share the array and it keeps the last call's
 // contents: every partial-sum slot a launch reads was written earlier in the
 // same launch, so nothing needs clearing per call; the status word is zero
-// when the module loads. Calls that overlap on the GPU (for example on two
-// streams without ordering between them) race on the array and may produce
-// wrong results: serialise them.
+// when the module loads, collects the time-out bits of every later call, and
+// is read and cleared by sgemm_noalloc_check_status (a copy to a host
+// variable and a memset on the caller's stream, nothing allocated). Calls
+// that overlap on the GPU (for example on two streams without ordering
+// between them) race on the array and may produce wrong results: serialise
+// them.
 #include <cstddef>
 #include <cstdint>
 #include <mutex>
@@ -98,4 +101,23 @@ extern "C" int sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alpha, const
     int* status = reinterpret_cast<int*>(scratch);
     float* ws = pl.ws_bytes > 0 ? reinterpret_cast<float*>(scratch + kScratchStatusBytes) : nullptr;
     return launch_plan(&pl, status, ws, stream);
+}
+
+extern "C" int sgemm_noalloc_check_status(cudaStream_t stream, int* bits) {
+    const DeviceInfo* dev = nullptr;
+    int rc = device_info(&dev);
+    if (rc != SGEMM_OK) return rc;
+    unsigned char* scratch = nullptr;
+    if ((rc = scratch_address(dev->device, &scratch)) != SGEMM_OK) return rc;
+    int* status = reinterpret_cast<int*>(scratch);
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_CUDA);
+    int v = 0;
+    if ((e = cudaMemcpyAsync(&v, status, sizeof(int), cudaMemcpyDeviceToHost, stream)) !=
+            cudaSuccess ||
+        (e = cudaMemsetAsync(status, 0, sizeof(int), stream)) != cudaSuccess ||
+        (e = cudaStreamSynchronize(stream)) != cudaSuccess)
+        return cuda_fail(e, SGEMM_ERR_CUDA);
+    if (bits != nullptr) *bits = v;
+    return v != 0 ? SGEMM_ERR_DEVICE_TIMEOUT : SGEMM_OK;
 }

@@ -270,6 +270,31 @@ SGEMM_API int sgemm_set_wait_timeout_ns(uint64_t ns);
 SGEMM_API int sgemm_fp32_peak(double target_ms, double* gflops, double* ms, double* flops,
                     cudaStream_t stream);
 
+/* Instruction forms of the ceiling microbenchmark. */
+#define SGEMM_PEAK_FFMA 0    /* scalar FFMA chains (what sgemm_fp32_peak runs)        */
+#define SGEMM_PEAK_FFMA2 1   /* packed fma.rn.f32x2 chains, the form the SGEMM issues */
+
+/*
+ * sgemm_fp32_peak_ex — sgemm_fp32_peak in a chosen instruction form. With
+ * SGEMM_PEAK_FFMA2 every thread runs 8 independent chains of the packed
+ * two-lane FMA (two single-rounding FP32 FMAs per instruction, 4 FLOP), the
+ * instruction the SGEMM's inner loop is built from, so the ceiling is
+ * measured on what the GEMM actually issues. Same grid, calibration, timing,
+ * outputs and blocking as sgemm_fp32_peak; a form other than the two above
+ * returns SGEMM_ERR_INVALID_VALUE.
+ */
+SGEMM_API int sgemm_fp32_peak_ex(int form, double target_ms, double* gflops, double* ms,
+                                 double* flops, cudaStream_t stream);
+
+/*
+ * sgemm_null_launch — enqueue one kernel that does nothing (one CTA of 32
+ * threads) on `stream`. Timed like a call, it gives the launch-latency floor
+ * below which no call of this library can go on the device; the small
+ * problems (256^3) are measured against it. Returns SGEMM_ERR_LAUNCH if the
+ * launch fails (no device, for instance).
+ */
+SGEMM_API int sgemm_null_launch(cudaStream_t stream);
+
 /*
  * sgemm_selftest_wait_timeout — launch one CTA whose bounded mbarrier wait
  * can never be satisfied (nothing arrives) with a limit of timeout_ns, to
@@ -337,11 +362,28 @@ SGEMM_API int sgemm_3xtf32_ex(int opa, int opb, int64_t M, int64_t N, int64_t K,
  * if the problem's stream-K workspace would not fit in the scratch (never on
  * a 152-SM GB300, which needs at most 19.5 MB). Time-outs of bounded waits
  * inside its kernels are recorded in the scratch, not in the word that
- * sgemm_check_status reads.
+ * sgemm_check_status reads: sgemm_noalloc_check_status reads and clears
+ * them.
  */
 SGEMM_API int sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
                             int64_t lda, const float* B, int64_t ldb, float beta, float* C,
                             int64_t ldc, cudaStream_t stream);
+
+/*
+ * sgemm_noalloc_check_status — sgemm_check_status for sgemm_noalloc: it
+ * synchronises `stream`, then reads and clears the status word kept in the
+ * fixed scratch of the current device, where the kernels sgemm_noalloc
+ * launches record bounded-wait time-outs. It allocates nothing (the copy
+ * goes to a host variable of the call). Returns SGEMM_OK,
+ * SGEMM_ERR_DEVICE_TIMEOUT if a kernel launched by sgemm_noalloc since the
+ * last check gave up on a wait (its output is then incomplete), or
+ * SGEMM_ERR_CUDA if the synchronisation or the copy failed. If `bits` is not
+ * NULL it receives the raw status bits, with the meaning sgemm_check_status
+ * gives them. Like sgemm_noalloc, a first call on a device looks up the
+ * scratch address; the check itself should not overlap a running
+ * sgemm_noalloc on another stream.
+ */
+SGEMM_API int sgemm_noalloc_check_status(cudaStream_t stream, int* bits);
 
 #ifdef __cplusplus
 }

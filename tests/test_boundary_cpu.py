@@ -158,3 +158,25 @@ def test_transposed_leading_dimensions_follow_the_stored_shape(lib):
     assert sg.sgemm_plan_ex(0, 0, 8, 4, 4, 1.0, A_PTR, 4, B_PTR, 4, 0.0, C_PTR, 4)[0] != \
         sg.SGEMM_ERR_INVALID_VALUE
     assert sg.sgemm_ex(1, 1, 0, 4, 4, 1.0, A_PTR, 1, B_PTR, 4, 0.0, C_PTR, 4, 0) == sg.SGEMM_OK
+
+
+def test_ceiling_forms_and_noalloc_status_without_gpu(lib):
+    # An unknown instruction form or a bad target is refused before any
+    # device work; the valid forms need a device and report a CUDA error here.
+    assert sg.sgemm_fp32_peak_ex(2, 10.0)[0] == sg.SGEMM_ERR_INVALID_VALUE
+    assert sg.sgemm_fp32_peak_ex(-1, 10.0)[0] == sg.SGEMM_ERR_INVALID_VALUE
+    assert sg.sgemm_fp32_peak_ex(sg.SGEMM_PEAK_FFMA2, 0.5)[0] == sg.SGEMM_ERR_INVALID_VALUE
+    for form in (sg.SGEMM_PEAK_FFMA, sg.SGEMM_PEAK_FFMA2):
+        rc = sg.sgemm_fp32_peak_ex(form, 10.0)[0]
+        assert rc not in (sg.SGEMM_OK, sg.SGEMM_ERR_INVALID_VALUE)
+    # The scratch status check needs the device's scratch address: without a
+    # device it returns an error (never SGEMM_OK) and leaves `bits` alone;
+    # a NULL `bits` is accepted.
+    rc, bits = sg.sgemm_noalloc_check_status(0)
+    assert rc not in (sg.SGEMM_OK, sg.SGEMM_ERR_DEVICE_TIMEOUT) and bits == 0
+    assert sg.load().sgemm_noalloc_check_status(None, None) not in (
+        sg.SGEMM_OK, sg.SGEMM_ERR_DEVICE_TIMEOUT)
+
+
+def test_null_launch_without_gpu_is_a_launch_error(lib):
+    assert sg.sgemm_null_launch(0) == sg.SGEMM_ERR_LAUNCH
