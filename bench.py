@@ -24,13 +24,23 @@ oracle timed on this host on a row block of the same problem.
 accumulation, same error bound) on the same workload, with its own roofline
 against the TF32 tensor peak.
 
+``workloads`` (one GPU only) reports all five synthetic workloads the same
+way: GFLOP/s, the fractions of the measured ceiling and of the datasheet
+rate, the plan, the clocks seen while each was timed, the 3xTF32 path and
+cuBLAS FP32 as context, and each workload's CPU oracle timed on this host
+(the whole problem; for the 8192 x 14336 x 4096 projection a 256-row block
+plus the 65,536 sampled entries, with the full-problem time extrapolated;
+single-thread rows for 256^3 and 1024^3). The 256^3 entry also carries the
+launch-latency floor (one empty kernel, timed the same way).
+
 ``--impl reference`` times that CPU oracle instead (the reference arm): each
 step is a bounded row block of the workload.
 
 With --gpus N > 1 (launched by torchrun) every rank runs an independent
 replica of the workload (the problem is single-GPU; there is no collective
 on the data path); ``value`` is the sum over ranks of the work divided by
-the slowest rank's time.
+the slowest rank's time. The 3xTF32 leg never runs then: its CTA pairs
+share A tiles by TMA multicast, which is kept to one-GPU runs.
 """
 from __future__ import annotations
 
@@ -54,7 +64,7 @@ L2_BYTES = 129 * 1024 * 1024
 FP32_LANES_PER_SM = 128
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
@@ -70,10 +80,23 @@ def parse():
                     help="skip the cuBLAS FP32 context measurement")
     ap.add_argument("--cpu-rows", type=int, default=0,
                     help="rows of C in the CPU baseline sample (0: sized to ~10 s)")
-    return ap.parse_args()
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the five-workload report")
+    return ap.parse_args(argv)
 
 
 # ---------------------------------------------------------------------------
+THROTTLE_NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+def summarise_clocks(sm, mx, power, reasons, how):
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "sampler": how}
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "sm_mhz_min": min(sm),
+            "samples": len(sm), "power_w_max": max(power) if power else None,
+            "reasons": sorted(reasons), "sampler": how}
+
+
 class ClockSampler:
     """nvidia-smi sampling of SM clock and throttle reasons (every 200 ms)."""
 
@@ -114,7 +137,6 @@ class ClockSampler:
             self.proc.kill()
         self.t.join(timeout=5)
         sm, mx, power, reasons = [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
@@ -125,13 +147,107 @@ class ClockSampler:
                 power.append(float(parts[3]))
             except ValueError:
                 continue
-            for name, val in zip(names, parts[5:9]):
+            for name, val in zip(THROTTLE_NAMES, parts[5:9]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "power_w_max": max(power) if power else None, "reasons": sorted(reasons)}
+        return summarise_clocks(sm, mx, power, reasons, "nvidia-smi every 200 ms")
+
+
+class NvmlSampler:
+    """In-process NVML reads of the SM clock, its maximum, board power and
+    the clock-event (throttle) reasons every `period_s` (5 ms), so that even
+    a timed region of a few tens of milliseconds gets samples. Read-only: it
+    changes no setting. Raises OSError from the constructor when NVML or the
+    device cannot be found (the caller then falls back to nvidia-smi)."""
+
+    # nvmlClocksEventReason* bits
+    BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+            "hw_thermal_slowdown": 0x40}
+    NVML_CLOCK_SM = 1
+
+    def __init__(self, torch_index: int, period_s: float = 0.005):
+        import ctypes
+        self.ct = ctypes
+        self.period = period_s
+        lib = None
+        for name in ("libnvidia-ml.so.1", "libnvidia-ml.so"):
+            try:
+                lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        if lib is None or lib.nvmlInit_v2() != 0:
+            raise OSError("NVML unavailable")
+        self.lib = lib
+        self.h = ctypes.c_void_p()
+        if not self._handle(torch_index):
+            raise OSError("NVML device not found")
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        self.samples = []
+        self.stop_evt = threading.Event()
+        self.t = None
+
+    def _handle(self, torch_index):
+        import torch
+        props = torch.cuda.get_device_properties(torch_index)
+        uuid = getattr(props, "uuid", None)
+        if uuid is not None:
+            u = str(uuid)
+            u = u if u.startswith("GPU-") else "GPU-" + u
+            if self.lib.nvmlDeviceGetHandleByUUID(u.encode(), self.ct.byref(self.h)) == 0:
+                return True
+        bus = getattr(props, "pci_bus_id", None)
+        if bus is not None:
+            pci = "%08X:%02X:%02X.0" % (getattr(props, "pci_domain_id", 0), bus,
+                                        getattr(props, "pci_device_id", 0))
+            if self.lib.nvmlDeviceGetHandleByPciBusId_v2(pci.encode(),
+                                                        self.ct.byref(self.h)) == 0:
+                return True
+        return False
+
+    def _one(self):
+        ct = self.ct
+        sm, mx, pw, rs = ct.c_uint(0), ct.c_uint(0), ct.c_uint(0), ct.c_ulonglong(0)
+        if self.lib.nvmlDeviceGetClockInfo(self.h, self.NVML_CLOCK_SM, ct.byref(sm)) != 0:
+            return None
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.NVML_CLOCK_SM, ct.byref(mx))
+        self.lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(pw))
+        self.reasons_fn(self.h, ct.byref(rs))
+        return float(sm.value), float(mx.value), pw.value / 1000.0, int(rs.value)
+
+    def _run(self):
+        while not self.stop_evt.is_set():
+            v = self._one()
+            if v is not None:
+                self.samples.append(v)
+            self.stop_evt.wait(self.period)
+
+    def start(self):
+        self.t = threading.Thread(target=self._run, daemon=True)
+        self.t.start()
+        return self
+
+    def stop(self):
+        self.stop_evt.set()
+        if self.t is not None:
+            self.t.join(timeout=5)
+        v = self._one()          # one reading at the very end as well
+        if v is not None:
+            self.samples.append(v)
+        sm = [x[0] for x in self.samples]
+        mx = [x[1] for x in self.samples]
+        power = [x[2] for x in self.samples]
+        reasons = {n for x in self.samples for n, b in self.BITS.items() if x[3] & b}
+        return summarise_clocks(sm, mx, power, reasons, "NVML every 5 ms")
+
+
+def clock_sampler(torch_index: int):
+    """An NVML sampler where NVML is available, else nvidia-smi."""
+    try:
+        return NvmlSampler(torch_index)
+    except (OSError, AttributeError, ImportError):
+        return ClockSampler(torch_index)
 
 
 # ---------------------------------------------------------------------------
@@ -209,8 +325,58 @@ def cpu_baseline(w, A, B, C0, rows: int):
         rows = int(min(w.M, max(1, 10.0 * rate / (2.0 * w.N * w.K))))
     dt, fl = cpu_oracle_rows(w, A, B, C0, rows)
     return {"value": fl / dt / 1e9, "unit": "GFLOP/s", "cores": threads, "kind": "oracle",
+            "seconds": dt, "rows": min(rows, w.M),
             "sample": f"first {min(rows, w.M)} of {w.M} rows of C (all N={w.N}, K={w.K}), "
                       f"{fl / 1e9:.1f} GFLOP in {dt:.2f} s, double accumulation, OpenMP"}
+
+
+# Workloads whose CPU oracle also runs on one thread (the T4 article's CPU
+# column is a single-threaded triple loop), and the row block the oracle
+# times where the whole problem would take minutes.
+SINGLE_THREAD_WORKLOADS = ("sq256_uniform", "sq1024_int")
+CPU_FULL_LIMIT_FLOP = 200e9      # above this: a 256-row block + the sampled entries
+CPU_BLOCK_ROWS = 256
+
+
+def workload_cpu_baseline(w, A, B, C0, full=None):
+    """The CPU oracle on workload `w`, on this host's cores.
+
+    The whole problem when it is at most 200 GFLOP (``full``: an already
+    measured ``cpu_baseline`` dict of the whole problem, reused); otherwise a
+    256-row block and the 65,536 seeded sampled entries (plus the last row and
+    column) the parity tests check, with the full-problem time extrapolated
+    from the block's rate. Single-threaded too for 256^3 and 1024^3."""
+    import oracle
+    from dense_fp32_matrix_strict_gb300 import inputs
+    oracle.build()
+    threads = oracle.num_threads()
+    if w.flops <= CPU_FULL_LIMIT_FLOP:
+        out = dict(full) if full is not None else cpu_baseline(w, A, B, C0, w.M)
+        out["sample"] = f"the whole problem ({w.M} x {w.N} x {w.K}), " + out["sample"]
+        out["extrapolated"] = False
+    else:
+        dt, fl = cpu_oracle_rows(w, A, B, C0, CPU_BLOCK_ROWS)
+        rows, cols = inputs.sample_entries(w.M, w.N)
+        c0 = C0 if w.beta != 0 else None
+        t0 = time.perf_counter()
+        oracle.sgemm_ref_sampled(w.alpha, A, B, w.beta, c0, rows, cols)
+        ds = time.perf_counter() - t0
+        fs = 2.0 * w.K * rows.shape[0]
+        out = {"value": fl / dt / 1e9, "unit": "GFLOP/s", "cores": threads, "kind": "oracle",
+               "seconds": dt, "extrapolated": True,
+               "full_problem_seconds_extrapolated": w.flops / (fl / dt),
+               "sampled_entries": int(rows.shape[0]), "sampled_seconds": ds,
+               "sampled_gflops": fs / ds / 1e9,
+               "sample": f"rows 0..{CPU_BLOCK_ROWS - 1} of {w.M} (all N={w.N}, K={w.K}), "
+                         f"{fl / 1e9:.1f} GFLOP in {dt:.2f} s; plus the {rows.shape[0]} "
+                         f"sampled entries the parity tests check ({ds:.2f} s); the "
+                         f"full-problem time ({w.flops / (fl / dt):.0f} s) is extrapolated "
+                         f"from the block's rate"}
+    if w.name in SINGLE_THREAD_WORKLOADS:
+        dt1, fl1 = cpu_oracle_rows(w, A, B, C0, w.M, nthreads=1)
+        out["single_thread"] = {"value": fl1 / dt1 / 1e9, "unit": "GFLOP/s", "cores": 1,
+                                "seconds": dt1, "ms_per_call": 1e3 * dt1}
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -289,9 +455,192 @@ def config_of(w, kernel, grid):
     return cfg
 
 
+def tf32x3_allowed(args, world: int) -> bool:
+    """Whether this run times the 3xTF32 entry point: one-GPU runs only. Its
+    default kernel runs CTA pairs that share A tiles by TMA multicast (within
+    the calling GPU's own workspace); that load is kept out of every run on
+    two or more GPUs, whatever the flags say."""
+    return (not args.no_tf32x3) and world == 1
+
+
+def time_per_call(torch, stream, fn, n: int, flush=None, each: bool = False) -> float:
+    """Mean device milliseconds of fn() over n calls on `stream`, by CUDA
+    events on that stream: one pair around all n calls, or one pair around
+    each call alone when `each` is set or `flush` (a buffer larger than L2)
+    is given; the flush buffer is then filled before every call, outside its
+    events."""
+    if flush is None and not each:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    for a, b in evs:
+        if flush is not None:
+            flush.zero_()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs) / n
+
+
+def lib_call(lib, name, args_):
+    rc = getattr(lib, name)(*args_)
+    if rc != 0:
+        import dense_fp32_matrix_strict_gb300 as sg
+        raise sg.SgemmError(name, rc)
+
+
+def measure_3xtf32(args, world, lib, call, torch, stream, flush, w, n):
+    """The separately reported tcgen05 3xTF32 path on the same operands, or
+    None where it must not run (see tf32x3_allowed)."""
+    if not tf32x3_allowed(args, world):
+        return None
+    import dense_fp32_matrix_strict_gb300 as sg
+    for _ in range(3):
+        lib_call(lib, "sgemm_3xtf32", call)
+    torch.cuda.synchronize()
+    ms3 = time_per_call(torch, stream, lambda: lib_call(lib, "sgemm_3xtf32", call), n, flush)
+    sg.check_status()
+    mp_ = measured_peaks()
+    bf16 = float(mp_.get("bf16_tflops") or 1900.0)
+    tf32_peak = bf16 * (1.1 / 2.25)      # nominal TF32 : BF16 dense ratio
+    tf32_rate = 3.0 * w.flops / (ms3 * 1e-3) / 1e12
+    t3, t3_note = (None, None)
+    if os.environ.get("SGEMM_3XTF32_TILE", "128x128c2") == "128x128c2" and w.N > 128:
+        t3, t3_note = recorded_traffic("tf32x3_kernel<TcCfg<128,3,2>>", w.name, "tf32x3")
+    return {"value": w.flops / (ms3 * 1e-3) / 1e9, "unit": "GFLOP/s", "ms_per_step": ms3,
+            "steps": n,
+            "note": "sgemm_3xtf32: A, B split into TF32 hi/lo, 3 tcgen05 MMAs per product, "
+                    "FP32 accumulation in TMEM; same FP32 error bound; times include the "
+                    "split pre-passes" + ("; L2 flushed before each call, outside its events"
+                                          if flush is not None else ""),
+            "roofline": {"bound": "tensor", "achieved": tf32_rate, "peak": tf32_peak,
+                         "unit": "TFLOP/s", "frac": tf32_rate / tf32_peak,
+                         "peak_basis": f"measured bf16 {bf16:.1f} TFLOP/s x 1.1/2.25 "
+                                       "(nominal TF32:BF16 dense ratio)",
+                         "achieved_basis": "3 x 2MNK TF32 FLOP per step / step time",
+                         "traffic": t3, "traffic_note": t3_note},
+            "gpu_launches_per_step": 3}
+
+
+def measure_cublas(torch, stream, dA, dB, dC, w, n, flush):
+    """Context only, not part of the product: cuBLAS FP32 (torch.addmm with
+    TF32 off) on the same operands, timed the same way on the same stream."""
+    prev_tf32 = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        out = torch.empty_like(dC)
+
+        def f():
+            torch.addmm(dC, dA, dB, beta=w.beta, alpha=w.alpha, out=out)
+
+        for _ in range(3):
+            f()
+        torch.cuda.synchronize()
+        msc = time_per_call(torch, stream, f, n, flush)
+        del out
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev_tf32
+    return {"value": w.flops / (msc * 1e-3) / 1e9, "unit": "GFLOP/s", "ms_per_step": msc,
+            "steps": n,
+            "note": "context only: torch.addmm FP32 with TF32 off (cuBLAS), same operands "
+                    "and stream, L2 handled as in the timed region"}
+
+
+def alg_bytes_of(w) -> int:
+    """The algorithmic minimum of HBM bytes one call moves: A and B read
+    once, C written once (and read once when beta != 0)."""
+    return 4 * (w.M * w.K + w.K * w.N + w.M * w.N * (2 if w.beta != 0 else 1))
+
+
+def launches_of(kernel: str) -> int:
+    """Kernels one sgemm call enqueues: the SGEMM kernel, plus the stream-K
+    fixup and any operand packing copy."""
+    return 1 + sum(kernel.count(tag) for tag in ("+sk", "+packA", "+packB"))
+
+
+def workload_report(args, lib, torch, stream, dev, w, host, ceiling, datasheet, headline=None):
+    """One entry of the five-workload report (GPU side) on the host inputs
+    `host` = (A, B, C0). `headline`: the already timed numbers of this
+    workload from the main timed region."""
+    import dense_fp32_matrix_strict_gb300 as sg
+    A, B, C0 = host
+    dA = torch.from_numpy(A).cuda()
+    dB = torch.from_numpy(B).cuda()
+    dC = torch.from_numpy(C0).cuda()
+    nbytes = 4 * (w.M * w.K + w.K * w.N + w.M * w.N)
+    flush = None
+    if nbytes <= L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+    kernel, grid = sg.plan_tensors(w.alpha, dA, dB, w.beta, dC)
+    call = (w.M, w.N, w.K, float(w.alpha), dA.data_ptr(), w.K, dB.data_ptr(), w.N,
+            float(w.beta), dC.data_ptr(), w.N, stream.cuda_stream)
+
+    def step():
+        lib_call(lib, "sgemm", call)
+
+    if headline is None:
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        probe = time_per_call(torch, stream, step, 3, flush)
+        n = int(min(400, max(20, 0.15 / max(probe * 1e-3, 1e-7))))
+        clk = clock_sampler(dev).start()
+        ms = time_per_call(torch, stream, step, n, flush)
+        clocks = clk.stop()
+        sg.check_status()
+    else:
+        ms, n, clocks = headline["ms"], headline["steps"], headline["clocks"]
+    gflops = w.flops / (ms * 1e-3) / 1e9
+    entry = {
+        "M": w.M, "N": w.N, "K": w.K, "alpha": w.alpha, "beta": w.beta,
+        "dist": f"A~{w.dist_a}, B~{w.dist_b}, C0~{w.dist_c}", "seed": w.seed,
+        "kernel": kernel, "grid": grid, "gpu_launches_per_call": launches_of(kernel),
+        "gflops": gflops, "ms_per_call": ms, "steps": n,
+        "frac_of_measured_fp32_ceiling": gflops / ceiling,
+        "frac_of_datasheet_fp32": gflops / datasheet,
+        "hbm_achieved_gbs": alg_bytes_of(w) / (ms * 1e-3) / 1e9,
+        "algorithmic_bytes": alg_bytes_of(w),
+        "l2": ("inputs larger than L2, no flush" if flush is None else
+               "L2 flushed (258 MB fill) before every call, outside the call's events"),
+        "clocks": clocks,
+        "parity": ("bit-exact against the oracle (integer inputs)" if w.exact else
+                   "every element within 4K 2^-24 S + 1e-6 of the oracle" if w.full_check else
+                   "65,536 sampled entries + last row and column within the bound") +
+                  " (tests/test_gpu_parity.py, same plan)",
+    }
+    if w.name == "sq256_uniform":
+        # The launch-latency floor, timed the same way (L2 flush, events).
+        floor_fn = lambda: lib_call(lib, "sgemm_null_launch", (stream.cuda_stream,))
+        for _ in range(3):
+            floor_fn()
+        entry["latency_floor_ms"] = time_per_call(torch, stream, floor_fn, n, flush)
+        entry["latency_floor_note"] = ("one empty kernel (sgemm_null_launch) between the same "
+                                       "event pair after the same L2 flush")
+    t3 = measure_3xtf32(args, 1, lib, call, torch, stream, flush, w, max(10, n // 4))
+    if t3 is not None:
+        entry["tcgen05_3xtf32_gflops"] = t3["value"]
+        entry["tcgen05_3xtf32_ms"] = t3["ms_per_step"]
+    if not args.no_cublas:
+        cb = measure_cublas(torch, stream, dA, dB, dC, w, max(10, n // 4), flush)
+        entry["cublas_fp32_context_gflops"] = cb["value"]
+        entry["cublas_fp32_context_ms"] = cb["ms_per_step"]
+    del dA, dB, dC, flush
+    torch.cuda.empty_cache()
+    return entry
+
+
 def run_ours(args, w):
     import torch
     import dense_fp32_matrix_strict_gb300 as sg
+    from dense_fp32_matrix_strict_gb300 import inputs
 
     world, rank, local = dist_env()
     if world > 1:
@@ -315,8 +664,7 @@ def run_ours(args, w):
     if nbytes_in <= L2_BYTES:
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
     kernel, grid = sg.plan_tensors(w.alpha, dA, dB, w.beta, dC)
-    # the SGEMM kernel, plus the stream-K fixup and any operand packing copy
-    launches_per_step = 1 + sum(kernel.count(tag) for tag in ("+sk", "+packA", "+packB"))
+    launches_per_step = launches_of(kernel)
 
     # The timed loop calls the C ABI directly: arguments are marshalled once.
     lib = sg.load()
@@ -326,21 +674,23 @@ def run_ours(args, w):
     def step():
         if flush is not None:
             flush.zero_()
-        rc = lib.sgemm(*call)
-        if rc != 0:
-            raise sg.SgemmError("sgemm", rc)
+        lib_call(lib, "sgemm", call)
 
-    # Measured FFMA ceiling, same process, right before the GEMM.
-    clk_peak = ClockSampler(dev).start()
-    peak = sg.fp32_peak(target_ms=args.peak_ms)
+    # Measured FP32 ceiling, same process, right before the GEMM, in both
+    # instruction forms (scalar FFMA and the packed FFMA2 the kernel issues);
+    # the higher is the metric's denominator.
+    clk_peak = clock_sampler(dev).start()
+    peak = sg.fp32_peak(target_ms=args.peak_ms, form=sg.SGEMM_PEAK_FFMA)
+    peak2 = sg.fp32_peak(target_ms=args.peak_ms, form=sg.SGEMM_PEAK_FFMA2)
     peak_clocks = clk_peak.stop()
+    ceiling = max(peak["gflops"], peak2["gflops"])
 
     for _ in range(max(args.warmup, 3)):
         step()
     sg.check_status()
 
     # Timed region: K steps between barriers + syncs.
-    clk = ClockSampler(dev).start()
+    clk = clock_sampler(dev).start()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -360,10 +710,8 @@ def run_ours(args, w):
         for i in range(args.steps):
             flush.zero_()
             step_ev[i][0].record(stream)
-            rc = lib.sgemm(*call)
+            lib_call(lib, "sgemm", call)
             step_ev[i][1].record(stream)
-            if rc != 0:
-                raise sg.SgemmError("sgemm", rc)
         t_end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -379,106 +727,24 @@ def run_ours(args, w):
     # events on the launching stream (covers the SGEMM kernel and, with the
     # stream-K tail, its fixup kernel).
     nev = max(10, min(args.steps, 100))
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(nev)]
-    for i in range(nev):
-        if flush is not None:
-            flush.zero_()
-        ev[i][0].record(stream)
-        rc = lib.sgemm(*call)
-        ev[i][1].record(stream)
-        if rc != 0:
-            raise sg.SgemmError("sgemm", rc)
-    torch.cuda.synchronize()
+    kernel_ms = time_per_call(torch, stream, lambda: lib_call(lib, "sgemm", call), nev, flush,
+                              each=True)
     sg.check_status()
-    launch_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = max_over_ranks(total_ms, world)
 
     flops = w.flops
     ms_step = total_ms / args.steps
-    kernel_ms = statistics.mean(launch_ms)
     value = replica_throughput(flops, ms_step, world)
 
-    # The tcgen05 3xTF32 path, reported separately (same workload, same
-    # FP32 error bound, different arithmetic unit).
-    tf32x3 = None
-    if not args.no_tf32x3:
-        call3 = call
-        for _ in range(3):
-            rc = lib.sgemm_3xtf32(*call3)
-            if rc != 0:
-                raise sg.SgemmError("sgemm_3xtf32", rc)
-        torch.cuda.synchronize()
-        n3 = max(10, args.steps // 5)
-        x0 = torch.cuda.Event(enable_timing=True)
-        x1 = torch.cuda.Event(enable_timing=True)
-        x0.record(stream)
-        for _ in range(n3):
-            if flush is not None:
-                flush.zero_()
-            rc = lib.sgemm_3xtf32(*call3)
-            if rc != 0:
-                raise sg.SgemmError("sgemm_3xtf32", rc)
-        x1.record(stream)
-        torch.cuda.synchronize()
-        sg.check_status()
-        ms3 = max_over_ranks(x0.elapsed_time(x1) / n3, world)
-        mp_ = measured_peaks()
-        bf16 = float(mp_.get("bf16_tflops") or 1900.0)
-        tf32_peak = bf16 * (1.1 / 2.25)      # nominal TF32 : BF16 dense ratio
-        tf32_rate = 3.0 * flops / (ms3 * 1e-3) / 1e12
-        t3, t3_note = (None, None)
-        if os.environ.get("SGEMM_3XTF32_TILE", "128x128c2") == "128x128c2" and w.N > 128:
-            t3, t3_note = recorded_traffic("tf32x3_kernel<TcCfg<128,3,2>>", w.name, "tf32x3")
-        tf32x3 = {"value": replica_throughput(flops, ms3, world), "unit": "GFLOP/s",
-                  "ms_per_step": ms3, "steps": n3,
-                  "note": "sgemm_3xtf32: A, B split into TF32 hi/lo, 3 tcgen05 MMAs per product, "
-                          "FP32 accumulation in TMEM; same FP32 error bound; times include the "
-                          "split pre-passes" + (" and the L2 flush" if flush is not None else ""),
-                  "roofline": {"bound": "tensor", "achieved": tf32_rate, "peak": tf32_peak,
-                               "unit": "TFLOP/s", "frac": tf32_rate / tf32_peak,
-                               "peak_basis": f"measured bf16 {bf16:.1f} TFLOP/s x 1.1/2.25 "
-                                             "(nominal TF32:BF16 dense ratio)",
-                               "achieved_basis": "3 x 2MNK TF32 FLOP per step / step time",
-                               "traffic": t3, "traffic_note": t3_note},
-                  "gpu_launches_per_step": 3}
-
-    # Context only, not part of the product: cuBLAS FP32 (torch.addmm with
-    # TF32 off) on the same operands, timed the same way on the same stream.
+    # The tcgen05 3xTF32 path, reported separately (same workload, same FP32
+    # error bound, different arithmetic unit); one-GPU runs only.
+    tf32x3 = measure_3xtf32(args, world, lib, call, torch, stream, flush, w,
+                            max(10, args.steps // 5))
     cublas = None
     if not args.no_cublas:
-        prev_tf32 = torch.backends.cuda.matmul.allow_tf32
-        torch.backends.cuda.matmul.allow_tf32 = False
-        try:
-            out = torch.empty_like(dC)
-            for _ in range(3):
-                torch.addmm(dC, dA, dB, beta=w.beta, alpha=w.alpha, out=out)
-            torch.cuda.synchronize()
-            nc = max(10, args.steps // 5)
-            # As in the timed region: with an L2 flush, events around each
-            # call only; otherwise one pair around all of them.
-            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(nc if flush is not None else 1)]
-            if flush is None:
-                evs[0][0].record(stream)
-            for i in range(nc):
-                if flush is not None:
-                    flush.zero_()
-                    evs[i][0].record(stream)
-                torch.addmm(dC, dA, dB, beta=w.beta, alpha=w.alpha, out=out)
-                if flush is not None:
-                    evs[i][1].record(stream)
-            if flush is None:
-                evs[0][1].record(stream)
-            torch.cuda.synchronize()
-            msc = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs) / nc, world)
-            cublas = {"value": replica_throughput(flops, msc, world), "unit": "GFLOP/s",
-                      "ms_per_step": msc, "steps": nc,
-                      "note": "context only: torch.addmm FP32 with TF32 off (cuBLAS), same "
-                              "operands and stream, L2 handled as in the timed region"}
-            del out
-        finally:
-            torch.backends.cuda.matmul.allow_tf32 = prev_tf32
+        cublas = measure_cublas(torch, stream, dA, dB, dC, w, max(10, args.steps // 5), flush)
+        cublas["ms_per_step"] = max_over_ranks(cublas["ms_per_step"], world)
+        cublas["value"] = replica_throughput(flops, cublas["ms_per_step"], world)
 
     # End to end through the C ABI with HOST buffers: sgemm_host copies A, B
     # (and C when beta != 0) in and C out, inside the timed region, every
@@ -494,23 +760,11 @@ def run_ours(args, w):
     d2h = 4 * w.M * w.N
     hcall = (w.M, w.N, w.K, w.alpha, hA.data_ptr(), w.K, hB.data_ptr(), w.N, w.beta,
              hOut.data_ptr(), w.N, int(stream.cuda_stream))
-
-    def e2e_step():
-        rc = lib.sgemm_host(*hcall)
-        if rc != 0:
-            raise sg.SgemmError("sgemm_host", rc)
-
     for _ in range(3):
-        e2e_step()
+        lib_call(lib, "sgemm_host", hcall)
     torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    e2e_ms = time_per_call(torch, stream, lambda: lib_call(lib, "sgemm_host", hcall),
+                           args.e2e_steps)
     e2e_ms = max_over_ranks(e2e_ms, world)
     sg.check_status()
 
@@ -524,10 +778,9 @@ def run_ours(args, w):
     datasheet = props.multi_processor_count * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e9
     achieved = flops / (kernel_ms * 1e-3) / 1e12
     traffic, traffic_note = recorded_traffic(kernel, w.name, "ffma", grid)
-    # The algorithmic minimum of HBM bytes one call moves: A and B read once,
-    # C written once (and read once when beta != 0). At the small sizes the
-    # path is latency-bound, and the HBM rate says how far from either roof.
-    alg_bytes = 4 * (w.M * w.K + w.K * w.N + w.M * w.N * (2 if w.beta != 0 else 1))
+    # At the small sizes the path is latency-bound, and the HBM rate says how
+    # far from either roof.
+    alg_bytes = alg_bytes_of(w)
     hbm_peak = float(mp.get("hbm_gbs") or 6800.0)
     hbm_achieved = alg_bytes / (kernel_ms * 1e-3) / 1e9
     line = {
@@ -535,17 +788,21 @@ def run_ours(args, w):
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": config_of(w, kernel, grid),
-        "frac_of_measured_fp32_ceiling": value / world / peak["gflops"],
+        "frac_of_measured_fp32_ceiling": value / world / ceiling,
         "frac_of_datasheet_fp32": value / world / datasheet,
-        "fp32_ceiling": {"measured_gflops": peak["gflops"], "ms": peak["ms"],
+        "fp32_ceiling": {"measured_gflops": ceiling,
+                         "ffma_gflops": peak["gflops"], "ffma_ms": peak["ms"],
+                         "ffma2_gflops": peak2["gflops"], "ffma2_ms": peak2["ms"],
+                         "basis": "the higher of the scalar FFMA and the packed FFMA2 "
+                                  "(fma.rn.f32x2) chain microbenchmarks, this process",
                          "clocks": peak_clocks, "datasheet_gflops": datasheet,
                          "datasheet_basis": f"{props.multi_processor_count} SMs x 128 FP32 lanes "
                                             f"x 2 FLOP x {sm_max:.0f} MHz"},
         "roofline": {"bound": "alu", "achieved": achieved, "peak": datasheet / 1e3,
                      "unit": "TFLOP/s", "frac": achieved / (datasheet / 1e3),
                      "peak_basis": "FP32 CUDA-core FFMA: SMs x 128 x 2 x max SM clock",
-                     "measured_ceiling": peak["gflops"] / 1e3,
-                     "frac_of_measured_ceiling": achieved / (peak["gflops"] / 1e3),
+                     "measured_ceiling": ceiling / 1e3,
+                     "frac_of_measured_ceiling": achieved / (ceiling / 1e3),
                      "kernel": kernel, "kernel_ms": kernel_ms,
                      "kernel_ms_covers": "every kernel of one sgemm call",
                      "traffic": traffic, "traffic_note": traffic_note,
@@ -570,13 +827,38 @@ def run_ours(args, w):
     }
     if tf32x3 is not None:
         line["tcgen05_3xtf32"] = tf32x3
+    elif world > 1 and not args.no_tf32x3:
+        line["tcgen05_3xtf32_skipped"] = ("not run on more than one GPU: its CTA pairs share "
+                                          "A tiles by TMA multicast")
     if cublas is not None:
         line["cublas_fp32_context"] = cublas
     if world > 1:
         torch.distributed.destroy_process_group()
-    # The CPU oracle baseline is a single-GPU figure: rank 0 times it at N = 1 only.
-    if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(w, A, B, C0, args.cpu_rows)
+    # The CPU oracle baseline and the five-workload report are single-GPU
+    # figures: rank 0 takes them at N = 1 only.
+    if world == 1:
+        del dA, dB, dC, hA, hB, hOut
+        torch.cuda.empty_cache()
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w, A, B, C0, args.cpu_rows)
+        report = {}
+        if not args.no_workloads:
+            for name, wl in inputs.WORKLOADS.items():
+                host = (A, B, C0) if name == w.name else wl.make()
+                head = ({"ms": ms_step, "steps": args.steps, "clocks": clocks}
+                        if name == w.name else None)
+                ent = workload_report(args, lib, torch, stream, dev, wl, host, ceiling,
+                                      datasheet, head)
+                if not args.no_cpu_baseline:
+                    full = None
+                    if name == w.name and line["cpu_baseline"]["rows"] == w.M:
+                        full = line["cpu_baseline"]
+                    ent["cpu_baseline"] = workload_cpu_baseline(wl, *host, full=full)
+                    ent["gpu_over_cpu_oracle"] = ent["gflops"] / ent["cpu_baseline"]["value"]
+                report[name] = ent
+                del host
+        if report:
+            line["workloads"] = report
     print(json.dumps(line), flush=True)
 
 

@@ -24,7 +24,9 @@ own):
 """
 from __future__ import annotations
 
+import concurrent.futures
 import dataclasses
+import os
 
 import numpy as np
 
@@ -71,27 +73,43 @@ def _int9(z):
 
 
 def fill(dist: str, seed: int, tid: int, rows: int, cols: int, sigma: float = 1.0,
-         chunk: int = 1 << 23) -> np.ndarray:
-    """A dense row-major float32 (rows x cols) matrix from stream (seed, tid)."""
+         chunk: int = 1 << 22) -> np.ndarray:
+    """A dense row-major float32 (rows x cols) matrix from stream (seed, tid).
+
+    Element e depends only on (seed, tid, e), so chunks are generated
+    independently, on several host threads for large matrices (numpy releases
+    the interpreter lock inside its array operations); the values do not
+    depend on the chunking or the thread count.
+    """
+    if dist not in ("zeros", "uniform", "int", "normal"):
+        raise ValueError(f"unknown distribution {dist!r}")
     n = rows * cols
     out = np.empty(n, dtype=np.float32)
     if dist == "zeros":
         out[:] = 0.0
         return out.reshape(rows, cols)
-    for s in range(0, n, chunk):
+
+    def one(s):
         m = min(n, s + chunk) - s
         if dist == "uniform":
             out[s:s + m] = _uniform(raw(seed, tid, m, offset=s))
         elif dist == "int":
             out[s:s + m] = _int9(raw(seed, tid, m, offset=s))
-        elif dist == "normal":
+        else:
             z = raw(seed, tid, 2 * m, offset=2 * s)
             u1 = ((z[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * 2.0 ** -53
             u2 = (z[1::2] >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
             out[s:s + m] = (sigma * np.sqrt(-2.0 * np.log(u1))
                             * np.cos(2.0 * np.pi * u2)).astype(np.float32)
-        else:
-            raise ValueError(f"unknown distribution {dist!r}")
+
+    starts = range(0, n, chunk)
+    if n <= chunk:
+        for s in starts:
+            one(s)
+    else:
+        workers = max(1, min(16, os.cpu_count() or 1, len(starts)))
+        with concurrent.futures.ThreadPoolExecutor(max_workers=workers) as ex:
+            list(ex.map(one, starts))
     return out.reshape(rows, cols)
 
 

@@ -47,3 +47,62 @@ def test_replica_throughput_counts_every_rank():
     one = bench.replica_throughput(2.0 * 4096 ** 3, 2.0, 1)
     assert abs(one - 2.0 * 4096 ** 3 / 2e-3 / 1e9) < 1e-6
     assert abs(bench.replica_throughput(2.0 * 4096 ** 3, 2.0, 8) - 8 * one) < 1e-6
+
+
+class _RecordingLib:
+    """Stands in for the CUDA library: records every entry point touched."""
+
+    def __init__(self):
+        self.calls = []
+
+    def __getattr__(self, name):
+        def entry(*args):
+            self.calls.append(name)
+            return 0
+        return entry
+
+
+def test_3xtf32_leg_never_runs_on_two_or_more_gpus():
+    # Its default kernel shares A tiles between CTA pairs by TMA multicast,
+    # which is kept out of every run on two or more GPUs.
+    from dense_fp32_matrix_strict_gb300 import inputs
+    w = inputs.WORKLOADS["sq4096_uniform"]
+    call = (w.M, w.N, w.K, 1.0, 1 << 20, w.K, 2 << 20, w.N, 0.0, 3 << 20, w.N, 0)
+    args = bench.parse([])
+    assert bench.tf32x3_allowed(args, 1)
+    assert not bench.tf32x3_allowed(bench.parse(["--no-tf32x3"]), 1)
+    for world in (2, 4, 8):
+        assert not bench.tf32x3_allowed(args, world)
+        lib = _RecordingLib()
+        out = bench.measure_3xtf32(args, world, lib, call, torch=None, stream=None, flush=None,
+                                   w=w, n=10)
+        assert out is None and lib.calls == []
+
+
+def test_only_the_guarded_leg_names_the_3xtf32_entry_points():
+    # Every use of sgemm_3xtf32* in bench.py sits inside measure_3xtf32, which
+    # returns before touching the library unless the run is on one GPU; the
+    # per-workload report that also calls it runs only when world == 1.
+    import inspect
+    src = inspect.getsource(bench)
+    leg = inspect.getsource(bench.measure_3xtf32)
+    assert src.count('"sgemm_3xtf32"') == leg.count('"sgemm_3xtf32"') > 0
+    assert "sgemm_3xtf32_ex" not in src
+    run = inspect.getsource(bench.run_ours)
+    assert "measure_3xtf32(args, world," in run
+    report_at = run.index("workload_report(")
+    assert run.rfind("if world == 1:", 0, report_at) >= 0
+
+
+def test_cpu_baseline_plan_per_workload():
+    # The whole problem for the four smaller workloads, a 256-row block plus
+    # the sampled entries (extrapolated) for the LLM projection; single-thread
+    # rows for 256^3 and 1024^3.
+    from dense_fp32_matrix_strict_gb300 import inputs
+    whole = [n for n, w in inputs.WORKLOADS.items() if w.flops <= bench.CPU_FULL_LIMIT_FLOP]
+    assert whole == ["sq256_uniform", "sq1024_int", "sq4096_uniform",
+                     "ragged_4093x5120x1531_normal"]
+    assert bench.SINGLE_THREAD_WORKLOADS == ("sq256_uniform", "sq1024_int")
+    assert bench.launches_of("ws_128x128x32_s4_ATtma_Btma+packAT+sk") == 3
+    assert bench.launches_of("ws_128x64x32_s4_k2_Axp_Btma") == 1
+    assert bench.alg_bytes_of(inputs.WORKLOADS["sq1024_int"]) == 4 * 1024 * 1024 * 4

@@ -1,7 +1,13 @@
 """The autotuning sweep on the GPU: every configuration it times must agree
-with the default one within the FP32 bound, and the per-shape rule it
-installs must change the plan of that shape only."""
+with the default one within the FP32 bound (the sweep's own self-consistency
+column) and with the CPU oracle on sampled entries (an independent check the
+test hands the sweep), and the per-shape rule it installs must change the
+plan of that shape only."""
+import numpy as np
 import pytest
+
+import oracle
+from dense_fp32_matrix_strict_gb300 import inputs
 
 import dense_fp32_matrix_strict_gb300 as sg
 from dense_fp32_matrix_strict_gb300 import autotune
@@ -30,14 +36,29 @@ def _plan(M, N, K):
     return sg.plan_tensors(1.0, A, B, 0.0, C)[0]
 
 
+def oracle_check(A, B, C):
+    """Worst |C - ref| / bound over 4,096 seeded entries (plus the last row
+    and column) against the CPU oracle, alpha = 1, beta = 0."""
+    M, K = A.shape
+    N = B.shape[1]
+    rows, cols = inputs.sample_entries(M, N, n=4096)
+    ref, S = oracle.sgemm_ref_sampled(1.0, A, B, 0.0, None, rows, cols)
+    got = C[rows, cols].astype(np.float64)
+    if not np.all(np.isfinite(got)):
+        return float("inf")
+    return float(np.max(np.abs(got - ref) / oracle.error_bound(K, S)))
+
+
 def test_sweep_rows_are_checked_and_one_is_best(tmp_path):
     shapes = [(300, 260, 200), (1024, 768, 512)]
     configs = autotune.all_configs()
-    rows = autotune.sweep(shapes, configs, reps=2, warmup=1)
+    rows = autotune.sweep(shapes, configs, reps=2, warmup=1, check=oracle_check)
     assert len(rows) == len(shapes) * len(configs)
     for r in rows:
         assert r["ok"] == 1, r
         assert r["ms"] > 0 and r["err_over_bound"] <= 1.0
+        # every configuration against the CPU oracle, not only against "auto"
+        assert r["ref_err_over_bound"] <= 1.0, r
     for s in shapes:
         assert sum(r["best"] for r in rows if (r["M"], r["N"], r["K"]) == s) == 1
     p = tmp_path / "sweep.csv"
