@@ -1,5 +1,5 @@
 // ptx.cuh — thin inline-PTX wrappers for sm_103a: mbarrier, TMA tile loads,
-// element-wise cp.async, timers.
+// element-wise cp.async, GPU-scope flags, timers.
 //
 // Every wait built on these is bounded by the caller (see sgemm_kernel.cuh):
 // nothing here spins.
@@ -177,6 +177,21 @@ __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
 // semantics the callers rely on: every address passed is inside its matrix).
 __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" :: "l"(p));
+}
+
+// ---- flags between the CTAs of one grid (global memory, GPU scope) ----------
+
+// Load with acquire semantics at GPU scope: writes released before the flag
+// by another CTA are visible to this thread after it reads the flag.
+__device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Store with release semantics at GPU scope.
+__device__ __forceinline__ void st_release_gpu(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
 }
 
 // ---- timers ----------------------------------------------------------------

@@ -77,7 +77,13 @@ std::atomic<int> g_force_cp{0};
 // the workspace and run the transposed-A kernel on it.
 std::atomic<int> g_force_at{-1};
 std::atomic<int> g_force_sk{-1};
+// fx = 1: split tiles finished by the separate fixup kernel instead of in
+// the GEMM kernel (":fixup").
+std::atomic<int> g_force_fx{0};
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+// Flag value of the next launch that finishes split tiles in the kernel:
+// unique per launch in this process and never 0.
+std::atomic<unsigned long long> g_sk_tag{1};
 
 thread_local int t_last_cuda_error = 0;
 
@@ -88,8 +94,8 @@ thread_local int t_last_cuda_error = 0;
 // (-1 auto, 0 never), how a row-major A reaches the consumers (-1 auto, 0 as
 // stored, 1 through a transposed copy in HBM, 2 transposed in shared memory).
 struct Config {
-    int family = -1, cp = 0, sk = -1, at = -1;
-    bool is_auto() const { return family < 0 && cp == 0 && sk < 0 && at < 0; }
+    int family = -1, cp = 0, sk = -1, at = -1, fx = 0;
+    bool is_auto() const { return family < 0 && cp == 0 && sk < 0 && at < 0 && fx == 0; }
 };
 
 struct ShapeRule {
@@ -113,14 +119,14 @@ bool shape_rule(int64_t M, int64_t N, int64_t K, Config* cfg) {
     return false;
 }
 
-// "<family>[:cpasync][:dp][:at|:noat]" with <family> one of auto, 128x128,
-// 64x64, 128x64 or a registry name.
+// "<family>[:cpasync][:dp][:at|:noat|:xp][:fixup]" with <family> one of
+// auto, 128x128, 64x64, 128x64 or a registry name.
 int parse_config(const char* name, Config* out) {
     if (name == nullptr) return SGEMM_ERR_INVALID_VALUE;
     char buf[128];
     std::strncpy(buf, name, sizeof(buf) - 1);
     buf[sizeof(buf) - 1] = '\0';
-    int want_cp = 0, want_sk = -1, want_at = -1;
+    int want_cp = 0, want_sk = -1, want_at = -1, want_fx = 0;
     char* mod = std::strchr(buf, ':');
     if (mod != nullptr) *mod++ = '\0';
     while (mod != nullptr) {
@@ -131,6 +137,7 @@ int parse_config(const char* name, Config* out) {
         else if (std::strcmp(mod, "at") == 0) want_at = 1;
         else if (std::strcmp(mod, "noat") == 0) want_at = 0;
         else if (std::strcmp(mod, "xp") == 0) want_at = 2;
+        else if (std::strcmp(mod, "fixup") == 0) want_fx = 1;
         else return SGEMM_ERR_INVALID_VALUE;
         mod = next;
     }
@@ -149,6 +156,7 @@ int parse_config(const char* name, Config* out) {
     out->cp = want_cp;
     out->sk = want_sk;
     out->at = want_at;
+    out->fx = want_fx;
     return SGEMM_OK;
 }
 
@@ -157,6 +165,7 @@ void set_global_config(const Config& c) {
     g_force_cp = c.cp;
     g_force_sk = c.sk;
     g_force_at = c.at;
+    g_force_fx = c.fx;
 }
 
 void read_env_locked() {
@@ -505,7 +514,9 @@ int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, 
     cfg.cp = g_force_cp.load();
     cfg.sk = g_force_sk.load();
     cfg.at = g_force_at.load();
+    cfg.fx = g_force_fx.load();
     if (cfg.is_auto()) shape_rule(M, N, K, &cfg);
+    pl->sk_fixup = cfg.fx != 0;
     int fi = cfg.family;
     const int force_cp_flag = cfg.cp;
     const int force_sk = cfg.sk;
@@ -541,9 +552,15 @@ int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, 
             // common to all and left out. Per k-iteration of one tile: a
             // 128 x 64 CTA alone on its SM 0.63 units, two co-resident ones
             // 1.06 for both; 128 x 64 in two k-groups 0.54; 64 x 64 in four
-            // k-groups 0.31. The stream-K tail adds its partial sums and the
-            // fixup launch: ~5 units for 128 x 128 tiles (taken as 6, so
-            // that a tie goes to whole tiles), ~4 for 64 x 64.
+            // k-groups 0.31. The stream-K tail adds its partial sums and
+            // their hand-over. Finished inside the kernel: ~2 units plus
+            // ~0.26 for every segment of a split tile beyond two (the
+            // finishing CTA reads one slot per segment; fitted on GB300 to
+            // 1024^3, 2048^3, 512 x 2048 x 1024, 256^2 x 8192, 200 x 300 x
+            // 6000 and 130 x 72 x 4100 across the three tile families).
+            // With the separate fixup kernel: ~5 units for 128 x 128 tiles
+            // and ~4 for 64 x 64 (taken as 6 and 4, so that a tie goes to
+            // whole tiles).
             const double inf = 1e300;
             int best_f = 0;
             bool best_sk = false;
@@ -558,18 +575,29 @@ int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, 
             // Whole waves of tiles plus, with the stream-K tail, the last
             // partial wave's k-iterations spread over the CTAs (the schedule
             // further down: ranges at least kt/32 iterations long).
-            auto sk_iters = [&](int64_t tiles, int64_t cap) {
+            auto sk_ctas = [&](int64_t tiles, int64_t cap) {
                 const int64_t S = (tiles % cap) * kt;
                 int64_t G = S / cdiv(kt, 32);
                 if (G > cap) G = cap;
                 if (G < 1) G = 1;
-                return static_cast<double>((tiles / cap) * kt + cdiv(S, G));
+                return G;
             };
+            auto sk_iters = [&](int64_t tiles, int64_t cap) {
+                const int64_t S = (tiles % cap) * kt;
+                return static_cast<double>((tiles / cap) * kt + cdiv(S, sk_ctas(tiles, cap)));
+            };
+            // The hand-over cost of the tail finished inside the kernel.
+            auto sk_handover = [&](int64_t tiles, int64_t cap) {
+                const int64_t parts = cdiv(sk_ctas(tiles, cap), tiles % cap) + 1;
+                return 2.0 + 0.26 * static_cast<double>(parts > 2 ? parts - 2 : 0);
+            };
+            const bool fix = cfg.fx != 0;
             const int64_t cap128 = static_cast<int64_t>(dev->ctas_per_sm[0][0]) * nsm;
             if (cap128 > 0) {
                 offer(0, false, static_cast<double>(cdiv(tiles128, cap128)) * dkt + 1);
                 if (sk_possible && tiles128 % cap128 != 0)
-                    offer(0, true, sk_iters(tiles128, cap128) + 6);
+                    offer(0, true, sk_iters(tiles128, cap128) +
+                                       (fix ? 6.0 : sk_handover(tiles128, cap128)));
             }
             if (tma_both) {
                 if (dev->ctas_per_sm[2][mi_tt] >= 2)
@@ -578,13 +606,18 @@ int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, 
                               ? 0.63 * dkt
                               : static_cast<double>(cdiv(tiles128x64, 2 * nsm)) * 1.06 * dkt);
                 const int64_t cap_k2 = static_cast<int64_t>(dev->ctas_per_sm[3][mi_tt]) * nsm;
-                if (cap_k2 > 0)
+                if (cap_k2 > 0) {
                     offer(3, false, static_cast<double>(cdiv(tiles128x64, cap_k2)) * 0.54 * dkt);
+                    if (sk_possible && !fix && tiles128x64 % cap_k2 != 0)
+                        offer(3, true, sk_iters(tiles128x64, cap_k2) * 0.54 +
+                                           sk_handover(tiles128x64, cap_k2));
+                }
                 const int64_t cap_k4 = static_cast<int64_t>(dev->ctas_per_sm[4][mi_tt]) * nsm;
                 if (cap_k4 > 0) {
                     offer(4, false, static_cast<double>(cdiv(tiles64, cap_k4)) * 0.31 * dkt);
                     if (sk_possible && tiles64 % cap_k4 != 0)
-                        offer(4, true, sk_iters(tiles64, cap_k4) * 0.31 + 4);
+                        offer(4, true, sk_iters(tiles64, cap_k4) * 0.31 +
+                                           (fix ? 4.0 : sk_handover(tiles64, cap_k4)));
                 }
                 // The same tile in clusters of cs CTAs that split each tile's
                 // k-tiles: a cs-th of the k-loop per CTA, plus the hand-over of
@@ -803,9 +836,16 @@ int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, 
     p.dp_tiles = static_cast<int>(waves * cap);
     p.sk_ctas = static_cast<int>(G);
     p.sk_iters = S;
+    p.sk_fixup = pl->sk_fixup ? 1 : 0;
     pl->grid = static_cast<int>(waves > 0 ? cap : G);
     pl->sk_tiles = static_cast<int>(rest);
-    pl->sk_bytes = static_cast<size_t>(2 * G) * static_cast<size_t>(bm) * bn * sizeof(float);
+    // Slots of BM x BN floats: one per CTA when split tiles are finished in
+    // the kernel (followed by one 8-byte flag per CTA), two per CTA for the
+    // fixup kernel.
+    const size_t slot_bytes = static_cast<size_t>(bm) * bn * sizeof(float);
+    pl->sk_bytes = pl->sk_fixup ? static_cast<size_t>(2 * G) * slot_bytes
+                                : static_cast<size_t>(G) * slot_bytes +
+                                      align256(static_cast<size_t>(G) * 8);
     pl->ws_bytes = pl->pack_a_bytes + pl->pack_b_bytes + pl->sk_bytes;
     return SGEMM_OK;
 }
@@ -871,8 +911,18 @@ int launch_plan(Plan* pl, int* status, float* ws, cudaStream_t stream) {
     p.ws = pl->sk_bytes > 0
                ? reinterpret_cast<float*>(w + pl->pack_a_bytes + pl->pack_b_bytes)
                : nullptr;
+    p.sk_flags = nullptr;
+    p.sk_tag = 0;
+    if (pl->sk_bytes > 0 && !pl->sk_fixup) {
+        p.sk_flags = reinterpret_cast<unsigned long long*>(
+            w + pl->pack_a_bytes + pl->pack_b_bytes +
+            static_cast<size_t>(p.sk_ctas) * pl->fam->bm * pl->fam->bn * sizeof(float));
+        unsigned long long tag = g_sk_tag.fetch_add(1);
+        if (tag == 0) tag = g_sk_tag.fetch_add(1);   // after a wrap-around
+        p.sk_tag = tag;
+    }
     e = pl->k->launch(&pl->tmA, &pl->tmB, &pl->p, pl->grid, stream, pdl && prior);
-    if (e == cudaSuccess && pl->sk_tiles > 0) {
+    if (e == cudaSuccess && pl->sk_tiles > 0 && pl->sk_fixup) {
         // Enough fixup CTAs for about two per SM, at most 8 per tile.
         const int want = (2 * pl->sms + pl->sk_tiles - 1) / pl->sk_tiles;
         const int split = want < 1 ? 1 : (want > 8 ? 8 : want);
@@ -889,7 +939,7 @@ void plan_name(const Plan& pl, char* buf, int buflen) {
     else std::snprintf(buf, static_cast<size_t>(buflen), "%s%s%s%s", pl.k->name,
                        pl.pack_a ? (pl.a_pre ? "+packAT" : "+packA") : "",
                        pl.pack_b ? (pl.b_t ? "+packBT" : "+packB") : "",
-                       pl.sk_tiles > 0 ? "+sk" : "");
+                       pl.sk_tiles > 0 ? (pl.sk_fixup ? "+skfix" : "+sk") : "");
 }
 
 int device_memory_handles(const DeviceInfo* dev, int** status, cudaMemPool_t* pool) {

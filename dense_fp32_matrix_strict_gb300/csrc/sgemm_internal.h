@@ -36,7 +36,10 @@ struct Plan {
     GemmParams p;
     int grid = 0;
     int sms = 0;                  // SMs of the device (grid of the packing copies)
-    int sk_tiles = 0;             // tiles finished by the stream-K fixup
+    int sk_tiles = 0;             // stream-K tiles (split across CTAs)
+    // Split tiles finished by the separate fixup kernel (":fixup") instead
+    // of inside the GEMM kernel.
+    bool sk_fixup = false;
     // Operand transposition: a_t, A stored K x M (loaded as [BK][BM] boxes);
     // b_t, B stored N x K (transposed into the packed B buffer first).
     bool a_t = false, b_t = false;
@@ -88,8 +91,9 @@ int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, 
 int launch_plan(Plan* pl, int* status, float* ws, cudaStream_t stream);
 
 // Human-readable plan name into buf ("none", "scale", or the kernel name,
-// with "+packA" / "+packB" for operands copied to aligned buffers and "+sk"
-// when the stream-K tail is used).
+// with "+packA" / "+packB" for operands copied to aligned buffers, "+sk"
+// when the stream-K tail is used and finished in the kernel, "+skfix" when
+// the fixup kernel finishes it).
 void plan_name(const Plan& pl, char* buf, int buflen);
 
 // Records a CUDA error for sgemm_last_cuda_error and returns `code`.

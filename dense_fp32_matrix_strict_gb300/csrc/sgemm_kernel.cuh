@@ -22,10 +22,16 @@
 // are whole work items handed out round-robin (tile = CTA + wave * grid).
 // The k-iterations of the remaining tiles are split into sk_ctas equal
 // contiguous ranges, one per CTA, so the last, partial wave costs a fraction
-// of a tile instead of a whole one. A range segment that does not cover a
-// whole tile writes its raw partial sums to a workspace slot; sk_fixup_kernel
-// then adds each split tile's partials in k order and applies the epilogue.
-// No CTA ever waits for another.
+// of a tile instead of a whole one. A split tile is finished by the CTA that
+// holds its first k-segment, which is that CTA's last work item: the CTAs
+// holding the later segments processed them first (as their first items),
+// wrote their raw sums to workspace slots and set a flag each, so by the
+// time the finishing CTA gets there the flags are normally set already; it
+// waits for them (bounded), adds the slots in k order and runs the
+// epilogue. Such a wait is only ever on a CTA with a higher index, and the
+// grid never has more CTAs than the GPU holds at once. The older form,
+// every partial segment to a slot and a second kernel (sk_fixup_kernel) to
+// finish the tiles, with no CTA waiting for another, stays selectable.
 //
 // The pages this follows ("The road to a fast GEMM": sections "v4:
 // two-dimensional register tiling", "v5: vectorized loads", "Where to go
@@ -84,7 +90,18 @@ struct GemmParams {
     int dp_tiles;
     int sk_ctas;
     long long sk_iters;
-    float* ws;          // 2 * sk_ctas partial-tile slots of BM x BN floats
+    // How split tiles are finished. sk_fixup == 0: inside this kernel, by the
+    // CTA that holds the tile's first k-segment (its last work item); every
+    // other segment's CTA leaves its raw sums in slot blockIdx.x of ws and
+    // then sets sk_flags[blockIdx.x] = sk_tag (release), and the finishing
+    // CTA waits (bounded, acquire) for those flags, adds the slots in k order,
+    // resets the flags to 0 and runs the epilogue. sk_fixup == 1: every
+    // partial segment goes to a slot (2c for a range's first segment, 2c + 1
+    // for its last) and sk_fixup_kernel finishes the tiles.
+    float* ws;          // sk_ctas (or 2 sk_ctas) partial-tile slots of BM x BN floats
+    unsigned long long* sk_flags;   // sk_ctas flags (sk_fixup == 0)
+    unsigned long long sk_tag;      // this launch's flag value, never 0
+    int sk_fixup;
 };
 
 // Kernel configuration. FORDER: FMA form of the outer product (0: scalar
@@ -171,7 +188,7 @@ struct Cfg {
     static constexpr int CKS_BYTES = (CS - 1) * BM * BN * 4;        // other ranks' sums
     static constexpr int SMEM_BYTES = 1024 /* alignment slack */ +
                                       STAGES * (A_BYTES + B_BYTES + RAW_BYTES) + RED_BYTES +
-                                      CKS_BYTES + (3 * STAGES + 3) * 8;
+                                      CKS_BYTES + (3 * STAGES + 6) * 8;
     static constexpr bool FITS = SMEM_BYTES <= 227 * 1024;
     // Tiles of at most 128 x 64 are sized to run two CTAs per SM.
     static constexpr int MIN_BLOCKS = (BM * BN * KSPLIT <= 128 * 64) ? 2 : 1;
@@ -191,9 +208,14 @@ __device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& tm,
 
 // ---- work schedule ----------------------------------------------------------
 
-// One work item: k-tiles [kb, ke) of tile `tile`. slot < 0: the item covers
-// the whole tile and ends in the epilogue; otherwise its raw sums go to
-// workspace slot `slot` for sk_fixup_kernel.
+// One work item: k-tiles [kb, ke) of tile `tile`. slot == kWhole: the item
+// covers the whole tile and ends in the epilogue; slot == kFinish: the item
+// holds the tile's first k-segment and finishes the tile (adds the other
+// segments' slots, then the epilogue); slot >= 0: its raw sums go to
+// workspace slot `slot`.
+constexpr int kWhole = -1;
+constexpr int kFinish = -2;
+
 struct Item {
     int tile, kb, ke, slot;
 };
@@ -233,7 +255,7 @@ struct Schedule {
             it.tile = t_dp;
             it.kb = static_cast<int>(s);
             it.ke = static_cast<int>(e);
-            it.slot = -1;
+            it.slot = kWhole;
             t_dp = -1;
             return true;
         }
@@ -241,7 +263,7 @@ struct Schedule {
             it.tile = t_dp;
             it.kb = 0;
             it.ke = p.k_tiles;
-            it.slot = -1;
+            it.slot = kWhole;
             t_dp += static_cast<int>(gridDim.x);
             return true;
         }
@@ -254,11 +276,17 @@ struct Schedule {
         it.tile = p.dp_tiles + static_cast<int>(u);
         it.kb = kb;
         it.ke = ke;
-        // Only the first and the last segment of a range can be partial:
-        // the first goes to slot 2c, any later one to slot 2c + 1.
-        it.slot = (kb == 0 && ke == p.k_tiles)
-                      ? -1
-                      : 2 * static_cast<int>(blockIdx.x) + (i == s ? 0 : 1);
+        // Only the first and the last segment of a range can be partial. A
+        // partial segment that starts at k-tile 0 is the range's last item
+        // and, finishing in the kernel, completes the tile; one that starts
+        // later is the range's first item and goes to slot c. For the fixup
+        // kernel: the first segment to slot 2c, any later one to 2c + 1.
+        if (kb == 0 && ke == p.k_tiles)
+            it.slot = kWhole;
+        else if (p.sk_fixup)
+            it.slot = 2 * static_cast<int>(blockIdx.x) + (i == s ? 0 : 1);
+        else
+            it.slot = kb == 0 ? kFinish : static_cast<int>(blockIdx.x);
         i += ke - kb;
         return true;
     }
@@ -298,6 +326,31 @@ __device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t pari
             return false;
         }
     }
+}
+
+// Bounded wait until *flag == tag (acquire at GPU scope). Returns false
+// (after setting `code` in the status word) if it did not happen within
+// p.timeout_ns.
+__device__ __forceinline__ bool wait_flag_bounded(const unsigned long long* flag,
+                                                  unsigned long long tag, const GemmParams& p,
+                                                  int code) {
+    if (ld_acquire_gpu(flag) == tag) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i)
+            if (ld_acquire_gpu(flag) == tag) return true;
+        if (globaltimer_ns() - t0 > p.timeout_ns) {
+            atomicOr(p.status, code);
+            return false;
+        }
+    }
+}
+
+// The stream-K CTA whose range holds k-iteration g: the largest c with
+// sk_start(c) <= g.
+__device__ __forceinline__ long long sk_cta_of(long long g, const GemmParams& p) {
+    return ((g + 1) * p.sk_ctas + p.sk_iters - 1) / p.sk_iters - 1;
 }
 
 // ---- producer -----------------------------------------------------------------
@@ -522,7 +575,8 @@ template <class C>
 __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_ptr,
                                          const uint8_t* sB_ptr, uint32_t full0, uint32_t empty0,
                                          float4* red, uint32_t red_full, uint32_t red_empty,
-                                         float4* cks, uint32_t cks_full, int warp, int lane) {
+                                         float4* cks, uint32_t cks_full, volatile int* sk_fail,
+                                         uint32_t sk_pub, uint32_t sk_go, int warp, int lane) {
     // k-group of this warp (KSPLIT > 1) and its place in the group's tile.
     const int grp = C::KSPLIT > 1 ? warp / C::GROUP_WARPS : 0;
     const int wq = C::KSPLIT > 1 ? warp % C::GROUP_WARPS : warp;
@@ -541,6 +595,14 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
 
     int s = 0;
     uint32_t ph = 0;
+    // Slot whose flag this thread (group 0's first) still has to release:
+    // the stores of group 0 land in the slot, everyone arrives on sk_pub,
+    // and the release waits until sk_pub has completed, which it checks
+    // without blocking at each stage of the next item (the stores' write
+    // acknowledgements can take microseconds when L2 is busy, and a
+    // blocking wait there would hold up the whole CTA's pipeline).
+    int pend_slot = -1;
+    const bool publisher = wq == 0 && lane == 0 && grp == 0;
     Schedule<C::CS> sched(p);
     Item it;
     while (sched.next(p, it)) {
@@ -568,6 +630,10 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
 
         bool ready = false;   // EARLY: stage s already seen complete
         for (int kt = it.kb; kt < it.ke; ++kt) {
+            if (publisher && pend_slot >= 0 && mbar_test_wait(sk_pub, 0)) {
+                st_release_gpu(p.sk_flags + pend_slot, p.sk_tag);
+                pend_slot = -1;
+            }
             if (!ready && !wait_bounded(full0 + 8 * s, ph, p, STATUS_CONSUMER_TIMEOUT)) return;
             ready = false;
             // [BK][BM] stages: a transposed A is addressed directly; the
@@ -715,9 +781,12 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
             }
         }
 
+        // From here on only group 0's consumer threads hold the tile's sums
+        // (the other k-groups have moved on to their next item).
         if (it.slot >= 0) {
             // Partial tile: raw sums to the workspace slot, row-major BM x BN,
-            // bypassing L1 (sk_fixup_kernel reads them from L2).
+            // bypassing L1 (the finishing CTA or sk_fixup_kernel reads them
+            // from L2).
             float* slot = p.ws + static_cast<long long>(it.slot) * (C::BM * C::BN);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -728,7 +797,75 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
                            make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2],
                                        acc[i][4 * h + 3]));
             }
+            if (!p.sk_fixup) {
+                // Publish the slot: every thread arrives on sk_pub (release
+                // at CTA scope) after its stores; the publisher releases the
+                // flag at GPU scope once sk_pub has completed (acquire), which
+                // by cumulativity covers the stores it has synchronised with.
+                // A CTA writes at most one slot per launch, so the barrier's
+                // phase is 0.
+                mbar_arrive(sk_pub);
+                if (publisher) pend_slot = it.slot;
+            }
             continue;
+        }
+        if (it.slot == kFinish) {
+            // This CTA holds the tile's first k-segment [0, ke): add the
+            // segments [ke, k_tiles) that the next CTAs left in their slots,
+            // in increasing k order (the order sk_fixup_kernel uses, so the
+            // bits are the same). Warp 0 of the group waits for their flags,
+            // a lane per flag (a tile split over many CTAs costs one round
+            // trip, not one per segment), resets them to 0 for a later
+            // replay of the same launch and arrives on sk_go, which the
+            // other warps wait on (bounded): that hands the lanes' acquires
+            // to them. A CTA finishes at most one tile per launch (phase 0).
+            const long long u = it.tile - p.dp_tiles;
+            const long long c0 = sk_cta_of(u * p.k_tiles + it.ke, p);
+            const long long c1 = sk_cta_of(u * p.k_tiles + p.k_tiles - 1, p);
+            if (wq == 0) {
+                int fail = 0;
+                // This CTA's own slot first (its first item): a CTA before it
+                // may be waiting for it.
+                if (lane == 0 && pend_slot >= 0) {
+                    if (wait_bounded(sk_pub, 0, p, STATUS_CONSUMER_TIMEOUT))
+                        st_release_gpu(p.sk_flags + pend_slot, p.sk_tag);
+                    else
+                        fail = 1;
+                    pend_slot = -1;
+                }
+                fail = __shfl_sync(0xffffffffu, fail, 0);
+                for (long long c = c0 + lane; c <= c1 && !fail; c += 32)
+                    if (!wait_flag_bounded(p.sk_flags + c, p.sk_tag, p, STATUS_CONSUMER_TIMEOUT))
+                        fail = 1;
+                fail = __any_sync(0xffffffffu, fail);
+                if (!fail)
+                    for (long long c = c0 + lane; c <= c1; c += 32) p.sk_flags[c] = 0ull;
+                __syncwarp();
+                if (lane == 0) {
+                    *sk_fail = fail;
+                    mbar_arrive(sk_go);
+                }
+                __syncwarp();
+            } else if (!wait_bounded(sk_go, 0, p, STATUS_CONSUMER_TIMEOUT)) {
+                return;
+            }
+            if (*sk_fail) return;
+#pragma unroll 1
+            for (long long c = c0; c <= c1; ++c) {
+                const float* slot = p.ws + c * (C::BM * C::BN);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float* row = slot + (row_base + lane_row<C>(i)) * C::BN + col_base;
+#pragma unroll
+                    for (int h = 0; h < C::TN / 4; ++h) {
+                        const float4 v = __ldcg(reinterpret_cast<const float4*>(row + 32 * h));
+                        acc[i][4 * h] += v.x;
+                        acc[i][4 * h + 1] += v.y;
+                        acc[i][4 * h + 2] += v.z;
+                        acc[i][4 * h + 3] += v.w;
+                    }
+                }
+            }
         }
 
         // Epilogue: C = alpha * acc + beta * C, straight from registers.
@@ -793,6 +930,9 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
             }
         }
     }
+    // A slot written by the last item (or not yet released): release it now.
+    if (publisher && pend_slot >= 0 && wait_bounded(sk_pub, 0, p, STATUS_CONSUMER_TIMEOUT))
+        st_release_gpu(p.sk_flags + pend_slot, p.sk_tag);
 }
 
 template <class C>
@@ -818,6 +958,9 @@ sgemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const uint32_t red_full = smem_u32(bars + 3 * C::STAGES);
     const uint32_t red_empty = red_full + 8;
     const uint32_t cks_full = red_full + 16;
+    volatile int* sk_fail = reinterpret_cast<volatile int*>(bars + 3 * C::STAGES + 3);
+    const uint32_t sk_pub = red_full + 32;
+    const uint32_t sk_go = red_full + 40;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -830,6 +973,11 @@ sgemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             mbar_init(red_empty, C::GROUP_WARPS * 32);
         }
         if (C::CS > 1) mbar_init(cks_full, (C::CS - 1) * C::GROUP_WARPS * 32);
+        // In-kernel stream-K finishing: group 0's consumers publish a slot
+        // through sk_pub; the flag-waiting thread releases the others
+        // through sk_go.
+        mbar_init(sk_pub, C::GROUP_WARPS * 32);
+        mbar_init(sk_go, 1);
         fence_barrier_init();
     }
     __syncthreads();
@@ -850,8 +998,8 @@ sgemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             producer<C>(&tmA, &tmB, p, smem_u32(sA), smem_u32(sB), smem_u32(sRaw), full0, empty0,
                         raw0, pw, lane);
     } else {
-        consumer<C>(p, sA, sB, full0, empty0, red, red_full, red_empty, cks, cks_full, warp,
-                    lane);
+        consumer<C>(p, sA, sB, full0, empty0, red, red_full, red_empty, cks, cks_full, sk_fail,
+                    sk_pub, sk_go, warp, lane);
     }
     // No CTA of a cluster leaves while another may still write its shared
     // memory: every role returns here (all of their waits are bounded).

@@ -94,7 +94,7 @@ def test_null_ab_allowed_when_not_read(lib):
 
 def test_config_names(lib):
     for good in ["auto", "128x128", "64x64", "128x64", "128x128:cpasync", "auto:cpasync",
-                 "auto:at", "128x128:noat:dp"]:
+                 "auto:at", "128x128:noat:dp", "128x128:fixup", "auto:dp:fixup"]:
         assert sg.sgemm_set_config(good) == sg.SGEMM_OK
     for bad in ["", "x", "256x256", "128x128:tma", "auto:"]:
         if bad == "":
@@ -180,3 +180,9 @@ def test_ceiling_forms_and_noalloc_status_without_gpu(lib):
 
 def test_null_launch_without_gpu_is_a_launch_error(lib):
     assert sg.sgemm_null_launch(0) == sg.SGEMM_ERR_LAUNCH
+
+
+def test_tf32_mma_peak_arguments(lib):
+    assert sg.sgemm_tf32_mma_peak(64, 10.0)[0] == sg.SGEMM_ERR_INVALID_VALUE
+    assert sg.sgemm_tf32_mma_peak(128, 0.0)[0] == sg.SGEMM_ERR_INVALID_VALUE
+    assert sg.sgemm_tf32_mma_peak(256, 10.0)[0] not in (sg.SGEMM_OK, sg.SGEMM_ERR_INVALID_VALUE)
