@@ -27,7 +27,7 @@ EXPORTED_SYMBOLS = (
     "sgemm_selftest_wait_timeout", "sgemm_config_names", "sgemm_noalloc", "sgemm_3xtf32",
     "sgemm_set_shape_config", "sgemm_clear_shape_configs", "sgemm_ex", "sgemm_plan_ex",
     "sgemm_3xtf32_ex", "sgemm_host", "sgemm_noalloc_check_status", "sgemm_fp32_peak_ex",
-    "sgemm_null_launch",
+    "sgemm_null_launch", "sgemm_tf32_mma_peak",
 )
 
 SGEMM_PEAK_FFMA, SGEMM_PEAK_FFMA2 = 0, 1
@@ -99,6 +99,8 @@ def load():
         lib.sgemm_fp32_peak_ex.argtypes = [ci, ctypes.c_double, f64p, f64p, f64p, vp]
         lib.sgemm_fp32_peak_ex.restype = ci
         lib.sgemm_null_launch.argtypes = [vp]
+        lib.sgemm_tf32_mma_peak.argtypes = [ci, ctypes.c_double, f64p, f64p, f64p, vp]
+        lib.sgemm_tf32_mma_peak.restype = ci
         lib.sgemm_null_launch.restype = ci
         lib.sgemm_3xtf32.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
         lib.sgemm_3xtf32.restype = ci
@@ -233,6 +235,14 @@ def sgemm_fp32_peak_ex(form: int, target_ms: float = 200.0, stream=0):
     rc = load().sgemm_fp32_peak_ex(int(form), float(target_ms), ctypes.byref(g),
                                    ctypes.byref(m), ctypes.byref(f), stream)
     return rc, g.value, m.value, f.value
+
+
+def sgemm_tf32_mma_peak(n: int = 128, target_ms: float = 100.0, stream=0):
+    """Returns (code, tflops, ms, flops) of the TF32 tcgen05 MMA ceiling."""
+    t, m, f = ctypes.c_double(0), ctypes.c_double(0), ctypes.c_double(0)
+    rc = load().sgemm_tf32_mma_peak(int(n), float(target_ms), ctypes.byref(t), ctypes.byref(m),
+                                    ctypes.byref(f), stream)
+    return rc, t.value, m.value, f.value
 
 
 def sgemm_null_launch(stream=0) -> int:

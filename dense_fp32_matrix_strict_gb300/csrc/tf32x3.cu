@@ -509,6 +509,69 @@ tf32x3_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ 
     if (T::CL > 1) cluster_sync();
 }
 
+// ---- the TF32 tensor-core ceiling -----------------------------------------------
+
+// One CTA per SM (its shared memory keeps a second one off the SM). One
+// thread issues `iters` x 4 back-to-back tcgen05.mma.kind::tf32 (M 128, N BN,
+// K 8; the instruction shape and descriptors of tf32x3_kernel) on a 128 x 32
+// A tile and a BN x 32 B tile of zeros resident in shared memory, all into
+// one TMEM accumulator, then commits and waits (bounded) for them before the
+// TMEM is freed. Nothing is read from or written to global memory except
+// the status word on a time-out: the rate is the tensor pipe's alone.
+constexpr int kPeakSmem = 160 * 1024;
+
+template <int BN>
+__global__ void __launch_bounds__(128, 1) tf32_mma_peak_kernel(long long iters, Params p) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    constexpr int TILE_BYTES = A_BYTES + BN * BK * 4;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + TILE_BYTES);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
+    const int warp = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < TILE_BYTES / 16; i += blockDim.x)
+        reinterpret_cast<float4*>(smem)[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(bar), 1);
+        fence_barrier_init();
+    }
+    // The zeros written by the threads above must be visible to the tensor
+    // core's (async-proxy) reads of the operands.
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     :: "r"(smem_u32(tmem_slot)), "r"(BN) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = *tmem_slot;
+    if (threadIdx.x == 0) {
+        constexpr uint32_t IDESC = (1u << 4) | (2u << 7) | (2u << 10) |
+                                   (static_cast<uint32_t>(BN >> 3) << 17) |
+                                   (static_cast<uint32_t>(BM >> 4) << 24);
+        const uint32_t s0 = smem_u32(smem);
+        const uint64_t a = desc_k_sw128(s0), b = desc_k_sw128(s0 + A_BYTES);
+        for (long long it = 0; it < iters; ++it) {
+#pragma unroll
+            for (int kk = 0; kk < BK / 8; ++kk) {
+                const uint64_t off = static_cast<uint64_t>((kk * 32) >> 4);
+                mma_tf32(tmem, a + off, b + off, IDESC, (it == 0 && kk == 0) ? 0u : 1u);
+            }
+        }
+        mma_commit(smem_u32(bar));
+        wait_bar(smem_u32(bar), 0, p, STATUS_DRAIN_TIMEOUT);
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (warp == 0) {
+        __syncwarp();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                     :: "r"(tmem), "r"(BN) : "memory");
+    }
+}
+
 bool encode(CUtensorMap* map, const float* base, int64_t rows, int64_t cols, int64_t ld, int box_rows,
             PFN_cuTensorMapEncodeTiled_v12000 enc) {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
@@ -708,4 +771,68 @@ extern "C" int sgemm_3xtf32_ex(int opa, int opb, int64_t M, int64_t N, int64_t K
                                const float* A, int64_t lda, const float* B, int64_t ldb,
                                float beta, float* C, int64_t ldc, cudaStream_t stream) {
     return run_3xtf32(opa, opb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+}
+
+extern "C" int sgemm_tf32_mma_peak(int n, double target_ms, double* tflops, double* ms,
+                                   double* flops, cudaStream_t stream) {
+    using namespace sg::tf32x3;
+    if (n != 128 && n != 256) return SGEMM_ERR_INVALID_VALUE;
+    if (!(target_ms >= 1.0) || target_ms > 60000.0) return SGEMM_ERR_INVALID_VALUE;
+    const DeviceInfo* dev = nullptr;
+    int rc = device_info(&dev);
+    if (rc != SGEMM_OK) return rc;
+    int* status = nullptr;
+    cudaMemPool_t pool = nullptr;
+    if ((rc = device_memory_handles(dev, &status, &pool)) != SGEMM_OK) return rc;
+    auto kernel = n == 256 ? &tf32_mma_peak_kernel<256> : &tf32_mma_peak_kernel<128>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kPeakSmem);
+    if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_CUDA);
+    Params p;
+    std::memset(&p, 0, sizeof(p));
+    p.status = status;
+    // A run is calibrated below 60 s; its single wait is allowed twice that.
+    p.timeout_ns = 120000000000ull;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if ((e = cudaEventCreate(&e0)) != cudaSuccess || (e = cudaEventCreate(&e1)) != cudaSuccess) {
+        if (e0) cudaEventDestroy(e0);
+        return cuda_fail(e, SGEMM_ERR_CUDA);
+    }
+    const int grid = dev->sm_count;
+    auto run = [&](long long iters, float* out_ms) -> cudaError_t {
+        cudaError_t err = cudaEventRecord(e0, stream);
+        if (err != cudaSuccess) return err;
+        kernel<<<grid, 128, kPeakSmem, stream>>>(iters, p);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        if ((err = cudaEventRecord(e1, stream)) != cudaSuccess) return err;
+        if ((err = cudaEventSynchronize(e1)) != cudaSuccess) return err;
+        return cudaEventElapsedTime(out_ms, e0, e1);
+    };
+    float t = 0.0f;
+    long long iters = 1024;
+    int result = SGEMM_OK;
+    // Calibrate: grow until a launch takes >= 5 ms, then scale to the target.
+    for (;;) {
+        if ((e = run(iters, &t)) != cudaSuccess) { result = SGEMM_ERR_LAUNCH; break; }
+        if (t >= 5.0f || iters > (1ll << 36)) break;
+        iters *= 4;
+    }
+    if (result == SGEMM_OK) {
+        long long want = static_cast<long long>(static_cast<double>(iters) * target_ms / t);
+        if (want < 1) want = 1;
+        // Warm-up of the same length, then the timed launch.
+        if ((e = run(want, &t)) != cudaSuccess || (e = run(want, &t)) != cudaSuccess) {
+            result = SGEMM_ERR_LAUNCH;
+        } else {
+            // 2 M N K FLOP per MMA (M 128, K 8), 4 MMAs per iteration.
+            const double f = 2.0 * BM * n * 8.0 * 4.0 * static_cast<double>(want) * grid;
+            if (tflops) *tflops = f / (static_cast<double>(t) * 1e-3) / 1e12;
+            if (ms) *ms = t;
+            if (flops) *flops = f;
+        }
+    }
+    if (result != SGEMM_OK) cuda_fail(e, result);
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    return result;
 }

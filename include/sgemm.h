@@ -287,6 +287,21 @@ SGEMM_API int sgemm_fp32_peak_ex(int form, double target_ms, double* gflops, dou
                                  double* flops, cudaStream_t stream);
 
 /*
+ * sgemm_tf32_mma_peak — the TF32 tensor-core ceiling that sgemm_3xtf32 is
+ * measured against: one CTA per SM issues back-to-back
+ * tcgen05.mma.kind::tf32 instructions of the shape sgemm_3xtf32 uses
+ * (M 128, N = n, K 8; n is 128 or 256) on operands resident in shared
+ * memory, accumulating in TMEM; nothing else runs. Calibrated to last about
+ * target_ms (>= 1) and timed with CUDA events on `stream` after one untimed
+ * warm-up launch of the same length. Outputs (each may be NULL): *tflops =
+ * 2 M N K per MMA x MMAs / time, *ms = time of the timed launch, *flops =
+ * floating-point operations of the timed launch. Blocking: synchronises
+ * `stream`. SGEMM_ERR_INVALID_VALUE for another n or target.
+ */
+SGEMM_API int sgemm_tf32_mma_peak(int n, double target_ms, double* tflops, double* ms,
+                                  double* flops, cudaStream_t stream);
+
+/*
  * sgemm_null_launch — enqueue one kernel that does nothing (one CTA of 32
  * threads) on `stream`. Timed like a call, it gives the launch-latency floor
  * below which no call of this library can go on the device; the small
