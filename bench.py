@@ -497,9 +497,26 @@ def lib_call(lib, name, args_):
         raise sg.SgemmError(name, rc)
 
 
-def measure_3xtf32(args, world, lib, call, torch, stream, flush, w, n):
+def tf32_ceiling(args, world):
+    """The measured TF32 tensor-core ceiling (back-to-back tcgen05.mma of
+    the 3xTF32 kernel's shape on smem-resident operands), one-GPU runs only;
+    None where the 3xTF32 leg does not run."""
+    if not tf32x3_allowed(args, world):
+        return None
+    import dense_fp32_matrix_strict_gb300 as sg
+    rc, tflops, ms, _ = sg.sgemm_tf32_mma_peak(128, 100.0)
+    if rc != sg.SGEMM_OK:
+        raise sg.SgemmError("sgemm_tf32_mma_peak", rc)
+    return {"tflops": tflops, "ms": ms,
+            "basis": "measured: tcgen05.mma.cta_group::1.kind::tf32 M128 N128 K8 back to back "
+                     "on shared-memory operands, one CTA per SM (sgemm_tf32_mma_peak)"}
+
+
+def measure_3xtf32(args, world, lib, call, torch, stream, flush, w, n, peak=None):
     """The separately reported tcgen05 3xTF32 path on the same operands, or
-    None where it must not run (see tf32x3_allowed)."""
+    None where it must not run (see tf32x3_allowed). `peak`: the measured TF32
+    ceiling (tf32_ceiling); without it the nominal TF32:BF16 ratio times the
+    measured bf16 peak is used, and said so."""
     if not tf32x3_allowed(args, world):
         return None
     import dense_fp32_matrix_strict_gb300 as sg
@@ -508,9 +525,14 @@ def measure_3xtf32(args, world, lib, call, torch, stream, flush, w, n):
     torch.cuda.synchronize()
     ms3 = time_per_call(torch, stream, lambda: lib_call(lib, "sgemm_3xtf32", call), n, flush)
     sg.check_status()
-    mp_ = measured_peaks()
-    bf16 = float(mp_.get("bf16_tflops") or 1900.0)
-    tf32_peak = bf16 * (1.1 / 2.25)      # nominal TF32 : BF16 dense ratio
+    if peak is not None:
+        tf32_peak, peak_basis = peak["tflops"], peak["basis"]
+    else:
+        mp_ = measured_peaks()
+        bf16 = float(mp_.get("bf16_tflops") or 1900.0)
+        tf32_peak = bf16 * (1.1 / 2.25)      # nominal TF32 : BF16 dense ratio
+        peak_basis = (f"derived: measured bf16 {bf16:.1f} TFLOP/s x 1.1/2.25 "
+                      "(nominal TF32:BF16 dense ratio)")
     tf32_rate = 3.0 * w.flops / (ms3 * 1e-3) / 1e12
     t3, t3_note = (None, None)
     if os.environ.get("SGEMM_3XTF32_TILE", "128x128c2") == "128x128c2" and w.N > 128:
@@ -523,8 +545,7 @@ def measure_3xtf32(args, world, lib, call, torch, stream, flush, w, n):
                                           if flush is not None else ""),
             "roofline": {"bound": "tensor", "achieved": tf32_rate, "peak": tf32_peak,
                          "unit": "TFLOP/s", "frac": tf32_rate / tf32_peak,
-                         "peak_basis": f"measured bf16 {bf16:.1f} TFLOP/s x 1.1/2.25 "
-                                       "(nominal TF32:BF16 dense ratio)",
+                         "peak_basis": peak_basis,
                          "achieved_basis": "3 x 2MNK TF32 FLOP per step / step time",
                          "traffic": t3, "traffic_note": t3_note},
             "gpu_launches_per_step": 3}
@@ -566,7 +587,8 @@ def launches_of(kernel: str) -> int:
     return 1 + sum(kernel.count(tag) for tag in ("+sk", "+packA", "+packB"))
 
 
-def workload_report(args, lib, torch, stream, dev, w, host, ceiling, datasheet, headline=None):
+def workload_report(args, lib, torch, stream, dev, w, host, ceiling, datasheet, headline=None,
+                    tf32_peak=None):
     """One entry of the five-workload report (GPU side) on the host inputs
     `host` = (A, B, C0). `headline`: the already timed numbers of this
     workload from the main timed region."""
@@ -624,10 +646,11 @@ def workload_report(args, lib, torch, stream, dev, w, host, ceiling, datasheet, 
         entry["latency_floor_ms"] = time_per_call(torch, stream, floor_fn, n, flush)
         entry["latency_floor_note"] = ("one empty kernel (sgemm_null_launch) between the same "
                                        "event pair after the same L2 flush")
-    t3 = measure_3xtf32(args, 1, lib, call, torch, stream, flush, w, max(10, n // 4))
+    t3 = measure_3xtf32(args, 1, lib, call, torch, stream, flush, w, max(10, n // 4), tf32_peak)
     if t3 is not None:
         entry["tcgen05_3xtf32_gflops"] = t3["value"]
         entry["tcgen05_3xtf32_ms"] = t3["ms_per_step"]
+        entry["tcgen05_3xtf32_frac_of_tf32_ceiling"] = t3["roofline"]["frac"]
     if not args.no_cublas:
         cb = measure_cublas(torch, stream, dA, dB, dC, w, max(10, n // 4), flush)
         entry["cublas_fp32_context_gflops"] = cb["value"]
@@ -738,8 +761,9 @@ def run_ours(args, w):
 
     # The tcgen05 3xTF32 path, reported separately (same workload, same FP32
     # error bound, different arithmetic unit); one-GPU runs only.
+    tf32_peak = tf32_ceiling(args, world)
     tf32x3 = measure_3xtf32(args, world, lib, call, torch, stream, flush, w,
-                            max(10, args.steps // 5))
+                            max(10, args.steps // 5), tf32_peak)
     cublas = None
     if not args.no_cublas:
         cublas = measure_cublas(torch, stream, dA, dB, dC, w, max(10, args.steps // 5), flush)
@@ -848,7 +872,7 @@ def run_ours(args, w):
                 head = ({"ms": ms_step, "steps": args.steps, "clocks": clocks}
                         if name == w.name else None)
                 ent = workload_report(args, lib, torch, stream, dev, wl, host, ceiling,
-                                      datasheet, head)
+                                      datasheet, head, tf32_peak)
                 if not args.no_cpu_baseline:
                     full = None
                     if name == w.name and line["cpu_baseline"]["rows"] == w.M:

@@ -77,6 +77,7 @@ def test_3xtf32_leg_never_runs_on_two_or_more_gpus():
         out = bench.measure_3xtf32(args, world, lib, call, torch=None, stream=None, flush=None,
                                    w=w, n=10)
         assert out is None and lib.calls == []
+        assert bench.tf32_ceiling(args, world) is None
 
 
 def test_only_the_guarded_leg_names_the_3xtf32_entry_points():
@@ -87,6 +88,8 @@ def test_only_the_guarded_leg_names_the_3xtf32_entry_points():
     src = inspect.getsource(bench)
     leg = inspect.getsource(bench.measure_3xtf32)
     assert src.count('"sgemm_3xtf32"') == leg.count('"sgemm_3xtf32"') > 0
+    # The TF32 tensor-core ceiling runs under the same guard.
+    assert "tf32x3_allowed(args, world)" in inspect.getsource(bench.tf32_ceiling)
     assert "sgemm_3xtf32_ex" not in src
     run = inspect.getsource(bench.run_ours)
     assert "measure_3xtf32(args, world," in run
