@@ -94,11 +94,22 @@ extern "C" {
  * The call is asynchronous: it returns once the kernel is enqueued. Device
  * time-outs are reported later by sgemm_check_status. A, B and C must stay
  * valid until the stream reaches the kernel. A call enqueues one GEMM kernel,
- * preceded by up to two packing copies and followed by the stream-K fixup
- * where its plan says so (sgemm_plan); a GEMM that follows a copy of the same
- * call is launched with programmatic stream serialisation (it waits for the
- * copy on the device), unless the environment variable SGEMM_PDL is "0" when
- * the library first launches.
+ * preceded by up to two packing copies where its plan says so (sgemm_plan)
+ * and, only with the ":fixup" configuration, followed by the stream-K fixup
+ * kernel; a GEMM that follows a copy of the same call is launched with
+ * programmatic stream serialisation (it waits for the copy on the device),
+ * unless the environment variable SGEMM_PDL is "0" when the library first
+ * launches.
+ *
+ * Workspace: the pages' kernels need no scratch, so the plainest contract is
+ * "nothing allocated per call". This entry point keeps a weaker one: no call
+ * grows the library's device memory in steady state or waits to allocate.
+ * Scratch (the transposed copy of A, an aligned copy of an operand, the
+ * stream-K slots and flags) is borrowed from the library's stream-ordered
+ * pool on `stream` and handed back on `stream`; the pool keeps what it
+ * returns, so from the second call of a size on the borrow is a pool hit
+ * (host bookkeeping only). Callers that can take no allocation at all use
+ * sgemm_noalloc.
  */
 SGEMM_API int sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float* A, int64_t lda,
           const float* B, int64_t ldb, float beta, float* C, int64_t ldc,
