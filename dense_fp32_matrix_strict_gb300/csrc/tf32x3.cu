@@ -509,6 +509,283 @@ tf32x3_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ 
     if (T::CL > 1) cluster_sync();
 }
 
+// ---- CTA pairs on one 256 x 256 tile: tcgen05.mma.cta_group::2 -----------------
+
+// The two CTAs of a cluster of two (ranks 0 and 1, a CTA pair) share one
+// 256 x 256 output tile. Each holds in its shared memory the 128 rows of A
+// (hi and lo) for its half of the tile's rows and the 128 rows of B^T (hi and
+// lo) for its half of the tile's columns; one thread of rank 0 issues
+// tcgen05.mma.cta_group::2 (M 256, N 256, K 8), which reads A and B from both
+// CTAs at the same shared-memory offsets and leaves rows 0..127 of the
+// accumulator in rank 0's TMEM and rows 128..255 in rank 1's. Per stage a CTA
+// thus loads 64 KB for 128 x 256 outputs, half what one CTA on a 128 x 128
+// tile needs per output, and three stages still fit (192 KB).
+//   * both producers (warp 0, one thread) wait on their own "empty" barrier
+//     (released by rank 0's MMA commit, multicast to both CTAs) and TMA their
+//     four tiles into their own stage, completing the bytes on rank 0's
+//     "full" barrier (cp.async.bulk.tensor .cta_group::2), which rank 0's
+//     producer armed for both CTAs' bytes;
+//   * rank 0's MMA thread (warp 1) waits on "full", issues the MMAs and
+//     commits: the stage's "empty" in both CTAs, and at the end of a tile the
+//     accumulator's "full" in both CTAs;
+//   * both epilogues (warps 2-5) read their 128 TMEM lanes and write their
+//     rows of C, then arrive on rank 0's accumulator-"empty" barrier, which
+//     counts both CTAs' 256 threads.
+// Both CTAs allocate the same 512 TMEM columns (two 256-column accumulators)
+// with tcgen05.alloc.cta_group::2 and free them after a cluster barrier that
+// follows the last MMA's completion.
+namespace pair {
+constexpr int TILE = 256;                         // M and N of the pair's tile
+constexpr int HALF = 128;                         // rows of A and of B^T per CTA
+constexpr int STAGES = 3;
+constexpr int B_BYTES = HALF * BK * 4;            // 16 KB
+constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;   // 64 KB
+constexpr int TMEM_COLS = 2 * TILE;               // 512: all of a CTA's TMEM
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+static_assert(SMEM_BYTES <= 227 * 1024, "ring too large");
+// kind::tf32, D FP32, A and B TF32 K-major, N = 256 (N >> 3 in bits 17-22),
+// M = 256 (M >> 4 in bits 24-28).
+constexpr uint32_t IDESC = (1u << 4) | (2u << 7) | (2u << 10) |
+                           (static_cast<uint32_t>(TILE >> 3) << 17) |
+                           (static_cast<uint32_t>(TILE >> 4) << 24);
+}  // namespace pair
+
+__device__ __forceinline__ void mma_tf32_pair(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                              uint32_t idesc, uint32_t acc) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
+                 :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+
+// Arrive once on the barrier at offset bar in each CTA of the pair named in
+// mask when every tcgen05.mma this thread issued has completed.
+__device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t mask) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster"
+                 ".multicast::cluster.b64 [%0], %1;" :: "r"(bar), "h"(mask) : "memory");
+}
+
+// The same, on this CTA's barrier only.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(bar) : "memory");
+}
+
+// 2-D TMA tile load into this CTA's shared memory at dst whose bytes complete
+// on the barrier at cluster address bar, which may be in either CTA of the
+// pair. x * 4 bytes is a multiple of 16 (x is a multiple of BK).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* desc, uint32_t bar,
+                                                 int32_t x, int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+tf32x3_pair_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmAl,
+                   const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmBl,
+                   const Params p) {
+    using namespace pair;
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t s0 = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    // barriers: full[3], empty[3], acc_full[2], acc_empty[2], done; then the TMEM address
+    const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * STAGES;
+    const uint32_t accf0 = empty0 + 8 * STAGES, acce0 = accf0 + 16, done_bar = acce0 + 16;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            // "full" (used in rank 0): rank 0's producer arms it for both
+            // CTAs' bytes; "empty": rank 0's MMA commit.
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf0 + 8 * b, 1);
+            mbar_init(acce0 + 8 * b, 2 * 128);   // both CTAs' epilogue threads (rank 0's)
+        }
+        mbar_init(done_bar, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                     :: "r"(smem_u32(tmem_slot)), "r"(TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = *tmem_slot;
+    // Both CTAs' barriers exist before the peer completes bytes or arrives on
+    // them, or the MMA commits to them.
+    cluster_sync();
+
+    Params q = p;
+    q.tiles_m = (p.M + TILE - 1) / TILE;
+    q.tiles_n = (p.N + TILE - 1) / TILE;
+    const int num_tiles = q.tiles_m * q.tiles_n;
+    const int first_item = static_cast<int>(cluster_id_x());
+    const int item_step = static_cast<int>(gridDim.x) / 2;
+    if (warp == 0) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tmAh);
+            tma_prefetch_desc(&tmAl);
+            tma_prefetch_desc(&tmBh);
+            tma_prefetch_desc(&tmBl);
+            // Rank 0's "full" barriers, as cluster addresses.
+            const uint32_t full_r0 = mapa_shared(full0, 0);
+            int s = 0;
+            uint32_t ph = 0;
+            // A producer that gives up has waited the whole time limit for a
+            // stage to be released, far longer than any copy it issued
+            // before takes to land; the copies are done by then.
+            for (int t = first_item; t < num_tiles; t += item_step) {
+                int tm, tn;
+                tile_of(t, q, tm, tn);
+                const int a_row = tm * TILE + static_cast<int>(rank) * HALF;
+                const int b_row = tn * TILE + static_cast<int>(rank) * HALF;
+                bool ok = true;
+                for (int kt = 0; kt < p.k_tiles; ++kt) {
+                    if (!wait_bar(empty0 + 8 * s, ph ^ 1u, p, STATUS_PRODUCER_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    if (leader) mbar_arrive_expect_tx(full0 + 8 * s, 2 * STAGE_BYTES);
+                    const uint32_t st = s0 + s * STAGE_BYTES;
+                    const uint32_t bar = full_r0 + 8 * s;
+                    tma_load_2d_pair(st, &tmAh, bar, kt * BK, a_row);
+                    tma_load_2d_pair(st + A_BYTES, &tmAl, bar, kt * BK, a_row);
+                    tma_load_2d_pair(st + 2 * A_BYTES, &tmBh, bar, kt * BK, b_row);
+                    tma_load_2d_pair(st + 2 * A_BYTES + B_BYTES, &tmBl, bar, kt * BK, b_row);
+                    if (++s == STAGES) { s = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+            }
+        }
+    } else if (warp == 1) {
+        if (leader && lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int it = 0;
+            bool ok = true;
+            for (int t = first_item; t < num_tiles && ok; t += item_step, ++it) {
+                const int b = it & 1;
+                const uint32_t acc_phase = static_cast<uint32_t>((it >> 1) & 1);
+                // Wait until both CTAs' epilogues have emptied this accumulator.
+                if (!wait_bar(acce0 + 8 * b, acc_phase ^ 1u, p, STATUS_CONSUMER_TIMEOUT)) break;
+                fence_after();
+                const uint32_t d = tmem + static_cast<uint32_t>(b * TILE);
+                for (int kt = 0; kt < p.k_tiles; ++kt) {
+                    if (!wait_bar(full0 + 8 * s, ph, p, STATUS_CONSUMER_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after();
+                    const uint32_t st = s0 + s * STAGE_BYTES;
+                    const uint64_t ah = desc_k_sw128(st), al = desc_k_sw128(st + A_BYTES);
+                    const uint64_t bh = desc_k_sw128(st + 2 * A_BYTES);
+                    const uint64_t bl = desc_k_sw128(st + 2 * A_BYTES + B_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 8; ++kk) {
+                        const uint64_t off = static_cast<uint64_t>((kk * 32) >> 4);
+                        const uint32_t first = (kt == 0 && kk == 0) ? 0u : 1u;
+                        mma_tf32_pair(d, ah + off, bh + off, IDESC, first);
+                        mma_tf32_pair(d, ah + off, bl + off, IDESC, 1u);
+                        mma_tf32_pair(d, al + off, bh + off, IDESC, 1u);
+                    }
+                    // The stage is free in both CTAs once these finish.
+                    mma_commit_pair_mc(empty0 + 8 * s, 0x3);
+                    if (++s == STAGES) { s = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                mma_commit_pair_mc(accf0 + 8 * b, 0x3);   // accumulator ready in both
+            }
+            // Every MMA issued has finished before the TMEM is freed.
+            mma_commit_pair(done_bar);
+            wait_bar(done_bar, 0, p, STATUS_DRAIN_TIMEOUT);
+        }
+    } else {
+        // Epilogue warpgroup: warp w reads TMEM lanes 32 (w % 4) .. + 31, which
+        // hold rows 128 rank + 32 (w % 4) .. of the pair's tile.
+        const int wq = warp & 3;
+        const uint32_t acce_r0 = mapa_shared(acce0, 0);
+        int it = 0;
+        for (int t = first_item; t < num_tiles; t += item_step, ++it) {
+            const int b = it & 1;
+            const uint32_t acc_phase = static_cast<uint32_t>((it >> 1) & 1);
+            if (!wait_bar(accf0 + 8 * b, acc_phase, p, STATUS_CONSUMER_TIMEOUT)) break;
+            __syncwarp();          // tcgen05.ld is warp-collective: reconverge first
+            fence_after();
+            int tm, tn;
+            tile_of(t, q, tm, tn);
+            const int m = tm * TILE + static_cast<int>(rank) * HALF + 32 * wq + lane;
+            const bool row_ok = m < p.M;
+            float* crow = p.C + static_cast<long long>(row_ok ? m : 0) * p.ldc;
+            const bool use_c = p.beta != 0.0f;
+            for (int ch = 0; ch < TILE / 32; ++ch) {
+                float v[32];
+                tmem_ld32(tmem + (static_cast<uint32_t>(32 * wq) << 16) +
+                              static_cast<uint32_t>(b * TILE + ch * 32), v);
+                if (!row_ok) continue;
+                const int n0 = tn * TILE + ch * 32;
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    const int n = n0 + j;
+                    float o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[e] = p.alpha * v[j + e];
+                    if (p.c_vec && n + 3 < p.N) {
+                        float4* cp = reinterpret_cast<float4*>(crow + n);
+                        if (use_c) {
+                            const float4 c = *cp;
+                            o[0] = fmaf(p.beta, c.x, o[0]);
+                            o[1] = fmaf(p.beta, c.y, o[1]);
+                            o[2] = fmaf(p.beta, c.z, o[2]);
+                            o[3] = fmaf(p.beta, c.w, o[3]);
+                        }
+                        *cp = make_float4(o[0], o[1], o[2], o[3]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            if (n + e < p.N) {
+                                float out = o[e];
+                                if (use_c) out = fmaf(p.beta, crow[n + e], out);
+                                crow[n + e] = out;
+                            }
+                        }
+                    }
+                }
+            }
+            fence_before();
+            // This accumulator may be reused once both CTAs' threads arrive.
+            if (leader) mbar_arrive(acce0 + 8 * b);
+            else mbar_arrive_remote(acce_r0 + 8 * b);
+        }
+    }
+
+    // Single exit: every role is done (or gave up after its bounded waits);
+    // rank 0's MMA thread has seen its last MMA finish before it got here, and
+    // the cluster barrier makes the peer wait for that too before the TMEM of
+    // both CTAs is freed; no CTA leaves while its peer may still arrive on its
+    // barriers.
+    fence_before();
+    __syncthreads();
+    cluster_sync();
+    fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;"
+                     :: "r"(tmem), "r"(TMEM_COLS) : "memory");
+    }
+    cluster_sync();
+}
+
 // ---- the TF32 tensor-core ceiling -----------------------------------------------
 
 // One CTA per SM (its shared memory keeps a second one off the SM). One
@@ -583,14 +860,17 @@ bool encode(CUtensorMap* map, const float* base, int64_t rows, int64_t cols, int
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Kernel variant. By default clusters of two CTAs that share A by multicast
-// (128 x 128 tiles, 3 stages) wherever a tile row holds two tiles, else one
-// CTA per tile. The environment variable SGEMM_3XTF32_TILE forces one:
-// "128x128c2", "128x128" (one CTA per tile) or "128x256" (2 stages).
+// Kernel variant. By default CTA pairs on 256 x 256 tiles (tcgen05
+// cta_group::2) when those tiles fill every pair the GPU runs at once, else
+// clusters of two CTAs that share A by multicast (128 x 128 tiles, 3 stages)
+// wherever a tile row holds two tiles, else one CTA per tile. The
+// environment variable SGEMM_3XTF32_TILE forces one:
+// "128x128c2", "128x128" (one CTA per tile), "128x256" (2 stages) or
+// "256x256" (CTA pairs on one tile, tcgen05.mma.cta_group::2).
 // Measured on GB300 (clusters against single CTAs, same box, interleaved):
 // 4096^3 0.571 against 0.581 ms, 8192x14336x4096 3.52 against 3.58 ms,
 // 4093x5120x1531 0.322 against 0.380 ms, 2048^3 even.
-enum { VARIANT_AUTO = 0, VARIANT_WIDE = 1, VARIANT_PAIR = 2, VARIANT_SINGLE = 3 };
+enum { VARIANT_AUTO = 0, VARIANT_WIDE = 1, VARIANT_PAIR = 2, VARIANT_SINGLE = 3, VARIANT_MMA2 = 4 };
 
 int tile_variant(const DeviceInfo*) {
     static const int v = [] {
@@ -599,6 +879,7 @@ int tile_variant(const DeviceInfo*) {
         if (std::strcmp(env, "128x256") == 0) return static_cast<int>(VARIANT_WIDE);
         if (std::strcmp(env, "128x128c2") == 0) return static_cast<int>(VARIANT_PAIR);
         if (std::strcmp(env, "128x128") == 0) return static_cast<int>(VARIANT_SINGLE);
+        if (std::strcmp(env, "256x256") == 0) return static_cast<int>(VARIANT_MMA2);
         return static_cast<int>(VARIANT_AUTO);
     }();
     return v;
@@ -656,6 +937,68 @@ cudaError_t launch(const DeviceInfo* dev, const float* a_hi, const float* a_lo, 
     const int clusters = static_cast<int>(items < ncl ? items : ncl);
     cfg.gridDim = dim3(static_cast<unsigned>(clusters * T::CL));
     return cudaLaunchKernelEx(&cfg, tf32x3_kernel<T>, mah, mal, mbh, mbl, p);
+}
+
+// How many clusters of the CTA-pair kernel the device runs at once (a
+// cluster sits whole in one GPC), queried once per device; 0 if none fits.
+int pair_clusters(const DeviceInfo* dev) {
+    static std::atomic<int> max_clusters[64] = {};
+    int ncl = max_clusters[dev->device].load(std::memory_order_acquire);
+    if (ncl != 0) return ncl < 0 ? 0 : ncl;
+    ncl = -1;
+    if (cudaFuncSetAttribute(tf32x3_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             pair::SMEM_BYTES) == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = pair::SMEM_BYTES;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.gridDim = dim3(2);
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, tf32x3_pair_kernel, &cfg) == cudaSuccess && n > 0)
+            ncl = n;
+    }
+    (void)cudaGetLastError();
+    max_clusters[dev->device].store(ncl, std::memory_order_release);
+    return ncl < 0 ? 0 : ncl;
+}
+
+// The CTA-pair kernel on 256 x 256 tiles (tcgen05.mma.cta_group::2).
+cudaError_t launch_pair(const DeviceInfo* dev, const float* a_hi, const float* a_lo,
+                        const float* b_hi, const float* b_lo, int64_t kp, Params p,
+                        cudaStream_t stream) {
+    const int ncl = pair_clusters(dev);
+    if (ncl <= 0) return cudaErrorInvalidConfiguration;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    CUtensorMap mah, mal, mbh, mbl;
+    // Boxes of BK x 128 rows: each CTA loads its half of the tile's rows of
+    // A and of B^T.
+    if (!(encode(&mah, a_hi, p.M, p.K, kp, pair::HALF, enc) &&
+          encode(&mal, a_lo, p.M, p.K, kp, pair::HALF, enc) &&
+          encode(&mbh, b_hi, p.N, p.K, kp, pair::HALF, enc) &&
+          encode(&mbl, b_lo, p.N, p.K, kp, pair::HALF, enc)))
+        return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = pair::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int64_t items = ((p.M + pair::TILE - 1) / pair::TILE) *
+                          static_cast<int64_t>((p.N + pair::TILE - 1) / pair::TILE);
+    const int clusters = static_cast<int>(items < ncl ? items : ncl);
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+    return cudaLaunchKernelEx(&cfg, tf32x3_pair_kernel, mah, mal, mbh, mbl, p);
 }
 
 }  // namespace tf32x3
@@ -741,13 +1084,28 @@ int run_3xtf32(int opa, int opb, int64_t M, int64_t N, int64_t K, float alpha, c
         p.timeout_ns = wait_timeout_ns();
         p.status = status;
         int v = tile_variant(dev);
-        if (v == VARIANT_AUTO) v = N > 128 ? VARIANT_PAIR : VARIANT_SINGLE;
+        if (v == VARIANT_AUTO) {
+            // 256 x 256 tiles on CTA pairs (tcgen05.mma.cta_group::2) once
+            // they fill every pair the GPU runs at once; below that the
+            // 128 x 128 tiles keep more SMs busy (1024^3: 16 such tiles,
+            // 49.9 against 37.8 us). Measured on GB300: 4096^3 0.511 against
+            // 0.566 ms, 8192 x 14336 x 4096 2.84 against 3.53 ms, 4093 x 5120
+            // x 1531 0.279 against 0.314 ms, the same bits.
+            const int64_t tiles256 = ((M + pair::TILE - 1) / pair::TILE) *
+                                     ((N + pair::TILE - 1) / pair::TILE);
+            const int ncl = pair_clusters(dev);
+            if (ncl > 0 && tiles256 >= ncl) v = VARIANT_MMA2;
+            else v = N > 128 ? VARIANT_PAIR : VARIANT_SINGLE;
+        }
         switch (v) {
             case VARIANT_WIDE:
                 e = launch<TcCfg<256, 2>>(dev, a_hi, a_lo, b_hi, b_lo, kp, p, stream);
                 break;
             case VARIANT_PAIR:
                 e = launch<TcCfg<128, 3, 2>>(dev, a_hi, a_lo, b_hi, b_lo, kp, p, stream);
+                break;
+            case VARIANT_MMA2:
+                e = launch_pair(dev, a_hi, a_lo, b_hi, b_lo, kp, p, stream);
                 break;
             default:
                 e = launch<TcCfg<128, 3>>(dev, a_hi, a_lo, b_hi, b_lo, kp, p, stream);

@@ -346,9 +346,13 @@ SGEMM_API int sgemm_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stre
  * NaN, so an output the definition makes +-inf comes out NaN (NaN inputs
  * still give NaN).
  *
- * Where a tile row of C holds two 128 x 128 tiles (N > 128) the kernel's CTAs
- * run in thread-block clusters of two that share each A tile by TMA
- * multicast; the result is the same bit for bit.
+ * Large problems (enough 256 x 256 output tiles to give one to every CTA
+ * pair the GPU runs at once) run on CTA pairs: the two CTAs of a cluster
+ * share one 256 x 256 tile through tcgen05.mma.cta_group::2, each holding
+ * half of the tile's rows of A and half of its columns of B. Otherwise,
+ * where a tile row of C holds two 128 x 128 tiles (N > 128), the CTAs run in
+ * thread-block clusters of two that share each A tile by TMA multicast.
+ * Every variant gives the same bits.
  *
  * Each call splits A and the transpose of B into a workspace of
  * 8 * (M + N) * K bytes (K rounded up to 4) taken from the library's

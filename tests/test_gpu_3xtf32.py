@@ -150,3 +150,31 @@ def test_cluster_pairs_give_the_single_cta_bits(shape, tmp_path):
     assert np.array_equal(pair, single)
     ref, S = oracle.sgemm_ref(0.7, A, B, -1.3, C0)
     assert oracle.check(pair, ref, S, K)["ok"]
+
+
+@pytest.mark.parametrize("shape", [(300, 640, 500), (4096, 4096, 256), (1100, 2000, 1531)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_cta_pair_mma_gives_the_single_cta_bits(shape, tmp_path):
+    # CTA pairs on 256 x 256 tiles (tcgen05.mma.cta_group::2, forced in a
+    # child process; the default for large problems) against one CTA per
+    # 128 x 128 tile (also forced): every tile sees the same MMAs in the same
+    # order, so the bits agree, and both are within the bound of the oracle.
+    import os
+    import subprocess
+    import sys
+    M, N, K = shape
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    outs = {}
+    for tile in ("256x256", "128x128"):
+        out = str(tmp_path / f"{tile}.npy")
+        env = dict(os.environ, SGEMM_3XTF32_TILE=tile, PYTHONPATH=root)
+        subprocess.run([sys.executable, "-c", _SINGLE_CTA_CHILD, str(M), str(N), str(K), out],
+                       check=True, env=env, cwd=root, timeout=300)
+        outs[tile] = np.load(out)
+    assert np.array_equal(outs["256x256"], outs["128x128"])
+    A = inputs.fill("normal", 620, inputs.TID_A, M, K)
+    B = inputs.fill("normal", 620, inputs.TID_B, K, N)
+    C0 = inputs.fill("normal", 620, inputs.TID_C, M, N)
+    rows, cols = inputs.sample_entries(M, N, n=8192)
+    ref, S = oracle.sgemm_ref_sampled(0.7, A, B, -1.3, C0, rows, cols)
+    assert oracle.check(outs["256x256"][rows, cols], ref, S, K)["ok"]
