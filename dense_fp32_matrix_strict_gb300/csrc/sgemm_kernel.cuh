@@ -365,7 +365,7 @@ template <class C>
 __device__ __forceinline__ void producer(const CUtensorMap* tmA, const CUtensorMap* tmB,
                                          const GemmParams& p, uint32_t sA, uint32_t sB,
                                          uint32_t sRaw, uint32_t full0, uint32_t empty0,
-                                         uint32_t raw0, int pw, int lane) {
+                                         uint32_t raw0, uint32_t sk_pub, int pw, int lane) {
     const bool tma_thread = C::ANY_TMA && pw == 0 && lane == 0;
     if (!C::ANY_CP && !tma_thread) return;
     if (tma_thread) {
@@ -379,9 +379,21 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmA, const CUtensorM
     uint32_t ph = 0;
     int issued = 0;
     bool ok = true;
+    // The slot this CTA's consumers fill (an item finished by another CTA;
+    // at most one per launch) and whose flag this thread releases, at GPU
+    // scope, once the consumers have all arrived on sk_pub after their
+    // stores (cumulativity carries their stores with the release). It checks
+    // without blocking before each stage it issues later, and blocks
+    // (bounded) only once it has nothing left to issue. The release is kept
+    // off the consumers: their stores' write acknowledgements can take
+    // microseconds when L2 is busy, and the extra state in their loop cost
+    // registers in the hot loop.
+    const bool publisher = pw == 0 && lane == 0;
+    int pend = -1;
     Schedule<C::CS> sched(p);
     Item it;
     while (ok && sched.next(p, it)) {
+        if (publisher && !p.sk_fixup && it.slot >= 0) pend = it.slot;
         int tm, tn;
         tile_coords(it.tile, p, tm, tn);
         const int m0 = tm * C::BM, n0 = tn * C::BN;
@@ -389,6 +401,10 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmA, const CUtensorM
             if (!wait_bounded(empty0 + 8 * s, ph ^ 1u, p, STATUS_PRODUCER_TIMEOUT)) {
                 ok = false;
                 break;
+            }
+            if (pend >= 0 && mbar_test_wait(sk_pub, 0)) {
+                st_release_gpu(p.sk_flags + pend, p.sk_tag);
+                pend = -1;
             }
             const uint32_t full = full0 + 8 * s;
             const uint32_t tx = tx0 + 8 * s;
@@ -432,6 +448,8 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmA, const CUtensorM
             if (++s == C::STAGES) { s = 0; ph ^= 1u; }
         }
     }
+    if (ok && pend >= 0 && wait_bounded(sk_pub, 0, p, STATUS_PRODUCER_TIMEOUT))
+        st_release_gpu(p.sk_flags + pend, p.sk_tag);
     if (!ok) {
         // Let the copies this thread started land before the CTA can exit:
         // wait (bounded) for the last phase of each stage it filled.
@@ -595,14 +613,6 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
 
     int s = 0;
     uint32_t ph = 0;
-    // Slot whose flag this thread (group 0's first) still has to release:
-    // the stores of group 0 land in the slot, everyone arrives on sk_pub,
-    // and the release waits until sk_pub has completed, which it checks
-    // without blocking at each stage of the next item (the stores' write
-    // acknowledgements can take microseconds when L2 is busy, and a
-    // blocking wait there would hold up the whole CTA's pipeline).
-    int pend_slot = -1;
-    const bool publisher = wq == 0 && lane == 0 && grp == 0;
     Schedule<C::CS> sched(p);
     Item it;
     while (sched.next(p, it)) {
@@ -630,10 +640,6 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
 
         bool ready = false;   // EARLY: stage s already seen complete
         for (int kt = it.kb; kt < it.ke; ++kt) {
-            if (publisher && pend_slot >= 0 && mbar_test_wait(sk_pub, 0)) {
-                st_release_gpu(p.sk_flags + pend_slot, p.sk_tag);
-                pend_slot = -1;
-            }
             if (!ready && !wait_bounded(full0 + 8 * s, ph, p, STATUS_CONSUMER_TIMEOUT)) return;
             ready = false;
             // [BK][BM] stages: a transposed A is addressed directly; the
@@ -797,16 +803,10 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
                            make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2],
                                        acc[i][4 * h + 3]));
             }
-            if (!p.sk_fixup) {
-                // Publish the slot: every thread arrives on sk_pub (release
-                // at CTA scope) after its stores; the publisher releases the
-                // flag at GPU scope once sk_pub has completed (acquire), which
-                // by cumulativity covers the stores it has synchronised with.
-                // A CTA writes at most one slot per launch, so the barrier's
-                // phase is 0.
-                mbar_arrive(sk_pub);
-                if (publisher) pend_slot = it.slot;
-            }
+            // Publish the slot: every thread arrives on sk_pub (release at CTA
+            // scope) after its stores; the producer thread releases the flag
+            // at GPU scope once sk_pub has completed (see producer()).
+            if (!p.sk_fixup) mbar_arrive(sk_pub);
             continue;
         }
         if (it.slot == kFinish) {
@@ -824,16 +824,6 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
             const long long c1 = sk_cta_of(u * p.k_tiles + p.k_tiles - 1, p);
             if (wq == 0) {
                 int fail = 0;
-                // This CTA's own slot first (its first item): a CTA before it
-                // may be waiting for it.
-                if (lane == 0 && pend_slot >= 0) {
-                    if (wait_bounded(sk_pub, 0, p, STATUS_CONSUMER_TIMEOUT))
-                        st_release_gpu(p.sk_flags + pend_slot, p.sk_tag);
-                    else
-                        fail = 1;
-                    pend_slot = -1;
-                }
-                fail = __shfl_sync(0xffffffffu, fail, 0);
                 for (long long c = c0 + lane; c <= c1 && !fail; c += 32)
                     if (!wait_flag_bounded(p.sk_flags + c, p.sk_tag, p, STATUS_CONSUMER_TIMEOUT))
                         fail = 1;
@@ -930,9 +920,6 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
             }
         }
     }
-    // A slot written by the last item (or not yet released): release it now.
-    if (publisher && pend_slot >= 0 && wait_bounded(sk_pub, 0, p, STATUS_CONSUMER_TIMEOUT))
-        st_release_gpu(p.sk_flags + pend_slot, p.sk_tag);
 }
 
 template <class C>
@@ -996,7 +983,7 @@ sgemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             transposer<C>(p, sRaw, sA, raw0, full0, (pw - 1) * 32 + lane);
         else
             producer<C>(&tmA, &tmB, p, smem_u32(sA), smem_u32(sB), smem_u32(sRaw), full0, empty0,
-                        raw0, pw, lane);
+                        raw0, sk_pub, pw, lane);
     } else {
         consumer<C>(p, sA, sB, full0, empty0, red, red_full, red_empty, cks, cks_full, sk_fail,
                     sk_pub, sk_go, warp, lane);
