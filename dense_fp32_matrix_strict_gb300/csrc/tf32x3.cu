@@ -88,6 +88,10 @@ struct Params {
     float alpha, beta;
     unsigned long long timeout_ns;
     int* status;
+    // CTA-pair kernel only: items [0, full_items) are whole 256 x 256 tiles;
+    // the half_items after them cover the remaining tiles as 256 x 128
+    // halves (two per tile), so a short last wave takes half as long.
+    int full_items, half_items;
 };
 
 // ---- tcgen05 helpers ---------------------------------------------------------
@@ -548,7 +552,31 @@ static_assert(SMEM_BYTES <= 227 * 1024, "ring too large");
 constexpr uint32_t IDESC = (1u << 4) | (2u << 7) | (2u << 10) |
                            (static_cast<uint32_t>(TILE >> 3) << 17) |
                            (static_cast<uint32_t>(TILE >> 4) << 24);
+// The same with N = 128, for the half tiles (each CTA then holds 64 rows
+// of B^T).
+constexpr uint32_t IDESC_HALF = (1u << 4) | (2u << 7) | (2u << 10) |
+                                (static_cast<uint32_t>((TILE / 2) >> 3) << 17) |
+                                (static_cast<uint32_t>(TILE >> 4) << 24);
+constexpr int HALF_B_BYTES = (HALF / 2) * BK * 4;        // 8 KB of B^T per CTA
 }  // namespace pair
+
+// Item i of the CTA-pair kernel: a whole 256 x 256 tile, or one 256 x 128
+// half of a tile; `col` is the first column of C it covers, `width` 256 or
+// 128.
+__device__ __forceinline__ void pair_item(int i, const Params& q, int& tm, int& col,
+                                          int& width) {
+    int tn;
+    if (i < q.full_items) {
+        tile_of(i, q, tm, tn);
+        col = tn * pair::TILE;
+        width = pair::TILE;
+    } else {
+        const int h = i - q.full_items;
+        tile_of(q.full_items + h / 2, q, tm, tn);
+        col = tn * pair::TILE + (h & 1) * (pair::TILE / 2);
+        width = pair::TILE / 2;
+    }
+}
 
 __device__ __forceinline__ void mma_tf32_pair(uint32_t d_tmem, uint64_t a, uint64_t b,
                                               uint32_t idesc, uint32_t acc) {
@@ -585,7 +613,8 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* desc,
 __global__ void __launch_bounds__(THREADS, 1)
 tf32x3_pair_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmAl,
                    const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmBl,
-                   const Params p) {
+                   const __grid_constant__ CUtensorMap tmBh64,
+                   const __grid_constant__ CUtensorMap tmBl64, const Params p) {
     using namespace pair;
     extern __shared__ __align__(16) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -629,7 +658,7 @@ tf32x3_pair_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_consta
     Params q = p;
     q.tiles_m = (p.M + TILE - 1) / TILE;
     q.tiles_n = (p.N + TILE - 1) / TILE;
-    const int num_tiles = q.tiles_m * q.tiles_n;
+    const int num_tiles = p.full_items + p.half_items;
     const int first_item = static_cast<int>(cluster_id_x());
     const int item_step = static_cast<int>(gridDim.x) / 2;
     if (warp == 0) {
@@ -638,6 +667,10 @@ tf32x3_pair_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_consta
             tma_prefetch_desc(&tmAl);
             tma_prefetch_desc(&tmBh);
             tma_prefetch_desc(&tmBl);
+            if (p.half_items > 0) {
+                tma_prefetch_desc(&tmBh64);
+                tma_prefetch_desc(&tmBl64);
+            }
             // Rank 0's "full" barriers, as cluster addresses.
             const uint32_t full_r0 = mapa_shared(full0, 0);
             int s = 0;
@@ -646,23 +679,28 @@ tf32x3_pair_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_consta
             // stage to be released, far longer than any copy it issued
             // before takes to land; the copies are done by then.
             for (int t = first_item; t < num_tiles; t += item_step) {
-                int tm, tn;
-                tile_of(t, q, tm, tn);
+                int tm, col, width;
+                pair_item(t, q, tm, col, width);
+                const bool half = width < TILE;
                 const int a_row = tm * TILE + static_cast<int>(rank) * HALF;
-                const int b_row = tn * TILE + static_cast<int>(rank) * HALF;
+                // Each CTA holds half of the item's columns of B (as rows of B^T).
+                const int b_row = col + static_cast<int>(rank) * (width / 2);
+                const uint32_t bytes = 2 * (2 * A_BYTES + 2 * (half ? HALF_B_BYTES : B_BYTES));
+                const CUtensorMap* mbh = half ? &tmBh64 : &tmBh;
+                const CUtensorMap* mbl = half ? &tmBl64 : &tmBl;
                 bool ok = true;
                 for (int kt = 0; kt < p.k_tiles; ++kt) {
                     if (!wait_bar(empty0 + 8 * s, ph ^ 1u, p, STATUS_PRODUCER_TIMEOUT)) {
                         ok = false;
                         break;
                     }
-                    if (leader) mbar_arrive_expect_tx(full0 + 8 * s, 2 * STAGE_BYTES);
+                    if (leader) mbar_arrive_expect_tx(full0 + 8 * s, bytes);
                     const uint32_t st = s0 + s * STAGE_BYTES;
                     const uint32_t bar = full_r0 + 8 * s;
                     tma_load_2d_pair(st, &tmAh, bar, kt * BK, a_row);
                     tma_load_2d_pair(st + A_BYTES, &tmAl, bar, kt * BK, a_row);
-                    tma_load_2d_pair(st + 2 * A_BYTES, &tmBh, bar, kt * BK, b_row);
-                    tma_load_2d_pair(st + 2 * A_BYTES + B_BYTES, &tmBl, bar, kt * BK, b_row);
+                    tma_load_2d_pair(st + 2 * A_BYTES, mbh, bar, kt * BK, b_row);
+                    tma_load_2d_pair(st + 2 * A_BYTES + B_BYTES, mbl, bar, kt * BK, b_row);
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
@@ -681,6 +719,7 @@ tf32x3_pair_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_consta
                 if (!wait_bar(acce0 + 8 * b, acc_phase ^ 1u, p, STATUS_CONSUMER_TIMEOUT)) break;
                 fence_after();
                 const uint32_t d = tmem + static_cast<uint32_t>(b * TILE);
+                const uint32_t idesc = t < p.full_items ? IDESC : IDESC_HALF;
                 for (int kt = 0; kt < p.k_tiles; ++kt) {
                     if (!wait_bar(full0 + 8 * s, ph, p, STATUS_CONSUMER_TIMEOUT)) {
                         ok = false;
@@ -695,9 +734,9 @@ tf32x3_pair_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_consta
                     for (int kk = 0; kk < BK / 8; ++kk) {
                         const uint64_t off = static_cast<uint64_t>((kk * 32) >> 4);
                         const uint32_t first = (kt == 0 && kk == 0) ? 0u : 1u;
-                        mma_tf32_pair(d, ah + off, bh + off, IDESC, first);
-                        mma_tf32_pair(d, ah + off, bl + off, IDESC, 1u);
-                        mma_tf32_pair(d, al + off, bh + off, IDESC, 1u);
+                        mma_tf32_pair(d, ah + off, bh + off, idesc, first);
+                        mma_tf32_pair(d, ah + off, bl + off, idesc, 1u);
+                        mma_tf32_pair(d, al + off, bh + off, idesc, 1u);
                     }
                     // The stage is free in both CTAs once these finish.
                     mma_commit_pair_mc(empty0 + 8 * s, 0x3);
@@ -722,18 +761,18 @@ tf32x3_pair_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_consta
             if (!wait_bar(accf0 + 8 * b, acc_phase, p, STATUS_CONSUMER_TIMEOUT)) break;
             __syncwarp();          // tcgen05.ld is warp-collective: reconverge first
             fence_after();
-            int tm, tn;
-            tile_of(t, q, tm, tn);
+            int tm, col, width;
+            pair_item(t, q, tm, col, width);
             const int m = tm * TILE + static_cast<int>(rank) * HALF + 32 * wq + lane;
             const bool row_ok = m < p.M;
             float* crow = p.C + static_cast<long long>(row_ok ? m : 0) * p.ldc;
             const bool use_c = p.beta != 0.0f;
-            for (int ch = 0; ch < TILE / 32; ++ch) {
+            for (int ch = 0; ch < width / 32; ++ch) {
                 float v[32];
                 tmem_ld32(tmem + (static_cast<uint32_t>(32 * wq) << 16) +
                               static_cast<uint32_t>(b * TILE + ch * 32), v);
                 if (!row_ok) continue;
-                const int n0 = tn * TILE + ch * 32;
+                const int n0 = col + ch * 32;
 #pragma unroll
                 for (int j = 0; j < 32; j += 4) {
                     const int n = n0 + j;
@@ -975,13 +1014,15 @@ cudaError_t launch_pair(const DeviceInfo* dev, const float* a_hi, const float* a
     const int ncl = pair_clusters(dev);
     if (ncl <= 0) return cudaErrorInvalidConfiguration;
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-    CUtensorMap mah, mal, mbh, mbl;
+    CUtensorMap mah, mal, mbh, mbl, mbh64, mbl64;
     // Boxes of BK x 128 rows: each CTA loads its half of the tile's rows of
-    // A and of B^T.
+    // A and of B^T; boxes of 64 rows of B^T for the half tiles.
     if (!(encode(&mah, a_hi, p.M, p.K, kp, pair::HALF, enc) &&
           encode(&mal, a_lo, p.M, p.K, kp, pair::HALF, enc) &&
           encode(&mbh, b_hi, p.N, p.K, kp, pair::HALF, enc) &&
-          encode(&mbl, b_lo, p.N, p.K, kp, pair::HALF, enc)))
+          encode(&mbl, b_lo, p.N, p.K, kp, pair::HALF, enc) &&
+          encode(&mbh64, b_hi, p.N, p.K, kp, pair::HALF / 2, enc) &&
+          encode(&mbl64, b_lo, p.N, p.K, kp, pair::HALF / 2, enc)))
         return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(THREADS);
@@ -994,11 +1035,20 @@ cudaError_t launch_pair(const DeviceInfo* dev, const float* a_hi, const float* a
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const int64_t items = ((p.M + pair::TILE - 1) / pair::TILE) *
+    const int64_t tiles = ((p.M + pair::TILE - 1) / pair::TILE) *
                           static_cast<int64_t>((p.N + pair::TILE - 1) / pair::TILE);
+    if (tiles > 0x3fffffffll) return cudaErrorInvalidValue;
+    // A last wave that is at most half full is run as half tiles: the pairs
+    // then take half as long over it (4096^3: 256 tiles on 76 pairs, 3.5
+    // waves of work instead of 4).
+    const int64_t rest = tiles % ncl;
+    const bool split = tiles > ncl && rest > 0 && 2 * rest <= ncl;
+    p.full_items = static_cast<int>(split ? tiles - rest : tiles);
+    p.half_items = static_cast<int>(split ? 2 * rest : 0);
+    const int64_t items = static_cast<int64_t>(p.full_items) + p.half_items;
     const int clusters = static_cast<int>(items < ncl ? items : ncl);
     cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
-    return cudaLaunchKernelEx(&cfg, tf32x3_pair_kernel, mah, mal, mbh, mbl, p);
+    return cudaLaunchKernelEx(&cfg, tf32x3_pair_kernel, mah, mal, mbh, mbl, mbh64, mbl64, p);
 }
 
 }  // namespace tf32x3
