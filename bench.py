@@ -255,6 +255,9 @@ def clock_sampler(torch_index: int):
 # helpers, the family instantiation). A recorded DRAM-traffic figure is
 # reused only while these files are unchanged and the plan (kernel name,
 # schedule suffixes, grid) is the one it was captured on.
+# The kernel sgemm_3xtf32's default variant runs on the workloads whose DRAM
+# traffic is recorded (CTA pairs on 256 x 256 tiles).
+TF32X3_DEFAULT_KERNEL = "tf32x3_pair_kernel"
 KERNEL_SOURCES = {
     "ffma": ("sgemm_kernel.cuh", "ptx.cuh", "sgemm_ws_128x128.cu"),
     "tf32x3": ("tf32x3.cu", "ptx.cuh"),
@@ -535,8 +538,10 @@ def measure_3xtf32(args, world, lib, call, torch, stream, flush, w, n, peak=None
                       "(nominal TF32:BF16 dense ratio)")
     tf32_rate = 3.0 * w.flops / (ms3 * 1e-3) / 1e12
     t3, t3_note = (None, None)
-    if os.environ.get("SGEMM_3XTF32_TILE", "128x128c2") == "128x128c2" and w.N > 128:
-        t3, t3_note = recorded_traffic("tf32x3_kernel<TcCfg<128,3,2>>", w.name, "tf32x3")
+    if "SGEMM_3XTF32_TILE" not in os.environ:
+        # The record names the kernel the default variant ran when it was
+        # captured; it is used only while the sources are unchanged.
+        t3, t3_note = recorded_traffic(TF32X3_DEFAULT_KERNEL, w.name, "tf32x3")
     return {"value": w.flops / (ms3 * 1e-3) / 1e9, "unit": "GFLOP/s", "ms_per_step": ms3,
             "steps": n,
             "note": "sgemm_3xtf32: A, B split into TF32 hi/lo, 3 tcgen05 MMAs per product, "
