@@ -7,7 +7,7 @@ build step (``build``) and the seeded synthetic inputs used to test and
 measure it (``inputs``). PyTorch serves only for device memory and streams.
 """
 from ._binding import (  # noqa: F401
-    EXPORTED_SYMBOLS, SGEMM_ERR_CUDA, SGEMM_ERR_DEVICE_TIMEOUT, SGEMM_ERR_INVALID_VALUE,
+    EXPORTED_SYMBOLS, SGEMM_ERR_CUDA, SGEMM_ERR_DEVICE_CHECK, SGEMM_ERR_DEVICE_TIMEOUT, SGEMM_ERR_INVALID_VALUE,
     SGEMM_ERR_LAUNCH, SGEMM_ERR_UNSUPPORTED_DEVICE, SGEMM_OK, SgemmError, check_status,
     fp32_peak, library_path, load, plan_tensors, sgemm, sgemm_check_status, sgemm_error_string,
     sgemm_config_names, sgemm_fp32_peak, sgemm_last_cuda_error, sgemm_noalloc, sgemm_plan, sgemm_selftest_wait_timeout,

@@ -19,6 +19,7 @@ SGEMM_ERR_UNSUPPORTED_DEVICE = 2
 SGEMM_ERR_LAUNCH = 3
 SGEMM_ERR_DEVICE_TIMEOUT = 4
 SGEMM_ERR_CUDA = 5
+SGEMM_ERR_DEVICE_CHECK = 6
 
 # Every function include/sgemm.h declares.
 EXPORTED_SYMBOLS = (
@@ -50,7 +51,7 @@ class SgemmError(RuntimeError):
 
 
 def library_path() -> str:
-    return _build.LIB_PATH
+    return os.environ.get("SGEMM_LIBRARY") or _build.LIB_PATH
 
 
 def load():
@@ -59,7 +60,9 @@ def load():
     with _lock:
         if _lib is not None:
             return _lib
-        path = _build.LIB_PATH
+        # SGEMM_LIBRARY selects another build of the same library (the
+        # debug build, for instance); by default the in-tree release build.
+        path = os.environ.get("SGEMM_LIBRARY") or _build.LIB_PATH
         if not os.path.exists(path):
             raise RuntimeError(
                 f"{path} is missing: the CUDA library has not been built "

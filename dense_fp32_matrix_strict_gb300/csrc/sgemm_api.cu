@@ -373,6 +373,13 @@ int device_memory(const DeviceInfo* info, DeviceMemory** out) {
 
 }  // namespace
 
+int status_code(int bits) {
+    if (bits & (STATUS_CONSUMER_TIMEOUT | STATUS_PRODUCER_TIMEOUT | STATUS_DRAIN_TIMEOUT))
+        return SGEMM_ERR_DEVICE_TIMEOUT;
+    if (bits != 0) return SGEMM_ERR_DEVICE_CHECK;
+    return SGEMM_OK;
+}
+
 int cuda_fail(cudaError_t e, int code) {
     t_last_cuda_error = static_cast<int>(e);
     return code;
@@ -1064,7 +1071,7 @@ extern "C" int sgemm_check_status(cudaStream_t stream, int* bits) {
         (e = cudaStreamSynchronize(stream)) != cudaSuccess)
         return cuda_fail(e, SGEMM_ERR_CUDA);
     if (bits != nullptr) *bits = v;
-    return v != 0 ? SGEMM_ERR_DEVICE_TIMEOUT : SGEMM_OK;
+    return status_code(v);
 }
 
 extern "C" const char* sgemm_error_string(int code) {
@@ -1075,6 +1082,7 @@ extern "C" const char* sgemm_error_string(int code) {
         case SGEMM_ERR_LAUNCH: return "kernel launch failed";
         case SGEMM_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel timed out";
         case SGEMM_ERR_CUDA: return "CUDA runtime error";
+        case SGEMM_ERR_DEVICE_CHECK: return "a device-side schedule or index check failed";
         default: return "unknown error code";
     }
 }

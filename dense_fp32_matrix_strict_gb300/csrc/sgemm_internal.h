@@ -96,6 +96,11 @@ int launch_plan(Plan* pl, int* status, float* ws, cudaStream_t stream);
 // the fixup kernel finishes it).
 void plan_name(const Plan& pl, char* buf, int buflen);
 
+// The return code of a status word: SGEMM_ERR_DEVICE_TIMEOUT for any
+// time-out bit, else SGEMM_ERR_DEVICE_CHECK for a schedule or index bit,
+// else SGEMM_OK.
+int status_code(int bits);
+
 // Records a CUDA error for sgemm_last_cuda_error and returns `code`.
 int cuda_fail(cudaError_t e, int code);
 

@@ -71,7 +71,23 @@ enum : int {
     STATUS_PRODUCER_TIMEOUT = 2,
     STATUS_DRAIN_TIMEOUT = 4,
     STATUS_SCHEDULE = 8,
+    STATUS_INDEX = 16,
 };
+
+// Device-side invariant checks of the debug build (-DSGEMM_DEBUG): a check
+// that fails sets STATUS_INDEX in the status word and execution carries on
+// (no trap), so the host sees it in the status check. In the ordinary build
+// they compile to nothing.
+#ifdef SGEMM_DEBUG
+#define SG_DCHECK(p, cond)                                       \
+    do {                                                         \
+        if (!(cond)) atomicOr((p).status, ::sg::STATUS_INDEX);  \
+    } while (0)
+#else
+#define SG_DCHECK(p, cond) \
+    do {                   \
+    } while (0)
+#endif
 
 struct GemmParams {
     int M, N, K;
@@ -257,6 +273,7 @@ struct Schedule {
             it.ke = static_cast<int>(e);
             it.slot = kWhole;
             t_dp = -1;
+            check(p, it);
             return true;
         }
         if (t_dp < p.dp_tiles) {
@@ -265,6 +282,7 @@ struct Schedule {
             it.ke = p.k_tiles;
             it.slot = kWhole;
             t_dp += static_cast<int>(gridDim.x);
+            check(p, it);
             return true;
         }
         if (i >= e) return false;
@@ -288,7 +306,18 @@ struct Schedule {
         else
             it.slot = kb == 0 ? kFinish : static_cast<int>(blockIdx.x);
         i += ke - kb;
+        check(p, it);
         return true;
+    }
+
+    // Debug build: every item names an existing tile, a non-empty k-range
+    // inside it and a slot the workspace has.
+    __device__ __forceinline__ static void check(const GemmParams& p, const Item& it) {
+        SG_DCHECK(p, it.tile >= 0 && it.tile < p.tiles_m * p.tiles_n);
+        SG_DCHECK(p, it.kb >= 0 && it.kb < it.ke && it.ke <= p.k_tiles);
+        SG_DCHECK(p, it.slot == kWhole || it.slot == kFinish ||
+                         (it.slot >= 0 && it.slot < (p.sk_fixup ? 2 : 1) * p.sk_ctas));
+        SG_DCHECK(p, it.slot != kFinish || (it.kb == 0 && !p.sk_fixup));
     }
 };
 
@@ -420,6 +449,7 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmA, const CUtensorM
                 }
                 if (C::B_MODE == LOAD_TMA) tma_load_2d(dB, tmB, tx, n0, k0);
             }
+            SG_DCHECK(p, s >= 0 && s < C::STAGES);
             if (C::A_MODE == LOAD_CPASYNC) {
                 // One row of BK = 32 floats per warp instruction, lane = k.
                 const int k = k0 + lane;
@@ -427,6 +457,7 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmA, const CUtensorM
                     const int m = m0 + r;
                     const bool v = (m < p.M) && (k < p.K);
                     const float* src = v ? p.A + (long long)m * p.lda + k : p.A;
+                    SG_DCHECK(p, a_swz(r, lane) + 4 <= static_cast<uint32_t>(C::A_BYTES));
                     cp_async_4(dA + a_swz(r, lane), src, v);
                 }
             }
@@ -439,6 +470,7 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmA, const CUtensorM
                         const int n = n0 + nn;
                         const bool v = (k < p.K) && (n < p.N);
                         const float* src = v ? p.B + (long long)k * p.ldb + n : p.B;
+                        SG_DCHECK(p, (kr * C::BN + nn) * 4 + 4 <= C::B_BYTES);
                         cp_async_4(dB + (kr * C::BN + nn) * 4, src, v);
                     }
                 }
@@ -498,6 +530,8 @@ __device__ __forceinline__ void transposer(const GemmParams& p, const uint8_t* r
                 }
                 const int chunk = mb ^ kb;
                 uint8_t* d = dst + (4 * kb) * (C::BM * 4) + (chunk << 4);
+                SG_DCHECK(p, (4 * mb + 3) * 128 + 128 <= C::A_BYTES);
+                SG_DCHECK(p, (4 * kb + 3) * (C::BM * 4) + (chunk << 4) + 16 <= C::A_BYTES);
                 *reinterpret_cast<float4*>(d) = make_float4(v[0].x, v[1].x, v[2].x, v[3].x);
                 *reinterpret_cast<float4*>(d + C::BM * 4) = make_float4(v[0].y, v[1].y, v[2].y, v[3].y);
                 *reinterpret_cast<float4*>(d + 2 * C::BM * 4) = make_float4(v[0].z, v[1].z, v[2].z, v[3].z);
@@ -665,6 +699,10 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
                 const int xq1 = (((((row_base >> 2) + 4) ^ kq) & 7) | (((row_base >> 2) + 4) & ~7)) << 4;
                 // Byte offsets of the lane's chunk kq in even and odd rows.
                 const int c0 = ((kq ^ tr) & 7) << 4, c1 = c0 ^ 64;
+                SG_DCHECK(p, ((kq * 4 + 3) * C::BN + col_base + 32 * (C::TN / 4 - 1)) * 4 + 16 <=
+                                 C::B_BYTES);
+                SG_DCHECK(p, C::A_KROWS ? ((kq * 4 + 3) * C::BM + row_base + 16) * 4 + 16 <= C::A_BYTES
+                                        : (row_base + 28) * 128 + 128 <= C::A_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint8_t* brow = b_st + (kq * 4 + kk) * C::BN * 4;
@@ -719,6 +757,8 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
             if (grp > 0) {
                 if (!wait_bounded(red_empty, red_ph ^ 1u, p, STATUS_CONSUMER_TIMEOUT)) return;
                 float4* dst = red + (((grp - 1) * C::GROUP_WARPS + wq) * NF4) * 32 + lane;
+                SG_DCHECK(p, ((((grp - 1) * C::GROUP_WARPS + wq) * NF4 + NF4 - 1) * 32 + lane + 1) * 16 <=
+                                 C::RED_BYTES);
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
 #pragma unroll
@@ -757,7 +797,10 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
             // them in rank order. One item per CTA, so the phase is 0.
             constexpr int NF4 = 8 * C::TN / 4;
             const uint32_t rank = cluster_ctarank();
+            SG_DCHECK(p, rank < static_cast<uint32_t>(C::CS));
             if (rank > 0) {
+                SG_DCHECK(p, ((((rank - 1) * C::GROUP_WARPS + wq) * NF4 + NF4 - 1) * 32 + lane + 1) * 16 <=
+                                 static_cast<uint32_t>(C::CKS_BYTES));
                 const uint32_t dst = mapa_shared(
                     smem_u32(cks + (((rank - 1) * C::GROUP_WARPS + wq) * NF4) * 32 + lane), 0);
 #pragma unroll
@@ -794,6 +837,8 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
             // bypassing L1 (the finishing CTA or sk_fixup_kernel reads them
             // from L2).
             float* slot = p.ws + static_cast<long long>(it.slot) * (C::BM * C::BN);
+            SG_DCHECK(p, p.ws != nullptr && it.slot < (p.sk_fixup ? 2 : 1) * p.sk_ctas);
+            SG_DCHECK(p, row_base + lane_row<C>(7) < C::BM && col_base + 32 * (C::TN / 4 - 1) + 4 <= C::BN);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 float* row = slot + (row_base + lane_row<C>(i)) * C::BN + col_base;
@@ -822,6 +867,8 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
             const long long u = it.tile - p.dp_tiles;
             const long long c0 = sk_cta_of(u * p.k_tiles + it.ke, p);
             const long long c1 = sk_cta_of(u * p.k_tiles + p.k_tiles - 1, p);
+            SG_DCHECK(p, c0 > static_cast<long long>(blockIdx.x) && c0 <= c1 && c1 < p.sk_ctas);
+            SG_DCHECK(p, p.sk_flags != nullptr && p.sk_tag != 0ull);
             if (wq == 0) {
                 int fail = 0;
                 for (long long c = c0 + lane; c <= c1 && !fail; c += 32)
@@ -891,6 +938,7 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
                 const int m = m0 + lane_row<C>(i);
                 if (m >= p.M) continue;
                 float* crow = p.C + (long long)m * p.ldc;
+                SG_DCHECK(p, m >= 0 && n0 >= 0 && n0 % 4 == 0);
 #pragma unroll
                 for (int h = 0; h < C::TN / 4; ++h) {
                     const int n = n0 + 32 * h;

@@ -119,5 +119,5 @@ extern "C" int sgemm_noalloc_check_status(cudaStream_t stream, int* bits) {
         (e = cudaStreamSynchronize(stream)) != cudaSuccess)
         return cuda_fail(e, SGEMM_ERR_CUDA);
     if (bits != nullptr) *bits = v;
-    return v != 0 ? SGEMM_ERR_DEVICE_TIMEOUT : SGEMM_OK;
+    return status_code(v);
 }

@@ -15,6 +15,11 @@ const KernelFamily* sweep_family_j();
 const KernelFamily* sweep_family_l();
 
 const KernelFamily* const* sweep_families(int* count) {
+#ifdef SGEMM_DEBUG
+    // The debug build compiles only the families "auto" chooses between.
+    *count = 0;
+    return nullptr;
+#endif
     static const KernelFamily* const list[] = {sweep_family_a(), sweep_family_b(), sweep_family_c(),
                                                sweep_family_d(), sweep_family_e(), sweep_family_g(),
                                                sweep_family_h(), sweep_family_i(),

@@ -76,6 +76,7 @@ sk_fixup_kernel(const GemmParams p, int split) {
         const int n = tn * BN + c4;
         if (m >= p.M || n >= p.N) continue;
         const float4* src = ws + q;
+        SG_DCHECK(p, q < Q && parts[0] >= 0 && parts[np - 1] < 2 * p.sk_ctas);
         float4 sum = __ldcg(src + parts[0] * SLOT);
         int j = 1;
 #pragma unroll 1

@@ -686,6 +686,7 @@ tf32x3_pair_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_consta
                 // Each CTA holds half of the item's columns of B (as rows of B^T).
                 const int b_row = col + static_cast<int>(rank) * (width / 2);
                 const uint32_t bytes = 2 * (2 * A_BYTES + 2 * (half ? HALF_B_BYTES : B_BYTES));
+                SG_DCHECK(p, tm >= 0 && tm < q.tiles_m && col >= 0 && col < q.tiles_n * TILE);
                 const CUtensorMap* mbh = half ? &tmBh64 : &tmBh;
                 const CUtensorMap* mbl = half ? &tmBl64 : &tmBl;
                 bool ok = true;
@@ -767,6 +768,7 @@ tf32x3_pair_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_consta
             const bool row_ok = m < p.M;
             float* crow = p.C + static_cast<long long>(row_ok ? m : 0) * p.ldc;
             const bool use_c = p.beta != 0.0f;
+            SG_DCHECK(p, b * TILE + width <= TMEM_COLS && (width == TILE || width == TILE / 2));
             for (int ch = 0; ch < width / 32; ++ch) {
                 float v[32];
                 tmem_ld32(tmem + (static_cast<uint32_t>(32 * wq) << 16) +

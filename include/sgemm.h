@@ -58,6 +58,8 @@ extern "C" {
 #define SGEMM_ERR_LAUNCH 3             /* a kernel launch failed; see sgemm_last_cuda_error */
 #define SGEMM_ERR_DEVICE_TIMEOUT 4     /* a bounded wait inside a kernel gave up          */
 #define SGEMM_ERR_CUDA 5               /* another CUDA runtime call failed               */
+#define SGEMM_ERR_DEVICE_CHECK 6       /* a kernel found a schedule or index invariant
+                                          broken (index checks: debug build only)    */
 
 /*
  * sgemm — C = alpha * A * B + beta * C (row-major, FP32).
@@ -183,9 +185,18 @@ SGEMM_API int sgemm_ex(int opa, int opb, int64_t M, int64_t N, int64_t K, float 
  * sgemm_check_status — synchronise `stream`, then read and clear the current
  * device's status word. Returns SGEMM_OK, SGEMM_ERR_DEVICE_TIMEOUT if any
  * kernel since the last check gave up on a bounded wait (its output is then
- * incomplete), or SGEMM_ERR_CUDA if the synchronisation reported an error.
- * If `bits` is not NULL it receives the raw status bits (1: a consumer
- * timed out, 2: a producer timed out, 4: draining copies timed out).
+ * incomplete), SGEMM_ERR_DEVICE_CHECK if a kernel found a schedule invariant
+ * broken or, in the library built with -DSGEMM_DEBUG, an index check failed
+ * (the result may then be wrong), or SGEMM_ERR_CUDA if the synchronisation
+ * reported an error. If `bits` is not NULL it receives the raw status bits
+ * (1: a consumer timed out, 2: a producer timed out, 4: draining copies
+ * timed out, 8: a schedule invariant failed, 16: an index check failed).
+ *
+ * The debug build (libsgemm_gb300_debug.so, the package's build with
+ * debug=True) compiles the same kernels with device-side checks of every
+ * shared-memory, workspace and C index and of each work item against the
+ * schedule; a failed check sets bit 16 and the kernel carries on (no trap),
+ * so a test reads it here. It is slower and not meant for timing.
  */
 SGEMM_API int sgemm_check_status(cudaStream_t stream, int* bits);
 
