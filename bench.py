@@ -251,15 +251,16 @@ def clock_sampler(torch_index: int):
 
 
 # ---------------------------------------------------------------------------
-# Sources each timed kernel's device code is built from (kernel body, PTX
-# helpers, the family instantiation). A recorded DRAM-traffic figure is
-# reused only while these files are unchanged and the plan (kernel name,
-# schedule suffixes, grid) is the one it was captured on.
+# Sources each timed kernel's DRAM traffic depends on (kernel body, PTX
+# helpers, the family instantiation, and for the FFMA kernel the planner,
+# which sets the tile raster). A recorded DRAM-traffic figure is reused only
+# while these files are unchanged and the plan (kernel name, schedule
+# suffixes, grid) is the one it was captured on.
 # The kernel sgemm_3xtf32's default variant runs on the workloads whose DRAM
 # traffic is recorded (CTA pairs on 256 x 256 tiles).
 TF32X3_DEFAULT_KERNEL = "tf32x3_pair_kernel"
 KERNEL_SOURCES = {
-    "ffma": ("sgemm_kernel.cuh", "ptx.cuh", "sgemm_ws_128x128.cu"),
+    "ffma": ("sgemm_kernel.cuh", "ptx.cuh", "sgemm_ws_128x128.cu", "sgemm_api.cu"),
     "tf32x3": ("tf32x3.cu", "ptx.cuh"),
 }
 
@@ -281,11 +282,15 @@ def recorded_traffic(kernel: str, workload: str, which: str = "ffma", grid=None)
         return None, None
     with open(path) as f:
         data = json.load(f)
-    rec = data.get(which + ":" + workload, {})
-    if rec.get("kernel") != kernel or rec.get("csrc_digest") != kernel_sources_digest(which):
+    rec = data.get(which + ":" + workload)
+    if rec is None:
         return None, None
-    if grid is not None and rec.get("grid") != grid:
-        return None, None
+    if rec.get("kernel") != kernel or (grid is not None and rec.get("grid") != grid):
+        return None, ("the committed ncu record (profiles/ncu_traffic.json) was taken on "
+                      "another plan: %s, grid %s" % (rec.get("kernel"), rec.get("grid")))
+    if rec.get("csrc_digest") != kernel_sources_digest(which):
+        return None, ("the kernel sources changed since the committed ncu record "
+                      "(profiles/ncu_traffic.json) was taken")
     return rec.get("dram_bytes_per_launch"), rec.get("note")
 
 
@@ -587,9 +592,11 @@ def alg_bytes_of(w) -> int:
 
 
 def launches_of(kernel: str) -> int:
-    """Kernels one sgemm call enqueues: the SGEMM kernel, plus the stream-K
-    fixup and any operand packing copy."""
-    return 1 + sum(kernel.count(tag) for tag in ("+sk", "+packA", "+packB"))
+    """Kernels one sgemm call enqueues: the SGEMM kernel, plus any operand
+    packing copy and, when split tiles are finished by a second kernel
+    ("+skfix"), that kernel. A stream-K tail finished inside the GEMM kernel
+    ("+sk") adds no launch."""
+    return 1 + sum(kernel.count(tag) for tag in ("+skfix", "+packA", "+packB"))
 
 
 def workload_report(args, lib, torch, stream, dev, w, host, ceiling, datasheet, headline=None,
@@ -847,7 +854,7 @@ def run_ours(args, w):
                        "GEMMs of row blocks inside the call)"},
         "gpu_launches": args.steps * launches_per_step,
         "gpu_launches_note": ("per step: the sgemm kernel" +
-                              (" + stream-K fixup" if "+sk" in kernel else "") +
+                              (" + stream-K fixup kernel" if "+skfix" in kernel else "") +
                               (" + transposing copy of A" if "+packAT" in kernel else
                                " + packing copy of A" if "+packA" in kernel else "") +
                               (" + transposing copy of B" if "+packBT" in kernel else

@@ -788,7 +788,12 @@ int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, 
     p.tiles_m = static_cast<int>((M + bm - 1) / bm);
     p.tiles_n = static_cast<int>((N + bn - 1) / bn);
     p.k_tiles = static_cast<int>((K + bk - 1) / bk);
-    p.group_m = 8;      // 4, 16 and 32 measured within 0.03 % at 4096^3 and 8192x14336x4096
+    // Tile rows per raster group. The time hardly depends on it (8, 16 and 32
+    // within 0.1 % at 4096^3, 8192x14336x4096 and 4093x5120x1531 on GB300),
+    // the DRAM traffic does: at 4096^3 one launch read 318 MB with 8, 273 MB
+    // with 16 (B's column blocks are re-read once per group) and 521 MB with
+    // 32 (the whole of A per wave no longer stays in L2).
+    p.group_m = 16;
     p.c_vec = (aligned(C, 16) && (ldc % 4) == 0) ? 1 : 0;
     p.A = A;
     p.B = B;

@@ -27,7 +27,9 @@
  * and return it with cudaFreeAsync on the same stream (so concurrent calls
  * on different streams never share it and stream capture records it as an
  * allocation node): a problem whose last wave of tiles is split across all
- * SMs (the stream-K tail, at most 2 x SMs x 64 KB); a row-major A large
+ * SMs (the stream-K tail: one slot of BM x BN floats, at most 64 KB, and one
+ * 8-byte flag per CTA; two slots per CTA when the configuration suffix
+ * ":fixup" selects the separate fixup kernel); a row-major A large
  * enough that the kernel runs faster on its transpose, which is copied
  * first (K x M floats, M rounded up to 4); and an operand that TMA cannot
  * load in place (base or leading dimension not 16-byte aligned) but that

@@ -21,7 +21,7 @@ def test_traffic_record_applies_only_to_its_kernel_sources_and_plan():
     if fresh:
         assert got == rec["dram_bytes_per_launch"] and note
     else:
-        assert got is None
+        assert got is None and "changed" in note
     # Another plan, another grid or another workload never borrows it.
     assert bench.recorded_traffic(kernel + "x", "sq4096_uniform", "ffma", grid)[0] is None
     assert bench.recorded_traffic(kernel, "sq4096_uniform", "ffma", grid + 1)[0] is None
@@ -31,7 +31,8 @@ def test_traffic_record_applies_only_to_its_kernel_sources_and_plan():
 def test_traffic_record_is_null_once_the_sources_change(monkeypatch):
     rec = _records()["tf32x3:sq4096_uniform"]
     monkeypatch.setattr(bench, "kernel_sources_digest", lambda which="ffma": "0" * 16)
-    assert bench.recorded_traffic(rec["kernel"], "sq4096_uniform", "tf32x3")[0] is None
+    got, note = bench.recorded_traffic(rec["kernel"], "sq4096_uniform", "tf32x3")
+    assert got is None and "changed" in note
 
 
 def test_recorded_traffic_is_at_least_the_algorithmic_bytes():
@@ -106,6 +107,8 @@ def test_cpu_baseline_plan_per_workload():
     assert whole == ["sq256_uniform", "sq1024_int", "sq4096_uniform",
                      "ragged_4093x5120x1531_normal"]
     assert bench.SINGLE_THREAD_WORKLOADS == ("sq256_uniform", "sq1024_int")
-    assert bench.launches_of("ws_128x128x32_s4_ATtma_Btma+packAT+sk") == 3
+    assert bench.launches_of("ws_128x128x32_s4_ATtma_Btma+packAT+sk") == 2
+    assert bench.launches_of("ws_128x128x32_s4_ATtma_Btma+packAT+skfix") == 3
+    assert bench.launches_of("ws_128x128x32_s4_Atma_Btma+sk") == 1
     assert bench.launches_of("ws_128x64x32_s4_k2_Axp_Btma") == 1
     assert bench.alg_bytes_of(inputs.WORKLOADS["sq1024_int"]) == 4 * 1024 * 1024 * 4
