@@ -310,11 +310,13 @@ struct Schedule {
         return true;
     }
 
-    // Debug build: every item names an existing tile, a non-empty k-range
-    // inside it and a slot the workspace has.
+    // Debug build: every item names an existing tile, a k-range inside it
+    // (non-empty, but for a cluster rank's share of a tile with fewer
+    // k-tiles than ranks) and a slot the workspace has.
     __device__ __forceinline__ static void check(const GemmParams& p, const Item& it) {
         SG_DCHECK(p, it.tile >= 0 && it.tile < p.tiles_m * p.tiles_n);
-        SG_DCHECK(p, it.kb >= 0 && it.kb < it.ke && it.ke <= p.k_tiles);
+        SG_DCHECK(p, it.kb >= 0 && (CS > 1 ? it.kb <= it.ke : it.kb < it.ke) &&
+                         it.ke <= p.k_tiles);
         SG_DCHECK(p, it.slot == kWhole || it.slot == kFinish ||
                          (it.slot >= 0 && it.slot < (p.sk_fixup ? 2 : 1) * p.sk_ctas));
         SG_DCHECK(p, it.slot != kFinish || (it.kb == 0 && !p.sk_fixup));

@@ -52,6 +52,9 @@ CASES = [
     ("128x64", 513, 640, 96, None, None, None, (0, 0, 0), False, False, "sgemm"),
     ("ws_128x64x32_s4_k2", 1024, 1024, 1024, None, None, None, (0, 0, 0), False, False, "sgemm"),
     ("ws_64x64x32_s4_k4_c4", 256, 256, 256, None, None, None, (0, 0, 0), False, False, "sgemm"),
+    # fewer k-tiles than CTAs in the cluster: some ranks have nothing to add
+    ("ws_64x64x32_s4_k4_c4", 70, 90, 20, None, None, None, (0, 0, 0), False, False, "sgemm"),
+    ("ws_64x64x32_s4_k4_c4:at", 70, 90, 40, None, None, None, (0, 0, 0), False, False, "sgemm"),
     ("auto:xp", 2048, 2048, 2048, None, None, None, (0, 0, 0), False, False, "sgemm"),
     ("128x128", 1000, 1100, 2000, None, None, None, (0, 0, 0), False, False, "noalloc"),
     ("auto", 4096, 4096, 256, None, None, None, (0, 0, 0), False, False, "3xtf32"),
@@ -103,7 +106,7 @@ def test_debug_build_runs_every_plan_with_clear_status():
                        capture_output=True, text=True)
     assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
     results = json.loads(r.stdout.strip().splitlines()[-1])
-    assert len(results) == 22
+    assert len(results) == 24
     for res in results:
         assert res["rc"] == 0 and res["bits"] == 0, res
         assert res["guards"] and res["ok"], res
