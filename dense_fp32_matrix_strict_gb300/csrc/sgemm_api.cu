@@ -307,19 +307,6 @@ cudaError_t launch_transpose_pack(const float* src, long long lds, float* dst, l
                          dst, ldd, R, C);
 }
 
-// A kernel that follows a packing copy of the same call is launched by
-// programmatic stream serialisation (it is scheduled while the copy
-// finishes and waits for it on the device), unless the environment variable
-// SGEMM_PDL is "0" when the library first launches. On GB300 this saves
-// ~1.5 us of the 4096^3 call (transposing copy of A, then the GEMM).
-bool pdl_enabled() {
-    static const bool on = [] {
-        const char* v = std::getenv("SGEMM_PDL");
-        return !(v != nullptr && std::strcmp(v, "0") == 0);
-    }();
-    return on;
-}
-
 size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
 
 __global__ void wait_timeout_kernel(GemmParams p) {
@@ -372,6 +359,19 @@ int device_memory(const DeviceInfo* info, DeviceMemory** out) {
 }
 
 }  // namespace
+
+// A kernel that follows a packing copy of the same call is launched by
+// programmatic stream serialisation (it is scheduled while the copy
+// finishes and waits for it on the device), unless the environment variable
+// SGEMM_PDL is "0" when the library first launches. On GB300 this saves
+// ~1.5 us of the 4096^3 call (transposing copy of A, then the GEMM).
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char* v = std::getenv("SGEMM_PDL");
+        return !(v != nullptr && std::strcmp(v, "0") == 0);
+    }();
+    return on;
+}
 
 int status_code(int bits) {
     if (bits & (STATUS_CONSUMER_TIMEOUT | STATUS_PRODUCER_TIMEOUT | STATUS_DRAIN_TIMEOUT))

@@ -114,4 +114,9 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 // Current limit of the kernels' bounded waits.
 unsigned long long wait_timeout_ns();
 
+// Whether kernels that follow one of the same call's own kernels on the
+// stream are launched by programmatic stream serialisation (on unless the
+// environment variable SGEMM_PDL is "0" when first asked).
+bool pdl_enabled();
+
 }  // namespace sg

@@ -200,6 +200,13 @@ __device__ __forceinline__ void tile_of(int t, const Params& p, int& tm, int& tn
 }
 
 // ---- split pre-passes ---------------------------------------------------------
+// The call splits A, then B, then runs the MMA kernel. The B split reads
+// only the caller's B and writes its own buffers, so it is launched by
+// programmatic stream serialisation and runs alongside the A split (both
+// let the next kernel be scheduled as soon as they start); it waits for the
+// A split at its very end, so that the MMA kernel, waiting for the B split
+// in turn, finds both done. In a kernel launched the ordinary way
+// griddep_wait returns at once.
 
 // hi/lo (rows x ldd) <- src (rows x cols, row stride lds), zeros in the
 // padding columns [cols, ldd). ldd is a multiple of 4, so every thread writes
@@ -207,6 +214,7 @@ __device__ __forceinline__ void tile_of(int t, const Params& p, int& tm, int& tn
 // aligned and lds % 4 == 0), else four scalars. blockIdx.y walks rows.
 __global__ void split_rows_kernel(const float* __restrict__ src, long long lds, float* __restrict__ hi,
                                   float* __restrict__ lo, long long ldd, int rows, int cols, int vec) {
+    griddep_launch_dependents();
     const int quads = static_cast<int>(ldd >> 2);
     for (long long r = blockIdx.y; r < rows; r += gridDim.y) {
         const float* srow = src + r * lds;
@@ -228,6 +236,7 @@ __global__ void split_rows_kernel(const float* __restrict__ src, long long lds, 
             *reinterpret_cast<float4*>(lo + r * ldd + c) = l;
         }
     }
+    griddep_wait();
 }
 
 // hiT/loT (cols x ldd) <- transpose of src (rows x cols, row stride lds):
@@ -244,6 +253,7 @@ __global__ void __launch_bounds__(256) split_transpose_kernel(const float* __res
                                                               float* __restrict__ loT,
                                                               long long ldd, int rows, int cols) {
     __shared__ float tile[kSplitTile][kSplitTile + 1];
+    griddep_launch_dependents();
     const bool vec = (reinterpret_cast<uintptr_t>(src) % 16 == 0) && (lds % 4 == 0);
     const long long n0 = static_cast<long long>(blockIdx.x) * kSplitTile;
     const long long tiles_k = (ldd + kSplitTile - 1) / kSplitTile;
@@ -293,6 +303,7 @@ __global__ void __launch_bounds__(256) split_transpose_kernel(const float* __res
         }
         __syncthreads();
     }
+    griddep_wait();
 }
 
 // ---- the tensor-core kernel ---------------------------------------------------
@@ -654,6 +665,9 @@ tf32x3_pair_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_consta
     // Both CTAs' barriers exist before the peer completes bytes or arrives on
     // them, or the MMA commits to them.
     cluster_sync();
+    // Launched behind the split passes (programmatic stream serialisation):
+    // nothing above touched global memory; wait for them here.
+    griddep_wait();
 
     Params q = p;
     q.tiles_m = (p.M + TILE - 1) / TILE;
@@ -1030,13 +1044,20 @@ cudaError_t launch_pair(const DeviceInfo* dev, const float* a_hi, const float* a
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = pair::SMEM_BYTES;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (pdl_enabled()) {
+        // Scheduled while the split passes finish; it waits for them on the
+        // device before its first global-memory access.
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 2;
+    }
     const int64_t tiles = ((p.M + pair::TILE - 1) / pair::TILE) *
                           static_cast<int64_t>((p.N + pair::TILE - 1) / pair::TILE);
     if (tiles > 0x3fffffffll) return cudaErrorInvalidValue;
@@ -1093,30 +1114,33 @@ int run_3xtf32(int opa, int opb, int64_t M, int64_t N, int64_t K, float alpha, c
     // Each split writes a K-major (rows x kp) hi/lo pair: a row-wise split
     // of an operand already stored K-major (A, or a transposed B), a
     // transposing split otherwise (B, or a transposed A).
-    auto split_kmajor = [&](const float* X, int64_t ldx, float* hi, float* lo, int64_t rows) {
+    // The A split is launched the ordinary way (after whatever the caller
+    // queued before), the B split alongside it (programmatic stream
+    // serialisation, see the split kernels).
+    auto split_kmajor = [&](const float* X, int64_t ldx, float* hi, float* lo, int64_t rows,
+                            bool pdl) {
         const int vec = ((reinterpret_cast<uintptr_t>(X) % 16) == 0 && (ldx % 4) == 0) ? 1 : 0;
         const int64_t quads = kp / 4;
         const int gx = static_cast<int>(quads < 256 * 8 ? (quads + 255) / 256 : 8);
         const int gy = static_cast<int>(rows < 8192 ? rows : 8192);
-        split_rows_kernel<<<dim3(gx, gy), 256, 0, stream>>>(X, ldx, hi, lo, kp,
-                                                           static_cast<int>(rows),
-                                                           static_cast<int>(K), vec);
+        return launch_kernel(split_rows_kernel, dim3(gx, gy), dim3(256), 0, stream, pdl, 1, X,
+                             static_cast<long long>(ldx), hi, lo, static_cast<long long>(kp),
+                             static_cast<int>(rows), static_cast<int>(K), vec);
     };
-    auto split_transposed = [&](const float* X, int64_t ldx, float* hi, float* lo, int64_t cols) {
+    auto split_transposed = [&](const float* X, int64_t ldx, float* hi, float* lo, int64_t cols,
+                                bool pdl) {
         const int64_t tiles_k = (kp + kSplitTile - 1) / kSplitTile;
         const dim3 grid(static_cast<unsigned>((cols + kSplitTile - 1) / kSplitTile),
                         static_cast<unsigned>(tiles_k < 65535 ? tiles_k : 65535));
-        split_transpose_kernel<<<grid, 256, 0, stream>>>(X, ldx, hi, lo, kp, static_cast<int>(K),
-                                                         static_cast<int>(cols));
+        return launch_kernel(split_transpose_kernel, grid, dim3(256), 0, stream, pdl, 1, X,
+                             static_cast<long long>(ldx), hi, lo, static_cast<long long>(kp),
+                             static_cast<int>(K), static_cast<int>(cols));
     };
-    cudaError_t e;
-    if (opa) split_transposed(A, lda, a_hi, a_lo, M);
-    else split_kmajor(A, lda, a_hi, a_lo, M);
-    if ((e = cudaGetLastError()) == cudaSuccess) {
-        if (opb) split_kmajor(B, ldb, b_hi, b_lo, N);
-        else split_transposed(B, ldb, b_hi, b_lo, N);
-        e = cudaGetLastError();
-    }
+    const bool pdl = pdl_enabled();
+    cudaError_t e = opa ? split_transposed(A, lda, a_hi, a_lo, M, false)
+                        : split_kmajor(A, lda, a_hi, a_lo, M, false);
+    if (e == cudaSuccess)
+        e = opb ? split_kmajor(B, ldb, b_hi, b_lo, N, pdl) : split_transposed(B, ldb, b_hi, b_lo, N, pdl);
     if (e == cudaSuccess) {
         Params p;
         std::memset(&p, 0, sizeof(p));

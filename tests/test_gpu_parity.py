@@ -661,6 +661,45 @@ def test_programmatic_launch_changes_no_bit():
     assert np.array_equal(here, there)
 
 
+@pytest.mark.parametrize("shape", [(2304, 2304, 1024), (512, 640, 500)],
+                         ids=["cta_pairs_256", "tiles_128"])
+def test_programmatic_launch_changes_no_bit_3xtf32(shape):
+    # sgemm_3xtf32 runs its B split alongside the A split and the MMA kernel
+    # behind them by programmatic stream serialisation; with SGEMM_PDL=0
+    # (ordinary launches) the bits are the same. 2304^2 takes the CTA-pair
+    # kernel (81 tiles of 256 x 256), 512 x 640 the 128 x 128 kernel.
+    import os
+    import subprocess
+    import sys
+    torch = pytest.importorskip("torch")
+    M, N, K = shape
+    A, B, C0 = gen(M, N, K, seed=406)
+    dC = torch.from_numpy(C0).cuda()
+    sg.sgemm_3xtf32_tensors(0.7, torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda(), -1.3, dC)
+    sg.check_status()
+    here = dC.cpu().numpy()
+    ref, S = oracle.sgemm_ref(0.7, A, B, -1.3, C0)
+    assert oracle.check(here, ref, S, K)["ok"]
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    script = (
+        "import sys, numpy as np, torch\n"
+        "import dense_fp32_matrix_strict_gb300 as sg\n"
+        "from dense_fp32_matrix_strict_gb300 import inputs as I\n"
+        f"A = I.fill('normal', 406, I.TID_A, {M}, {K})\n"
+        f"B = I.fill('normal', 406, I.TID_B, {K}, {N})\n"
+        f"C0 = I.fill('normal', 406, I.TID_C, {M}, {N})\n"
+        "dC = torch.from_numpy(C0).cuda()\n"
+        "sg.sgemm_3xtf32_tensors(0.7, torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda(), -1.3, dC)\n"
+        "sg.check_status()\n"
+        "sys.stdout.buffer.write(dC.cpu().numpy().tobytes())\n")
+    env = dict(os.environ, SGEMM_PDL="0")
+    out = subprocess.run([sys.executable, "-c", script], cwd=root, env=env, capture_output=True,
+                         timeout=600)
+    assert out.returncode == 0, out.stderr.decode()[-2000:]
+    there = np.frombuffer(out.stdout, dtype=np.float32).reshape(M, N)
+    assert np.array_equal(here, there)
+
+
 @pytest.mark.parametrize("config", ["128x128", "128x128:dp", "128x64:dp", "64x64:dp"])
 @pytest.mark.parametrize("aligned", [True, False], ids=["aligned", "unaligned"])
 def test_a_paths_give_the_same_bits(config, aligned):
