@@ -31,7 +31,7 @@ EXPORTED_SYMBOLS = (
     "sgemm_null_launch", "sgemm_tf32_mma_peak",
 )
 
-SGEMM_PEAK_FFMA, SGEMM_PEAK_FFMA2 = 0, 1
+SGEMM_PEAK_FFMA, SGEMM_PEAK_FFMA2, SGEMM_PEAK_OUTER = 0, 1, 2
 
 SGEMM_OP_N, SGEMM_OP_T = 0, 1
 
@@ -427,8 +427,9 @@ def check_status(stream=None, device=None) -> int:
 
 
 def fp32_peak(target_ms: float = 200.0, stream=None, device=None, form: int = SGEMM_PEAK_FFMA):
-    """Measured FP32 ceiling in one instruction form (SGEMM_PEAK_FFMA or
-    SGEMM_PEAK_FFMA2): dict(gflops, ms, flops)."""
+    """Measured FP32 ceiling in one instruction form (SGEMM_PEAK_FFMA,
+    SGEMM_PEAK_FFMA2, or SGEMM_PEAK_OUTER: the GEMM's register outer product
+    without its loads): dict(gflops, ms, flops)."""
     import torch
     dev = device if device is not None else torch.cuda.current_device()
     with torch.cuda.device(dev):

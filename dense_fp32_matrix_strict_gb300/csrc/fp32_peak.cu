@@ -9,7 +9,14 @@
 //     clock;
 //   * FFMA2 (form 1): the same with kChains independent chains of the packed
 //     fma.rn.f32x2 (two IEEE single-precision FMAs, each rounded once, in
-//     one instruction), the form the SGEMM's inner loop uses.
+//     one instruction), the form the SGEMM's inner loop uses;
+//   * the SGEMM's register outer product alone (form 2): one CTA of eight
+//     warps per SM (two per scheduler, as in the 128 x 128 kernel), every
+//     lane updating 8 x 8 accumulators per k-step with 32 packed FMAs in the
+//     kernel's order (column pairs outer), its 8 A and 8 B values made
+//     opaque to the compiler at every k-step, and no memory instruction: the
+//     rate the kernel's instruction mix could reach if its shared-memory
+//     loads cost nothing.
 // The loop body is kUnroll x kChains FMA instructions against two
 // loop-control instructions. The result is stored only under a condition the
 // host never makes true, so the chains stay live without memory traffic.
@@ -75,16 +82,78 @@ fp32_peak2_kernel(float mul, float add, long long iters, int sink_key) {
     if (static_cast<int>(blockIdx.x) == sink_key) g_peak_sink[threadIdx.x] = s;
 }
 
+// Form 2. kOuterThreads lanes each own an 8 x 8 block of accumulators. The
+// k-loop is unrolled four times (fully unrolled, 32 k-steps of 32 packed
+// FMAs, it measured 4 % slower on GB300); the launch bound of twice the
+// threads caps registers at 128 a thread, above the 84 the loop needs.
+constexpr int kOuterThreads = 256;
+constexpr int kOuterSteps = 32;           // k-steps per iteration
+constexpr int kOuterSmem = 120 * 1024;    // more than half an SM's shared memory: one CTA per SM
+
+__global__ void __launch_bounds__(2 * kOuterThreads, 1)
+outer_peak_kernel(long long iters, int sink_key) {
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+    const float t = static_cast<float>(threadIdx.x);
+    float av[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) av[i] = 1e-3f * (t + static_cast<float>(i));
+    float4 bq[2];
+    bq[0] = make_float4(t, t + 1.0f, t + 2.0f, t + 3.0f);
+    bq[1] = make_float4(t + 4.0f, t + 5.0f, t + 6.0f, t + 7.0f);
+    for (long long it = 0; it < iters; ++it) {
+#pragma unroll 4
+        for (int k = 0; k < kOuterSteps; ++k) {
+            // New values as far as the compiler knows (no instruction).
+#pragma unroll
+            for (int i = 0; i < 8; ++i) asm volatile("" : "+f"(av[i]));
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                asm volatile("" : "+f"(bq[h].x), "+f"(bq[h].y), "+f"(bq[h].z), "+f"(bq[h].w));
+            // The kernel's k-step: B as column pairs, pairs outer, rows inner.
+            const float2 bp[4] = {make_float2(bq[0].x, bq[0].y), make_float2(bq[0].z, bq[0].w),
+                                  make_float2(bq[1].x, bq[1].y), make_float2(bq[1].z, bq[1].w)};
+#pragma unroll
+            for (int jp = 0; jp < 4; ++jp)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    float2 c = make_float2(acc[i][2 * jp], acc[i][2 * jp + 1]);
+                    c = __ffma2_rn(make_float2(av[i], av[i]), bp[jp], c);
+                    acc[i][2 * jp] = c.x;
+                    acc[i][2 * jp + 1] = c.y;
+                }
+        }
+    }
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s += acc[i][j];
+    if (static_cast<int>(blockIdx.x) == sink_key) g_peak_sink[threadIdx.x] = s;
+}
+
 }  // namespace
 
 extern "C" int sgemm_fp32_peak_ex(int form, double target_ms, double* gflops, double* ms,
                                   double* flops, cudaStream_t stream) {
-    if (form != SGEMM_PEAK_FFMA && form != SGEMM_PEAK_FFMA2) return SGEMM_ERR_INVALID_VALUE;
+    if (form != SGEMM_PEAK_FFMA && form != SGEMM_PEAK_FFMA2 && form != SGEMM_PEAK_OUTER)
+        return SGEMM_ERR_INVALID_VALUE;
     if (!(target_ms >= 1.0) || target_ms > 60000.0) return SGEMM_ERR_INVALID_VALUE;
     int rc = sgemm_internal_device_ready();
     if (rc != SGEMM_OK) return rc;
     const int sms = sgemm_internal_sm_count();
-    const int grid = sms * kCtasPerSm;
+    const int grid = form == SGEMM_PEAK_OUTER ? sms : sms * kCtasPerSm;
+    if (form == SGEMM_PEAK_OUTER) {
+        const cudaError_t ea = cudaFuncSetAttribute(
+            outer_peak_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kOuterSmem);
+        if (ea != cudaSuccess) {
+            sgemm_internal_set_cuda_error(static_cast<int>(ea));
+            return SGEMM_ERR_CUDA;
+        }
+    }
     // mul slightly below 1 and a small add keep the chains bounded and finite.
     const float mul = 0.999999f, add = 1e-6f;
     const int no_sink = -1;   // blockIdx.x is never -1: the store never happens
@@ -98,7 +167,9 @@ extern "C" int sgemm_fp32_peak_ex(int form, double target_ms, double* gflops, do
     auto run = [&](long long iters, float* out_ms) -> cudaError_t {
         cudaError_t err = cudaEventRecord(e0, stream);
         if (err != cudaSuccess) return err;
-        if (form == SGEMM_PEAK_FFMA2)
+        if (form == SGEMM_PEAK_OUTER)
+            outer_peak_kernel<<<grid, kOuterThreads, kOuterSmem, stream>>>(iters, no_sink);
+        else if (form == SGEMM_PEAK_FFMA2)
             fp32_peak2_kernel<<<grid, kThreads, 0, stream>>>(mul, add, iters, no_sink);
         else
             fp32_peak_kernel<<<grid, kThreads, 0, stream>>>(mul, add, iters, no_sink);
@@ -123,10 +194,15 @@ extern "C" int sgemm_fp32_peak_ex(int form, double target_ms, double* gflops, do
         if ((e = run(want, &t)) != cudaSuccess || (e = run(want, &t)) != cudaSuccess) {
             result = SGEMM_ERR_LAUNCH;
         } else {
-            // 2 FLOP per FMA; an FFMA2 instruction performs two FMAs.
+            // 2 FLOP per FMA; an FFMA2 instruction performs two FMAs. Form 2:
+            // 64 FMAs per lane and k-step.
             const double fmas_per_instr = form == SGEMM_PEAK_FFMA2 ? 2.0 : 1.0;
-            const double f = 2.0 * fmas_per_instr * kChains * kUnroll *
-                             static_cast<double>(want) * static_cast<double>(grid) * kThreads;
+            const double f =
+                form == SGEMM_PEAK_OUTER
+                    ? 2.0 * 64.0 * kOuterSteps * static_cast<double>(want) *
+                          static_cast<double>(grid) * kOuterThreads
+                    : 2.0 * fmas_per_instr * kChains * kUnroll * static_cast<double>(want) *
+                          static_cast<double>(grid) * kThreads;
             if (gflops) *gflops = f / (static_cast<double>(t) * 1e-3) / 1e9;
             if (ms) *ms = t;
             if (flops) *flops = f;

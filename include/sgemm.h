@@ -297,6 +297,7 @@ SGEMM_API int sgemm_fp32_peak(double target_ms, double* gflops, double* ms, doub
 /* Instruction forms of the ceiling microbenchmark. */
 #define SGEMM_PEAK_FFMA 0    /* scalar FFMA chains (what sgemm_fp32_peak runs)        */
 #define SGEMM_PEAK_FFMA2 1   /* packed fma.rn.f32x2 chains, the form the SGEMM issues */
+#define SGEMM_PEAK_OUTER 2   /* the SGEMM's register outer product, no memory access  */
 
 /*
  * sgemm_fp32_peak_ex — sgemm_fp32_peak in a chosen instruction form. With
@@ -304,8 +305,14 @@ SGEMM_API int sgemm_fp32_peak(double target_ms, double* gflops, double* ms, doub
  * two-lane FMA (two single-rounding FP32 FMAs per instruction, 4 FLOP), the
  * instruction the SGEMM's inner loop is built from, so the ceiling is
  * measured on what the GEMM actually issues. Same grid, calibration, timing,
- * outputs and blocking as sgemm_fp32_peak; a form other than the two above
- * returns SGEMM_ERR_INVALID_VALUE.
+ * outputs and blocking as sgemm_fp32_peak. With SGEMM_PEAK_OUTER one CTA of
+ * 8 warps per SM (two per scheduler, the 128 x 128 kernel's occupancy) runs
+ * the GEMM's inner loop without its loads: each lane's 8 x 8 accumulators
+ * take 32 packed FMAs per k-step in the kernel's order, on A and B values
+ * held in registers (opaque to the compiler at every k-step); 128 FLOP per
+ * lane and k-step. It is the rate that instruction mix reaches when shared
+ * memory costs nothing, not a device peak. Another form returns
+ * SGEMM_ERR_INVALID_VALUE.
  */
 SGEMM_API int sgemm_fp32_peak_ex(int form, double target_ms, double* gflops, double* ms,
                                  double* flops, cudaStream_t stream);

@@ -31,6 +31,16 @@ def test_header_declares_the_binding_symbols():
     assert sorted(declared_functions()) == sorted(sg.EXPORTED_SYMBOLS)
 
 
+def test_header_constants_match_the_binding():
+    # Every SGEMM_* constant the header defines has the binding's value.
+    with open(os.path.join(ROOT, "include", "sgemm.h")) as f:
+        text = f.read()
+    defs = dict(re.findall(r"^#define (SGEMM_(?:ERR|OK|OP|PEAK)\w*)\s+(\d+)", text, flags=re.M))
+    assert {"SGEMM_OK", "SGEMM_PEAK_FFMA", "SGEMM_PEAK_FFMA2", "SGEMM_PEAK_OUTER"} <= set(defs)
+    for name, value in defs.items():
+        assert getattr(sg, name) == int(value), name
+
+
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
@@ -163,10 +173,11 @@ def test_transposed_leading_dimensions_follow_the_stored_shape(lib):
 def test_ceiling_forms_and_noalloc_status_without_gpu(lib):
     # An unknown instruction form or a bad target is refused before any
     # device work; the valid forms need a device and report a CUDA error here.
-    assert sg.sgemm_fp32_peak_ex(2, 10.0)[0] == sg.SGEMM_ERR_INVALID_VALUE
+    assert sg.sgemm_fp32_peak_ex(3, 10.0)[0] == sg.SGEMM_ERR_INVALID_VALUE
     assert sg.sgemm_fp32_peak_ex(-1, 10.0)[0] == sg.SGEMM_ERR_INVALID_VALUE
     assert sg.sgemm_fp32_peak_ex(sg.SGEMM_PEAK_FFMA2, 0.5)[0] == sg.SGEMM_ERR_INVALID_VALUE
-    for form in (sg.SGEMM_PEAK_FFMA, sg.SGEMM_PEAK_FFMA2):
+    assert sg.sgemm_fp32_peak_ex(sg.SGEMM_PEAK_OUTER, 0.5)[0] == sg.SGEMM_ERR_INVALID_VALUE
+    for form in (sg.SGEMM_PEAK_FFMA, sg.SGEMM_PEAK_FFMA2, sg.SGEMM_PEAK_OUTER):
         rc = sg.sgemm_fp32_peak_ex(form, 10.0)[0]
         assert rc not in (sg.SGEMM_OK, sg.SGEMM_ERR_INVALID_VALUE)
     # The scratch status check needs the device's scratch address: without a
