@@ -178,3 +178,36 @@ def test_cta_pair_mma_gives_the_single_cta_bits(shape, tmp_path):
     rows, cols = inputs.sample_entries(M, N, n=8192)
     ref, S = oracle.sgemm_ref_sampled(0.7, A, B, -1.3, C0, rows, cols)
     assert oracle.check(outs["256x256"][rows, cols], ref, S, K)["ok"]
+
+
+@pytest.mark.parametrize("shape", [(2304, 2304, 512), (512, 640, 500)],
+                         ids=["cta_pairs_256", "tiles_128"])
+def test_replays_of_a_captured_graph_give_the_eager_bits(shape):
+    # The call's split passes, the MMA kernel launched behind them by
+    # programmatic stream serialisation, and its stream-ordered workspace
+    # all go into a captured CUDA graph; three replays give the eager bits.
+    torch = pytest.importorskip("torch")
+    M, N, K = shape
+    A = inputs.fill("normal", 412, inputs.TID_A, M, K)
+    B = inputs.fill("normal", 412, inputs.TID_B, K, N)
+    C0 = inputs.fill("normal", 412, inputs.TID_C, M, N)
+    dA, dB, dC0 = (torch.from_numpy(x).cuda() for x in (A, B, C0))
+    eager = dC0.clone()
+    sg.sgemm_3xtf32_tensors(0.7, dA, dB, -1.3, eager)
+    sg.check_status()
+    want = eager.cpu().numpy()
+    ref, S = oracle.sgemm_ref(0.7, A, B, -1.3, C0)
+    assert oracle.check(want, ref, S, K)["ok"]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    work = dC0.clone()
+    with torch.cuda.graph(g, stream=s):
+        sg.sgemm_3xtf32_tensors(0.7, dA, dB, -1.3, work, stream=s)
+    for _ in range(3):
+        work.copy_(dC0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(work.cpu().numpy(), want)
+    sg.check_status()
