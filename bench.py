@@ -595,8 +595,10 @@ def launches_of(kernel: str) -> int:
     """Kernels one sgemm call enqueues: the SGEMM kernel, plus any operand
     packing copy and, when split tiles are finished by a second kernel
     ("+skfix"), that kernel. A stream-K tail finished inside the GEMM kernel
-    ("+sk") adds no launch."""
-    return 1 + sum(kernel.count(tag) for tag in ("+skfix", "+packA", "+packB"))
+    ("+sk") and a transposed copy of A the GEMM kernel makes itself
+    ("+packATfused") add no launch."""
+    n = 1 + sum(kernel.count(tag) for tag in ("+skfix", "+packA", "+packB"))
+    return n - kernel.count("+packATfused")
 
 
 def workload_report(args, lib, torch, stream, dev, w, host, ceiling, datasheet, headline=None,
@@ -864,7 +866,9 @@ def run_ours(args, w):
         "gpu_launches": args.steps * launches_per_step,
         "gpu_launches_note": ("per step: the sgemm kernel" +
                               (" + stream-K fixup kernel" if "+skfix" in kernel else "") +
-                              (" + transposing copy of A" if "+packAT" in kernel else
+                              (" (transposed copy of A made inside it)"
+                               if "+packATfused" in kernel else
+                               " + transposing copy of A" if "+packAT" in kernel else
                                " + packing copy of A" if "+packA" in kernel else "") +
                               (" + transposing copy of B" if "+packBT" in kernel else
                                " + packing copy of B" if "+packB" in kernel else "")) + (

@@ -97,7 +97,7 @@ cudaError_t fixup_launch(const GemmParams* p, int sk_tiles, int split, cudaStrea
 // One kernel family: a CTA tile and tuning knobs, instantiated for the four
 // (A, B) load-mode pairs of a row-major A and the two B load modes of a
 // transposed A (TMA) in mode_index order, plus its stream-K fixup.
-constexpr int kModes = 7;
+constexpr int kModes = 8;
 
 struct KernelFamily {
     const char* name;
@@ -109,15 +109,18 @@ struct KernelFamily {
 
 // Index into a family's modes: TMA/TMA, CP/TMA, TMA/CP, CP/CP for a
 // row-major A; then transposed A (TMA) with B by TMA, with B by cp.async;
-// then a row-major A transposed in shared memory, with B by TMA.
+// then a row-major A transposed in shared memory, with B by TMA; then the
+// transposed-A path on a transposed copy the kernel makes itself (Cfg::FUSED,
+// B by TMA; only the 128 x 128 family has it).
+constexpr int kModeFused = 7;
 inline constexpr int mode_index(int a_mode, int b_mode, int a_t = 0) {
     return a_mode == LOAD_TMA_XP ? 6 : a_t ? 4 + b_mode : a_mode + 2 * b_mode;
 }
 
 template <int BM, int BN, int S, int AM, int BMD, int FORDER, int EARLY, int LMAP, int AT = 0,
-          int ALOAD = 4, int TN = 8, int KSPLIT = 1, int CS = 1>
+          int ALOAD = 4, int TN = 8, int KSPLIT = 1, int CS = 1, int FUSED = 0>
 constexpr KernelEntry make_entry(const char* name) {
-    using C = Cfg<BM, BN, 32, S, AM, BMD, FORDER, EARLY, LMAP, AT, ALOAD, TN, KSPLIT, CS>;
+    using C = Cfg<BM, BN, 32, S, AM, BMD, FORDER, EARLY, LMAP, AT, ALOAD, TN, KSPLIT, CS, FUSED>;
     // A variant whose ring does not fit in shared memory is left out (no
     // entry points); the planner never picks it.
     if constexpr (!C::FITS)
@@ -128,7 +131,21 @@ constexpr KernelEntry make_entry(const char* name) {
                            &ws_prepare<C>, &ws_launch<C>};
 }
 
-#define SG_FAMILY_A(NAME, BM, BN, S, FORDER, EARLY, LMAP, ALOAD)                           \
+// A mode a family does not have (never planned).
+constexpr KernelEntry no_entry(const char* name, int bm, int bn) {
+    return KernelEntry{name, bm, bn, 32, 0, 0, 0, 0, 0, nullptr, nullptr};
+}
+
+// The fused transposed-copy mode of a family (kModeFused).
+template <int BM, int BN, int S, int FORDER, int EARLY, int LMAP>
+constexpr KernelEntry fused_entry(const char* name) {
+    return make_entry<BM, BN, S, LOAD_TMA, LOAD_TMA, FORDER, EARLY, LMAP, 1, 4, 8, 1, 1, 1>(name);
+}
+
+#define SG_FAMILY_A(NAME, BM, BN, S, FORDER, EARLY, LMAP, ALOAD) \
+    SG_FAMILY_AX(NAME, BM, BN, S, FORDER, EARLY, LMAP, ALOAD, no_entry(NAME "_ATtma_Btma", BM, BN))
+
+#define SG_FAMILY_AX(NAME, BM, BN, S, FORDER, EARLY, LMAP, ALOAD, FUSED_ENTRY)             \
     KernelFamily {                                                                          \
         NAME, BM, BN,                                                                       \
             {                                                                               \
@@ -146,6 +163,7 @@ constexpr KernelEntry make_entry(const char* name) {
                     NAME "_ATtma_Bcp"),                                                     \
                 make_entry<BM, BN, S, LOAD_TMA_XP, LOAD_TMA, FORDER, EARLY, LMAP>(            \
                     NAME "_Axp_Btma"),                                                      \
+                FUSED_ENTRY,                                                                \
             },                                                                              \
             &fixup_launch<BM, BN>                                                           \
     }
@@ -169,6 +187,7 @@ constexpr KernelEntry make_entry(const char* name) {
                     NAME "_ATtma_Bcp"),                                                     \
                 make_entry<BM, BN, S, LOAD_TMA_XP, LOAD_TMA, FORDER, EARLY, LMAP, 0, 4, TN>(  \
                     NAME "_Axp_Btma"),                                                      \
+                no_entry(NAME "_ATtma_Btma", BM, BN),                                       \
             },                                                                              \
             &fixup_launch<BM, BN>                                                           \
     }
@@ -193,6 +212,7 @@ constexpr KernelEntry make_entry(const char* name) {
                     NAME "_ATtma_Bcp"),                                                     \
                 make_entry<BM, BN, S, LOAD_TMA_XP, LOAD_TMA, 3, 1, 0, 0, 4, 8, KS, CS>(       \
                     NAME "_Axp_Btma"),                                                      \
+                no_entry(NAME "_ATtma_Btma", BM, BN),                                       \
             },                                                                              \
             &fixup_launch<BM, BN>, CS                                                       \
     }
@@ -201,6 +221,11 @@ constexpr KernelEntry make_entry(const char* name) {
 
 #define SG_FAMILY(NAME, BM, BN, S, FORDER, EARLY, LMAP) \
     SG_FAMILY_A(NAME, BM, BN, S, FORDER, EARLY, LMAP, 4)
+
+// The same with the fused transposed-copy mode.
+#define SG_FAMILY_FUSED(NAME, BM, BN, S, FORDER, EARLY, LMAP)    \
+    SG_FAMILY_AX(NAME, BM, BN, S, FORDER, EARLY, LMAP, 4,        \
+                 (fused_entry<BM, BN, S, FORDER, EARLY, LMAP>(NAME "_ATtma_Btma")))
 
 // Families, one translation unit each (compiled in parallel). The first
 // seven are the ones "auto" chooses between; the rest are tuning

@@ -194,6 +194,20 @@ __device__ __forceinline__ void st_release_gpu(unsigned long long* p, unsigned l
     asm volatile("st.release.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
 }
 
+// Orders this thread's accesses to global memory through the generic proxy
+// (ordinary loads and stores) with its accesses through the async proxy
+// (TMA): data another thread stored and released, and this thread acquired,
+// is then what a TMA load that follows reads.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Named barrier `id` (1..15) among `count` threads (a multiple of 32) of
+// the CTA; barrier 0 is __syncthreads.
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
+}
+
 // ---- timers ----------------------------------------------------------------
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {

@@ -119,8 +119,10 @@ bool shape_rule(int64_t M, int64_t N, int64_t K, Config* cfg) {
     return false;
 }
 
-// "<family>[:cpasync][:dp][:at|:noat|:xp][:fixup]" with <family> one of
-// auto, 128x128, 64x64, 128x64 or a registry name.
+// "<family>[:cpasync][:dp][:at|:atcopy|:noat|:xp][:fixup]" with <family> one
+// of auto, 128x128, 64x64, 128x64 or a registry name. ":at" takes the
+// transposed copy of A (made inside the GEMM kernel where the family can),
+// ":atcopy" the same copy made by a kernel of its own.
 int parse_config(const char* name, Config* out) {
     if (name == nullptr) return SGEMM_ERR_INVALID_VALUE;
     char buf[128];
@@ -137,6 +139,7 @@ int parse_config(const char* name, Config* out) {
         else if (std::strcmp(mod, "at") == 0) want_at = 1;
         else if (std::strcmp(mod, "noat") == 0) want_at = 0;
         else if (std::strcmp(mod, "xp") == 0) want_at = 2;
+        else if (std::strcmp(mod, "atcopy") == 0) want_at = 3;
         else if (std::strcmp(mod, "fixup") == 0) want_fx = 1;
         else return SGEMM_ERR_INVALID_VALUE;
         mod = next;
@@ -679,7 +682,7 @@ int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, 
     const bool xp_auto = xp_possible && fi != 2 && item_kt >= 4;
     pl->a_pre = false;
     pl->a_xp = false;
-    if (cfg.at == 1) {
+    if (cfg.at == 1 || cfg.at == 3) {
         pl->a_pre = copy_ok;
     } else if (cfg.at == 2) {
         pl->a_xp = xp_possible;
@@ -700,6 +703,8 @@ int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, 
     // (to make sure it accepts the shape) and encoded again on the real
     // workspace buffer at launch.
     const float* kPlaceholder = reinterpret_cast<const float*>(uintptr_t{1} << 20);
+    pl->a_fused = false;
+    pl->at_flags_off = 0;
     if (pl->a_pre) {
         const int64_t ld = (M + 3) & ~int64_t{3};
         if (tma_ok(kPlaceholder, ld, K, M) &&
@@ -777,7 +782,22 @@ int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, 
         if (a_mode == LOAD_TMA && b_mode == LOAD_TMA) a_mode = LOAD_TMA_XP;
         else pl->a_xp = false;
     }
-    const int mi = mode_index(a_mode, b_mode, (pl->a_t || pl->a_pre) ? 1 : 0);
+    int mi = mode_index(a_mode, b_mode, (pl->a_t || pl->a_pre) ? 1 : 0);
+    // The transposed copy made inside the GEMM kernel, where the family has
+    // that mode with the same CTAs per SM (so grid and schedule are those of
+    // the copy by a separate kernel) and ":atcopy" does not ask otherwise:
+    // the copy's ~20-28 us at 4096^3 then overlap the first tiles' work. The
+    // flags (one per unit of BK k-rows x BM columns) follow the copy.
+    if (pl->a_pre && b_mode == LOAD_TMA && cfg.at != 3 &&
+        dev->ctas_per_sm[fi][kModeFused] > 0 &&
+        dev->ctas_per_sm[fi][kModeFused] == dev->ctas_per_sm[fi][mi]) {
+        const size_t units = static_cast<size_t>((M + bm - 1) / bm) *
+                             static_cast<size_t>((K + bk - 1) / bk);
+        pl->a_fused = true;
+        pl->at_flags_off = pl->pack_a_bytes;
+        pl->pack_a_bytes += align256(units * 8);
+        mi = kModeFused;
+    }
     pl->k = &fam->modes[mi];
 
     GemmParams& p = pl->p;
@@ -883,9 +903,22 @@ int launch_plan(Plan* pl, int* status, float* ws, cudaStream_t stream) {
     // then be launched by programmatic serialisation behind it.
     const bool pdl = pdl_enabled();
     bool prior = false;
+    p.at_src = nullptr;
+    p.at_lds = 0;
+    p.at_flags = nullptr;
+    p.at_tag = 0;
     if (pl->pack_a) {
         float* a2 = reinterpret_cast<float*>(w);
-        if (pl->a_pre) {
+        if (pl->a_pre && pl->a_fused) {
+            // The GEMM kernel's transposer warps write the transpose of the
+            // row-major A (M x K) into a2 (K x lda_pack) themselves.
+            p.at_src = p.A;
+            p.at_lds = p.lda;
+            p.at_flags = reinterpret_cast<unsigned long long*>(w + pl->at_flags_off);
+            unsigned long long tag = g_sk_tag.fetch_add(1);
+            if (tag == 0) tag = g_sk_tag.fetch_add(1);   // after a wrap-around
+            p.at_tag = tag;
+        } else if (pl->a_pre) {
             // Row-major A (M x K) -> its transpose (K x lda_pack).
             e = launch_transpose_pack(p.A, p.lda, a2, pl->lda_pack, p.M, p.K, stream, false);
         } else {
@@ -895,7 +928,7 @@ int launch_plan(Plan* pl, int* status, float* ws, cudaStream_t stream) {
                               p.A, p.lda, a2, pl->lda_pack, rows, cols);
         }
         if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
-        prior = true;
+        prior = !pl->a_fused;
         const bool kt = pl->a_t || pl->a_pre;
         const bool ok = kt ? encode_2d(&pl->tmA, a2, p.K, p.M, pl->lda_pack, 32, pl->fam->bm, false)
                            : encode_2d(&pl->tmA, a2, p.M, p.K, pl->lda_pack, pl->fam->bm, 32, true);
@@ -944,12 +977,19 @@ int launch_plan(Plan* pl, int* status, float* ws, cudaStream_t stream) {
     return SGEMM_OK;
 }
 
+void unfuse_plan(Plan* pl) {
+    if (!pl->a_fused) return;
+    pl->a_fused = false;
+    pl->k = &pl->fam->modes[mode_index(LOAD_TMA, LOAD_TMA, 1)];
+}
+
 void plan_name(const Plan& pl, char* buf, int buflen) {
     if (buf == nullptr || buflen <= 0) return;
     if (pl.kind == 0) std::snprintf(buf, static_cast<size_t>(buflen), "none");
     else if (pl.kind == 1) std::snprintf(buf, static_cast<size_t>(buflen), "scale");
     else std::snprintf(buf, static_cast<size_t>(buflen), "%s%s%s%s", pl.k->name,
-                       pl.pack_a ? (pl.a_pre ? "+packAT" : "+packA") : "",
+                       pl.pack_a ? (pl.a_pre ? (pl.a_fused ? "+packATfused" : "+packAT") : "+packA")
+                                 : "",
                        pl.pack_b ? (pl.b_t ? "+packBT" : "+packB") : "",
                        pl.sk_tiles > 0 ? (pl.sk_fixup ? "+skfix" : "+sk") : "");
 }
@@ -1012,6 +1052,17 @@ int run_sgemm(int opa, int opb, int64_t M, int64_t N, int64_t K, float alpha, co
         } else {
             ws = static_cast<float*>(w);
         }
+    }
+    if (pl.a_fused) {
+        // A graph replays its flag value: with the fused copy a replay could
+        // take the previous run's flags for its own, so a call being captured
+        // makes the copy with a kernel of its own.
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+            (void)cudaGetLastError();
+            cap = cudaStreamCaptureStatusActive;
+        }
+        if (cap != cudaStreamCaptureStatusNone) unfuse_plan(&pl);
     }
     rc = launch_plan(&pl, mem->status, ws, stream);
     if (ws != nullptr) cudaFreeAsync(ws, stream);

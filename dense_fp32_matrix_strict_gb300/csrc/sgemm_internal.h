@@ -46,6 +46,13 @@ struct Plan {
     // a_pre: a row-major A copied transposed (K x lda_pack) into the packed
     // A buffer, then read through the transposed-A kernel path.
     bool a_pre = false;
+    // a_fused (with a_pre): that copy is made inside the GEMM kernel by its
+    // transposer warps (Cfg::FUSED), unit by unit with a flag per unit after
+    // the copy at offset at_flags_off of the packed A buffer, instead of by
+    // a kernel before it. Not used for a call being captured into a graph
+    // (a replay would see the flags its previous run left).
+    bool a_fused = false;
+    size_t at_flags_off = 0;
     // a_xp: a row-major A transposed in shared memory by the kernel's
     // transposer warps (mode LOAD_TMA_XP).
     bool a_xp = false;
@@ -90,10 +97,16 @@ int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, 
 // ws_bytes == 0).
 int launch_plan(Plan* pl, int* status, float* ws, cudaStream_t stream);
 
+// Turns a fused transposed copy of A (a_fused) into the copy by a kernel of
+// its own, same kernel otherwise; for calls captured into a CUDA graph.
+void unfuse_plan(Plan* pl);
+
 // Human-readable plan name into buf ("none", "scale", or the kernel name,
-// with "+packA" / "+packB" for operands copied to aligned buffers, "+sk"
-// when the stream-K tail is used and finished in the kernel, "+skfix" when
-// the fixup kernel finishes it).
+// with "+packA" / "+packB" for operands copied to aligned buffers, "+packAT"
+// for the transposed copy of A by a kernel of its own, "+packATfused" for
+// that copy made inside the GEMM kernel, "+sk" when the stream-K tail is
+// used and finished in the kernel, "+skfix" when the fixup kernel finishes
+// it).
 void plan_name(const Plan& pl, char* buf, int buflen);
 
 // The return code of a status word: SGEMM_ERR_DEVICE_TIMEOUT for any

@@ -118,6 +118,16 @@ struct GemmParams {
     unsigned long long* sk_flags;   // sk_ctas flags (sk_fixup == 0)
     unsigned long long sk_tag;      // this launch's flag value, never 0
     int sk_fixup;
+    // Transposed A made inside the kernel (Cfg::FUSED): the transposer warps
+    // of every CTA write A (row-major at at_src, row stride at_lds) as its
+    // transpose into the workspace at A (K rows of lda floats), one unit of
+    // BK k-rows x BM columns at a time, and set at_flags[tm * k_tiles + kt]
+    // to at_tag (release) when unit (tm, kt) is complete; the TMA producer
+    // waits (bounded, acquire) for a unit's flag before it loads the unit.
+    const float* at_src;
+    long long at_lds;
+    unsigned long long* at_flags;
+    unsigned long long at_tag;      // this launch's flag value, never 0
 };
 
 // Kernel configuration. FORDER: FMA form of the outer product (0: scalar
@@ -148,7 +158,7 @@ struct GemmParams {
 //   grid is tiles x CS, one tile per cluster, no stream-K tail.
 template <int BM_, int BN_, int BK_, int STAGES_, int A_MODE_, int B_MODE_, int FORDER_ = 2,
           int EARLY_ = 0, int LMAP_ = 0, int A_T_ = 0, int ALOAD_ = 4, int TN_ = 8,
-          int KSPLIT_ = 1, int CS_ = 1>
+          int KSPLIT_ = 1, int CS_ = 1, int FUSED_ = 0>
 struct Cfg {
     static constexpr int BM = BM_, BN = BN_, BK = BK_, STAGES = STAGES_;
     static constexpr int A_MODE = A_MODE_, B_MODE = B_MODE_;
@@ -181,13 +191,17 @@ struct Cfg {
     static constexpr int CONSUMER_WARPS = GROUP_WARPS * KSPLIT;
     static constexpr int CONSUMERS = CONSUMER_WARPS * 32;
     static constexpr bool ANY_CP = (A_MODE == LOAD_CPASYNC) || (B_MODE == LOAD_CPASYNC);
+    // FUSED: the transposed-A path with the transposed copy of a row-major A
+    // made inside this kernel by three transposer warps per CTA (see
+    // GemmParams::at_flags and at_transposer()) instead of a kernel before it.
+    static constexpr bool FUSED = FUSED_ != 0;
     static constexpr bool ANY_TMA = (A_MODE != LOAD_CPASYNC) || (B_MODE == LOAD_TMA);
     // cp.async producers: one warp per SM sub-partition so the copy
     // instructions do not all land on one scheduler. With the in-smem
     // transpose: one TMA warp and three transposer warps (12 warps in all
     // for 128 x 128, still three per scheduler, so 168 registers a thread).
-    static constexpr int PRODUCER_WARPS = (ANY_CP || A_XP) ? 4 : 1;
-    static constexpr int TRANSPOSERS = A_XP ? 96 : 0;
+    static constexpr int PRODUCER_WARPS = (ANY_CP || A_XP || FUSED) ? 4 : 1;
+    static constexpr int TRANSPOSERS = (A_XP || FUSED) ? 96 : 0;
     static constexpr int THREADS = CONSUMERS + 32 * PRODUCER_WARPS;
     static constexpr int A_BYTES = BM * BK * 4;
     static constexpr int B_BYTES = BK * BN * 4;
@@ -202,10 +216,14 @@ struct Cfg {
     static constexpr int CS = CS_;
     static_assert(CS == 1 || CS == 2 || CS == 4, "CS is 1, 2 or 4");
     static constexpr int CKS_BYTES = (CS - 1) * BM * BN * 4;        // other ranks' sums
+    // FUSED: the transposer warps' staging tile, BM rows of BK + 1 floats.
+    static constexpr int XT_BYTES = FUSED ? BM * (BK + 1) * 4 : 0;
     static constexpr int SMEM_BYTES = 1024 /* alignment slack */ +
                                       STAGES * (A_BYTES + B_BYTES + RAW_BYTES) + RED_BYTES +
-                                      CKS_BYTES + (3 * STAGES + 6) * 8;
-    static constexpr bool FITS = SMEM_BYTES <= 227 * 1024;
+                                      CKS_BYTES + XT_BYTES + (3 * STAGES + 6) * 8;
+    static constexpr bool FUSED_OK = !FUSED || (A_T && A_MODE == LOAD_TMA &&
+                                                B_MODE == LOAD_TMA && KSPLIT == 1 && CS == 1);
+    static constexpr bool FITS = SMEM_BYTES <= 227 * 1024 && FUSED_OK;
     // Tiles of at most 128 x 64 are sized to run two CTAs per SM.
     static constexpr int MIN_BLOCKS = (BM * BN * KSPLIT <= 128 * 64) ? 2 : 1;
 };
@@ -441,6 +459,18 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmA, const CUtensorM
             const uint32_t tx = tx0 + 8 * s;
             const uint32_t dA = sA + s * C::A_BYTES, dB = sB + s * C::B_BYTES;
             const int k0 = kt * C::BK;
+            if (C::FUSED && tma_thread) {
+                // The unit of the transposed A this stage reads is written
+                // by some CTA's transposer warps in this kernel: wait for
+                // its flag, then order the async-proxy load after it.
+                SG_DCHECK(p, tm < p.tiles_m && kt < p.k_tiles);
+                if (!wait_flag_bounded(p.at_flags + static_cast<long long>(tm) * p.k_tiles + kt,
+                                       p.at_tag, p, STATUS_PRODUCER_TIMEOUT)) {
+                    ok = false;
+                    break;
+                }
+                fence_proxy_async_global();
+            }
             if (tma_thread) {
                 mbar_arrive_expect_tx(tx, C::TX_BYTES);
                 if (C::A_XP) {
@@ -542,6 +572,85 @@ __device__ __forceinline__ void transposer(const GemmParams& p, const uint8_t* r
             mbar_arrive(full0 + 8 * s);
             if (++s == C::STAGES) { s = 0; ph ^= 1u; }
         }
+    }
+}
+
+// ---- transposer warps of the fused transposed copy (Cfg::FUSED) -------------------
+
+// Three warps (t = 0..95) of every CTA write the transposed copy of the
+// row-major A that the TMA producers load, unit by unit: unit (tm, kt) is A's
+// rows tm BM .. + BM and columns kt BK .. + BK, stored at rows kt BK .. and
+// columns tm BM .. of the copy. The units are taken in the order the tiles
+// first need them (raster group by raster group, then k-tile, then tile row)
+// and dealt out round-robin over the CTAs, so the first wave's first k-tiles
+// are done first, by many CTAs at once. A unit goes through a staging tile
+// in shared memory (BM rows of BK + 1 floats: the 128-byte row reads and the
+// column reads both stay within a bank or two), rows of A in, rows of the
+// copy out, both 16-byte vectors where A allows. Elements past M or K are
+// neither read nor written (the tensor map's bounds cover them with zeros).
+// After a unit's stores every thread fences them for the async proxy and
+// at GPU scope, the 96 threads meet at named barrier 1, and one releases
+// the unit's flag. Nothing here waits on another CTA, so every unit gets
+// done.
+template <class C>
+__device__ __forceinline__ void at_transposer(const GemmParams& p, float* xt, int t) {
+    constexpr int BM = C::BM, BK = C::BK, LD = C::BK + 1;
+    static_assert(BK == 32 && BM % 4 == 0, "unit of 32 k-rows");
+    float* at = const_cast<float*>(p.A);
+    const bool vec = (reinterpret_cast<uintptr_t>(p.at_src) % 16 == 0) && (p.at_lds % 4 == 0);
+    const long long per_group = static_cast<long long>(p.group_m) * p.k_tiles;
+    const long long units = static_cast<long long>(p.tiles_m) * p.k_tiles;
+    for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+        const int g = static_cast<int>(u / per_group);
+        const long long r = u - g * per_group;
+        const int gm = min(p.tiles_m - g * p.group_m, p.group_m);
+        const int kt = static_cast<int>(r / gm);
+        const int tm = g * p.group_m + static_cast<int>(r - static_cast<long long>(kt) * gm);
+        SG_DCHECK(p, tm >= 0 && tm < p.tiles_m && kt >= 0 && kt < p.k_tiles);
+        const int m0 = tm * BM, k0 = kt * BK;
+        // A rows in: BM rows x BK / 4 float4.
+#pragma unroll 2
+        for (int q = t; q < BM * (BK / 4); q += C::TRANSPOSERS) {
+            const int rr = q / (BK / 4), c4 = (q % (BK / 4)) * 4;
+            const int m = m0 + rr, k = k0 + c4;
+            float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (m < p.M) {
+                const float* sp = p.at_src + static_cast<long long>(m) * p.at_lds + k;
+                if (vec && k + 3 < p.K) {
+                    v = *reinterpret_cast<const float4*>(sp);
+                } else {
+                    if (k < p.K) v.x = sp[0];
+                    if (k + 1 < p.K) v.y = sp[1];
+                    if (k + 2 < p.K) v.z = sp[2];
+                    if (k + 3 < p.K) v.w = sp[3];
+                }
+            }
+            SG_DCHECK(p, (rr * LD + c4 + 3) * 4 + 4 <= C::XT_BYTES);
+            float* d = xt + rr * LD + c4;
+            d[0] = v.x;
+            d[1] = v.y;
+            d[2] = v.z;
+            d[3] = v.w;
+        }
+        named_bar_sync(1, C::TRANSPOSERS);
+        // Rows of the copy out: BK rows x BM / 4 float4 (lda is a multiple of
+        // 4 and m a multiple of 4 below M, so the float4 stays in the row).
+#pragma unroll 2
+        for (int q = t; q < BK * (BM / 4); q += C::TRANSPOSERS) {
+            const int kk = q / (BM / 4), m4 = (q % (BM / 4)) * 4;
+            const int k = k0 + kk, m = m0 + m4;
+            if (k < p.K && m < p.M) {
+                SG_DCHECK(p, m + 3 < p.lda && ((m4 + 3) * LD + kk) * 4 + 4 <= C::XT_BYTES);
+                *reinterpret_cast<float4*>(at + static_cast<long long>(k) * p.lda + m) =
+                    make_float4(xt[m4 * LD + kk], xt[(m4 + 1) * LD + kk], xt[(m4 + 2) * LD + kk],
+                                xt[(m4 + 3) * LD + kk]);
+            }
+        }
+        fence_proxy_async_global();
+        __threadfence();
+        named_bar_sync(1, C::TRANSPOSERS);
+        if (t == 0)
+            st_release_gpu(p.at_flags + static_cast<long long>(tm) * p.k_tiles + kt, p.at_tag);
     }
 }
 
@@ -987,8 +1096,10 @@ sgemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     uint8_t* sRaw = sB + C::STAGES * C::B_BYTES;      // C::RAW_BYTES per stage
     float4* red = reinterpret_cast<float4*>(sRaw + C::STAGES * C::RAW_BYTES);  // RED_BYTES
     float4* cks = reinterpret_cast<float4*>(sRaw + C::STAGES * C::RAW_BYTES + C::RED_BYTES);
+    float* xt = reinterpret_cast<float*>(sRaw + C::STAGES * C::RAW_BYTES + C::RED_BYTES +
+                                         C::CKS_BYTES);   // C::XT_BYTES
     uint64_t* bars = reinterpret_cast<uint64_t*>(sRaw + C::STAGES * C::RAW_BYTES + C::RED_BYTES +
-                                                 C::CKS_BYTES);
+                                                 C::CKS_BYTES + C::XT_BYTES);
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = smem_u32(bars + C::STAGES);
     const uint32_t raw0 = smem_u32(bars + 2 * C::STAGES);
@@ -1031,6 +1142,8 @@ sgemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         const int pw = warp - C::CONSUMER_WARPS;
         if (C::A_XP && pw > 0)
             transposer<C>(p, sRaw, sA, raw0, full0, (pw - 1) * 32 + lane);
+        else if (C::FUSED && pw > 0)
+            at_transposer<C>(p, xt, (pw - 1) * 32 + lane);
         else
             producer<C>(&tmA, &tmB, p, smem_u32(sA), smem_u32(sB), smem_u32(sRaw), full0, empty0,
                         raw0, sk_pub, pw, lane);

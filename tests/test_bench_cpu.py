@@ -108,6 +108,8 @@ def test_cpu_baseline_plan_per_workload():
                      "ragged_4093x5120x1531_normal"]
     assert bench.SINGLE_THREAD_WORKLOADS == ("sq256_uniform", "sq1024_int")
     assert bench.launches_of("ws_128x128x32_s4_ATtma_Btma+packAT+sk") == 2
+    assert bench.launches_of("ws_128x128x32_s4_ATtma_Btma+packATfused+sk") == 1
+    assert bench.launches_of("ws_128x128x32_s4_ATtma_Btma+packATfused+packB+skfix") == 3
     assert bench.launches_of("ws_128x128x32_s4_ATtma_Btma+packAT+skfix") == 3
     assert bench.launches_of("ws_128x128x32_s4_Atma_Btma+sk") == 1
     assert bench.launches_of("ws_128x64x32_s4_k2_Axp_Btma") == 1
