@@ -30,12 +30,14 @@
  * SMs (the stream-K tail: one slot of BM x BN floats, at most 64 KB, and one
  * 8-byte flag per CTA; two slots per CTA when the configuration suffix
  * ":fixup" selects the separate fixup kernel); a row-major A large
- * enough that the kernel runs faster on its transpose, which is copied
- * first (K x M floats, M rounded up to 4); and an operand that TMA cannot
- * load in place (base or leading dimension not 16-byte aligned) but that
- * the kernel reads often enough (A when N >= 256, B when M >= 256), copied
- * to an aligned buffer (rows x cols rounded up to 4 floats). If that
- * allocation fails the call uses none of them.
+ * enough that the kernel runs faster on its transpose (K x M floats, M
+ * rounded up to 4, written by the GEMM kernel itself while its first tiles
+ * run, with one 8-byte flag per 32 x 128 block of it; by a copy kernel
+ * before it when the call is being captured into a CUDA graph); and an
+ * operand that TMA cannot load in place (base or leading dimension not
+ * 16-byte aligned) but that the kernel reads often enough (A when N >= 256,
+ * B when M >= 256), copied to an aligned buffer (rows x cols rounded up to
+ * 4 floats). If that allocation fails the call uses none of them.
  */
 #ifndef SGEMM_GB300_H
 #define SGEMM_GB300_H
@@ -241,7 +243,10 @@ SGEMM_API int sgemm_plan_ex(int opa, int opb, int64_t M, int64_t N, int64_t K, f
  * with cp.async even when TMA could be used (a transposed A excepted: it is
  * always loaded by TMA), ":dp" never splits the last
  * wave (plain data-parallel schedule), ":at" / ":noat" always / never
- * copy a row-major A transposed first (the default decides by size), e.g.
+ * read a row-major A through a transposed copy (the default decides by
+ * size; the 128 x 128 kernel makes the copy itself), ":atcopy" the same
+ * copy made by a copy kernel first, ":xp" the transpose in shared memory
+ * instead, ":fixup" the stream-K tail finished by a second kernel, e.g.
  * "128x128:cpasync:dp" or "auto:dp". Returns SGEMM_ERR_INVALID_VALUE for an
  * unknown name. The environment variable SGEMM_FORCE_CONFIG, read on the
  * first call, sets the same thing.
