@@ -62,7 +62,7 @@ int64_t round4(int64_t n) { return (n + 3) & ~int64_t{3}; }
 // Events of one call; destroyed when the call returns (the driver releases
 // an event still pending once it completes).
 struct CallEvents {
-    static constexpr int kCount = 11;
+    static constexpr int kCount = 23;
     cudaEvent_t ev[kCount] = {};
     int made = 0;
     cudaError_t create() {
@@ -163,11 +163,21 @@ extern "C" int sgemm_host(int64_t M, int64_t N, int64_t K, float alpha, const fl
     cudaEvent_t ev_in[2] = {evs.ev[1], evs.ev[2]};      // block inputs landed
     cudaEvent_t ev_done[2] = {evs.ev[3], evs.ev[4]};    // block GEMM finished
     cudaEvent_t ev_out[2] = {evs.ev[5], evs.ev[6]};     // block of C back on the host
-    cudaEvent_t ev_bc[4] = {evs.ev[7], evs.ev[8], evs.ev[9], evs.ev[10]};   // B chunks landed
-    // Block 0 starts on the first quarter of B instead of all of it: with
-    // several row blocks and N >= 2048, B comes in 4 column chunks (whole
-    // multiples of 128 columns) and block 0's GEMM runs chunk by chunk.
-    int nbc = (nblk > 1 && N >= 2048 && reads_ab) ? 4 : 1;
+    cudaEvent_t* ev_part = evs.ev + 7;   // up to 16: B chunks or k-slabs landed
+    // Block 0 starts before all of its inputs are on the device. With
+    // several row blocks and K >= 1024 its A rows and B come in k-slabs (512
+    // k each, whole k-tiles, at most 16 slabs) and its GEMM runs slab by slab,
+    // adding each slab's product to C (beta on the first, 1 after): the first
+    // GEMM starts once 512 k of A's first block and of B have landed (10 MB
+    // at 4096^3) instead of the block's A and a quarter of B (29 MB). The
+    // extra rounding of C between slabs stays inside the error bound. With
+    // N >= 2048 and shorter K, B comes in 4 column chunks (whole multiples of
+    // 128 columns) and block 0's GEMM runs chunk by chunk.
+    const bool kslab = nblk > 1 && reads_ab && K >= 1024;
+    int64_t ks = 512;
+    if (kslab && (K + ks - 1) / ks > 16) ks = ((K + 15) / 16 + 31) / 32 * 32;
+    const int nks = kslab ? static_cast<int>((K + ks - 1) / ks) : 0;
+    int nbc = (!kslab && nblk > 1 && N >= 2048 && reads_ab) ? 4 : 1;
     int64_t nc = ((N + nbc - 1) / nbc + 127) / 128 * 128;
     if (nc > N) nc = N;
     nbc = static_cast<int>((N + nc - 1) / nc);
@@ -203,7 +213,7 @@ extern "C" int sgemm_host(int64_t M, int64_t N, int64_t K, float alpha, const fl
                 (e = cudaStreamWaitEvent(cs->h2d, ev_out[j], 0)) != cudaSuccess)
                 return fail(e, SGEMM_ERR_CUDA);
         }
-        if (reads_ab &&
+        if (reads_ab && !(i == 0 && kslab) &&
             (e = cudaMemcpy2DAsync(dA[j], ldk * 4, A + r0 * lda, lda * 4, K * 4, rows,
                                    cudaMemcpyHostToDevice, cs->h2d)) != cudaSuccess)
             return fail(e, SGEMM_ERR_CUDA);
@@ -216,7 +226,27 @@ extern "C" int sgemm_host(int64_t M, int64_t N, int64_t K, float alpha, const fl
             return fail(e, SGEMM_ERR_CUDA);
         if (i >= 2 && (e = cudaStreamWaitEvent(stream, ev_out[j], 0)) != cudaSuccess)
             return fail(e, SGEMM_ERR_CUDA);
-        if (i == 0 && reads_ab) {
+        if (i == 0 && kslab) {
+            // A's first block and B in k-slabs; block 0's GEMM follows them
+            // slab by slab.
+            for (int sl = 0; sl < nks; ++sl) {
+                const int64_t k0 = sl * ks;
+                const int64_t kl = (K - k0) < ks ? (K - k0) : ks;
+                if ((e = cudaMemcpy2DAsync(dA[j] + k0, ldk * 4, A + r0 * lda + k0, lda * 4, kl * 4,
+                                           rows, cudaMemcpyHostToDevice, cs->h2d)) != cudaSuccess ||
+                    (e = cudaMemcpy2DAsync(dB + k0 * ldn, ldn * 4, B + k0 * ldb, ldb * 4, N * 4, kl,
+                                           cudaMemcpyHostToDevice, cs->h2d)) != cudaSuccess ||
+                    (e = cudaEventRecord(ev_part[sl], cs->h2d)) != cudaSuccess ||
+                    (e = cudaStreamWaitEvent(stream, ev_part[sl], 0)) != cudaSuccess)
+                    return fail(e, SGEMM_ERR_CUDA);
+                rc = sgemm(rows, N, kl, alpha, dA[j] + k0, ldk, dB + k0 * ldn, ldn,
+                           sl == 0 ? beta : 1.0f, dC[j], ldn, stream);
+                if (rc != SGEMM_OK) {
+                    release();
+                    return rc;
+                }
+            }
+        } else if (i == 0 && reads_ab) {
             // B in column chunks behind block 0's inputs; block 0's GEMM
             // follows them chunk by chunk.
             for (int c = 0; c < nbc; ++c) {
@@ -224,8 +254,8 @@ extern "C" int sgemm_host(int64_t M, int64_t N, int64_t K, float alpha, const fl
                 const int64_t cols = (N - c0) < nc ? (N - c0) : nc;
                 if ((e = cudaMemcpy2DAsync(dB + c0, ldn * 4, B + c0, ldb * 4, cols * 4, K,
                                            cudaMemcpyHostToDevice, cs->h2d)) != cudaSuccess ||
-                    (e = cudaEventRecord(ev_bc[c], cs->h2d)) != cudaSuccess ||
-                    (e = cudaStreamWaitEvent(stream, ev_bc[c], 0)) != cudaSuccess)
+                    (e = cudaEventRecord(ev_part[c], cs->h2d)) != cudaSuccess ||
+                    (e = cudaStreamWaitEvent(stream, ev_part[c], 0)) != cudaSuccess)
                     return fail(e, SGEMM_ERR_CUDA);
                 rc = sgemm(rows, cols, K, alpha, dA[j], ldk, dB + c0, ldn, beta, dC[j] + c0, ldn,
                            stream);

@@ -126,9 +126,12 @@ SGEMM_API int sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float* A
  * and C in HOST memory (page-locked memory, from cudaHostAlloc or
  * cudaHostRegister, lets the copies overlap the computation; pageable memory
  * works but each copy then blocks). The library copies row blocks of A (and
- * of C when beta != 0) and B (in column chunks behind the first block of A)
+ * of C when beta != 0) and B (in k-slabs together with the first block of
+ * A when K >= 1024, else in column chunks behind it)
  * to the current device on a copy stream of its own, runs the GEMM of each
- * block on `stream` (the first block chunk by chunk as B arrives), and
+ * block on `stream` (the first block slab by slab, or chunk by chunk, as B
+ * arrives; slab by slab C takes one extra rounding per slab, inside the
+ * same error bound), and
  * copies each finished block of C back on a second copy stream, so the
  * transfers of one block overlap the GEMMs of others. Problems below 5 GFLOP run as one block;
  * larger ones end on a short block (128 to 256 rows, taking any ragged rows
