@@ -126,26 +126,27 @@ SGEMM_API int sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float* A
  * and C in HOST memory (page-locked memory, from cudaHostAlloc or
  * cudaHostRegister, lets the copies overlap the computation; pageable memory
  * works but each copy then blocks). The library copies row blocks of A (and
- * of C when beta != 0) and B (in k-slabs together with the first block of
- * A when K >= 1024, else in column chunks behind it)
- * to the current device on a copy stream of its own, runs the GEMM of each
- * block on `stream` (the first block slab by slab, or chunk by chunk, as B
- * arrives; slab by slab C takes one extra rounding per slab, inside the
- * same error bound), and
- * copies each finished block of C back on a second copy stream, so the
- * transfers of one block overlap the GEMMs of others. Problems below 5 GFLOP run as one block;
- * larger ones end on a short block (128 to 256 rows, taking any ragged rows
- * of M) after up to 8 blocks of about 1024 rows, the first of them shorter
- * where the rows do not divide evenly. The device buffers come
- * from the library's stream-ordered pool (B, plus two A and two C blocks:
- * 4 (K N + 2 mb (K + N)) bytes, mb the block height; SGEMM_ERR_CUDA if the
- * pool cannot supply them). The call is asynchronous and ordered on
- * `stream`: the copies start after the work already queued there, and
- * `stream` passes the end of the call only when all of C is in host memory,
- * so a host read of C must follow a synchronisation of `stream`. Host
- * buffers must stay valid until then. Elements between rows (ld > width)
- * are never read or written. Not part of the pages' design: it is this
- * library's host-resident entry point.
+ * of C when beta != 0) and B to the current device on a copy stream of its
+ * own, runs the GEMM of each block on `stream`, and copies each finished
+ * block of C back on a second copy stream, so the transfers of one block
+ * overlap the GEMMs of others. Problems below 5 GFLOP run as one block.
+ * Larger ones end on a short block (128 to 256 rows, taking any ragged rows
+ * of M). With K >= 1024 the first block's A rows and B arrive in k-slabs of
+ * 512 k and its GEMM runs slab by slab as they land (C then takes one extra
+ * rounding per slab, inside the same error bound); with beta == 0 the blocks
+ * are then 1024 rows, blocks of up to 2048, and 768 rows before the short
+ * one. Otherwise B comes in column chunks behind the first block, whose GEMM
+ * runs chunk by chunk, and the blocks are of about 1024 rows (at most 8),
+ * the first of them shorter where the rows do not divide evenly. The device
+ * buffers come from the library's stream-ordered pool (B, plus two A and
+ * two C blocks: 4 (K N + 2 mb (K + N)) bytes, mb the largest block height;
+ * SGEMM_ERR_CUDA if the pool cannot supply them). The call is asynchronous
+ * and ordered on `stream`: the copies start after the work already queued
+ * there, and `stream` passes the end of the call only when all of C is in
+ * host memory, so a host read of C must follow a synchronisation of
+ * `stream`. Host buffers must stay valid until then. Elements between rows
+ * (ld > width) are never read or written. Not part of the pages' design: it
+ * is this library's host-resident entry point.
  */
 SGEMM_API int sgemm_host(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
                          int64_t lda, const float* B, int64_t ldb, float beta, float* C,
