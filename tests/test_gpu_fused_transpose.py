@@ -137,3 +137,32 @@ def test_captured_call_copies_with_its_own_kernel():
         torch.cuda.synchronize()
         assert np.array_equal(work.cpu().numpy(), want)
     sg.check_status()
+
+
+def test_two_streams_concurrently():
+    # Two fused calls at a time on two streams with no ordering between them:
+    # each has its own workspace, flags and flag value; a kernel whose CTAs
+    # are not all on the GPU yet (the other kernel still holds SMs) waits for
+    # them within its bounded waits. Three rounds, every result checked.
+    torch = pytest.importorskip("torch")
+    M, N, K = 1000, 3000, 4000
+    A1, B1, C1 = gen(M, N, K, seed=1330)
+    A2, B2, C2 = gen(M, N, K, seed=1331)
+    d = [torch.from_numpy(x).cuda() for x in (A1, B1, C1, A2, B2, C2)]
+    name, _ = sg.plan_tensors(0.7, d[0], d[1], -1.3, d[2])
+    assert "+packATfused" in name, name
+    want1, _, _ = run_cfg("auto:atcopy", 0.7, A1, B1, -1.3, C1)
+    want2, _, _ = run_cfg("auto:atcopy", 0.7, A2, B2, -1.3, C2)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    for _ in range(3):
+        with torch.cuda.stream(s1):
+            c1 = d[2].clone()
+            sg.sgemm_tensors(0.7, d[0], d[1], -1.3, c1, stream=s1)
+        with torch.cuda.stream(s2):
+            c2 = d[5].clone()
+            sg.sgemm_tensors(0.7, d[3], d[4], -1.3, c2, stream=s2)
+        torch.cuda.synchronize()
+        sg.check_status()
+        assert np.array_equal(c1.cpu().numpy(), want1)
+        assert np.array_equal(c2.cpu().numpy(), want2)
