@@ -595,10 +595,10 @@ def launches_of(kernel: str) -> int:
     """Kernels one sgemm call enqueues: the SGEMM kernel, plus any operand
     packing copy and, when split tiles are finished by a second kernel
     ("+skfix"), that kernel. A stream-K tail finished inside the GEMM kernel
-    ("+sk") and a transposed copy of A the GEMM kernel makes itself
-    ("+packATfused") add no launch."""
+    ("+sk") and copies the GEMM kernel makes itself ("+packATfused",
+    "+packBTfused") add no launch."""
     n = 1 + sum(kernel.count(tag) for tag in ("+skfix", "+packA", "+packB"))
-    return n - kernel.count("+packATfused")
+    return n - kernel.count("+packATfused") - kernel.count("+packBTfused")
 
 
 def workload_report(args, lib, torch, stream, dev, w, host, ceiling, datasheet, headline=None,

@@ -788,14 +788,33 @@ int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, 
     // the copy by a separate kernel) and ":atcopy" does not ask otherwise:
     // the copy's ~20-28 us at 4096^3 then overlap the first tiles' work. The
     // flags (one per unit of BK k-rows x BM columns) follow the copy.
-    if (pl->a_pre && b_mode == LOAD_TMA && cfg.at != 3 &&
-        dev->ctas_per_sm[fi][kModeFused] > 0 &&
-        dev->ctas_per_sm[fi][kModeFused] == dev->ctas_per_sm[fi][mi]) {
+    // The same for the row-major copy of a transposed B, when A is read
+    // through the transposed-A path anyway (its copy made here too, or A
+    // given transposed and read in place). Both only with a first wave of
+    // whole tiles: the tail's CTAs start all along the k-range at once and
+    // would wait for units the round-robin has not reached (6.1).
+    pl->b_fused = false;
+    pl->bt_flags_off = 0;
+    const int64_t tiles_all = ((M + bm - 1) / bm) * ((N + bn - 1) / bn);
+    const bool fuse_ok = cfg.at != 3 && b_mode == LOAD_TMA &&
+                         dev->ctas_per_sm[fi][kModeFused] > 0 &&
+                         dev->ctas_per_sm[fi][kModeFused] == dev->ctas_per_sm[fi][mi] &&
+                         tiles_all >= static_cast<int64_t>(dev->ctas_per_sm[fi][kModeFused]) * sms;
+    if (fuse_ok && pl->a_pre) {
         const size_t units = static_cast<size_t>((M + bm - 1) / bm) *
                              static_cast<size_t>((K + bk - 1) / bk);
         pl->a_fused = true;
         pl->at_flags_off = pl->pack_a_bytes;
         pl->pack_a_bytes += align256(units * 8);
+        mi = kModeFused;
+    }
+    if (fuse_ok && pl->b_t && pl->pack_b &&
+        (pl->a_fused || (pl->a_t && !pl->pack_a && a_mode == LOAD_TMA))) {
+        const size_t units = static_cast<size_t>((N + bn - 1) / bn) *
+                             static_cast<size_t>((K + bk - 1) / bk);
+        pl->b_fused = true;
+        pl->bt_flags_off = pl->pack_b_bytes;
+        pl->pack_b_bytes += align256(units * 8);
         mi = kModeFused;
     }
     pl->k = &fam->modes[mi];
@@ -907,6 +926,14 @@ int launch_plan(Plan* pl, int* status, float* ws, cudaStream_t stream) {
     p.at_lds = 0;
     p.at_flags = nullptr;
     p.at_tag = 0;
+    p.bt_src = nullptr;
+    p.bt_lds = 0;
+    p.bt_flags = nullptr;
+    if (pl->a_fused || pl->b_fused) {
+        unsigned long long tag = g_sk_tag.fetch_add(1);
+        if (tag == 0) tag = g_sk_tag.fetch_add(1);   // after a wrap-around
+        p.at_tag = tag;
+    }
     if (pl->pack_a) {
         float* a2 = reinterpret_cast<float*>(w);
         if (pl->a_pre && pl->a_fused) {
@@ -915,9 +942,6 @@ int launch_plan(Plan* pl, int* status, float* ws, cudaStream_t stream) {
             p.at_src = p.A;
             p.at_lds = p.lda;
             p.at_flags = reinterpret_cast<unsigned long long*>(w + pl->at_flags_off);
-            unsigned long long tag = g_sk_tag.fetch_add(1);
-            if (tag == 0) tag = g_sk_tag.fetch_add(1);   // after a wrap-around
-            p.at_tag = tag;
         } else if (pl->a_pre) {
             // Row-major A (M x K) -> its transpose (K x lda_pack).
             e = launch_transpose_pack(p.A, p.lda, a2, pl->lda_pack, p.M, p.K, stream, false);
@@ -938,7 +962,14 @@ int launch_plan(Plan* pl, int* status, float* ws, cudaStream_t stream) {
     }
     if (pl->pack_b) {
         float* b2 = reinterpret_cast<float*>(w + pl->pack_a_bytes);
-        if (pl->b_t) {
+        if (pl->b_t && pl->b_fused) {
+            // The GEMM kernel's transposer warps write the row-major copy of
+            // B (stored N x K) into b2 (K x ldb_pack) themselves.
+            p.bt_src = p.B;
+            p.bt_lds = p.ldb;
+            p.bt_flags = reinterpret_cast<unsigned long long*>(w + pl->pack_a_bytes +
+                                                                 pl->bt_flags_off);
+        } else if (pl->b_t) {
             // B stored N x K -> row-major K x ldb_pack.
             e = launch_transpose_pack(p.B, p.ldb, b2, pl->ldb_pack, p.N, p.K, stream,
                                       pdl && prior);
@@ -947,7 +978,7 @@ int launch_plan(Plan* pl, int* status, float* ws, cudaStream_t stream) {
                               1, p.B, p.ldb, b2, pl->ldb_pack, p.K, p.N);
         }
         if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
-        prior = true;
+        if (!pl->b_fused) prior = true;
         if (!encode_2d(&pl->tmB, b2, p.K, p.N, pl->ldb_pack, 32, pl->fam->bn, false))
             return cuda_fail(cudaErrorInvalidValue, SGEMM_ERR_LAUNCH);
         p.B = b2;
@@ -978,8 +1009,9 @@ int launch_plan(Plan* pl, int* status, float* ws, cudaStream_t stream) {
 }
 
 void unfuse_plan(Plan* pl) {
-    if (!pl->a_fused) return;
+    if (!pl->a_fused && !pl->b_fused) return;
     pl->a_fused = false;
+    pl->b_fused = false;
     pl->k = &pl->fam->modes[mode_index(LOAD_TMA, LOAD_TMA, 1)];
 }
 
@@ -990,7 +1022,8 @@ void plan_name(const Plan& pl, char* buf, int buflen) {
     else std::snprintf(buf, static_cast<size_t>(buflen), "%s%s%s%s", pl.k->name,
                        pl.pack_a ? (pl.a_pre ? (pl.a_fused ? "+packATfused" : "+packAT") : "+packA")
                                  : "",
-                       pl.pack_b ? (pl.b_t ? "+packBT" : "+packB") : "",
+                       pl.pack_b ? (pl.b_t ? (pl.b_fused ? "+packBTfused" : "+packBT") : "+packB")
+                                 : "",
                        pl.sk_tiles > 0 ? (pl.sk_fixup ? "+skfix" : "+sk") : "");
 }
 
@@ -1053,7 +1086,7 @@ int run_sgemm(int opa, int opb, int64_t M, int64_t N, int64_t K, float alpha, co
             ws = static_cast<float*>(w);
         }
     }
-    if (pl.a_fused) {
+    if (pl.a_fused || pl.b_fused) {
         // A graph replays its flag value: with the fused copy a replay could
         // take the previous run's flags for its own, so a call being captured
         // makes the copy with a kernel of its own.

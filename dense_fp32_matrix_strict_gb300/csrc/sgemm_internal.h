@@ -53,6 +53,11 @@ struct Plan {
     // (a replay would see the flags its previous run left).
     bool a_fused = false;
     size_t at_flags_off = 0;
+    // b_fused (with b_t and pack_b): the row-major copy of the transposed B
+    // made inside the GEMM kernel the same way, its flags at offset
+    // bt_flags_off of the packed B buffer.
+    bool b_fused = false;
+    size_t bt_flags_off = 0;
     // a_xp: a row-major A transposed in shared memory by the kernel's
     // transposer warps (mode LOAD_TMA_XP).
     bool a_xp = false;
@@ -97,14 +102,16 @@ int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, 
 // ws_bytes == 0).
 int launch_plan(Plan* pl, int* status, float* ws, cudaStream_t stream);
 
-// Turns a fused transposed copy of A (a_fused) into the copy by a kernel of
-// its own, same kernel otherwise; for calls captured into a CUDA graph.
+// Turns copies made inside the GEMM kernel (a_fused, b_fused) into copies by
+// kernels of their own, same GEMM kernel otherwise; for calls captured into
+// a CUDA graph.
 void unfuse_plan(Plan* pl);
 
 // Human-readable plan name into buf ("none", "scale", or the kernel name,
 // with "+packA" / "+packB" for operands copied to aligned buffers, "+packAT"
 // for the transposed copy of A by a kernel of its own, "+packATfused" for
-// that copy made inside the GEMM kernel, "+sk" when the stream-K tail is
+// that copy made inside the GEMM kernel, "+packBT" / "+packBTfused" the same
+// for the row-major copy of a transposed B, "+sk" when the stream-K tail is
 // used and finished in the kernel, "+skfix" when the fixup kernel finishes
 // it).
 void plan_name(const Plan& pl, char* buf, int buflen);

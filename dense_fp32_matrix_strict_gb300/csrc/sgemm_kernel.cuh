@@ -128,6 +128,13 @@ struct GemmParams {
     long long at_lds;
     unsigned long long* at_flags;
     unsigned long long at_tag;      // this launch's flag value, never 0
+    // The same for a transposed B (stored N x K at bt_src, row stride
+    // bt_lds): its row-major copy at B (K rows of ldb floats), units of BK
+    // k-rows x BN columns, flags bt_flags[tn * k_tiles + kt] = at_tag. Either
+    // copy may be absent (source null).
+    const float* bt_src;
+    long long bt_lds;
+    unsigned long long* bt_flags;
 };
 
 // Kernel configuration. FORDER: FMA form of the outer product (0: scalar
@@ -192,8 +199,9 @@ struct Cfg {
     static constexpr int CONSUMERS = CONSUMER_WARPS * 32;
     static constexpr bool ANY_CP = (A_MODE == LOAD_CPASYNC) || (B_MODE == LOAD_CPASYNC);
     // FUSED: the transposed-A path with the transposed copy of a row-major A
-    // made inside this kernel by three transposer warps per CTA (see
-    // GemmParams::at_flags and at_transposer()) instead of a kernel before it.
+    // and/or the row-major copy of a transposed B made inside this kernel by
+    // three transposer warps per CTA (see GemmParams::at_flags, bt_flags and
+    // at_transposer()) instead of by kernels before it.
     static constexpr bool FUSED = FUSED_ != 0;
     static constexpr bool ANY_TMA = (A_MODE != LOAD_CPASYNC) || (B_MODE == LOAD_TMA);
     // cp.async producers: one warp per SM sub-partition so the copy
@@ -460,12 +468,16 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmA, const CUtensorM
             const uint32_t dA = sA + s * C::A_BYTES, dB = sB + s * C::B_BYTES;
             const int k0 = kt * C::BK;
             if (C::FUSED && tma_thread) {
-                // The unit of the transposed A this stage reads is written
-                // by some CTA's transposer warps in this kernel: wait for
-                // its flag, then order the async-proxy load after it.
-                SG_DCHECK(p, tm < p.tiles_m && kt < p.k_tiles);
-                if (!wait_flag_bounded(p.at_flags + static_cast<long long>(tm) * p.k_tiles + kt,
-                                       p.at_tag, p, STATUS_PRODUCER_TIMEOUT)) {
+                // The units of the transposed copies this stage reads are
+                // written by some CTA's transposer warps in this kernel: wait
+                // for their flags, then order the async-proxy loads after them.
+                SG_DCHECK(p, tm < p.tiles_m && tn < p.tiles_n && kt < p.k_tiles);
+                if ((p.at_src != nullptr &&
+                     !wait_flag_bounded(p.at_flags + static_cast<long long>(tm) * p.k_tiles + kt,
+                                        p.at_tag, p, STATUS_PRODUCER_TIMEOUT)) ||
+                    (p.bt_src != nullptr &&
+                     !wait_flag_bounded(p.bt_flags + static_cast<long long>(tn) * p.k_tiles + kt,
+                                        p.at_tag, p, STATUS_PRODUCER_TIMEOUT))) {
                     ok = false;
                     break;
                 }
@@ -575,82 +587,145 @@ __device__ __forceinline__ void transposer(const GemmParams& p, const uint8_t* r
     }
 }
 
-// ---- transposer warps of the fused transposed copy (Cfg::FUSED) -------------------
+// ---- transposer warps of the fused transposed copies (Cfg::FUSED) ------------------
 
-// Three warps (t = 0..95) of every CTA write the transposed copy of the
-// row-major A that the TMA producers load, unit by unit: unit (tm, kt) is A's
-// rows tm BM .. + BM and columns kt BK .. + BK, stored at rows kt BK .. and
-// columns tm BM .. of the copy. The units are taken in the order the tiles
-// first need them (raster group by raster group, then k-tile, then tile row)
-// and dealt out round-robin over the CTAs, so the first wave's first k-tiles
-// are done first, by many CTAs at once. A unit goes through a staging tile
-// in shared memory (BM rows of BK + 1 floats: the 128-byte row reads and the
-// column reads both stay within a bank or two), rows of A in, rows of the
-// copy out, both 16-byte vectors where A allows. Elements past M or K are
-// neither read nor written (the tensor map's bounds cover them with zeros).
-// After a unit's stores every thread fences them for the async proxy and
-// at GPU scope, the 96 threads meet at named barrier 1, and one releases
-// the unit's flag. Nothing here waits on another CTA, so every unit gets
-// done.
+// Three warps (t = 0..95) of every CTA write the transposed copies the TMA
+// producers load: of a row-major A (unit (tm, kt): A's rows tm BM .. + BM and
+// columns kt BK .. + BK, stored at rows kt BK .. and columns tm BM .. of the
+// copy) and of a transposed B (unit (tn, kt): rows tn BN .. of the stored
+// N x K B, columns kt BK .., stored at rows kt BK .. and columns tn BN .. of
+// B's row-major copy), whichever the call has. The units are taken in the
+// order the tiles first need them (see at_transposer) and dealt out
+// round-robin over the CTAs, so the first wave's first k-tiles are done
+// first, by many CTAs at once. A unit goes through a staging tile in shared
+// memory (BM rows of BK + 1 floats: the 128-byte row reads and the column
+// reads both stay within a bank or two), 128-byte rows in, 512-byte rows of
+// the copy out, both 16-byte vectors where the source allows. Elements past
+// the matrix are neither read nor written (the tensor maps' bounds supply
+// zeros). After a unit's stores every thread fences them for the async proxy
+// and at GPU scope, the 96 threads meet at named barrier 1, and one releases
+// the unit's flag. Nothing here waits on another CTA, so every unit gets done.
+template <class C>
+__device__ __forceinline__ void transpose_unit(const GemmParams& p, float* xt, int t,
+                                               const float* src, long long lds, bool vec,
+                                               float* dst, long long ldd, int rows, int r0, int k0) {
+    constexpr int BR = C::BM, BK = C::BK, LD = C::BK + 1;
+    // Source rows in: BR rows x BK / 4 float4.
+#pragma unroll 2
+    for (int q = t; q < BR * (BK / 4); q += C::TRANSPOSERS) {
+        const int rr = q / (BK / 4), c4 = (q % (BK / 4)) * 4;
+        const int r = r0 + rr, k = k0 + c4;
+        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (r < rows) {
+            const float* sp = src + static_cast<long long>(r) * lds + k;
+            if (vec && k + 3 < p.K) {
+                v = *reinterpret_cast<const float4*>(sp);
+            } else {
+                if (k < p.K) v.x = sp[0];
+                if (k + 1 < p.K) v.y = sp[1];
+                if (k + 2 < p.K) v.z = sp[2];
+                if (k + 3 < p.K) v.w = sp[3];
+            }
+        }
+        SG_DCHECK(p, (rr * LD + c4 + 3) * 4 + 4 <= C::XT_BYTES);
+        float* d = xt + rr * LD + c4;
+        d[0] = v.x;
+        d[1] = v.y;
+        d[2] = v.z;
+        d[3] = v.w;
+    }
+    named_bar_sync(1, C::TRANSPOSERS);
+    // Rows of the copy out: BK rows x BR / 4 float4 (ldd is a multiple of 4
+    // and r a multiple of 4 below rows, so the float4 stays in the row).
+#pragma unroll 2
+    for (int q = t; q < BK * (BR / 4); q += C::TRANSPOSERS) {
+        const int kk = q / (BR / 4), r4 = (q % (BR / 4)) * 4;
+        const int k = k0 + kk, r = r0 + r4;
+        if (k < p.K && r < rows) {
+            SG_DCHECK(p, r + 3 < ldd && ((r4 + 3) * LD + kk) * 4 + 4 <= C::XT_BYTES);
+            *reinterpret_cast<float4*>(dst + static_cast<long long>(k) * ldd + r) =
+                make_float4(xt[r4 * LD + kk], xt[(r4 + 1) * LD + kk], xt[(r4 + 2) * LD + kk],
+                            xt[(r4 + 3) * LD + kk]);
+        }
+    }
+    fence_proxy_async_global();
+    __threadfence();
+    named_bar_sync(1, C::TRANSPOSERS);
+}
+
 template <class C>
 __device__ __forceinline__ void at_transposer(const GemmParams& p, float* xt, int t) {
-    constexpr int BM = C::BM, BK = C::BK, LD = C::BK + 1;
-    static_assert(BK == 32 && BM % 4 == 0, "unit of 32 k-rows");
-    float* at = const_cast<float*>(p.A);
-    const bool vec = (reinterpret_cast<uintptr_t>(p.at_src) % 16 == 0) && (p.at_lds % 4 == 0);
+    static_assert(!C::FUSED || (C::BK == 32 && C::BM == C::BN && C::BM % 4 == 0),
+                  "units of 32 k x BM");
+    const bool do_a = p.at_src != nullptr, do_b = p.bt_src != nullptr;
+    const bool vec_a = do_a && (reinterpret_cast<uintptr_t>(p.at_src) % 16 == 0) &&
+                       (p.at_lds % 4 == 0);
+    const bool vec_b = do_b && (reinterpret_cast<uintptr_t>(p.bt_src) % 16 == 0) &&
+                       (p.bt_lds % 4 == 0);
+    // The raster visits raster group 0 (gmr tile rows) column by column, so
+    // the data-parallel wave w first needs B's column blocks up to tn_end(w).
+    const int gmr = min(p.tiles_m, p.group_m);
+    const int grid = static_cast<int>(gridDim.x);
+    auto tn_end = [&](int w) {
+        const long long e = (static_cast<long long>(w + 1) * grid + gmr - 1) / gmr;
+        return static_cast<int>(e < p.tiles_n ? e : p.tiles_n);
+    };
+    // Order: (1) k-tile by k-tile, group 0's A units and the first wave's B
+    // units; (2) wave by wave, k-tile by k-tile, the B units a later wave
+    // needs first; (3) the A units of raster groups 1.. in the order of A's
+    // copy alone.
     const long long per_group = static_cast<long long>(p.group_m) * p.k_tiles;
-    const long long units = static_cast<long long>(p.tiles_m) * p.k_tiles;
+    const int gm0 = do_a ? gmr : 0;
+    const int nb0 = do_b ? tn_end(0) : 0;
+    const int per_kt = gm0 + nb0;
+    const long long first = static_cast<long long>(per_kt) * p.k_tiles;
+    const long long b_rest = do_b ? static_cast<long long>(p.tiles_n - nb0) * p.k_tiles : 0;
+    const long long a_units = do_a ? static_cast<long long>(p.tiles_m) * p.k_tiles : 0;
+    const long long units =
+        first + b_rest + (a_units - static_cast<long long>(gm0) * p.k_tiles);
     for (long long u = blockIdx.x; u < units; u += gridDim.x) {
-        const int g = static_cast<int>(u / per_group);
-        const long long r = u - g * per_group;
-        const int gm = min(p.tiles_m - g * p.group_m, p.group_m);
-        const int kt = static_cast<int>(r / gm);
-        const int tm = g * p.group_m + static_cast<int>(r - static_cast<long long>(kt) * gm);
-        SG_DCHECK(p, tm >= 0 && tm < p.tiles_m && kt >= 0 && kt < p.k_tiles);
-        const int m0 = tm * BM, k0 = kt * BK;
-        // A rows in: BM rows x BK / 4 float4.
-#pragma unroll 2
-        for (int q = t; q < BM * (BK / 4); q += C::TRANSPOSERS) {
-            const int rr = q / (BK / 4), c4 = (q % (BK / 4)) * 4;
-            const int m = m0 + rr, k = k0 + c4;
-            float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            if (m < p.M) {
-                const float* sp = p.at_src + static_cast<long long>(m) * p.at_lds + k;
-                if (vec && k + 3 < p.K) {
-                    v = *reinterpret_cast<const float4*>(sp);
-                } else {
-                    if (k < p.K) v.x = sp[0];
-                    if (k + 1 < p.K) v.y = sp[1];
-                    if (k + 2 < p.K) v.z = sp[2];
-                    if (k + 3 < p.K) v.w = sp[3];
+        int kt = 0, tm = -1, tn = -1;
+        if (u < first) {
+            kt = static_cast<int>(u / per_kt);
+            const int r = static_cast<int>(u - static_cast<long long>(kt) * per_kt);
+            if (r < gm0) tm = r;
+            else tn = r - gm0;
+        } else if (u < first + b_rest) {
+            long long v = u - first;
+            int start = nb0;
+            for (int w = 1;; ++w) {
+                const int end = tn_end(w);
+                const long long cnt = static_cast<long long>(end - start) * p.k_tiles;
+                if (v < cnt) {
+                    kt = static_cast<int>(v / (end - start));
+                    tn = start + static_cast<int>(v - static_cast<long long>(kt) * (end - start));
+                    break;
                 }
+                v -= cnt;
+                start = end;
             }
-            SG_DCHECK(p, (rr * LD + c4 + 3) * 4 + 4 <= C::XT_BYTES);
-            float* d = xt + rr * LD + c4;
-            d[0] = v.x;
-            d[1] = v.y;
-            d[2] = v.z;
-            d[3] = v.w;
+        } else {
+            const long long ua = u - first - b_rest + static_cast<long long>(gm0) * p.k_tiles;
+            const int g = static_cast<int>(ua / per_group);
+            const long long r = ua - g * per_group;
+            const int gm = min(p.tiles_m - g * p.group_m, p.group_m);
+            kt = static_cast<int>(r / gm);
+            tm = g * p.group_m + static_cast<int>(r - static_cast<long long>(kt) * gm);
         }
-        named_bar_sync(1, C::TRANSPOSERS);
-        // Rows of the copy out: BK rows x BM / 4 float4 (lda is a multiple of
-        // 4 and m a multiple of 4 below M, so the float4 stays in the row).
-#pragma unroll 2
-        for (int q = t; q < BK * (BM / 4); q += C::TRANSPOSERS) {
-            const int kk = q / (BM / 4), m4 = (q % (BM / 4)) * 4;
-            const int k = k0 + kk, m = m0 + m4;
-            if (k < p.K && m < p.M) {
-                SG_DCHECK(p, m + 3 < p.lda && ((m4 + 3) * LD + kk) * 4 + 4 <= C::XT_BYTES);
-                *reinterpret_cast<float4*>(at + static_cast<long long>(k) * p.lda + m) =
-                    make_float4(xt[m4 * LD + kk], xt[(m4 + 1) * LD + kk], xt[(m4 + 2) * LD + kk],
-                                xt[(m4 + 3) * LD + kk]);
-            }
+        SG_DCHECK(p, kt >= 0 && kt < p.k_tiles && (tm >= 0) != (tn >= 0) &&
+                         tm < p.tiles_m && tn < p.tiles_n && (tm < 0 || do_a) &&
+                         (tn < 0 || do_b));
+        unsigned long long* flag;
+        if (tm >= 0) {
+            transpose_unit<C>(p, xt, t, p.at_src, p.at_lds, vec_a, const_cast<float*>(p.A), p.lda,
+                              p.M, tm * C::BM, kt * C::BK);
+            flag = p.at_flags + static_cast<long long>(tm) * p.k_tiles + kt;
+        } else {
+            transpose_unit<C>(p, xt, t, p.bt_src, p.bt_lds, vec_b, const_cast<float*>(p.B), p.ldb,
+                              p.N, tn * C::BN, kt * C::BK);
+            flag = p.bt_flags + static_cast<long long>(tn) * p.k_tiles + kt;
         }
-        fence_proxy_async_global();
-        __threadfence();
-        named_bar_sync(1, C::TRANSPOSERS);
-        if (t == 0)
-            st_release_gpu(p.at_flags + static_cast<long long>(tm) * p.k_tiles + kt, p.at_tag);
+        if (t == 0) st_release_gpu(flag, p.at_tag);
     }
 }
 

@@ -178,8 +178,10 @@ SGEMM_API int sgemm_host(int64_t M, int64_t N, int64_t K, float alpha, const flo
  * an opa or opb other than 0 or 1 returns SGEMM_ERR_INVALID_VALUE. A
  * transposed A is read by TMA in its stored layout when its base is 16-byte
  * aligned and lda % 4 == 0, else first copied (in that layout) to an aligned
- * workspace buffer; a transposed B is always first transposed into a
- * row-major K x N workspace buffer (one HBM pass over B). Those buffers come
+ * workspace buffer; a transposed B is always transposed into a row-major
+ * K x N workspace buffer (one HBM pass over B), by the GEMM kernel itself
+ * when A goes through the transposed-A path, else by a copy kernel before
+ * it. Those buffers come
  * from the library's stream-ordered pool like the stream-K workspace; if the
  * pool cannot supply one, the call returns SGEMM_ERR_CUDA with
  * cudaErrorMemoryAllocation kept for sgemm_last_cuda_error.
@@ -221,10 +223,12 @@ SGEMM_API int sgemm_last_cuda_error(void);
  * "ws_128x128x32_s4_Atma_Btma" into buf (at most buflen bytes) and the
  * launch grid into *grid (if not NULL). "+packA" / "+packB" mean that
  * operand is first copied to an aligned buffer by a small copy kernel;
- * "+packAT" that A is first copied transposed and read through the
- * transposed-A path ("_ATtma_" in the kernel name); a "+sk" suffix means the
- * last wave is split across the SMs (stream-K) and finished by a second,
- * small fixup kernel. Returns the same argument errors as sgemm, or
+ * "+packAT" that A is first copied transposed by a copy kernel and read
+ * through the transposed-A path ("_ATtma_" in the kernel name),
+ * "+packATfused" that the GEMM kernel makes that copy itself; a "+sk"
+ * suffix means the last wave is split across the SMs (stream-K) and
+ * finished inside the GEMM kernel, "+skfix" by a second, small fixup
+ * kernel. Returns the same argument errors as sgemm, or
  * SGEMM_OK. A name of "scale" means the alpha == 0 / K == 0 path; "none"
  * means M == 0 or N == 0.
  */
@@ -234,7 +238,8 @@ SGEMM_API int sgemm_plan(int64_t M, int64_t N, int64_t K, float alpha, const flo
 
 /* sgemm_plan for sgemm_ex's arguments. A transposed A shows as "_ATtma_"
  * in the kernel name; "+packBT" means B is first transposed into a
- * row-major buffer. */
+ * row-major buffer by a copy kernel, "+packBTfused" that the GEMM kernel
+ * makes that copy itself (when A is read through the transposed-A path). */
 SGEMM_API int sgemm_plan_ex(int opa, int opb, int64_t M, int64_t N, int64_t K, float alpha,
                             const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
                             const float* C, int64_t ldc, char* buf, int buflen, int* grid);
@@ -249,7 +254,8 @@ SGEMM_API int sgemm_plan_ex(int opa, int opb, int64_t M, int64_t N, int64_t K, f
  * wave (plain data-parallel schedule), ":at" / ":noat" always / never
  * read a row-major A through a transposed copy (the default decides by
  * size; the 128 x 128 kernel makes the copy itself), ":atcopy" the same
- * copy made by a copy kernel first, ":xp" the transpose in shared memory
+ * copy (and that of a transposed B) made by a copy kernel first, ":xp" the
+ * transpose in shared memory
  * instead, ":fixup" the stream-K tail finished by a second kernel, e.g.
  * "128x128:cpasync:dp" or "auto:dp". Returns SGEMM_ERR_INVALID_VALUE for an
  * unknown name. The environment variable SGEMM_FORCE_CONFIG, read on the

@@ -110,6 +110,8 @@ def test_cpu_baseline_plan_per_workload():
     assert bench.launches_of("ws_128x128x32_s4_ATtma_Btma+packAT+sk") == 2
     assert bench.launches_of("ws_128x128x32_s4_ATtma_Btma+packATfused+sk") == 1
     assert bench.launches_of("ws_128x128x32_s4_ATtma_Btma+packATfused+packB+skfix") == 3
+    assert bench.launches_of("ws_128x128x32_s4_ATtma_Btma+packATfused+packBTfused+sk") == 1
+    assert bench.launches_of("ws_128x128x32_s4_ATtma_Btma+packBT+sk") == 2
     assert bench.launches_of("ws_128x128x32_s4_ATtma_Btma+packAT+skfix") == 3
     assert bench.launches_of("ws_128x128x32_s4_Atma_Btma+sk") == 1
     assert bench.launches_of("ws_128x64x32_s4_k2_Axp_Btma") == 1

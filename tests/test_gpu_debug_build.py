@@ -58,6 +58,7 @@ CASES = [
     ("auto:xp", 2048, 2048, 2048, None, None, None, (0, 0, 0), False, False, "sgemm"),
     ("auto:atcopy", 1000, 3000, 4000, None, None, None, (0, 0, 0), False, False, "sgemm"),
     ("auto", 1021, 2600, 3001, None, None, None, (0, 0, 0), False, False, "sgemm"),
+    ("auto", 2000, 2100, 1900, None, None, None, (0, 0, 0), True, True, "sgemm"),
     ("128x128", 1000, 1100, 2000, None, None, None, (0, 0, 0), False, False, "noalloc"),
     ("auto", 4096, 4096, 256, None, None, None, (0, 0, 0), False, False, "3xtf32"),
     ("auto", 300, 640, 500, None, None, None, (0, 0, 0), False, False, "3xtf32"),
@@ -108,13 +109,14 @@ def test_debug_build_runs_every_plan_with_clear_status():
                        capture_output=True, text=True)
     assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
     results = json.loads(r.stdout.strip().splitlines()[-1])
-    assert len(results) == 26
+    assert len(results) == 27
     for res in results:
         assert res["rc"] == 0 and res["bits"] == 0, res
         assert res["guards"] and res["ok"], res
     plans = {res["plan"] for res in results}
     # The debug kernels covered the families and paths listed above.
-    for tag in ("+sk", "+skfix", "+packAT", "+packATfused", "+packBT", "_c4_", "_k2_", "_k4_",
+    for tag in ("+sk", "+skfix", "+packAT", "+packATfused", "+packBT", "+packBTfused", "_c4_",
+                "_k2_", "_k4_",
                 "_Axp_", "_Acp_",
                 "noalloc", "3xtf32"):
         assert any(tag in p for p in plans), (tag, sorted(plans))

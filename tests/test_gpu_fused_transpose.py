@@ -166,3 +166,30 @@ def test_two_streams_concurrently():
         sg.check_status()
         assert np.array_equal(c1.cpu().numpy(), want1)
         assert np.array_equal(c2.cpu().numpy(), want2)
+
+
+# (M, N, K, transa, transb): a transposed B whose row-major copy the kernel
+# makes itself, beside the transposed copy of a row-major A (N, T) or with A
+# given transposed and read in place (T, T); ragged edges in the last case.
+B_CASES = [(4096, 2048, 4096, False, True), (2048, 2048, 2048, True, True),
+           (2000, 2100, 1900, True, True)]
+
+
+@pytest.mark.parametrize("M,N,K,ta,tb", B_CASES,
+                         ids=["x".join(map(str, c[:3])) + ("_T" if c[3] else "_N") + "T"
+                              for c in B_CASES])
+def test_fused_copy_of_a_transposed_b(M, N, K, ta, tb):
+    A = inputs.fill("normal", 1340, inputs.TID_A, *((K, M) if ta else (M, K)))
+    B = inputs.fill("normal", 1340, inputs.TID_B, *((N, K) if tb else (K, N)))
+    C0 = inputs.fill("normal", 1340, inputs.TID_C, M, N)
+    C1, g1, plan1 = run_cfg("auto", 0.7, A, B, -1.3, C0, transa=ta, transb=tb)
+    C2, g2, plan2 = run_cfg("auto:atcopy", 0.7, A, B, -1.3, C0, transa=ta, transb=tb)
+    assert g1 and g2
+    assert "+packBTfused" in plan1[0], plan1
+    assert ("+packATfused" in plan1[0]) == (not ta), plan1
+    assert "+packBT" in plan2[0] and "fused" not in plan2[0], plan2
+    assert np.array_equal(C1, C2), int(np.count_nonzero(C1 != C2))
+    opA = A.T if ta else A
+    opB = B.T if tb else B
+    ref, S = oracle.sgemm_ref(0.7, np.ascontiguousarray(opA), np.ascontiguousarray(opB), -1.3, C0)
+    assert oracle.check(C1, ref, S, K)["ok"]
