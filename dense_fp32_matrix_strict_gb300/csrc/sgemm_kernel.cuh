@@ -159,10 +159,12 @@ struct GemmParams {
 //   16-byte chunks of k-row k XOR-swizzled by (k / 4) mod 8 so that both the
 //   transposing stores and the consumers' reads are free of bank conflicts.
 // CS: CTAs per thread-block cluster. With CS > 1 the CTAs of a cluster share
-//   one tile: CTA rank r takes k-tiles [r kt / CS, (r + 1) kt / CS), ranks
-//   1.. hand their sums to rank 0 through its shared memory (distributed
-//   shared memory), and rank 0 adds them in rank order and writes C. The
-//   grid is tiles x CS, one tile per cluster, no stream-K tail.
+//   one tile: CTA rank r takes k-tiles [r kt / CS, (r + 1) kt / CS); the
+//   ranks then exchange their sums through each other's shared memory
+//   (distributed shared memory) so that each adds, in rank order, the sums of
+//   8 / CS of every lane's 8 rows (a reduce-scatter) and writes those rows of
+//   C. The grid is tiles x CS, one tile per cluster, no
+//   stream-K tail.
 template <int BM_, int BN_, int BK_, int STAGES_, int A_MODE_, int B_MODE_, int FORDER_ = 2,
           int EARLY_ = 0, int LMAP_ = 0, int A_T_ = 0, int ALOAD_ = 4, int TN_ = 8,
           int KSPLIT_ = 1, int CS_ = 1, int FUSED_ = 0>
@@ -223,7 +225,8 @@ struct Cfg {
     static constexpr int RED_BYTES = (KSPLIT - 1) * BM * BN * 4;   // k-group sums
     static constexpr int CS = CS_;
     static_assert(CS == 1 || CS == 2 || CS == 4, "CS is 1, 2 or 4");
-    static constexpr int CKS_BYTES = (CS - 1) * BM * BN * 4;        // other ranks' sums
+    // Other ranks' sums of the rows this rank finishes (cluster k-split).
+    static constexpr int CKS_BYTES = (CS - 1) * BM * BN * 4 / CS;
     // FUSED: the transposer warps' staging tile, BM rows of BK + 1 floats.
     static constexpr int XT_BYTES = FUSED ? BM * (BK + 1) * 4 : 0;
     static constexpr int SMEM_BYTES = 1024 /* alignment slack */ +
@@ -976,43 +979,73 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
         }
 
         if (C::CS > 1) {
-            // Cluster k-split: ranks 1.. store their sums into rank 0's
-            // shared memory (float4 j of lane l of warp wq at
-            // ((r - 1) GROUP_WARPS + wq) 2 TN + j, lane-interleaved) and
-            // arrive on its barrier; rank 0 waits for all of them and adds
-            // them in rank order. One item per CTA, so the phase is 0.
-            constexpr int NF4 = 8 * C::TN / 4;
+            // Cluster k-split, reduce-scatter: rank r finishes the
+            // accumulator rows i in [r R, (r + 1) R), R = 8 / CS, of every
+            // lane of group 0, and writes only those rows of C. Each rank
+            // stores the rows another rank finishes into that rank's shared
+            // memory (its slot there: ranks below the receiver in rank order,
+            // then those above; float4 j of lane l of warp wq of slot s at
+            // (s GROUP_WARPS + wq) R TN / 4 + j, lane-interleaved), arrives on
+            // its barrier, then waits for its own and adds the ranks' sums in
+            // rank order: the order rank 0 alone would add them in, so the
+            // bits do not depend on which rank finishes a row. One item per
+            // CTA, so the phase is 0.
+            constexpr int R = 8 / C::CS;
+            constexpr int NF4 = R * C::TN / 4;
             const uint32_t rank = cluster_ctarank();
             SG_DCHECK(p, rank < static_cast<uint32_t>(C::CS));
-            if (rank > 0) {
-                SG_DCHECK(p, ((((rank - 1) * C::GROUP_WARPS + wq) * NF4 + NF4 - 1) * 32 + lane + 1) * 16 <=
-                                 static_cast<uint32_t>(C::CKS_BYTES));
-                const uint32_t dst = mapa_shared(
-                    smem_u32(cks + (((rank - 1) * C::GROUP_WARPS + wq) * NF4) * 32 + lane), 0);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
+            for (int d = 0; d < C::CS; ++d) {
+                if (static_cast<uint32_t>(d) == rank) continue;
+                const int slot = static_cast<int>(rank) < d ? static_cast<int>(rank)
+                                                            : static_cast<int>(rank) - 1;
+                SG_DCHECK(p, (((slot * C::GROUP_WARPS + wq) * NF4 + NF4 - 1) * 32 + lane + 1) * 16 <=
+                                 C::CKS_BYTES);
+                const uint32_t dst = mapa_shared(
+                    smem_u32(cks + ((slot * C::GROUP_WARPS + wq) * NF4) * 32 + lane),
+                    static_cast<uint32_t>(d));
+#pragma unroll
+                for (int ii = 0; ii < R; ++ii)
 #pragma unroll
                     for (int h = 0; h < C::TN / 4; ++h)
-                        st_cluster_v4(dst + (i * (C::TN / 4) + h) * 32 * 16,
-                                      make_float4(acc[i][4 * h], acc[i][4 * h + 1],
-                                                  acc[i][4 * h + 2], acc[i][4 * h + 3]));
-                mbar_arrive_remote(mapa_shared(cks_full, 0));
-                continue;
+                        st_cluster_v4(dst + (ii * (C::TN / 4) + h) * 32 * 16,
+                                      make_float4(acc[d * R + ii][4 * h], acc[d * R + ii][4 * h + 1],
+                                                  acc[d * R + ii][4 * h + 2],
+                                                  acc[d * R + ii][4 * h + 3]));
+                mbar_arrive_remote(mapa_shared(cks_full, static_cast<uint32_t>(d)));
             }
             if (!wait_bounded_cluster(cks_full, 0, p, STATUS_CONSUMER_TIMEOUT)) return;
-#pragma unroll 1
-            for (int r = 1; r < C::CS; ++r) {
-                const float4* srcr = cks + (((r - 1) * C::GROUP_WARPS + wq) * NF4) * 32 + lane;
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < 8; ++i) {
+                if (static_cast<uint32_t>(i / R) != rank) continue;
+                const int ii = i % R;
 #pragma unroll
-                    for (int h = 0; h < C::TN / 4; ++h) {
-                        const float4 v = srcr[(i * (C::TN / 4) + h) * 32];
-                        acc[i][4 * h] += v.x;
-                        acc[i][4 * h + 1] += v.y;
-                        acc[i][4 * h + 2] += v.z;
-                        acc[i][4 * h + 3] += v.w;
+                for (int h = 0; h < C::TN / 4; ++h) {
+                    const float4 own = make_float4(acc[i][4 * h], acc[i][4 * h + 1],
+                                                   acc[i][4 * h + 2], acc[i][4 * h + 3]);
+                    float4 t = own;
+#pragma unroll
+                    for (int r = 0; r < C::CS; ++r) {
+                        float4 v = own;
+                        if (static_cast<uint32_t>(r) != rank) {
+                            const int slot = r < static_cast<int>(rank) ? r : r - 1;
+                            v = cks[((slot * C::GROUP_WARPS + wq) * NF4 + ii * (C::TN / 4) + h) * 32 +
+                                    lane];
+                        }
+                        if (r == 0) {
+                            t = v;
+                        } else {
+                            t.x += v.x;
+                            t.y += v.y;
+                            t.z += v.z;
+                            t.w += v.w;
+                        }
                     }
+                    acc[i][4 * h] = t.x;
+                    acc[i][4 * h + 1] = t.y;
+                    acc[i][4 * h + 2] = t.z;
+                    acc[i][4 * h + 3] = t.w;
+                }
             }
         }
 
@@ -1091,7 +1124,10 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
             }
         }
 
-        // Epilogue: C = alpha * acc + beta * C, straight from registers.
+        // Epilogue: C = alpha * acc + beta * C, straight from registers; in
+        // a cluster k-split only the rows this rank finished.
+        const int own_lo = C::CS > 1 ? static_cast<int>(cluster_ctarank()) * (8 / C::CS) : 0;
+        const int own_hi = own_lo + 8 / C::CS;
         int tm, tn;
         tile_coords(it.tile, p, tm, tn);
         const int m0 = tm * C::BM + row_base;
@@ -1109,10 +1145,11 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
 #pragma unroll
                 for (int ii = 0; ii < 4; ++ii) {
                     const int m = m0 + lane_row<C>(4 * q + ii);
+                    const bool own = 4 * q + ii >= own_lo && 4 * q + ii < own_hi;
 #pragma unroll
                     for (int h = 0; h < C::TN / 4; ++h) {
                         const int n = n0 + 32 * h;
-                        cold[ii][h] = (m < p.M && p.c_vec && n + 3 < p.N)
+                        cold[ii][h] = (own && m < p.M && p.c_vec && n + 3 < p.N)
                                           ? *reinterpret_cast<const float4*>(p.C + (long long)m * p.ldc + n)
                                           : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
                     }
@@ -1122,7 +1159,7 @@ __device__ __forceinline__ void consumer(const GemmParams& p, const uint8_t* sA_
             for (int ii = 0; ii < 4; ++ii) {
                 const int i = 4 * q + ii;
                 const int m = m0 + lane_row<C>(i);
-                if (m >= p.M) continue;
+                if (m >= p.M || i < own_lo || i >= own_hi) continue;
                 float* crow = p.C + (long long)m * p.ldc;
                 SG_DCHECK(p, m >= 0 && n0 >= 0 && n0 % 4 == 0);
 #pragma unroll

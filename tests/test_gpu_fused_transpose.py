@@ -1,4 +1,5 @@
-"""The transposed copy of a row-major A made inside the GEMM kernel.
+"""The transposed copy of a row-major A, and the row-major copy of a
+transposed B, made inside the GEMM kernel.
 
 Where "auto" takes the transposed copy of A ("+packAT", the size rule of
 tests/test_plan_rule.py) the 128 x 128 kernel makes the copy itself: three
@@ -170,9 +171,13 @@ def test_two_streams_concurrently():
 
 # (M, N, K, transa, transb): a transposed B whose row-major copy the kernel
 # makes itself, beside the transposed copy of a row-major A (N, T) or with A
-# given transposed and read in place (T, T); ragged edges in the last case.
+# given transposed and read in place (T, T); ragged edges in the last three,
+# and in the last two a K that is not a multiple of 4, so that the rows of
+# the stored B (and in the last of A) are not 16-byte aligned and the units
+# are read by scalar loads.
 B_CASES = [(4096, 2048, 4096, False, True), (2048, 2048, 2048, True, True),
-           (2000, 2100, 1900, True, True)]
+           (2000, 2100, 1900, True, True), (2000, 2100, 1531, True, True),
+           (4093, 2560, 1531, False, True)]
 
 
 @pytest.mark.parametrize("M,N,K,ta,tb", B_CASES,
