@@ -81,9 +81,13 @@ std::atomic<int> g_force_sk{-1};
 // the GEMM kernel (":fixup").
 std::atomic<int> g_force_fx{0};
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
-// Flag value of the next launch that finishes split tiles in the kernel:
-// unique per launch in this process and never 0.
-std::atomic<unsigned long long> g_sk_tag{1};
+// Flag value of the next launch that finishes split tiles in the kernel or
+// makes an operand copy itself: unique per launch in this process and never
+// 0. The flags sit in recycled pool memory that may hold anything a call left
+// there (operand copies, partial sums), so a value a stale word could equal
+// by chance must not be easy to hit: the upper half starts as a quiet-NaN
+// pattern with an unusual payload (0x7fc5a5a5), the lower half counts.
+std::atomic<unsigned long long> g_sk_tag{0x7fc5a5a500000001ull};
 
 thread_local int t_last_cuda_error = 0;
 
