@@ -107,6 +107,19 @@ extern "C" {
  * unless the environment variable SGEMM_PDL is "0" when the library first
  * launches.
  *
+ * Sharing the GPU: the persistent kernels launch at most as many CTAs as
+ * the GPU runs at once, and some CTAs wait (bounded) for others: the CTA
+ * that finishes a split tile of the stream-K tail waits for the partial sums
+ * of the CTAs that share the tile ("+sk"), and where the GEMM kernel makes
+ * an operand copy itself ("+packATfused", "+packBTfused") a CTA waits for
+ * blocks of the copy that any CTA may write. A kernel on another stream that
+ * holds SMs while this one starts keeps some of its CTAs waiting for an SM
+ * until that kernel ends; if that takes longer than the wait limit
+ * (sgemm_set_wait_timeout_ns, 2 s by default), the result is incomplete and
+ * sgemm_check_status returns SGEMM_ERR_DEVICE_TIMEOUT. Under the
+ * configuration "auto:dp:atcopy" (sgemm_set_config) no CTA waits for
+ * another (clusters are scheduled whole).
+ *
  * Workspace: the pages' kernels need no scratch, so the plainest contract is
  * "nothing allocated per call". This entry point keeps a weaker one: no call
  * grows the library's device memory in steady state or waits to allocate.

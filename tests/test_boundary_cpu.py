@@ -104,7 +104,8 @@ def test_null_ab_allowed_when_not_read(lib):
 
 def test_config_names(lib):
     for good in ["auto", "128x128", "64x64", "128x64", "128x128:cpasync", "auto:cpasync",
-                 "auto:at", "128x128:noat:dp", "128x128:fixup", "auto:dp:fixup"]:
+                 "auto:at", "128x128:noat:dp", "128x128:fixup", "auto:dp:fixup",
+                 "auto:dp:atcopy"]:
         assert sg.sgemm_set_config(good) == sg.SGEMM_OK
     for bad in ["", "x", "256x256", "128x128:tma", "auto:"]:
         if bad == "":
