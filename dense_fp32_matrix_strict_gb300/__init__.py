@@ -13,6 +13,6 @@ from ._binding import (  # noqa: F401
     sgemm_config_names, sgemm_fp32_peak, sgemm_last_cuda_error, sgemm_noalloc, sgemm_plan, sgemm_selftest_wait_timeout,
     SGEMM_OP_N, SGEMM_OP_T, sgemm_ex, sgemm_plan_ex, sgemm_3xtf32_ex, sgemm_host,
     sgemm_host_tensors, sgemm_noalloc_check_status, sgemm_fp32_peak_ex, SGEMM_PEAK_FFMA,
-    SGEMM_PEAK_FFMA2, SGEMM_PEAK_OUTER, sgemm_null_launch, sgemm_tf32_mma_peak,
+    SGEMM_PEAK_FFMA2, SGEMM_PEAK_OUTER, sgemm_null_launch, sgemm_tf32_mma_peak, sgemm_selftest_occupy,
     sgemm_set_config, sgemm_set_shape_config, sgemm_clear_shape_configs, sgemm_set_wait_timeout_ns, sgemm_tensors, sgemm_3xtf32, sgemm_3xtf32_tensors,
 )

@@ -28,7 +28,7 @@ EXPORTED_SYMBOLS = (
     "sgemm_selftest_wait_timeout", "sgemm_config_names", "sgemm_noalloc", "sgemm_3xtf32",
     "sgemm_set_shape_config", "sgemm_clear_shape_configs", "sgemm_ex", "sgemm_plan_ex",
     "sgemm_3xtf32_ex", "sgemm_host", "sgemm_noalloc_check_status", "sgemm_fp32_peak_ex",
-    "sgemm_null_launch", "sgemm_tf32_mma_peak",
+    "sgemm_null_launch", "sgemm_tf32_mma_peak", "sgemm_selftest_occupy",
 )
 
 SGEMM_PEAK_FFMA, SGEMM_PEAK_FFMA2, SGEMM_PEAK_OUTER = 0, 1, 2
@@ -95,6 +95,8 @@ def load():
         lib.sgemm_fp32_peak.restype = ci
         lib.sgemm_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
         lib.sgemm_selftest_wait_timeout.restype = ci
+        lib.sgemm_selftest_occupy.argtypes = [ci, ctypes.c_uint64, vp]
+        lib.sgemm_selftest_occupy.restype = ci
         lib.sgemm_noalloc.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
         lib.sgemm_noalloc.restype = ci
         lib.sgemm_noalloc_check_status.argtypes = [vp, ctypes.POINTER(ci)]
@@ -255,6 +257,11 @@ def sgemm_null_launch(stream=0) -> int:
 
 def sgemm_selftest_wait_timeout(timeout_ns: int, stream=0) -> int:
     return load().sgemm_selftest_wait_timeout(int(timeout_ns), stream)
+
+
+def sgemm_selftest_occupy(ctas: int, ns: int, stream=0) -> int:
+    """`ctas` CTAs holding one SM each for `ns` ns on `stream`; raw code."""
+    return load().sgemm_selftest_occupy(int(ctas), int(ns), stream)
 
 
 # ---- torch tensor convenience (marshalling only) --------------------------

@@ -42,6 +42,19 @@ __device__ float g_peak_sink[kThreads];
 // Does nothing: the launch-latency floor every kernel of a call pays.
 __global__ void null_kernel() {}
 
+// Holds its SM for `ns` nanoseconds (by the global timer, sleeping between
+// reads) and does nothing else; launched with so much shared memory that no
+// SGEMM CTA fits beside it.
+constexpr int kOccupySmem = 200 * 1024;
+__global__ void occupy_kernel(unsigned long long ns) {
+    unsigned long long t0, t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    do {
+        __nanosleep(20000);
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    } while (t - t0 < ns);
+}
+
 __global__ void __launch_bounds__(kThreads)
 fp32_peak_kernel(float mul, float add, long long iters, int sink_key) {
     float x[kChains];
@@ -217,6 +230,24 @@ extern "C" int sgemm_fp32_peak_ex(int form, double target_ms, double* gflops, do
 extern "C" int sgemm_fp32_peak(double target_ms, double* gflops, double* ms, double* flops,
                                cudaStream_t stream) {
     return sgemm_fp32_peak_ex(SGEMM_PEAK_FFMA, target_ms, gflops, ms, flops, stream);
+}
+
+extern "C" int sgemm_selftest_occupy(int ctas, uint64_t ns, cudaStream_t stream) {
+    if (ctas < 1 || ns == 0 || ns > 2000000000ull) return SGEMM_ERR_INVALID_VALUE;
+    const int ready = sgemm_internal_device_ready();
+    if (ready != SGEMM_OK) return ready;
+    if (ctas > sgemm_internal_sm_count()) return SGEMM_ERR_INVALID_VALUE;
+    cudaError_t e = cudaFuncSetAttribute(occupy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kOccupySmem);
+    if (e == cudaSuccess) {
+        occupy_kernel<<<ctas, 32, kOccupySmem, stream>>>(static_cast<unsigned long long>(ns));
+        e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) {
+        sgemm_internal_set_cuda_error(static_cast<int>(e));
+        return SGEMM_ERR_LAUNCH;
+    }
+    return SGEMM_OK;
 }
 
 extern "C" int sgemm_null_launch(cudaStream_t stream) {

@@ -379,6 +379,17 @@ SGEMM_API int sgemm_null_launch(cudaStream_t stream);
 SGEMM_API int sgemm_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stream);
 
 /*
+ * sgemm_selftest_occupy — launch `ctas` CTAs on `stream`, each holding one
+ * SM (so much shared memory that no SGEMM CTA fits beside it) for `ns`
+ * nanoseconds and doing nothing else: another kernel holding SMs, for
+ * showing that an SGEMM started meanwhile on another stream still finishes
+ * while its CTAs start a few at a time (see "Sharing the GPU" at sgemm).
+ * Returns SGEMM_ERR_INVALID_VALUE unless 1 <= ctas <= the device's SM count
+ * and 0 < ns <= 2e9, else launch errors like sgemm.
+ */
+SGEMM_API int sgemm_selftest_occupy(int ctas, uint64_t ns, cudaStream_t stream);
+
+/*
  * sgemm_3xtf32 — the same operation, arguments and errors as sgemm, computed
  * on the tcgen05 tensor cores with the three-term TF32 split: each FP32
  * input x = x_hi + x_lo (x_hi = tf32(x), x_lo = tf32(x - x_hi)) and

@@ -120,6 +120,13 @@ def test_timeout_setting_bounds(lib):
     assert sg.sgemm_selftest_wait_timeout(10) == sg.SGEMM_ERR_INVALID_VALUE
 
 
+def test_occupy_selftest_argument_checks(lib):
+    for ctas, ns in [(0, 1000), (-1, 1000), (1, 0), (1, 2_000_000_001)]:
+        assert sg.sgemm_selftest_occupy(ctas, ns) == sg.SGEMM_ERR_INVALID_VALUE
+    # Valid arguments on a machine without a GPU: an error, never SGEMM_OK.
+    assert sg.sgemm_selftest_occupy(1, 1000) != sg.SGEMM_OK
+
+
 def test_tensor_wrapper_rejects_cpu_tensors(lib):
     torch = pytest.importorskip("torch")
     a = torch.zeros(4, 4)
