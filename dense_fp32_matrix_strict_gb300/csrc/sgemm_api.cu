@@ -697,6 +697,17 @@ int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, 
         } else {
             pl->a_pre = copy_ok && 0.085 * t_main > copy_cost;
         }
+        // A row-major A that TMA cannot read in place and that would be
+        // copied to an aligned buffer anyway (N >= 256, below) is better
+        // copied transposed: the same one HBM pass, then the transposed-A
+        // read (GB300: 1024x1024x1023 50.5 against 51.6 us, 768x768x767
+        // 28.7 against 29.8 us, 2048x1024x1023 80.0 against 84.2 us), where
+        // the main loop is long enough for its ~8.5 % to matter (0.085
+        // t_main > 1 us); on shorter ones the transposed copy came out slower
+        // (300x512x1001: 24.6 against 22.6 us).
+        const bool a_packs_anyway =
+            !pl->a_t && allow_pack && !force_cp && N >= 256 && !tma_ok(A, lda, M, K);
+        if (a_packs_anyway && 0.085 * t_main > 1e-6) pl->a_pre = copy_ok;
     }
     std::memset(&pl->tmA, 0, sizeof(CUtensorMap));
     std::memset(&pl->tmB, 0, sizeof(CUtensorMap));
