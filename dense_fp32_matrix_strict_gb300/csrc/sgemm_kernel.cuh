@@ -45,11 +45,15 @@
 // or k-major, [BK][BM], the layout of the pages' transposing store (each
 // lane reads two float4 of 4 rows per k-step; the FMA pipe stays busier).
 // The k-major layout comes from an A given transposed, from a transposed
-// copy of A, or from transposer warps that rewrite each TMA-landed stage.
+// copy of A (made by a kernel before this one, or by this kernel's own
+// transposer warps while its first tiles run, which then also make the
+// row-major copy of a transposed B), or from transposer warps that rewrite
+// each TMA-landed stage.
 //
-// Every mbarrier wait is bounded (globaltimer): on timeout the thread sets a
-// bit in the device status word, lets its own copies in flight land (again
-// bounded) and returns. Nothing spins forever.
+// Every wait, on an mbarrier or on another CTA's flag, is bounded
+// (globaltimer): on timeout the thread sets a bit in the device status word,
+// lets its own copies in flight land (again bounded) and returns. Nothing
+// spins forever.
 #pragma once
 
 #include <cuda.h>
@@ -675,8 +679,9 @@ __device__ __forceinline__ void at_transposer(const GemmParams& p, float* xt, in
     };
     // Order: (1) k-tile by k-tile, group 0's A units and the first wave's B
     // units; (2) wave by wave, k-tile by k-tile, the B units a later wave
-    // needs first; (3) the A units of raster groups 1.. in the order of A's
-    // copy alone.
+    // needs first; (3) raster group by raster group, k-tile by k-tile, tile
+    // row by tile row, the A units of groups 1.. (B's column blocks are all
+    // needed again by each group, A's rows only by their own).
     const long long per_group = static_cast<long long>(p.group_m) * p.k_tiles;
     const int gm0 = do_a ? gmr : 0;
     const int nb0 = do_b ? tn_end(0) : 0;
