@@ -302,9 +302,10 @@ SGEMM_API int sgemm_set_shape_config(int64_t M, int64_t N, int64_t K, const char
 SGEMM_API int sgemm_clear_shape_configs(void);
 
 /*
- * sgemm_set_wait_timeout_ns — limit on every bounded mbarrier wait inside
- * the kernels launched after this call (default 2e9 ns). Values below
- * 1000 ns are rejected with SGEMM_ERR_INVALID_VALUE.
+ * sgemm_set_wait_timeout_ns — limit on every bounded wait inside the
+ * kernels launched after this call, on an mbarrier or on another CTA's flag
+ * (default 2e9 ns). Values below 1000 ns are rejected with
+ * SGEMM_ERR_INVALID_VALUE.
  */
 SGEMM_API int sgemm_set_wait_timeout_ns(uint64_t ns);
 
