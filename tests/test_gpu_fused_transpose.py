@@ -198,3 +198,33 @@ def test_fused_copy_of_a_transposed_b(M, N, K, ta, tb):
     opB = B.T if tb else B
     ref, S = oracle.sgemm_ref(0.7, np.ascontiguousarray(opA), np.ascontiguousarray(opB), -1.3, C0)
     assert oracle.check(C1, ref, S, K)["ok"]
+
+
+# Stored operands with padded rows (NaN between them, which must never reach C)
+# and base addresses off the 16-byte grid, so both fused copies read their
+# units by scalar loads; C padded too, its guard bands checked.
+PADDED_B_CASES = [
+    ((2000, 2100, 1531, True, True), dict(lda=2004, ldb=1536, offsets=(0, 1, 0))),
+    ((4093, 2560, 1531, False, True), dict(lda=1533, ldb=1534, ldc=2564, offsets=(1, 2, 3))),
+]
+
+
+@pytest.mark.parametrize("case,layout", PADDED_B_CASES,
+                         ids=["x".join(map(str, c[:3])) + ("_T" if c[3] else "_N") + "T"
+                              for c, _ in PADDED_B_CASES])
+def test_fused_copies_of_padded_unaligned_operands(case, layout):
+    M, N, K, ta, tb = case
+    A = inputs.fill("normal", 1350, inputs.TID_A, *((K, M) if ta else (M, K)))
+    B = inputs.fill("normal", 1350, inputs.TID_B, *((N, K) if tb else (K, N)))
+    C0 = inputs.fill("normal", 1350, inputs.TID_C, M, N)
+    C1, g1, plan1 = run_cfg("auto", 0.7, A, B, -1.3, C0, transa=ta, transb=tb, **layout)
+    C2, g2, plan2 = run_cfg("auto:atcopy", 0.7, A, B, -1.3, C0, transa=ta, transb=tb, **layout)
+    assert g1 and g2
+    assert "+packBTfused" in plan1[0], plan1
+    assert ("+packATfused" in plan1[0]) == (not ta), plan1
+    assert "fused" not in plan2[0], plan2
+    assert np.array_equal(C1, C2), int(np.count_nonzero(C1 != C2))
+    opA = A.T if ta else A
+    opB = B.T if tb else B
+    ref, S = oracle.sgemm_ref(0.7, np.ascontiguousarray(opA), np.ascontiguousarray(opB), -1.3, C0)
+    assert oracle.check(C1, ref, S, K)["ok"]
