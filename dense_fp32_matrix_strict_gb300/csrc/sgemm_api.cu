@@ -807,7 +807,8 @@ int make_plan_ex(const DeviceInfo* dev, int opa, int opb, int64_t M, int64_t N, 
     // through the transposed-A path anyway (its copy made here too, or A
     // given transposed and read in place). Both only with a first wave of
     // whole tiles: the tail's CTAs start all along the k-range at once and
-    // would wait for units the round-robin has not reached (6.1).
+    // would wait for units the round-robin has not reached (1024^3 forced to
+    // it: 62.6 against 47.5 us).
     pl->b_fused = false;
     pl->bt_flags_off = 0;
     const int64_t tiles_all = ((M + bm - 1) / bm) * ((N + bn - 1) / bn);
