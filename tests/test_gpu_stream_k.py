@@ -56,6 +56,7 @@ CASES = [
     ("128x128:cpasync", (333, 4500, 777)),    # cp.async producers, ragged edges
     ("ws_128x64x32_s4_k2", (1024, 1024, 1024)),
     ("ws_64x64x32_s4_k4", (256, 256, 8192)),
+    ("auto", (2048, 2048, 8192)),             # transposed copy of A made in the kernel + tail
 ]
 
 
